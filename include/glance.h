@@ -1,0 +1,227 @@
+/*
+ * glance.h -- C ABI of the GLANCE verify-round library (sm_103a).
+ *
+ * One speculative-decoding round of GLANCE ("Vision Is Not Overhead: One-Pass
+ * Block Drafting for Lossless Speculative Decoding in Vision-Language Models",
+ * arXiv 2609.00355) has four data-parallel steps, one entry point each:
+ *
+ *   glance_build_tree      draft marginals q_1..q_L -> top-N candidate tree,
+ *                          packed (Assumption 1, Definition 1, Section 4.2)
+ *   glance_tree_attention  ancestor-masked GQA attention of the packed rows
+ *                          against the cached prefix (Definition 1)
+ *   glance_lmhead_argmax   LM head of the verified rows with per-row greedy
+ *                          argmax and top-2 gap (Section 3.1; Appendix B.1)
+ *   glance_accept_commit   acceptance walk A(S), KV commit, bonus root
+ *                          (Definition 1; Appendix B.1 proof of Theorem 1)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Memory: every array argument is a DEVICE pointer unless its comment says
+ *   host. The caller owns all memory; the library allocates and frees nothing.
+ *   Scratch space is a caller-provided device workspace whose size the
+ *   matching *_workspace_bytes() call returns. A workspace must be zero-filled
+ *   before its first use; every call leaves the counters it uses at zero, so
+ *   the same workspace can be reused by later calls on the same stream. Two
+ *   calls that may run at the same time need distinct workspaces.
+ * - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream). Every call only enqueues work on that stream and returns; no call
+ *   synchronises with the device, so rounds can be captured in a CUDA graph.
+ * - Errors: argument errors are found on the host before anything is
+ *   launched and are returned as a status; glance_last_error() then describes
+ *   them (thread-local text). A failed launch returns GLANCE_ERR_CUDA. Errors
+ *   that only the device can see (non-finite draft logits, a prefix length
+ *   that leaves no room for the tree rows, a pipeline wait that ran out) set a
+ *   device status word and the kernel returns early; glance_device_status()
+ *   reads it.
+ * - Packed tree layout (rows = N + 1; row 0 is the pending root b): rows are
+ *   in canonical order: root, then by depth ascending, then by parent row
+ *   ascending, then by the node's rank in its offset's candidate list
+ *   ascending. Every parent row precedes its children.
+ * - KV cache layout, per layer: K and V are separate arrays of
+ *   [n_kv_heads][t_cap][head_dim] elements (strides in glance_kv). Slots
+ *   0..T-1 hold the committed prefix; the verify pass writes the tree rows'
+ *   K/V to slots T..T+N (row r at slot T + r) before attention reads them.
+ *   T lives in device memory (*t_len) so that a captured round can be
+ *   replayed: kernels read it there and glance_accept_commit advances it.
+ */
+#ifndef GLANCE_H
+#define GLANCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GLANCE_OK = 0,
+  GLANCE_ERR_INVALID_ARG = 1, /* null pointer, size out of range, misaligned */
+  GLANCE_ERR_UNSUPPORTED = 2, /* a valid shape this build has no kernel for */
+  GLANCE_ERR_CAPACITY = 3,    /* workspace too small */
+  GLANCE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  GLANCE_ERR_DEVICE = 5       /* the device status word is set */
+} glance_status;
+
+typedef enum { GLANCE_F32 = 0, GLANCE_BF16 = 1 } glance_dtype;
+
+/* Device status word values (glance_device_status). */
+#define GLANCE_DEV_OK 0
+#define GLANCE_DEV_NONFINITE_LOGITS 1 /* a draft logit row held NaN or +-inf */
+#define GLANCE_DEV_TREE_CAPACITY 2    /* T + N + 1 > t_cap at run time */
+#define GLANCE_DEV_BAD_TREE 3         /* a tree array was inconsistent */
+#define GLANCE_DEV_PIPELINE_TIMEOUT 4 /* an mbarrier wait hit its iteration cap */
+
+/* A packed candidate tree: device arrays with N + 1 rows, caller-allocated. */
+typedef struct {
+  int32_t n;          /* N, the budget: non-root nodes (1 <= N <= 255) */
+  int32_t L;          /* maximum depth = number of draft offsets (1..16) */
+  int32_t mask_words; /* ceil((N+1)/64), 1..4 */
+  int32_t* token;     /* [N+1] token id of each row; row 0 = root b */
+  int32_t* parent;    /* [N+1] parent row; -1 at the root */
+  int32_t* depth;     /* [N+1] 0 at the root */
+  int32_t* pos_id;    /* [N+1] position id = T + depth */
+  float* score;       /* [N+1] log plug-in score sum_j log q_j(y_j); 0 at root */
+  uint64_t* anc;      /* [N+1][mask_words]; bit k of row i (word k/64, bit
+                         k%64) is set iff row k is row i, the root, or an
+                         ancestor of row i */
+} glance_tree;
+
+/* One layer's KV cache view. */
+typedef struct {
+  void* k;             /* device [n_kv_heads][t_cap][head_dim] elements */
+  void* v;             /* same shape as k */
+  glance_dtype dtype;  /* GLANCE_BF16 (head_dim 128) or GLANCE_F32 (any
+                          head_dim that is a multiple of 32, <= 128) */
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t t_cap;       /* slots per head */
+  int64_t head_stride; /* elements between heads (>= t_cap * row_stride) */
+  int64_t row_stride;  /* elements between slots (>= head_dim) */
+  int32_t* t_len;      /* device int32: T, the committed prefix length */
+} glance_kv;
+
+/* ------------------------------------------------------------------ build */
+
+/* Workspace bytes for glance_build_tree with these sizes (0 on bad sizes). */
+size_t glance_build_tree_workspace_bytes(int L, int V, int N);
+
+/*
+ * Draft-to-tree (Assumption 1; Definition 1; Section 4.2 "the builder keeps
+ * the prefixes of highest plug-in score").
+ *
+ * draft_logits: [L][V] row-major, dtype F32 or BF16; q_j = softmax(row j).
+ * For each offset j the kernel forms log q_j = x_j - logsumexp(x_j) and the
+ * K = min(N, V) best tokens by (logit desc, token id asc). It then keeps the N
+ * strings of highest plug-in score sum_{j<=d} log q_j(y_j) (fp32, summed in
+ * order j = 1..d), nodes ordered by (score desc, depth asc, rank vector
+ * lexicographic asc), and writes them in canonical packed order.
+ * root_token: device int32, the pending root b (row 0's token).
+ * t_len: device int32, T (pos_id = T + depth).
+ * tree: host struct holding device arrays sized for N+1 rows; tree->n must be
+ * N, tree->L must be L and tree->mask_words must be ceil((N+1)/64).
+ * Limits: 1 <= L <= 16, 2 <= V <= 262144, 1 <= N <= 255,
+ * N <= number of strings of length <= L over V tokens, and
+ * ceil(V / 8192) * min(N, V) <= 8192 (the per-row candidate merge).
+ */
+glance_status glance_build_tree(const void* draft_logits, glance_dtype dtype, int L, int V,
+                                int N, const int32_t* root_token, const int32_t* t_len,
+                                const glance_tree* tree, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* -------------------------------------------------------------- attention */
+
+/* Workspace bytes for glance_tree_attention (0 on bad sizes). */
+size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_heads, const glance_kv* kv);
+
+/*
+ * Ancestor-masked tree attention of one layer (Definition 1: each packed row
+ * of a depth-d node sees the cached prefix, the root and its own ancestors,
+ * so it yields the same row as the unpacked sequence x . b . y_{1:d}).
+ *
+ * q:   [N+1][n_q_heads][head_dim] (dtype of kv), rotary position already
+ *      applied by the caller.
+ * kv:  the layer's cache; prefix at slots 0..T-1, tree rows at T..T+N.
+ * For q head h the kv head is h / (n_q_heads / n_kv_heads). Row i attends to
+ * prefix slots 0..T-1 and tree slots T + k for every k with anc bit (i, k),
+ * with scores (q . k) * scale and a softmax over exactly those keys.
+ * out: [N+1][n_q_heads][head_dim], same dtype (bf16 rounded to nearest even).
+ * Supported: BF16 with head_dim 128, n_q_heads / n_kv_heads in {1,2,4,8},
+ * N + 1 <= 256; F32 with head_dim a multiple of 32 up to 128.
+ */
+glance_status glance_tree_attention(const void* q, int n_q_heads, const glance_kv* kv,
+                                    const glance_tree* tree, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------- LM head */
+
+/* Workspace bytes for glance_lmhead_argmax (0 on bad sizes). */
+size_t glance_lmhead_argmax_workspace_bytes(int M, int d, int V, glance_dtype dtype);
+
+/*
+ * LM head with fused greedy argmax and top-2 gap (Section 3.1: greedy emits
+ * argmax_w p(w | prefix); Appendix B.1: gamma = l_(1) - l_(2)).
+ *
+ * h: [M][d] row-major; W: [d][V] row-major (V contiguous); both dtype.
+ * logits[i][v] = sum_k h[i][k] * W[k][v], accumulated in fp32; they are
+ * never written out. argmax[i] (int32) is the lowest token id among equal
+ * maxima; gap[i] = max logit - largest logit of any other token (0 on an
+ * exact tie); maxlogit[i] the max logit (nullable).
+ * Supported: BF16 with d % 64 == 0, V % 8 == 0, 1 <= M <= 512; F32 with any
+ * d, V and M <= 512.
+ */
+glance_status glance_lmhead_argmax(const void* h, const void* W, glance_dtype dtype, int M,
+                                   int d, int V, int32_t* argmax, float* gap,
+                                   float* maxlogit, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* ------------------------------------------------------------------ commit */
+
+/* Workspace bytes for glance_accept_commit. */
+size_t glance_accept_commit_workspace_bytes(int n_layers);
+
+/*
+ * Acceptance walk and commit (Definition 1; Appendix B.1 proof of Theorem 1).
+ *
+ * argmax: [N+1] the target's greedy token of every packed row.
+ * Walk: u = root; while depth(u) < L and u has a child whose token equals
+ * argmax[u], move to that child. a = A(S) = depth of the last row; the
+ * accepted tokens are the tokens of the path rows 1..a; new_root = argmax of
+ * the last row.
+ * Commit, for every layer in layers[0..n_layers-1] (host array of views): the
+ * K and V of path rows path_0 = 0, ..., path_a move from slots T + path_i to
+ * slots T + i (all sources are read before any slot is written), then
+ * *t_len += a + 1 (every layer must share the same t_len pointer).
+ * Outputs (device): n_accepted (int32), accepted_tok ([L] int32, first a
+ * valid), new_root (int32; may alias the next round's root_token).
+ * Limits: 1 <= n_layers <= 128.
+ */
+glance_status glance_accept_commit(const glance_tree* tree, const int32_t* argmax,
+                                   const glance_kv* layers, int n_layers, int32_t* n_accepted,
+                                   int32_t* accepted_tok, int32_t* new_root, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Text of the last host-side error on this thread ("" if none). */
+const char* glance_last_error(void);
+
+/* Name of a status value. */
+const char* glance_status_string(glance_status s);
+
+/* Synchronises the current device, then stores the device status word (one
+ * of GLANCE_DEV_*; the first error since the last reset wins) in *code_out
+ * (host pointer). Returns GLANCE_ERR_DEVICE if it is non-zero. */
+glance_status glance_device_status(int32_t* code_out);
+
+/* Clears the device status word of the current device (synchronous). */
+glance_status glance_reset_device_status(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int glance_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLANCE_H */

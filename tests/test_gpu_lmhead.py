@@ -1,0 +1,99 @@
+"""LM head + argmax + top-2 gap on the GPU vs the oracle (fp64 on the same
+bf16 inputs): argmax bit-exact where the oracle gap exceeds 1e-3, gap and max
+logit within 2e-2 (bf16) / 1e-5 (fp32)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _util import bf16_tensor
+from oracle.bf16 import bf16_bits_to_f64
+from oracle.lmhead import lmhead_argmax as o_lmhead
+
+pytestmark = pytest.mark.gpu
+
+
+def run_bf16(hb, Wb, dev):
+    import tree_verified_block_gb300 as g
+    M, d = hb.shape
+    V = Wb.shape[1]
+    am = torch.full((M,), -1, dtype=torch.int32, device=dev)
+    gap = torch.empty(M, dtype=torch.float32, device=dev)
+    mx = torch.empty(M, dtype=torch.float32, device=dev)
+    ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.bfloat16), dev)
+    g.lmhead_argmax(bf16_tensor(hb, dev), bf16_tensor(Wb, dev), am, gap, mx, ws)
+    return am.cpu().numpy(), gap.cpu().numpy(), mx.cpu().numpy()
+
+
+def compare(got, ref, tol):
+    am, gap, mx = got
+    ra, rg, rm = ref
+    sure = rg > 1e-3
+    assert np.array_equal(am[sure], ra[sure])
+    assert np.all(np.abs(mx - rm) <= tol)
+    assert np.all(np.abs(gap - rg) <= tol)
+
+
+@pytest.mark.parametrize("M,d,V", [(1, 64, 8), (16, 128, 1000), (64, 256, 5000),
+                                   (128, 512, 4104), (200, 256, 3000), (64, 192, 136),
+                                   (512, 128, 2048)])
+def test_bf16_shapes(dev, clean_status, M, d, V):
+    gen = W.rng(M, d, V)
+    hb = W.normal_bf16(gen, (M, d))
+    Wb = W.normal_bf16(gen, (d, V), std=0.02)
+    got = run_bf16(hb, Wb, dev)
+    ref = o_lmhead(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb))
+    compare(got, ref, 2e-2)
+
+
+def test_bf16_qwen_lm_head_planted(dev, clean_status):
+    # [64, 4096] x [4096, 151936] with planted greedy tokens on half the rows
+    M, d, V = 64, 4096, 151936
+    gen = W.rng(31)
+    Wf = W.bf16_bits_to_f32(W.normal_bf16(gen, (d, V), std=0.02))
+    h = gen.standard_normal((M, d), dtype=np.float32)
+    rows = np.arange(0, M, 2)
+    toks = gen.integers(0, V, size=rows.size)
+    h = W.plant_greedy_path(h, Wf, rows, toks)
+    hb = W.to_bf16_bits(h)
+    Wb = W.to_bf16_bits(Wf)
+    got = run_bf16(hb, Wb, dev)
+    ref = o_lmhead(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb))
+    compare(got, ref, 2e-2)
+    assert np.array_equal(got[0][rows], toks)
+
+
+def test_bf16_exact_ties_lowest_id(dev, clean_status):
+    M, d, V = 4, 64, 4096
+    gen = W.rng(5)
+    Wb = W.normal_bf16(gen, (d, V), std=0.02)
+    for dst, src in ((3000, 17), (2049, 17), (4095, 100)):
+        Wb[:, dst] = Wb[:, src]        # duplicate columns: exact logit ties
+    hb = np.zeros((M, d), np.uint16)
+    hb[:] = W.to_bf16_bits(np.ones(d, np.float32))
+    h = bf16_bits_to_f64(hb)
+    col17 = bf16_bits_to_f64(Wb[:, 17])
+    Wbig = Wb.copy()
+    # make column 17 (and its copies) the clear winner for every row
+    Wbig[:, 17] = W.to_bf16_bits((col17 + 0.5).astype(np.float32))
+    for dst in (3000, 2049):
+        Wbig[:, dst] = Wbig[:, 17]
+    am, gap, mx = run_bf16(hb, Wbig, dev)
+    ref = o_lmhead(h, bf16_bits_to_f64(Wbig))
+    assert np.all(am == 17) and np.all(ref[0] == 17)
+    assert np.all(gap == 0.0) and np.all(ref[1] == 0.0)
+
+
+@pytest.mark.parametrize("M,d,V", [(16, 128, 512), (3, 100, 777), (64, 256, 300)])
+def test_fp32(dev, clean_status, M, d, V):
+    import tree_verified_block_gb300 as g
+    gen = np.random.default_rng(M + d + V)
+    h = gen.standard_normal((M, d)).astype(np.float32)
+    Wm = (gen.standard_normal((d, V)) * 0.02).astype(np.float32)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    gap = torch.empty(M, dtype=torch.float32, device=dev)
+    mx = torch.empty(M, dtype=torch.float32, device=dev)
+    ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.float32), dev)
+    g.lmhead_argmax(torch.from_numpy(h).to(dev), torch.from_numpy(Wm).to(dev), am, gap, mx, ws)
+    ref = o_lmhead(h, Wm)
+    compare((am.cpu().numpy(), gap.cpu().numpy(), mx.cpu().numpy()), ref, 1e-5)

@@ -1,0 +1,21 @@
+"""GLANCE verify-round hot path for GB300 (sm_103a).
+
+The compute lives in ``libglance.so`` (CUDA kernels behind a C ABI declared in
+``include/glance.h``); this package is its Python binding. Calls:
+
+* ``build_tree``      draft logits [L, V] -> packed top-N candidate tree
+* ``tree_attention``  ancestor-masked GQA attention of the packed rows
+* ``lmhead_argmax``   LM head with fused per-row argmax and top-2 gap
+* ``accept_commit``   acceptance walk A(S), KV commit, new root
+"""
+from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
+                       accept_commit_workspace_bytes, build_tree, build_tree_workspace_bytes,
+                       device_status, lib, lmhead_argmax, lmhead_argmax_workspace_bytes,
+                       reset_device_status, tree_attention, tree_attention_workspace_bytes,
+                       version, workspace)
+
+__all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
+           "accept_commit", "accept_commit_workspace_bytes", "build_tree",
+           "build_tree_workspace_bytes", "device_status", "lib", "lmhead_argmax",
+           "lmhead_argmax_workspace_bytes", "reset_device_status", "tree_attention",
+           "tree_attention_workspace_bytes", "version", "workspace"]

@@ -1,0 +1,223 @@
+"""ctypes binding of libglance.so: argument marshalling only.
+
+Every step runs in the library's CUDA kernels. PyTorch provides device memory
+and streams; tensors are passed as raw pointers. There is no fallback: if the
+library is not built, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libglance.so")
+
+F32, BF16 = 0, 1
+STATUS = {0: "GLANCE_OK", 1: "GLANCE_ERR_INVALID_ARG", 2: "GLANCE_ERR_UNSUPPORTED",
+          3: "GLANCE_ERR_CAPACITY", 4: "GLANCE_ERR_CUDA", 5: "GLANCE_ERR_DEVICE"}
+DEV_STATUS = {0: "ok", 1: "non-finite draft logits", 2: "tree does not fit the cache",
+              3: "inconsistent tree", 4: "pipeline wait timed out"}
+
+EXPORTS = [
+    "glance_build_tree_workspace_bytes", "glance_build_tree",
+    "glance_tree_attention_workspace_bytes", "glance_tree_attention",
+    "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax",
+    "glance_accept_commit_workspace_bytes", "glance_accept_commit",
+    "glance_last_error", "glance_status_string", "glance_device_status",
+    "glance_reset_device_status", "glance_version",
+]
+
+
+class GlanceError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class TreeC(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("L", ctypes.c_int32), ("mask_words", ctypes.c_int32),
+                ("token", ctypes.c_void_p), ("parent", ctypes.c_void_p),
+                ("depth", ctypes.c_void_p), ("pos_id", ctypes.c_void_p),
+                ("score", ctypes.c_void_p), ("anc", ctypes.c_void_p)]
+
+
+class KVC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dtype", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("t_cap", ctypes.c_int32), ("head_stride", ctypes.c_int64),
+                ("row_stride", ctypes.c_int64), ("t_len", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libglance.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; build it with "
+                           "tree_verified_block_gb300._build.build() (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    st = ctypes.c_int
+    L.glance_build_tree_workspace_bytes.argtypes = [i32, i32, i32]
+    L.glance_build_tree_workspace_bytes.restype = sz
+    L.glance_build_tree.argtypes = [vp, i32, i32, i32, i32, vp, vp, ctypes.POINTER(TreeC), vp, sz, vp]
+    L.glance_build_tree.restype = st
+    L.glance_tree_attention_workspace_bytes.argtypes = [i32, i32, ctypes.POINTER(KVC)]
+    L.glance_tree_attention_workspace_bytes.restype = sz
+    L.glance_tree_attention.argtypes = [vp, i32, ctypes.POINTER(KVC), ctypes.POINTER(TreeC),
+                                        ctypes.c_float, vp, vp, sz, vp]
+    L.glance_tree_attention.restype = st
+    L.glance_lmhead_argmax_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.glance_lmhead_argmax_workspace_bytes.restype = sz
+    L.glance_lmhead_argmax.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.glance_lmhead_argmax.restype = st
+    L.glance_accept_commit_workspace_bytes.argtypes = [i32]
+    L.glance_accept_commit_workspace_bytes.restype = sz
+    L.glance_accept_commit.argtypes = [ctypes.POINTER(TreeC), vp, ctypes.POINTER(KVC), i32, vp, vp,
+                                       vp, vp, sz, vp]
+    L.glance_accept_commit.restype = st
+    L.glance_last_error.argtypes = []
+    L.glance_last_error.restype = ctypes.c_char_p
+    L.glance_status_string.argtypes = [st]
+    L.glance_status_string.restype = ctypes.c_char_p
+    L.glance_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    L.glance_device_status.restype = st
+    L.glance_reset_device_status.argtypes = []
+    L.glance_reset_device_status.restype = st
+    L.glance_version.argtypes = []
+    L.glance_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != 0:
+        raise GlanceError(status, lib().glance_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def workspace(nbytes, device="cuda"):
+    """A zero-filled device workspace (the library leaves its counters at zero)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class Tree:
+    """Device arrays of one packed tree (N + 1 rows) and the C view of them."""
+
+    def __init__(self, N, L, device="cuda"):
+        rows = N + 1
+        self.N, self.L, self.rows = N, L, rows
+        self.mask_words = (rows + 63) // 64
+        i32 = dict(dtype=torch.int32, device=device)
+        self.token = torch.zeros(rows, **i32)
+        self.parent = torch.zeros(rows, **i32)
+        self.depth = torch.zeros(rows, **i32)
+        self.pos_id = torch.zeros(rows, **i32)
+        self.score = torch.zeros(rows, dtype=torch.float32, device=device)
+        self.anc = torch.zeros((rows, self.mask_words), dtype=torch.int64, device=device)
+        self.c = TreeC(N, L, self.mask_words, self.token.data_ptr(), self.parent.data_ptr(),
+                       self.depth.data_ptr(), self.pos_id.data_ptr(), self.score.data_ptr(),
+                       self.anc.data_ptr())
+
+    def to_host(self):
+        return dict(token=self.token.cpu().numpy(), parent=self.parent.cpu().numpy(),
+                    depth=self.depth.cpu().numpy(), pos_id=self.pos_id.cpu().numpy(),
+                    score=self.score.cpu().numpy(),
+                    anc=self.anc.cpu().numpy().view("uint64"))
+
+
+class KVLayer:
+    """One layer's cache view: k, v tensors [n_kv_heads][t_cap][head_dim]."""
+
+    def __init__(self, k, v, t_len):
+        assert k.shape == v.shape and k.dim() == 3 and k.stride() == v.stride()
+        assert k.stride(2) == 1, "head_dim must be contiguous"
+        self.k, self.v, self.t_len = k, v, t_len
+        Hkv, t_cap, D = k.shape
+        self.c = KVC(k.data_ptr(), v.data_ptr(), _dtype_code(k), Hkv, D, t_cap,
+                     k.stride(0), k.stride(1), t_len.data_ptr())
+
+
+# ------------------------------------------------------------------- calls
+
+def build_tree_workspace_bytes(L, V, N):
+    return lib().glance_build_tree_workspace_bytes(L, V, N)
+
+
+def build_tree(draft_logits, N, root_token, t_len, tree, ws, stream=None):
+    L, V = draft_logits.shape
+    assert draft_logits.is_contiguous()
+    _check(lib().glance_build_tree(_ptr(draft_logits), _dtype_code(draft_logits), L, V, N,
+                                   _ptr(root_token), _ptr(t_len), ctypes.byref(tree.c),
+                                   _ptr(ws), ws.numel(), _stream(stream, draft_logits.device)))
+
+
+def tree_attention_workspace_bytes(rows, n_q_heads, kv):
+    return lib().glance_tree_attention_workspace_bytes(rows, n_q_heads, ctypes.byref(kv.c))
+
+
+def tree_attention(q, kv, tree, scale, out, ws, stream=None):
+    assert q.is_contiguous() and out.is_contiguous() and q.shape == out.shape
+    _check(lib().glance_tree_attention(_ptr(q), q.shape[1], ctypes.byref(kv.c),
+                                       ctypes.byref(tree.c), float(scale), _ptr(out), _ptr(ws),
+                                       ws.numel(), _stream(stream, q.device)))
+
+
+def lmhead_argmax_workspace_bytes(M, d, V, dtype):
+    code = BF16 if dtype == torch.bfloat16 else F32
+    return lib().glance_lmhead_argmax_workspace_bytes(M, d, V, code)
+
+
+def lmhead_argmax(h, W, argmax, gap, maxlogit, ws, stream=None):
+    M, d = h.shape
+    assert W.shape[0] == d and h.is_contiguous() and W.is_contiguous() and h.dtype == W.dtype
+    _check(lib().glance_lmhead_argmax(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
+                                      _ptr(argmax), _ptr(gap), _ptr(maxlogit), _ptr(ws),
+                                      ws.numel(), _stream(stream, h.device)))
+
+
+def accept_commit_workspace_bytes(n_layers):
+    return lib().glance_accept_commit_workspace_bytes(n_layers)
+
+
+def accept_commit(tree, argmax, layers, n_accepted, accepted_tok, new_root, ws, stream=None):
+    arr = (KVC * len(layers))(*[l.c for l in layers])
+    _check(lib().glance_accept_commit(ctypes.byref(tree.c), _ptr(argmax), arr, len(layers),
+                                      _ptr(n_accepted), _ptr(accepted_tok), _ptr(new_root),
+                                      _ptr(ws), ws.numel(), _stream(stream, argmax.device)))
+
+
+def device_status():
+    """(code, text) of the device status word; synchronises the device."""
+    code = ctypes.c_int32(0)
+    lib().glance_device_status(ctypes.byref(code))
+    return code.value, DEV_STATUS.get(code.value, "unknown")
+
+
+def reset_device_status():
+    _check(lib().glance_reset_device_status())
+
+
+def version():
+    return lib().glance_version()

@@ -1,0 +1,672 @@
+// Draft-to-tree: per-offset log-softmax + top-K, best-first top-N builder,
+// canonical packing. One launch.
+//
+// Paper: "Vision Is Not Overhead ..." (arXiv 2609.00355), Assumption 1 (one
+// marginal q_j per offset, plug-in score pi_hat = prod_j q_j(y_j)),
+// Definition 1 (prefix-closed candidate tree, budget N, packed into one
+// ancestor-masked pass) and Section 4.2 (keep the N prefixes of highest
+// plug-in score).
+//
+// Layout of the work (grid = L rows x C chunks of 8192 logits, 256 threads):
+//  1. every CTA streams its chunk into registers (vectorised, coalesced),
+//     computes the chunk max and sum of exp, and selects the chunk's K best
+//     tokens by a radix select on unique 64-bit keys
+//     (order-preserving logit bits << 32 | ~token id), so that equal logits
+//     rank by ascending id without any extra pass;
+//  2. the last CTA of each row (atomic ticket, no spinning) merges the row's
+//     chunk candidates with a second radix select, sorts the K winners and
+//     writes (token, log q) using the row's log-sum-exp (accumulated in fp64);
+//  3. the last row-merger overall runs the best-first search in one warp
+//     (frontier in registers, 8 slots per lane, warp max-reduction per pop)
+//     and the whole CTA packs the N popped nodes into canonical order.
+#include "glance_internal.cuh"
+
+GLANCE_DEFINE_STATUS_WORD(status_build_tree)
+
+using namespace glance_dev;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPerThread = 32;
+constexpr int kChunk = kThreads * kPerThread;  // logits per CTA
+constexpr int kMaxL = 16;
+constexpr int kMaxN = 255;
+constexpr int kSlotsPerLane = 8;  // frontier capacity 256 >= N + 1
+
+struct BuildParams {
+  const void* logits;
+  int is_bf16;
+  int L, V, N, K, C;
+  const int32_t* root_token;
+  const int32_t* t_len;
+  glance_tree tree;
+  uint32_t* tickets;            // [kMaxL] row tickets, [kMaxL] global ticket
+  double* chunk_m;              // [L][C] chunk max
+  double* chunk_s;              // [L][C] chunk sum exp(x - m)
+  unsigned long long* cand;     // [L][C][K]
+  int32_t* top_tok;             // [L][K]
+  float* top_logq;              // [L][K]
+};
+
+struct SelectSmem {
+  uint32_t hist[256];
+  uint32_t warp_tot[kThreads / 32];
+  uint32_t digit, above, cnt;
+};
+
+__device__ __forceinline__ float inv_ord_key(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Inclusive block scan (sum) of one value per thread; 256 threads.
+__device__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  uint32_t add = 0;
+  for (int w = 0; w < warp; ++w) add += warp_tot[w];
+  __syncthreads();
+  return v + add;
+}
+
+// Threshold (prefix, mask) such that exactly `want` of the nonzero keys
+// satisfy (key & mask) >= prefix. Keys are unique.
+template <int E>
+__device__ void radix_select(const unsigned long long (&keys)[E], uint32_t want,
+                             unsigned long long& prefix_out, unsigned long long& mask_out,
+                             SelectSmem& sm) {
+  unsigned long long prefix = 0, mask = 0;
+  uint32_t krem = want;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    sm.hist[threadIdx.x] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const unsigned long long k = keys[e];
+      if (k != 0ull && (k & mask) == prefix)
+        atomicAdd(&sm.hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    // thread t holds bin b = 255 - t; the scan gives S[b] = sum_{d >= b} hist[d]
+    const uint32_t b = 255u - threadIdx.x;
+    const uint32_t v = sm.hist[b];
+    const uint32_t incl = block_incl_scan(v, sm.warp_tot);
+    const uint32_t excl = incl - v;
+    if (excl < krem && incl >= krem) {
+      sm.digit = b;
+      sm.above = excl;
+      sm.cnt = v;
+    }
+    __syncthreads();
+    prefix |= static_cast<unsigned long long>(sm.digit) << shift;
+    mask |= 0xFFull << shift;
+    krem -= sm.above;
+    const bool done = (sm.cnt == krem);
+    __syncthreads();
+    if (done) break;
+  }
+  prefix_out = prefix;
+  mask_out = mask;
+}
+
+// Writes the selected keys (any order) to out[0..want). Returns nothing; the
+// caller knows the count.
+template <int E>
+__device__ void compact_selected(const unsigned long long (&keys)[E], unsigned long long prefix,
+                                 unsigned long long mask, unsigned long long* out,
+                                 SelectSmem& sm) {
+  uint32_t c = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) c += (keys[e] != 0ull && (keys[e] & mask) >= prefix);
+  uint32_t pos = block_incl_scan(c, sm.warp_tot) - c;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (keys[e] != 0ull && (keys[e] & mask) >= prefix) out[pos++] = keys[e];
+}
+
+__device__ __forceinline__ unsigned long long make_key(float x, uint32_t id) {
+  return (static_cast<unsigned long long>(ord_key(x)) << 32) | (0xFFFFFFFFu - id);
+}
+
+// -------------------------------------------------------------- tree search
+
+struct NodeKey {
+  uint32_t ord;  // ord_key(score); 0 = empty
+  uint32_t dep;
+  unsigned long long hi, lo;  // rank bytes, offset 1 in the top byte of hi
+};
+
+__device__ __forceinline__ bool better(const NodeKey& a, const NodeKey& b) {
+  if (a.ord != b.ord) return a.ord > b.ord;
+  if (a.dep != b.dep) return a.dep < b.dep;
+  if (a.hi != b.hi) return a.hi < b.hi;
+  return a.lo < b.lo;
+}
+
+__device__ __forceinline__ void set_rank(unsigned long long& hi, unsigned long long& lo, int j,
+                                         uint32_t r) {
+  if (j < 8) {
+    const int sh = (7 - j) * 8;
+    hi = (hi & ~(0xFFull << sh)) | (static_cast<unsigned long long>(r) << sh);
+  } else {
+    const int sh = (15 - j) * 8;
+    lo = (lo & ~(0xFFull << sh)) | (static_cast<unsigned long long>(r) << sh);
+  }
+}
+__device__ __forceinline__ uint32_t get_rank(unsigned long long hi, unsigned long long lo, int j) {
+  return j < 8 ? static_cast<uint32_t>(hi >> ((7 - j) * 8)) & 0xFFu
+               : static_cast<uint32_t>(lo >> ((15 - j) * 8)) & 0xFFu;
+}
+
+struct TreeSmem {
+  float p_score[kMaxN];
+  unsigned long long p_hi[kMaxN], p_lo[kMaxN];
+  int16_t p_parent[kMaxN];
+  int16_t p_pos[kMaxN];
+  uint8_t p_dep[kMaxN];
+};
+
+__device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
+  // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
+  float* s_logq = reinterpret_cast<float*>(dyn);
+  int* s_tok = reinterpret_cast<int*>(dyn + sizeof(float) * p.L * p.K);
+  TreeSmem& ts = *reinterpret_cast<TreeSmem*>(dyn + 8 * ((sizeof(float) * 2 * p.L * p.K + 7) / 8));
+  const int LK = p.L * p.K;
+  for (int i = threadIdx.x; i < LK; i += kThreads) {
+    s_logq[i] = __ldcg(p.top_logq + i);
+    s_tok[i] = __ldcg(p.top_tok + i);
+  }
+  __syncthreads();
+  const int N = p.N, L = p.L, K = p.K;
+
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // frontier slots owned by this lane: slot s = lane + 32 * i
+    NodeKey sk[kSlotsPerLane];
+    int spar[kSlotsPerLane];
+    float spscore[kSlotsPerLane];
+#pragma unroll
+    for (int i = 0; i < kSlotsPerLane; ++i) {
+      sk[i].ord = 0;
+      sk[i].dep = 0;
+      sk[i].hi = sk[i].lo = 0;
+      spar[i] = -1;
+      spscore[i] = 0.f;
+    }
+    if (lane == 0) {  // first frontier entry: rank 0 at offset 1
+      sk[0].ord = ord_key(s_logq[0]);
+      sk[0].dep = 1;
+    }
+    int cnt = 1;
+    for (int k = 0; k < N; ++k) {
+      // local best of this lane
+      int bi = -1;
+      NodeKey bk;
+      bk.ord = 0;
+      bk.dep = 0;
+      bk.hi = bk.lo = 0;
+#pragma unroll
+      for (int i = 0; i < kSlotsPerLane; ++i)
+        if (sk[i].ord != 0 && (bi < 0 || better(sk[i], bk))) {
+          bk = sk[i];
+          bi = i;
+        }
+      const uint32_t m = __reduce_max_sync(0xffffffffu, bk.ord);
+      const unsigned tied = __ballot_sync(0xffffffffu, bi >= 0 && bk.ord == m);
+      if (tied == 0) {  // frontier exhausted: the host checks make this unreachable
+        if (lane == 0) report(GLANCE_DEV_BAD_TREE);
+        break;
+      }
+      int win = __ffs(tied) - 1;
+      if (__popc(tied) > 1) {  // exact score tie: depth, then rank vector
+        unsigned rest = tied & (tied - 1);
+        NodeKey wk;
+        wk.ord = m;
+        wk.dep = __shfl_sync(0xffffffffu, bk.dep, win);
+        wk.hi = __shfl_sync(0xffffffffu, bk.hi, win);
+        wk.lo = __shfl_sync(0xffffffffu, bk.lo, win);
+        while (rest) {
+          const int c = __ffs(rest) - 1;
+          rest &= rest - 1;
+          NodeKey ck;
+          ck.ord = m;
+          ck.dep = __shfl_sync(0xffffffffu, bk.dep, c);
+          ck.hi = __shfl_sync(0xffffffffu, bk.hi, c);
+          ck.lo = __shfl_sync(0xffffffffu, bk.lo, c);
+          if (better(ck, wk)) {
+            wk = ck;
+            win = c;
+          }
+        }
+      }
+      const int wslot_i = __shfl_sync(0xffffffffu, bi, win);
+      // winner's node data
+      float wpscore = 0.f;
+      int wpar = -1;
+#pragma unroll
+      for (int i = 0; i < kSlotsPerLane; ++i)
+        if (i == bi) {
+          wpscore = spscore[i];
+          wpar = spar[i];
+        }
+      const uint32_t d = __shfl_sync(0xffffffffu, bk.dep, win);
+      const unsigned long long hi = __shfl_sync(0xffffffffu, bk.hi, win);
+      const unsigned long long lo = __shfl_sync(0xffffffffu, bk.lo, win);
+      const float score = inv_ord_key(m);
+      wpscore = __shfl_sync(0xffffffffu, wpscore, win);
+      wpar = __shfl_sync(0xffffffffu, wpar, win);
+      const uint32_t r = get_rank(hi, lo, d - 1);
+      if (lane == 0) {
+        ts.p_score[k] = score;
+        ts.p_hi[k] = hi;
+        ts.p_lo[k] = lo;
+        ts.p_parent[k] = static_cast<int16_t>(wpar);
+        ts.p_dep[k] = static_cast<uint8_t>(d);
+      }
+      // successors: first child (rank 0 at offset d+1), next sibling (rank r+1)
+      const bool has_child = static_cast<int>(d) < L;
+      const bool has_sib = static_cast<int>(r) + 1 < K;
+      NodeKey ck, sbk;
+      float c_score = 0.f, s_score = 0.f;
+      if (has_child) {
+        c_score = score + s_logq[d * K + 0];
+        ck.ord = ord_key(c_score);
+        ck.dep = d + 1;
+        ck.hi = hi;
+        ck.lo = lo;
+        set_rank(ck.hi, ck.lo, d, 0);
+      }
+      if (has_sib) {
+        s_score = wpscore + s_logq[(d - 1) * K + r + 1];
+        sbk.ord = ord_key(s_score);
+        sbk.dep = d;
+        sbk.hi = hi;
+        sbk.lo = lo;
+        set_rank(sbk.hi, sbk.lo, d - 1, r + 1);
+      }
+      // slot of the popped node takes the child (else the sibling); a new
+      // slot takes the sibling when both exist
+      if (lane == win) {
+#pragma unroll
+        for (int i = 0; i < kSlotsPerLane; ++i)
+          if (i == wslot_i) {
+            if (has_child) {
+              sk[i] = ck;
+              spar[i] = k;
+              spscore[i] = score;
+            } else if (has_sib) {
+              sk[i] = sbk;
+              spar[i] = wpar;
+              spscore[i] = wpscore;
+            } else {
+              sk[i].ord = 0;
+            }
+          }
+      }
+      if (has_child && has_sib) {
+        const int ns = cnt++;
+        if (lane == (ns & 31)) {
+          const int ni = ns >> 5;
+#pragma unroll
+          for (int i = 0; i < kSlotsPerLane; ++i)
+            if (i == ni) {
+              sk[i] = sbk;
+              spar[i] = wpar;
+              spscore[i] = wpscore;
+            }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // canonical position: 1 + number of nodes before it in (depth, rank vector)
+  const int T = *p.t_len;
+  const int W = p.tree.mask_words;
+  for (int kk = threadIdx.x; kk < N; kk += kThreads) {
+    const uint32_t dk = ts.p_dep[kk];
+    const unsigned long long hk = ts.p_hi[kk], lk = ts.p_lo[kk];
+    int pos = 1;
+    for (int j = 0; j < N; ++j) {
+      const uint32_t dj = ts.p_dep[j];
+      const unsigned long long hj = ts.p_hi[j], lj = ts.p_lo[j];
+      pos += (dj < dk) || (dj == dk && (hj < hk || (hj == hk && lj < lk)));
+    }
+    ts.p_pos[kk] = static_cast<int16_t>(pos);
+  }
+  __syncthreads();
+  for (int kk = threadIdx.x; kk <= N; kk += kThreads) {
+    if (kk == N) {  // root row
+      p.tree.token[0] = *p.root_token;
+      p.tree.parent[0] = -1;
+      p.tree.depth[0] = 0;
+      p.tree.pos_id[0] = T;
+      p.tree.score[0] = 0.f;
+      for (int w = 0; w < W; ++w) p.tree.anc[w] = (w == 0) ? 1ull : 0ull;
+      continue;
+    }
+    const int row = ts.p_pos[kk];
+    const int d = ts.p_dep[kk];
+    const uint32_t r = get_rank(ts.p_hi[kk], ts.p_lo[kk], d - 1);
+    const int par = ts.p_parent[kk];
+    p.tree.token[row] = s_tok[(d - 1) * K + r];
+    p.tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
+    p.tree.depth[row] = d;
+    p.tree.pos_id[row] = T + d;
+    p.tree.score[row] = ts.p_score[kk];
+    unsigned long long words[4] = {1ull, 0ull, 0ull, 0ull};
+    words[row >> 6] |= 1ull << (row & 63);
+    for (int u = par; u >= 0; u = ts.p_parent[u]) {
+      const int pr = ts.p_pos[u];
+      words[pr >> 6] |= 1ull << (pr & 63);
+    }
+    for (int w = 0; w < W; ++w) p.tree.anc[row * W + w] = words[w];
+  }
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <bool kBF16, bool kVec>
+__global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams p) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ SelectSmem sm;
+  __shared__ double red_d[kThreads / 32];
+  __shared__ float red_f[kThreads / 32];
+  __shared__ uint32_t s_ticket;
+  __shared__ unsigned long long sel[256];
+
+  const int row = blockIdx.x / p.C;
+  const int chunk = blockIdx.x % p.C;
+  const int base = chunk * kChunk;
+  const int n_valid = min(kChunk, p.V - base);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // ---- 1. load the chunk: element e of thread t is id base + kVec ? ... :
+  float x[kPerThread];
+  if (kVec) {
+    // 4 consecutive ids per vector: vector v = t + 256 * q holds ids base + 4v .. 4v+3
+#pragma unroll
+    for (int q = 0; q < kPerThread / 4; ++q) {
+      const int v = threadIdx.x + kThreads * q;
+      const int id0 = base + 4 * v;
+      if (4 * v < n_valid) {  // n_valid % 4 == 0 when vectorised
+        if (kBF16) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(
+              static_cast<const uint16_t*>(p.logits) + static_cast<size_t>(row) * p.V + id0);
+          x[4 * q + 0] = bf16_to_f32(raw.x & 0xFFFFu);
+          x[4 * q + 1] = bf16_to_f32(raw.x >> 16);
+          x[4 * q + 2] = bf16_to_f32(raw.y & 0xFFFFu);
+          x[4 * q + 3] = bf16_to_f32(raw.y >> 16);
+        } else {
+          const float4 f = *reinterpret_cast<const float4*>(
+              static_cast<const float*>(p.logits) + static_cast<size_t>(row) * p.V + id0);
+          x[4 * q + 0] = f.x;
+          x[4 * q + 1] = f.y;
+          x[4 * q + 2] = f.z;
+          x[4 * q + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[4 * q + c] = -INFINITY;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      const int local = threadIdx.x + kThreads * e;
+      if (local < n_valid) {
+        const size_t gi = static_cast<size_t>(row) * p.V + base + local;
+        x[e] = kBF16 ? bf16_to_f32(static_cast<const uint16_t*>(p.logits)[gi])
+                     : static_cast<const float*>(p.logits)[gi];
+      } else {
+        x[e] = -INFINITY;
+      }
+    }
+  }
+  auto id_of = [&](int e) -> int {
+    if (kVec) return base + 4 * (threadIdx.x + kThreads * (e / 4)) + (e % 4);
+    return base + threadIdx.x + kThreads * e;
+  };
+  auto valid_of = [&](int e) -> bool { return id_of(e) - base < n_valid; };
+
+  // ---- chunk max and sum of exp
+  float m = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    if (valid_of(e)) {
+      bad |= !isfinite(x[e]);
+      m = fmaxf(m, x[e]);
+    }
+  }
+  if (bad) report(GLANCE_DEV_NONFINITE_LOGITS);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red_f[warp] = m;
+  __syncthreads();
+  m = red_f[0];
+  for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red_f[w]);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e)
+    if (valid_of(e)) s += expf(x[e] - m);
+  double sd = s;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+  if (lane == 0) red_d[warp] = sd;
+
+  // ---- chunk top-K
+  unsigned long long keys[kPerThread];
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e)
+    keys[e] = valid_of(e) ? make_key(x[e], static_cast<uint32_t>(id_of(e))) : 0ull;
+  const int kc = min(p.K, n_valid);
+  unsigned long long prefix, mask;
+  radix_select(keys, kc, prefix, mask, sm);  // contains __syncthreads
+  unsigned long long* my_cand =
+      p.cand + (static_cast<size_t>(row) * p.C + chunk) * p.K;
+  compact_selected(keys, prefix, mask, my_cand, sm);
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) tot += red_d[w];
+    p.chunk_m[row * p.C + chunk] = m;
+    p.chunk_s[row * p.C + chunk] = tot;
+  }
+
+  // ---- 2. last CTA of this row merges
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&p.tickets[row], 1u);
+  __syncthreads();
+  if (s_ticket != static_cast<uint32_t>(p.C - 1)) return;
+  __threadfence();
+  if (threadIdx.x == 0) p.tickets[row] = 0;  // ready for the next call
+
+  // candidates: flat index f = c * K + i, valid when i < min(K, chunk size)
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int f = threadIdx.x + kThreads * e;
+    const int c = f / p.K, i = f - c * p.K;
+    keys[e] = 0ull;
+    if (c < p.C) {
+      const int kc_c = min(p.K, min(kChunk, p.V - c * kChunk));
+      if (i < kc_c) keys[e] = __ldcg(p.cand + (static_cast<size_t>(row) * p.C + c) * p.K + i);
+    }
+  }
+  radix_select(keys, p.K, prefix, mask, sm);
+  sel[threadIdx.x] = 0ull;
+  __syncthreads();
+  compact_selected(keys, prefix, mask, sel, sm);
+  __syncthreads();
+  // bitonic sort of sel[0..256), descending
+  for (int size = 2; size <= 256; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int t = threadIdx.x;
+      const int partner = t ^ stride;
+      if (partner > t) {
+        const bool desc = (t & size) == 0;
+        const unsigned long long a = sel[t], b = sel[partner];
+        if ((a < b) == desc) {
+          sel[t] = b;
+          sel[partner] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // row log-sum-exp from chunk (max, sum) pairs, in fp64
+  __shared__ double s_lse;
+  if (warp == 0) {
+    double M = -INFINITY;
+    for (int c = lane; c < p.C; c += 32) M = fmax(M, __ldcg(p.chunk_m + row * p.C + c));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmax(M, __shfl_xor_sync(0xffffffffu, M, o));
+    double S = 0.0;
+    for (int c = lane; c < p.C; c += 32)
+      S += __ldcg(p.chunk_s + row * p.C + c) * exp(__ldcg(p.chunk_m + row * p.C + c) - M);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    if (lane == 0) s_lse = M + log(S);
+  }
+  __syncthreads();
+  if (threadIdx.x < p.K) {
+    const unsigned long long k = sel[threadIdx.x];
+    const float xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
+    const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
+    p.top_tok[row * p.K + threadIdx.x] = static_cast<int32_t>(id);
+    p.top_logq[row * p.K + threadIdx.x] = static_cast<float>(static_cast<double>(xv) - s_lse);
+  }
+
+  // ---- 3. last row-merger builds the tree
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&p.tickets[kMaxL], 1u);
+  __syncthreads();
+  if (s_ticket != static_cast<uint32_t>(p.L - 1)) return;
+  __threadfence();
+  if (threadIdx.x == 0) p.tickets[kMaxL] = 0;
+  tree_phase(p, dyn);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t tickets, chunk_m, chunk_s, cand, top_tok, top_logq, total;
+};
+
+WsLayout ws_layout(int L, int V, int N) {
+  const int K = N < V ? N : V;
+  const int C = (V + kChunk - 1) / kChunk;
+  WsLayout w;
+  size_t o = 0;
+  w.tickets = o;
+  o = align_up(o + sizeof(uint32_t) * (2 * kMaxL), 256);
+  w.chunk_m = o;
+  o = align_up(o + sizeof(double) * L * C, 256);
+  w.chunk_s = o;
+  o = align_up(o + sizeof(double) * L * C, 256);
+  w.cand = o;
+  o = align_up(o + sizeof(unsigned long long) * static_cast<size_t>(L) * C * K, 256);
+  w.top_tok = o;
+  o = align_up(o + sizeof(int32_t) * L * K, 256);
+  w.top_logq = o;
+  o = align_up(o + sizeof(float) * L * K, 256);
+  w.total = o;
+  return w;
+}
+
+bool sizes_ok(int L, int V, int N) {
+  if (L < 1 || L > kMaxL || V < 2 || N < 1 || N > kMaxN) return false;
+  if (V > (1 << 18)) return false;
+  const int K = N < V ? N : V;
+  const int C = (V + kChunk - 1) / kChunk;
+  if (static_cast<long long>(C) * K > kChunk) return false;
+  // N must not exceed the number of strings of length <= L over V tokens
+  long long total = 0, pw = 1;
+  for (int d = 1; d <= L && total < N; ++d) {
+    pw *= V;
+    total += pw;
+    if (pw > (1ll << 40)) total = 1ll << 40;
+  }
+  return total >= N;
+}
+
+}  // namespace
+
+extern "C" size_t glance_build_tree_workspace_bytes(int L, int V, int N) {
+  if (!sizes_ok(L, V, N)) return 0;
+  return ws_layout(L, V, N).total;
+}
+
+extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtype dtype, int L,
+                                           int V, int N, const int32_t* root_token,
+                                           const int32_t* t_len, const glance_tree* tree,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  using glance::fail;
+  if (!draft_logits || !root_token || !t_len || !tree || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: null pointer argument");
+  if (dtype != GLANCE_F32 && dtype != GLANCE_BF16)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: dtype must be F32 or BF16");
+  if (!sizes_ok(L, V, N))
+    return fail(GLANCE_ERR_INVALID_ARG,
+                "glance_build_tree: need 1<=L<=16, 2<=V<=262144, 1<=N<=255, N <= #strings, "
+                "ceil(V/8192)*min(N,V) <= 8192 (got L=%d V=%d N=%d)",
+                L, V, N);
+  if (tree->n != N || tree->L != L || tree->mask_words != (N + 1 + 63) / 64)
+    return fail(GLANCE_ERR_INVALID_ARG,
+                "glance_build_tree: tree struct sized for n=%d L=%d mask_words=%d, call has "
+                "N=%d L=%d (mask_words must be %d)",
+                tree->n, tree->L, tree->mask_words, N, L, (N + 64) / 64);
+  if (!tree->token || !tree->parent || !tree->depth || !tree->pos_id || !tree->score ||
+      !tree->anc)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: null tree array");
+  const WsLayout w = ws_layout(L, V, N);
+  if (workspace_bytes < w.total)
+    return fail(GLANCE_ERR_CAPACITY, "glance_build_tree: workspace %zu bytes < %zu needed",
+                workspace_bytes, w.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: workspace must be 256-byte aligned");
+
+  BuildParams p;
+  p.logits = draft_logits;
+  p.is_bf16 = dtype == GLANCE_BF16;
+  p.L = L;
+  p.V = V;
+  p.N = N;
+  p.K = N < V ? N : V;
+  p.C = (V + kChunk - 1) / kChunk;
+  p.root_token = root_token;
+  p.t_len = t_len;
+  p.tree = *tree;
+  char* ws = static_cast<char*>(workspace);
+  p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets);
+  p.chunk_m = reinterpret_cast<double*>(ws + w.chunk_m);
+  p.chunk_s = reinterpret_cast<double*>(ws + w.chunk_s);
+  p.cand = reinterpret_cast<unsigned long long*>(ws + w.cand);
+  p.top_tok = reinterpret_cast<int32_t*>(ws + w.top_tok);
+  p.top_logq = reinterpret_cast<float*>(ws + w.top_logq);
+
+  const size_t dyn = 8 * ((sizeof(float) * 2 * L * p.K + 7) / 8) + sizeof(TreeSmem);
+  const bool vec = p.is_bf16 ? (V % 4 == 0 && glance::aligned16(draft_logits))
+                             : (V % 4 == 0 && glance::aligned16(draft_logits));
+  void (*kern)(const BuildParams);
+  if (p.is_bf16)
+    kern = vec ? build_tree_kernel<true, true> : build_tree_kernel<true, false>;
+  else
+    kern = vec ? build_tree_kernel<false, true> : build_tree_kernel<false, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(dyn));
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_build_tree: smem attribute");
+  kern<<<L * p.C, kThreads, dyn, static_cast<cudaStream_t>(stream)>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_build_tree: launch");
+  return GLANCE_OK;
+}

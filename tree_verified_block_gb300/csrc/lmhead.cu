@@ -1,0 +1,452 @@
+// LM head with fused greedy argmax and top-2 gap.
+//
+// Paper: "Vision Is Not Overhead ..." (arXiv 2609.00355), Section 3.1
+// (greedy decoding emits argmax_w p(w | prefix)) and Theorem 1's full
+// statement in Appendix B.1 (top logit gap gamma = l_(1) - l_(2), the margin
+// the tie-aware gate of Section 4.2 reads).
+//
+// logits[i][v] = sum_k h[i][k] W[k][v]; per row: argmax (lowest id among
+// equal maxima), gap = max - (largest logit of any other id), max. The logits
+// never leave the chip.
+//
+// bf16 path (tcgen05): persistent CTAs, one per SM, each walking vocabulary
+// tiles of 256 columns. Warp 0 streams h (K-major, 128-byte swizzle) and W
+// ([d][V] row-major, so V is the MN-major side of the B operand) through a
+// 4-stage TMA ring; warp 1 issues M=128 x N=256 x K=16 MMAs into one of two
+// tensor-memory accumulators; warps 4..7 each own one row (one TMEM lane),
+// read the tile's 256 fp32 logits and fold them into a running
+// (max, argmax, second max) held in registers across tiles, while the MMA
+// warp fills the other accumulator. CTAs write per-row partials; the last CTA
+// (atomic ticket) merges them, one warp per row.
+// fp32 path: CUDA cores, 128 vocabulary columns x 8 rows per CTA.
+#include "glance_internal.cuh"
+
+GLANCE_DEFINE_STATUS_WORD(status_lmhead)
+
+using namespace glance_dev;
+
+namespace {
+
+struct Partial {
+  float m1;
+  int i1;
+  float m2;
+};
+
+__device__ __forceinline__ void fold(float x, int col, float& m1, int& i1, float& m2) {
+  // columns arrive in increasing order: a later equal maximum keeps the lower id
+  if (x > m1) {
+    m2 = m1;
+    m1 = x;
+    i1 = col;
+  } else if (x > m2) {
+    m2 = x;
+  }
+}
+
+__device__ __forceinline__ void merge(Partial& a, const Partial& b) {
+  if (b.m1 > a.m1 || (b.m1 == a.m1 && b.i1 < a.i1)) {
+    a.m2 = fmaxf(b.m2, a.m1);
+    a.m1 = b.m1;
+    a.i1 = b.i1;
+  } else {
+    a.m2 = fmaxf(a.m2, b.m1);
+  }
+}
+
+// Last CTA: one warp per row merges every CTA's partial for that row.
+__device__ void merge_partials(const Partial* part, int n_parts, int part_stride, int M,
+                               int32_t* argmax, float* gap, float* maxlogit) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int r = warp; r < M; r += nwarps) {
+    Partial a{-INFINITY, 0x7FFFFFFF, -INFINITY};
+    for (int c = lane; c < n_parts; c += 32) {
+      const Partial* q = part + static_cast<size_t>(c) * part_stride + r;
+      Partial b{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2)};
+      merge(a, b);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      Partial b{__shfl_xor_sync(0xffffffffu, a.m1, o), __shfl_xor_sync(0xffffffffu, a.i1, o),
+                __shfl_xor_sync(0xffffffffu, a.m2, o)};
+      merge(a, b);
+    }
+    if (lane == 0) {
+      argmax[r] = a.i1;
+      gap[r] = a.m1 - a.m2;
+      if (maxlogit) maxlogit[r] = a.m1;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ fp32 path
+
+constexpr int kF32Cols = 128;
+constexpr int kF32Rows = 8;
+constexpr int kF32KChunk = 256;
+
+struct F32Params {
+  const float* h;
+  const float* W;
+  int M, d, V;
+  int32_t* argmax;
+  float* gap;
+  float* maxlogit;
+  Partial* part;  // [n_colblk][M]
+  uint32_t* ticket;
+};
+
+__global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p) {
+  __shared__ float s_h[kF32Rows][kF32KChunk];
+  __shared__ Partial s_red[kF32Cols / 32][kF32Rows];
+  __shared__ uint32_t s_ticket;
+  const int colblk = blockIdx.x, rowgrp = blockIdx.y;
+  const int v = colblk * kF32Cols + threadIdx.x;
+  const int r0 = rowgrp * kF32Rows;
+  float acc[kF32Rows];
+#pragma unroll
+  for (int r = 0; r < kF32Rows; ++r) acc[r] = 0.f;
+  for (int k0 = 0; k0 < p.d; k0 += kF32KChunk) {
+    const int kn = min(kF32KChunk, p.d - k0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kF32Rows * kF32KChunk; i += kF32Cols) {
+      const int r = i / kF32KChunk, k = i % kF32KChunk;
+      s_h[r][k] = (r0 + r < p.M && k < kn) ? p.h[static_cast<size_t>(r0 + r) * p.d + k0 + k] : 0.f;
+    }
+    __syncthreads();
+    if (v < p.V) {
+      for (int k = 0; k < kn; ++k) {
+        const float w = p.W[static_cast<size_t>(k0 + k) * p.V + v];
+#pragma unroll
+        for (int r = 0; r < kF32Rows; ++r) acc[r] = fmaf(s_h[r][k], w, acc[r]);
+      }
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < kF32Rows; ++r) {
+    Partial a{v < p.V ? acc[r] : -INFINITY, v < p.V ? v : 0x7FFFFFFF, -INFINITY};
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      Partial b{__shfl_xor_sync(0xffffffffu, a.m1, o), __shfl_xor_sync(0xffffffffu, a.i1, o),
+                __shfl_xor_sync(0xffffffffu, a.m2, o)};
+      merge(a, b);
+    }
+    if (lane == 0) s_red[warp][r] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x < kF32Rows && r0 + threadIdx.x < p.M) {
+    Partial a = s_red[0][threadIdx.x];
+    for (int w = 1; w < kF32Cols / 32; ++w) merge(a, s_red[w][threadIdx.x]);
+    p.part[static_cast<size_t>(colblk) * p.M + r0 + threadIdx.x] = a;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(p.ticket, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x * gridDim.y - 1) return;
+  __threadfence();
+  if (threadIdx.x == 0) *p.ticket = 0;
+  merge_partials(p.part, gridDim.x, p.M, p.M, p.argmax, p.gap, p.maxlogit);
+}
+
+// ------------------------------------------------------------------ bf16 path
+
+constexpr int kBM = 128;   // rows per MMA (M), padded with zero rows
+constexpr int kBN = 256;   // vocabulary columns per tile (N)
+constexpr int kBK = 64;    // one 128-byte swizzle atom of K
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBBytes = kBK * kBN * 2;  // 32 KB
+constexpr uint32_t kWBoxBytes = kBK * 64 * 2;  // one 64 x 64 box of W: 8 KB
+constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256;
+
+struct Bf16Params {
+  int M, d, V, n_tiles, a_rows;
+  int32_t* argmax;
+  float* gap;
+  float* maxlogit;
+  Partial* part;  // [grid][kBM]
+  uint32_t* ticket;
+};
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fail_pipeline(Bars* bars) {
+  report(GLANCE_DEV_PIPELINE_TIMEOUT);
+  atomicExch(&bars->abort_flag, 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_bf16_kernel(const __grid_constant__ CUtensorMap map_h,
+                       const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kStages * kABytes;
+  Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kBBytes);
+  __shared__ uint32_t s_ticket;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_kb = p.d / kBK;
+  const int my_tiles = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 128);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  // rows a_rows..127 of every A stage stay zero (TMA only writes a_rows rows)
+  if (p.a_rows < kBM) {
+    for (int s = 0; s < kStages; ++s) {
+      uint4* dst = reinterpret_cast<uint4*>(sA + s * kABytes + p.a_rows * 128);
+      for (int i = threadIdx.x; i < (kBM - p.a_rows) * 8; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&map_h);
+      tma_prefetch_desc(&map_w);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBK * 2;
+      int it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int v0 = (blockIdx.x + i * gridDim.x) * kBN;
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % kStages;
+          if (it >= kStages && !wait_or_abort(&bars->empty[st], ((it / kStages) - 1) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[st], a_bytes + kBBytes);
+          tma_load_2d(sA + st * kABytes, &map_h, &bars->full[st], kb * kBK, 0, pol_h);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d(sB + st * kBBytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
+                        kb * kBK, pol_w);
+        }
+      }
+      if (!ok) {
+        fail_pipeline(bars);
+        for (int j = it > kStages ? it - kStages : 0; j < it; ++j)
+          (void)mbar_wait(&bars->full[j % kStages], (j / kStages) & 1, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, true);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      int it = 0;
+      bool ok = true;
+      const int total_it = my_tiles * n_kb;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !wait_or_abort(&bars->acc_empty[buf], ((i >> 1) - 1) & 1, bars)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * kBN;
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % kStages;
+          if (!wait_or_abort(&bars->full[st], (it / kStages) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = a0 + st * kABytes, b_addr = b0 + st * kBBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                        sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+          // only stages the producer will refill need a release
+          if (it + kStages < total_it) mma_commit(&bars->empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full[buf]);
+      }
+      if (!ok) fail_pipeline(bars);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m1 = -INFINITY, m2 = -INFINITY;
+    int i1 = 0x7FFFFFFF;
+    bool ok = true;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int buf = i & 1;
+      if (!wait_or_abort(&bars->acc_full[buf], (i >> 1) & 1, bars)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int v0 = (blockIdx.x + i * gridDim.x) * kBN;
+      const uint32_t t_acc = tmem + buf * kBN + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(t_acc + c * 32, r);
+        tmem_ld_wait();
+        const int col0 = v0 + c * 32;
+        if (col0 + 32 <= p.V) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1, i1, m2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1, i1, m2);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[buf]);
+    }
+    if (!ok) fail_pipeline(bars);
+    if (row < p.M) p.part[static_cast<size_t>(blockIdx.x) * kBM + row] = Partial{m1, i1, m2};
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(p.ticket, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
+  __threadfence();
+  if (threadIdx.x == 0) *p.ticket = 0;
+  merge_partials(p.part, gridDim.x, kBM, p.M, p.argmax, p.gap, p.maxlogit);
+}
+
+size_t ws_bytes_bf16(int M) {
+  (void)M;
+  const int grid = glance::num_sms();
+  return 256 + (static_cast<size_t>(grid) * kBM * sizeof(Partial) + 255) / 256 * 256;
+}
+
+size_t ws_bytes_f32(int M, int V) {
+  const int colblks = (V + kF32Cols - 1) / kF32Cols;
+  return 256 + (static_cast<size_t>(colblks) * M * sizeof(Partial) + 255) / 256 * 256;
+}
+
+}  // namespace
+
+extern "C" size_t glance_lmhead_argmax_workspace_bytes(int M, int d, int V, glance_dtype dtype) {
+  if (M < 1 || M > 512 || d < 1 || V < 1) return 0;
+  return dtype == GLANCE_BF16 ? ws_bytes_bf16(M) : ws_bytes_f32(M, V);
+}
+
+extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glance_dtype dtype,
+                                              int M, int d, int V, int32_t* argmax, float* gap,
+                                              float* maxlogit, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
+  using glance::fail;
+  if (!h || !W || !argmax || !gap || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: null pointer argument");
+  if (M < 1 || M > 512 || d < 1 || V < 1)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: need 1 <= M <= 512, d >= 1, V >= 1");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: workspace must be 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* ticket = static_cast<uint32_t*>(workspace);
+  Partial* part = reinterpret_cast<Partial*>(static_cast<char*>(workspace) + 256);
+  if (dtype == GLANCE_F32) {
+    if (workspace_bytes < ws_bytes_f32(M, V))
+      return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace too small");
+    F32Params p{static_cast<const float*>(h), static_cast<const float*>(W), M, d, V, argmax, gap,
+                maxlogit, part, ticket};
+    dim3 grid((V + kF32Cols - 1) / kF32Cols, (M + kF32Rows - 1) / kF32Rows);
+    lmhead_f32_kernel<<<grid, kF32Cols, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: launch");
+    return GLANCE_OK;
+  }
+  if (dtype != GLANCE_BF16)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: dtype must be F32 or BF16");
+  if (d % kBK != 0 || V % 8 != 0)
+    return fail(GLANCE_ERR_UNSUPPORTED, "glance_lmhead_argmax: bf16 needs d %% 64 == 0 and V %% 8 == 0");
+  if (!glance::aligned16(h) || !glance::aligned16(W))
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: h and W must be 16-byte aligned");
+  if (workspace_bytes < ws_bytes_bf16(M))
+    return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace %zu bytes < %zu needed",
+                workspace_bytes, ws_bytes_bf16(M));
+  const int n_tiles = (V + kBN - 1) / kBN;
+  int grid = glance::num_sms();
+  if (grid > n_tiles) grid = n_tiles;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: smem attribute");
+  CUtensorMap mw;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
+    const uint32_t box[2] = {64, kBK};
+    glance_status st = glance::make_map_bf16(&mw, W, 2, dims, strides, box,
+                                             CU_TENSOR_MAP_SWIZZLE_128B, "glance_lmhead_argmax: W map");
+    if (st != GLANCE_OK) return st;
+  }
+  // rows in blocks of 128: each block streams W once
+  for (int r0 = 0; r0 < M; r0 += kBM) {
+    const int mb = M - r0 < kBM ? M - r0 : kBM;
+    const int a_rows = (mb + 7) / 8 * 8;
+    CUtensorMap mh;
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(mb)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
+    glance_status st = glance::make_map_bf16(
+        &mh, static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, 2, dims, strides, box,
+        CU_TENSOR_MAP_SWIZZLE_128B, "glance_lmhead_argmax: h map");
+    if (st != GLANCE_OK) return st;
+    Bf16Params p{mb, d, V, n_tiles, a_rows, argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr,
+                 part, ticket};
+    lmhead_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mh, mw, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: launch");
+  }
+  return GLANCE_OK;
+}
