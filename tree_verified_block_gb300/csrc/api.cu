@@ -33,6 +33,26 @@ int num_sms() {
   return n;
 }
 
+cudaError_t ensure_smem(const void* func, int bytes) {
+  struct Entry {
+    const void* func;
+    int dev;
+    int bytes;
+  };
+  static Entry table[64];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (table[i].func == func && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n < 64) table[n++] = Entry{func, dev, bytes};
+  return e;
+}
+
 EncodeTiledFn encode_tiled() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;

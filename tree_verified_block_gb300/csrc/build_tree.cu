@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams 
   const int n_valid = min(kChunk, p.V - base);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // ---- 1. load the chunk: element e of thread t is id base + kVec ? ... :
+  // ---- 1. load the chunk into registers (ids: see id_of below)
   float x[kPerThread];
   if (kVec) {
     // 4 consecutive ids per vector: vector v = t + 256 * q holds ids base + 4v .. 4v+3
@@ -662,8 +662,7 @@ extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtyp
     kern = vec ? build_tree_kernel<true, true> : build_tree_kernel<true, false>;
   else
     kern = vec ? build_tree_kernel<false, true> : build_tree_kernel<false, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(dyn));
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(kern), static_cast<int>(dyn));
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_build_tree: smem attribute");
   kern<<<L * p.C, kThreads, dyn, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();

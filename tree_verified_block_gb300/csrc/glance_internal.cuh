@@ -21,6 +21,9 @@ namespace glance {
 glance_status fail(glance_status s, const char* fmt, ...);  // sets last error text
 glance_status cuda_fail(cudaError_t e, const char* what);
 int num_sms();  // SM count of the current device (cached per device)
+// Raise a kernel's dynamic shared-memory limit once per device (the call is
+// made outside any later stream capture of the same kernel).
+cudaError_t ensure_smem(const void* func, int bytes);
 
 // cuTensorMapEncodeTiled obtained from the driver through the runtime.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -418,8 +418,7 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
   const int n_tiles = (V + kBN - 1) / kBN;
   int grid = glance::num_sms();
   if (grid > n_tiles) grid = n_tiles;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel), static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: smem attribute");
   CUtensorMap mw;
   {

@@ -701,9 +701,7 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
   p.t_cap = kv->t_cap;
   p.box_rows = gm.box_rows;
   p.scale_log2 = scale * kLog2e;
-  cudaError_t e = cudaFuncSetAttribute(tree_attention_bf16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(tree_attention_bf16_kernel), static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: smem attribute");
   const int grid = kv->n_kv_heads * gm.n_qt * gm.n_split;
   tree_attention_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);

@@ -43,12 +43,19 @@ def bf16_bits_to_f32(b):
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def normal_bf16(g, shape, std=1.0):
-    """bf16 bit patterns of N(0, std^2) draws."""
-    x = g.standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        x *= np.float32(std)
-    return to_bf16_bits(x)
+def normal_bf16(g, shape, std=1.0, chunk=1 << 24):
+    """bf16 bit patterns of N(0, std^2) draws, generated in chunks of `chunk`
+    elements (same values as one draw of the whole array)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for c0 in range(0, n, chunk):
+        c1 = min(n, c0 + chunk)
+        x = g.standard_normal(size=c1 - c0, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        u = x.view(np.uint32)
+        out[c0:c1] = ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+    return out.reshape(shape)
 
 
 # ---------------------------------------------------------------- draft logits
