@@ -216,43 +216,50 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ timing
 
-def time_stage(fn, stream, iters):
+def graph_time_us(fn, reps=20):
+    """Device time of fn's launches, captured in a CUDA graph and replayed
+    `reps` times between two events on the launching stream (no host launch
+    latency in the measurement)."""
     import torch
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    for a, b in ev:
-        a.record(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
         fn()
-        b.record(stream)
+    g.replay()
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) * 1e3 for a, b in ev]  # microseconds
-
-
-def stage_times(wl, iters=5):
-    """Per-stage device times (us) with CUDA events on the launching stream."""
-    import torch
-    g, c = wl.g, wl.cfg
     s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(reps):
+        g.replay()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def stage_times(wl, reps=20):
+    """Per-stage device times (us), each stage graph-captured and replayed."""
+    g, c = wl.g, wl.cfg
     scale = c["D"] ** -0.5
     res = {}
-    wl.t_len.copy_(wl.t0)
-    res["tree"] = time_stage(lambda: g.build_tree(wl.x_dev, c["N"], wl.root, wl.t_len, wl.tree, wl.ws_tree), s, iters)
-    per_layer = []
-    for it in range(iters):
-        per_layer += time_stage(
-            lambda: [g.tree_attention(wl.q[l], wl.layers[l], wl.tree, scale, wl.out[l], wl.ws_attn)
-                     for l in range(c["n_layers"])], s, 1)
-    res["attention_36"] = per_layer
-    one = []
-    for l in range(c["n_layers"]):
-        one += time_stage(lambda: g.tree_attention(wl.q[l], wl.layers[l], wl.tree, scale, wl.out[l], wl.ws_attn), s, 1)
-    res["attention_layer"] = one
-    res["lmhead"] = time_stage(lambda: g.lmhead_argmax(wl.h, wl.W, wl.argmax, wl.gap, wl.maxlogit, wl.ws_lm), s, iters)
+
+    def tree():
+        wl.t_len.copy_(wl.t0)
+        g.build_tree(wl.x_dev, c["N"], wl.root, wl.t_len, wl.tree, wl.ws_tree)
+    res["tree"] = graph_time_us(tree, reps)
+    res["attention_36"] = graph_time_us(
+        lambda: [g.tree_attention(wl.q[l], wl.layers[l], wl.tree, scale, wl.out[l], wl.ws_attn)
+                 for l in range(c["n_layers"])], reps)
+    res["attention_layer"] = graph_time_us(
+        lambda: g.tree_attention(wl.q[0], wl.layers[0], wl.tree, scale, wl.out[0], wl.ws_attn), reps * 5)
+    res["lmhead"] = graph_time_us(
+        lambda: g.lmhead_argmax(wl.h, wl.W, wl.argmax, wl.gap, wl.maxlogit, wl.ws_lm), reps)
 
     def commit():
         wl.t_len.copy_(wl.t0)
         g.accept_commit(wl.tree, wl.argmax, wl.layers, wl.n_acc, wl.acc_tok, wl.new_root, wl.ws_c)
-    res["commit"] = time_stage(commit, s, iters)
-    return {k: statistics.median(v) for k, v in res.items()}
+    res["commit"] = graph_time_us(commit, reps)
+    res["t_reset_copy"] = graph_time_us(lambda: wl.t_len.copy_(wl.t0), reps)
+    return res
 
 
 def max_over_ranks(ms, dist, device):
@@ -314,7 +321,7 @@ def run_gpu(args):
     value = job_value(world, args.steps, ms)
 
     # per-stage times (eager, events on the launching stream)
-    st = stage_times(wl, iters=5)
+    st = stage_times(wl)
     bytes_ = wl.algorithmic_bytes()
     pk = peaks()
     attn_total = st["attention_36"]

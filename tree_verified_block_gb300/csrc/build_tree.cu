@@ -10,15 +10,19 @@
 // Layout of the work (grid = L rows x C chunks of 8192 logits, 256 threads):
 //  1. every CTA streams its chunk into registers (vectorised, coalesced),
 //     computes the chunk max and sum of exp, and selects the chunk's K best
-//     tokens by a radix select on unique 64-bit keys
-//     (order-preserving logit bits << 32 | ~token id), so that equal logits
-//     rank by ascending id without any extra pass;
-//  2. the last CTA of each row (atomic ticket, no spinning) merges the row's
-//     chunk candidates with a second radix select, sorts the K winners and
+//     tokens. Selection first histograms the gap to the chunk max in 2048
+//     buckets of 1/64 nat (exact: the bucket is monotone in the logit), then,
+//     only inside the boundary bucket, runs a radix select on unique 64-bit
+//     keys (order-preserving logit bits << 32 | ~token id), so that equal
+//     logits rank by ascending id;
+//  2. the last CTA of each row (atomic ticket, no spinning) selects the K best
+//     of the row's chunk candidates the same way, ranks them by counting and
 //     writes (token, log q) using the row's log-sum-exp (accumulated in fp64);
 //  3. the last row-merger overall runs the best-first search in one warp
-//     (frontier in registers, 8 slots per lane, warp max-reduction per pop)
-//     and the whole CTA packs the N popped nodes into canonical order.
+//     (frontier slots in shared memory, their 32-bit score keys in registers,
+//     8 slots per lane, one warp max-reduction per pop; exact score ties take
+//     a slow path that compares depth and rank vectors) and the whole CTA packs
+//     the N popped nodes into canonical order.
 #include "glance_internal.cuh"
 
 GLANCE_DEFINE_STATUS_WORD(status_build_tree)
@@ -49,15 +53,32 @@ struct BuildParams {
   float* top_logq;              // [L][K]
 };
 
+constexpr int kBuckets = 2048;      // first-pass buckets of the gap to the max
+constexpr float kBucketsPerNat = 64.f;
+
 struct SelectSmem {
-  uint32_t hist[256];
+  uint32_t hist[kBuckets];
   uint32_t warp_tot[kThreads / 32];
-  uint32_t digit, above, cnt;
+  int bstar;
+  uint32_t above, cnt;
+  uint32_t digit, above2, cnt2;
 };
 
 __device__ __forceinline__ float inv_ord_key(uint32_t k) {
   uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
   return __uint_as_float(u);
+}
+
+__device__ __forceinline__ unsigned long long make_key(float x, uint32_t id) {
+  return (static_cast<unsigned long long>(ord_key(x)) << 32) | (0xFFFFFFFFu - id);
+}
+
+// Bucket of a logit x given the maximum m (x <= m): floor((m - x) * 64),
+// clamped. Non-increasing in x, equal for equal x, so lower buckets hold
+// strictly larger logits.
+__device__ __forceinline__ int bucket_of(float m, float x) {
+  const float dd = (m - x) * kBucketsPerNat;
+  return dd < static_cast<float>(kBuckets - 1) ? static_cast<int>(dd) : kBuckets - 1;
 }
 
 // Inclusive block scan (sum) of one value per thread; 256 threads.
@@ -76,79 +97,107 @@ __device__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
   return v + add;
 }
 
-// Threshold (prefix, mask) such that exactly `want` of the nonzero keys
-// satisfy (key & mask) >= prefix. Keys are unique.
-template <int E>
-__device__ void radix_select(const unsigned long long (&keys)[E], uint32_t want,
-                             unsigned long long& prefix_out, unsigned long long& mask_out,
-                             SelectSmem& sm) {
-  unsigned long long prefix = 0, mask = 0;
-  uint32_t krem = want;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    sm.hist[threadIdx.x] = 0;
-    __syncthreads();
+// Selects the `want` best items (by unique 64-bit key) of kPerThread items per
+// thread and writes their keys, in any order, to out[0..want). item(e, v, x, k)
+// gives item e's validity, logit and key; m is the maximum valid logit.
+template <typename Item>
+__device__ void select_top(Item item, uint32_t want, float m, unsigned long long* out,
+                           SelectSmem& sm) {
+  if (want == 0) return;  // uniform across the block
+  for (int i = threadIdx.x; i < kBuckets; i += kThreads) sm.hist[i] = 0;
+  __syncthreads();
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const unsigned long long k = keys[e];
-      if (k != 0ull && (k & mask) == prefix)
-        atomicAdd(&sm.hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    // thread t holds bin b = 255 - t; the scan gives S[b] = sum_{d >= b} hist[d]
-    const uint32_t b = 255u - threadIdx.x;
-    const uint32_t v = sm.hist[b];
-    const uint32_t incl = block_incl_scan(v, sm.warp_tot);
-    const uint32_t excl = incl - v;
-    if (excl < krem && incl >= krem) {
-      sm.digit = b;
-      sm.above = excl;
-      sm.cnt = v;
-    }
-    __syncthreads();
-    prefix |= static_cast<unsigned long long>(sm.digit) << shift;
-    mask |= 0xFFull << shift;
-    krem -= sm.above;
-    const bool done = (sm.cnt == krem);
-    __syncthreads();
-    if (done) break;
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    if (v) atomicAdd(&sm.hist[bucket_of(m, x)], 1u);
   }
-  prefix_out = prefix;
-  mask_out = mask;
-}
-
-// Writes the selected keys (any order) to out[0..want). Returns nothing; the
-// caller knows the count.
-template <int E>
-__device__ void compact_selected(const unsigned long long (&keys)[E], unsigned long long prefix,
-                                 unsigned long long mask, unsigned long long* out,
-                                 SelectSmem& sm) {
-  uint32_t c = 0;
+  __syncthreads();
+  // boundary bucket: the first b whose cumulative count reaches `want`
+  constexpr int kPer = kBuckets / kThreads;
+  uint32_t loc = 0;
 #pragma unroll
-  for (int e = 0; e < E; ++e) c += (keys[e] != 0ull && (keys[e] & mask) >= prefix);
-  uint32_t pos = block_incl_scan(c, sm.warp_tot) - c;
+  for (int b = 0; b < kPer; ++b) loc += sm.hist[kPer * threadIdx.x + b];
+  const uint32_t incl = block_incl_scan(loc, sm.warp_tot);
+  uint32_t c = incl - loc;
+  if (c < want && incl >= want) {
+    for (int b = 0; b < kPer; ++b) {
+      const uint32_t h = sm.hist[kPer * threadIdx.x + b];
+      if (c + h >= want) {
+        sm.bstar = kPer * threadIdx.x + b;
+        sm.above = c;
+        sm.cnt = h;
+        break;
+      }
+      c += h;
+    }
+  }
+  __syncthreads();
+  const int bstar = sm.bstar;
+  const uint32_t need = want - sm.above;
+  const bool whole = sm.cnt == need;
+  // inside the boundary bucket: radix select on the full keys
+  unsigned long long prefix = 0, mask = 0;
+  if (!whole) {
+    uint32_t krem = need;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      sm.hist[threadIdx.x] = 0;
+      __syncthreads();
 #pragma unroll
-  for (int e = 0; e < E; ++e)
-    if (keys[e] != 0ull && (keys[e] & mask) >= prefix) out[pos++] = keys[e];
-}
-
-__device__ __forceinline__ unsigned long long make_key(float x, uint32_t id) {
-  return (static_cast<unsigned long long>(ord_key(x)) << 32) | (0xFFFFFFFFu - id);
+      for (int e = 0; e < kPerThread; ++e) {
+        bool v;
+        float x;
+        unsigned long long k;
+        item(e, v, x, k);
+        if (v && bucket_of(m, x) == bstar && (k & mask) == prefix)
+          atomicAdd(&sm.hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      // thread t holds digit d = 255 - t; the scan gives the count of digits >= d
+      const uint32_t d = 255u - threadIdx.x;
+      const uint32_t hv = sm.hist[d];
+      const uint32_t in2 = block_incl_scan(hv, sm.warp_tot);
+      const uint32_t ex2 = in2 - hv;
+      if (ex2 < krem && in2 >= krem) {
+        sm.digit = d;
+        sm.above2 = ex2;
+        sm.cnt2 = hv;
+      }
+      __syncthreads();
+      prefix |= static_cast<unsigned long long>(sm.digit) << shift;
+      mask |= 0xFFull << shift;
+      krem -= sm.above2;
+      const bool done = sm.cnt2 == krem;
+      __syncthreads();
+      if (done) break;
+    }
+  }
+  // compaction
+  uint32_t cntl = 0;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    const int b = v ? bucket_of(m, x) : kBuckets;
+    cntl += v && (b < bstar || (b == bstar && (whole || (k & mask) >= prefix)));
+  }
+  uint32_t pos = block_incl_scan(cntl, sm.warp_tot) - cntl;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    const int b = v ? bucket_of(m, x) : kBuckets;
+    if (v && (b < bstar || (b == bstar && (whole || (k & mask) >= prefix)))) out[pos++] = k;
+  }
 }
 
 // -------------------------------------------------------------- tree search
-
-struct NodeKey {
-  uint32_t ord;  // ord_key(score); 0 = empty
-  uint32_t dep;
-  unsigned long long hi, lo;  // rank bytes, offset 1 in the top byte of hi
-};
-
-__device__ __forceinline__ bool better(const NodeKey& a, const NodeKey& b) {
-  if (a.ord != b.ord) return a.ord > b.ord;
-  if (a.dep != b.dep) return a.dep < b.dep;
-  if (a.hi != b.hi) return a.hi < b.hi;
-  return a.lo < b.lo;
-}
 
 __device__ __forceinline__ void set_rank(unsigned long long& hi, unsigned long long& lo, int j,
                                          uint32_t r) {
@@ -165,13 +214,33 @@ __device__ __forceinline__ uint32_t get_rank(unsigned long long hi, unsigned lon
                : static_cast<uint32_t>(lo >> ((15 - j) * 8)) & 0xFFu;
 }
 
+// (depth, hi, lo) lexicographic: the order among nodes of equal score
+__device__ __forceinline__ bool tie_less(uint32_t da, unsigned long long ha, unsigned long long la,
+                                         uint32_t db, unsigned long long hb, unsigned long long lb) {
+  if (da != db) return da < db;
+  if (ha != hb) return ha < hb;
+  return la < lb;
+}
+
 struct TreeSmem {
+  // frontier slots (slot s is owned by lane s % 32)
+  float f_score[256], f_pscore[256];
+  unsigned long long f_hi[256], f_lo[256];
+  int16_t f_par[256];
+  uint8_t f_dep[256];
+  // popped nodes, in pop order
   float p_score[kMaxN];
   unsigned long long p_hi[kMaxN], p_lo[kMaxN];
   int16_t p_parent[kMaxN];
   int16_t p_pos[kMaxN];
   uint8_t p_dep[kMaxN];
 };
+
+__device__ __forceinline__ void set_reg(uint32_t (&a)[kSlotsPerLane], int i, uint32_t v) {
+#pragma unroll
+  for (int t = 0; t < kSlotsPerLane; ++t)
+    if (t == i) a[t] = v;
+}
 
 __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
@@ -188,141 +257,125 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
 
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    // frontier slots owned by this lane: slot s = lane + 32 * i
-    NodeKey sk[kSlotsPerLane];
-    int spar[kSlotsPerLane];
-    float spscore[kSlotsPerLane];
+    uint32_t ko[kSlotsPerLane];  // score keys of this lane's slots; 0 = empty
 #pragma unroll
-    for (int i = 0; i < kSlotsPerLane; ++i) {
-      sk[i].ord = 0;
-      sk[i].dep = 0;
-      sk[i].hi = sk[i].lo = 0;
-      spar[i] = -1;
-      spscore[i] = 0.f;
-    }
+    for (int i = 0; i < kSlotsPerLane; ++i) ko[i] = 0;
     if (lane == 0) {  // first frontier entry: rank 0 at offset 1
-      sk[0].ord = ord_key(s_logq[0]);
-      sk[0].dep = 1;
+      ts.f_score[0] = s_logq[0];
+      ts.f_pscore[0] = 0.f;
+      ts.f_hi[0] = 0ull;
+      ts.f_lo[0] = 0ull;
+      ts.f_par[0] = -1;
+      ts.f_dep[0] = 1;
+      ko[0] = ord_key(s_logq[0]);
     }
+    __syncwarp();
     int cnt = 1;
     for (int k = 0; k < N; ++k) {
-      // local best of this lane
-      int bi = -1;
-      NodeKey bk;
-      bk.ord = 0;
-      bk.dep = 0;
-      bk.hi = bk.lo = 0;
+      uint32_t bo = 0;
+      int bi = 0;
+      bool dup = false;
 #pragma unroll
-      for (int i = 0; i < kSlotsPerLane; ++i)
-        if (sk[i].ord != 0 && (bi < 0 || better(sk[i], bk))) {
-          bk = sk[i];
+      for (int i = 0; i < kSlotsPerLane; ++i) {
+        const uint32_t v = ko[i];
+        if (v > bo) {
+          bo = v;
           bi = i;
+          dup = false;
+        } else if (v == bo && v != 0) {
+          dup = true;
         }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, bk.ord);
-      const unsigned tied = __ballot_sync(0xffffffffu, bi >= 0 && bk.ord == m);
-      if (tied == 0) {  // frontier exhausted: the host checks make this unreachable
+      }
+      const uint32_t mmax = __reduce_max_sync(0xffffffffu, bo);
+      if (mmax == 0) {  // frontier exhausted: the host checks make this unreachable
         if (lane == 0) report(GLANCE_DEV_BAD_TREE);
         break;
       }
-      int win = __ffs(tied) - 1;
-      if (__popc(tied) > 1) {  // exact score tie: depth, then rank vector
-        unsigned rest = tied & (tied - 1);
-        NodeKey wk;
-        wk.ord = m;
-        wk.dep = __shfl_sync(0xffffffffu, bk.dep, win);
-        wk.hi = __shfl_sync(0xffffffffu, bk.hi, win);
-        wk.lo = __shfl_sync(0xffffffffu, bk.lo, win);
-        while (rest) {
-          const int c = __ffs(rest) - 1;
-          rest &= rest - 1;
-          NodeKey ck;
-          ck.ord = m;
-          ck.dep = __shfl_sync(0xffffffffu, bk.dep, c);
-          ck.hi = __shfl_sync(0xffffffffu, bk.hi, c);
-          ck.lo = __shfl_sync(0xffffffffu, bk.lo, c);
-          if (better(ck, wk)) {
-            wk = ck;
-            win = c;
+      const unsigned cand = __ballot_sync(0xffffffffu, bo == mmax);
+      const bool slow = __popc(cand) > 1 || __ballot_sync(0xffffffffu, bo == mmax && dup) != 0;
+      int ws;
+      if (!slow) {
+        ws = __shfl_sync(0xffffffffu, bi * 32 + lane, __ffs(cand) - 1);
+      } else {
+        // exact score tie: least (depth, rank vector) among slots with key mmax
+        int my = -1;
+        uint32_t md = 0;
+        unsigned long long mh = 0, ml = 0;
+#pragma unroll
+        for (int i = 0; i < kSlotsPerLane; ++i) {
+          if (ko[i] == mmax) {
+            const int sl = i * 32 + lane;
+            const uint32_t d = ts.f_dep[sl];
+            const unsigned long long h = ts.f_hi[sl], l = ts.f_lo[sl];
+            if (my < 0 || tie_less(d, h, l, md, mh, ml)) {
+              my = sl;
+              md = d;
+              mh = h;
+              ml = l;
+            }
           }
         }
-      }
-      const int wslot_i = __shfl_sync(0xffffffffu, bi, win);
-      // winner's node data
-      float wpscore = 0.f;
-      int wpar = -1;
 #pragma unroll
-      for (int i = 0; i < kSlotsPerLane; ++i)
-        if (i == bi) {
-          wpscore = spscore[i];
-          wpar = spar[i];
+        for (int o = 16; o; o >>= 1) {
+          const int oy = __shfl_xor_sync(0xffffffffu, my, o);
+          const uint32_t od = __shfl_xor_sync(0xffffffffu, md, o);
+          const unsigned long long oh = __shfl_xor_sync(0xffffffffu, mh, o);
+          const unsigned long long ol = __shfl_xor_sync(0xffffffffu, ml, o);
+          if (oy >= 0 && (my < 0 || tie_less(od, oh, ol, md, mh, ml))) {
+            my = oy;
+            md = od;
+            mh = oh;
+            ml = ol;
+          }
         }
-      const uint32_t d = __shfl_sync(0xffffffffu, bk.dep, win);
-      const unsigned long long hi = __shfl_sync(0xffffffffu, bk.hi, win);
-      const unsigned long long lo = __shfl_sync(0xffffffffu, bk.lo, win);
-      const float score = inv_ord_key(m);
-      wpscore = __shfl_sync(0xffffffffu, wpscore, win);
-      wpar = __shfl_sync(0xffffffffu, wpar, win);
+        ws = my;
+      }
+      const uint32_t d = ts.f_dep[ws];
+      const unsigned long long hi = ts.f_hi[ws], lo = ts.f_lo[ws];
+      const int par = ts.f_par[ws];
+      const float pscore = ts.f_pscore[ws];
+      const float score = ts.f_score[ws];
       const uint32_t r = get_rank(hi, lo, d - 1);
+      const bool has_child = static_cast<int>(d) < L;
+      const bool has_sib = static_cast<int>(r) + 1 < K;
+      // successors: first child (rank 0 at offset d+1), next sibling (rank r+1)
+      const float c_score = has_child ? score + s_logq[d * K] : 0.f;
+      const float s_score = has_sib ? pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
+      const int ns = cnt;
       if (lane == 0) {
         ts.p_score[k] = score;
         ts.p_hi[k] = hi;
         ts.p_lo[k] = lo;
-        ts.p_parent[k] = static_cast<int16_t>(wpar);
+        ts.p_parent[k] = static_cast<int16_t>(par);
         ts.p_dep[k] = static_cast<uint8_t>(d);
-      }
-      // successors: first child (rank 0 at offset d+1), next sibling (rank r+1)
-      const bool has_child = static_cast<int>(d) < L;
-      const bool has_sib = static_cast<int>(r) + 1 < K;
-      NodeKey ck, sbk;
-      float c_score = 0.f, s_score = 0.f;
-      if (has_child) {
-        c_score = score + s_logq[d * K + 0];
-        ck.ord = ord_key(c_score);
-        ck.dep = d + 1;
-        ck.hi = hi;
-        ck.lo = lo;
-        set_rank(ck.hi, ck.lo, d, 0);
-      }
-      if (has_sib) {
-        s_score = wpscore + s_logq[(d - 1) * K + r + 1];
-        sbk.ord = ord_key(s_score);
-        sbk.dep = d;
-        sbk.hi = hi;
-        sbk.lo = lo;
-        set_rank(sbk.hi, sbk.lo, d - 1, r + 1);
-      }
-      // slot of the popped node takes the child (else the sibling); a new
-      // slot takes the sibling when both exist
-      if (lane == win) {
-#pragma unroll
-        for (int i = 0; i < kSlotsPerLane; ++i)
-          if (i == wslot_i) {
-            if (has_child) {
-              sk[i] = ck;
-              spar[i] = k;
-              spscore[i] = score;
-            } else if (has_sib) {
-              sk[i] = sbk;
-              spar[i] = wpar;
-              spscore[i] = wpscore;
-            } else {
-              sk[i].ord = 0;
-            }
-          }
-      }
-      if (has_child && has_sib) {
-        const int ns = cnt++;
-        if (lane == (ns & 31)) {
-          const int ni = ns >> 5;
-#pragma unroll
-          for (int i = 0; i < kSlotsPerLane; ++i)
-            if (i == ni) {
-              sk[i] = sbk;
-              spar[i] = wpar;
-              spscore[i] = wpscore;
-            }
+        unsigned long long ch = hi, cl = lo, sh = hi, sl = lo;
+        set_rank(ch, cl, d, 0);
+        set_rank(sh, sl, d - 1, r + 1);
+        if (has_child) {
+          ts.f_score[ws] = c_score;
+          ts.f_pscore[ws] = score;
+          ts.f_hi[ws] = ch;
+          ts.f_lo[ws] = cl;
+          ts.f_par[ws] = static_cast<int16_t>(k);
+          ts.f_dep[ws] = static_cast<uint8_t>(d + 1);
+        }
+        const int sslot = has_child ? ns : ws;
+        if (has_sib) {
+          ts.f_score[sslot] = s_score;
+          ts.f_pscore[sslot] = pscore;
+          ts.f_hi[sslot] = sh;
+          ts.f_lo[sslot] = sl;
+          ts.f_par[sslot] = static_cast<int16_t>(par);
+          ts.f_dep[sslot] = static_cast<uint8_t>(d);
         }
       }
+      const uint32_t k_ws = has_child ? ord_key(c_score) : (has_sib ? ord_key(s_score) : 0u);
+      if (lane == (ws & 31)) set_reg(ko, ws >> 5, k_ws);
+      if (has_child && has_sib) {
+        if (lane == (ns & 31)) set_reg(ko, ns >> 5, ord_key(s_score));
+        ++cnt;
+      }
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -334,11 +387,8 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
     const uint32_t dk = ts.p_dep[kk];
     const unsigned long long hk = ts.p_hi[kk], lk = ts.p_lo[kk];
     int pos = 1;
-    for (int j = 0; j < N; ++j) {
-      const uint32_t dj = ts.p_dep[j];
-      const unsigned long long hj = ts.p_hi[j], lj = ts.p_lo[j];
-      pos += (dj < dk) || (dj == dk && (hj < hk || (hj == hk && lj < lk)));
-    }
+#pragma unroll 4
+    for (int j = 0; j < N; ++j) pos += tie_less(ts.p_dep[j], ts.p_hi[j], ts.p_lo[j], dk, hk, lk);
     ts.p_pos[kk] = static_cast<int16_t>(pos);
   }
   __syncthreads();
@@ -374,13 +424,14 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
 // ------------------------------------------------------------------- kernel
 
 template <bool kBF16, bool kVec>
-__global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams p) {
+__global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ SelectSmem sm;
   __shared__ double red_d[kThreads / 32];
   __shared__ float red_f[kThreads / 32];
   __shared__ uint32_t s_ticket;
   __shared__ unsigned long long sel[256];
+  __shared__ double s_lse;
 
   const int row = blockIdx.x / p.C;
   const int chunk = blockIdx.x % p.C;
@@ -391,7 +442,7 @@ __global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams 
   // ---- 1. load the chunk into registers (ids: see id_of below)
   float x[kPerThread];
   if (kVec) {
-    // 4 consecutive ids per vector: vector v = t + 256 * q holds ids base + 4v .. 4v+3
+    // vector v = t + 256 * q holds ids base + 4v .. 4v+3
 #pragma unroll
     for (int q = 0; q < kPerThread / 4; ++q) {
       const int v = threadIdx.x + kThreads * q;
@@ -463,16 +514,15 @@ __global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams 
   if (lane == 0) red_d[warp] = sd;
 
   // ---- chunk top-K
-  unsigned long long keys[kPerThread];
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e)
-    keys[e] = valid_of(e) ? make_key(x[e], static_cast<uint32_t>(id_of(e))) : 0ull;
   const int kc = min(p.K, n_valid);
-  unsigned long long prefix, mask;
-  radix_select(keys, kc, prefix, mask, sm);  // contains __syncthreads
-  unsigned long long* my_cand =
-      p.cand + (static_cast<size_t>(row) * p.C + chunk) * p.K;
-  compact_selected(keys, prefix, mask, my_cand, sm);
+  unsigned long long* my_cand = p.cand + (static_cast<size_t>(row) * p.C + chunk) * p.K;
+  select_top(
+      [&](int e, bool& v, float& xv, unsigned long long& k) {
+        v = valid_of(e);
+        xv = x[e];
+        k = make_key(x[e], static_cast<uint32_t>(id_of(e)));
+      },
+      static_cast<uint32_t>(kc), m, my_cand, sm);
   if (threadIdx.x == 0) {
     double tot = 0.0;
     for (int w = 0; w < kThreads / 32; ++w) tot += red_d[w];
@@ -489,40 +539,7 @@ __global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams 
   __threadfence();
   if (threadIdx.x == 0) p.tickets[row] = 0;  // ready for the next call
 
-  // candidates: flat index f = c * K + i, valid when i < min(K, chunk size)
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int f = threadIdx.x + kThreads * e;
-    const int c = f / p.K, i = f - c * p.K;
-    keys[e] = 0ull;
-    if (c < p.C) {
-      const int kc_c = min(p.K, min(kChunk, p.V - c * kChunk));
-      if (i < kc_c) keys[e] = __ldcg(p.cand + (static_cast<size_t>(row) * p.C + c) * p.K + i);
-    }
-  }
-  radix_select(keys, p.K, prefix, mask, sm);
-  sel[threadIdx.x] = 0ull;
-  __syncthreads();
-  compact_selected(keys, prefix, mask, sel, sm);
-  __syncthreads();
-  // bitonic sort of sel[0..256), descending
-  for (int size = 2; size <= 256; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int t = threadIdx.x;
-      const int partner = t ^ stride;
-      if (partner > t) {
-        const bool desc = (t & size) == 0;
-        const unsigned long long a = sel[t], b = sel[partner];
-        if ((a < b) == desc) {
-          sel[t] = b;
-          sel[partner] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  // row log-sum-exp from chunk (max, sum) pairs, in fp64
-  __shared__ double s_lse;
+  // row log-sum-exp and max from the chunks' (max, sum) pairs, in fp64
   if (warp == 0) {
     double M = -INFINITY;
     for (int c = lane; c < p.C; c += 32) M = fmax(M, __ldcg(p.chunk_m + row * p.C + c));
@@ -533,15 +550,43 @@ __global__ void __launch_bounds__(kThreads) build_tree_kernel(const BuildParams 
       S += __ldcg(p.chunk_s + row * p.C + c) * exp(__ldcg(p.chunk_m + row * p.C + c) - M);
 #pragma unroll
     for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    if (lane == 0) s_lse = M + log(S);
+    if (lane == 0) {
+      s_lse = M + log(S);
+      red_f[0] = static_cast<float>(M);
+    }
+  }
+  // candidates: flat index f = c * K + i, valid when i < min(K, chunk size)
+  unsigned long long keys[kPerThread];
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int f = threadIdx.x + kThreads * e;
+    const int c = f / p.K, i = f - c * p.K;
+    keys[e] = 0ull;
+    if (c < p.C) {
+      const int kc_c = min(p.K, min(kChunk, p.V - c * kChunk));
+      if (i < kc_c) keys[e] = __ldcg(p.cand + (static_cast<size_t>(row) * p.C + c) * p.K + i);
+    }
   }
   __syncthreads();
+  const float row_max = red_f[0];
+  select_top(
+      [&](int e, bool& v, float& xv, unsigned long long& k) {
+        k = keys[e];
+        v = k != 0ull;
+        xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
+      },
+      static_cast<uint32_t>(p.K), row_max, sel, sm);
+  __syncthreads();
+  // rank of each selected key among the K (keys are unique), by counting
   if (threadIdx.x < p.K) {
     const unsigned long long k = sel[threadIdx.x];
+    int rank = 0;
+#pragma unroll 4
+    for (int j = 0; j < p.K; ++j) rank += sel[j] > k;
     const float xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
     const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
-    p.top_tok[row * p.K + threadIdx.x] = static_cast<int32_t>(id);
-    p.top_logq[row * p.K + threadIdx.x] = static_cast<float>(static_cast<double>(xv) - s_lse);
+    p.top_tok[row * p.K + rank] = static_cast<int32_t>(id);
+    p.top_logq[row * p.K + rank] = static_cast<float>(static_cast<double>(xv) - s_lse);
   }
 
   // ---- 3. last row-merger builds the tree

@@ -55,19 +55,28 @@ __global__ void __launch_bounds__(kThreads) accept_commit_kernel(const CommitPar
   __shared__ int s_a, s_newroot, s_T;
   __shared__ __align__(16) unsigned char stage[kMaxPath * kMaxRowBytes];
   __shared__ uint32_t s_ticket;
+  __shared__ int s_tok[256], s_par[256], s_dep[256], s_arg[256];
 
+  // stage the tree and the argmax row tokens (coalesced), then walk in smem
+  for (int i = threadIdx.x; i < p.rows; i += kThreads) {
+    s_tok[i] = __ldg(p.token + i);
+    s_par[i] = __ldg(p.parent + i);
+    s_dep[i] = __ldg(p.depth + i);
+    s_arg[i] = __ldg(p.argmax + i);
+  }
+  if (threadIdx.x == 0) s_T = *p.t_len;
+  __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int u = 0, a = 0;
     if (lane == 0) s_path[0] = 0;
     for (int step = 0; step < p.L; ++step) {
-      if (__ldg(p.depth + u) >= p.L) break;
-      const int target = __ldg(p.argmax + u);
+      if (s_dep[u] >= p.L) break;
+      const int target = s_arg[u];
       int found = -1;
       for (int base = 0; base < p.rows; base += 32) {
         const int c = base + lane;
-        const bool hit = c < p.rows && c > 0 && __ldg(p.parent + c) == u &&
-                         __ldg(p.token + c) == target;
+        const bool hit = c < p.rows && c > 0 && s_par[c] == u && s_tok[c] == target;
         const unsigned m = __ballot_sync(0xffffffffu, hit);
         if (m) {
           found = base + __ffs(m) - 1;
@@ -81,8 +90,7 @@ __global__ void __launch_bounds__(kThreads) accept_commit_kernel(const CommitPar
     }
     if (lane == 0) {
       s_a = a;
-      s_newroot = __ldg(p.argmax + u);
-      s_T = *p.t_len;
+      s_newroot = s_arg[u];
     }
   }
   __syncthreads();
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) accept_commit_kernel(const CommitPar
     *p.new_root = s_newroot;
     if (room) *p.t_len = T + a + 1;
   }
-  if (threadIdx.x >= 1 && threadIdx.x <= a) p.accepted_tok[threadIdx.x - 1] = p.token[s_path[threadIdx.x]];
+  if (threadIdx.x >= 1 && threadIdx.x <= a) p.accepted_tok[threadIdx.x - 1] = s_tok[s_path[threadIdx.x]];
 }
 
 }  // namespace

@@ -182,10 +182,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
-// bit k (0 <= k < 256) of a row's ancestor mask, without dynamic indexing
-__device__ __forceinline__ bool anc_bit(const uint64_t (&a)[4], int k) {
-  const uint64_t w = k < 128 ? (k < 64 ? a[0] : a[1]) : (k < 192 ? a[2] : a[3]);
-  return (w >> (k & 63)) & 1ull;
+// word w (0..3) of a row's ancestor mask, 0 outside, without dynamic indexing
+__device__ __forceinline__ uint64_t anc_word(const uint64_t (&a)[4], int w) {
+  return w == 0 ? a[0] : w == 1 ? a[1] : w == 2 ? a[2] : w == 3 ? a[3] : 0ull;
+}
+
+// Visibility of 32 consecutive key slots starting at tree index kb (= slot - T;
+// negative for prefix slots): bit i is set iff slot kb + i is a prefix slot, or
+// a tree row (kb + i < rows) on the row's ancestor list.
+__device__ __forceinline__ uint32_t visible32(const uint64_t (&a)[4], int kb, int rows) {
+  if (kb <= -32) return 0xFFFFFFFFu;
+  uint32_t tree_bits;
+  if (kb < 0) {
+    tree_bits = static_cast<uint32_t>(a[0] << (-kb));
+  } else {
+    const int w = kb >> 6, o = kb & 63;
+    const uint64_t lo = anc_word(a, w), hi = anc_word(a, w + 1);
+    tree_bits = static_cast<uint32_t>(o ? (lo >> o) | (hi << (64 - o)) : lo);
+  }
+  const int lim = rows - kb;  // bits i < lim are tree rows
+  const uint32_t rows_mask = lim >= 32 ? 0xFFFFFFFFu : lim <= 0 ? 0u : ((1u << lim) - 1u);
+  const uint32_t prefix_mask = kb < 0 ? ((1u << (-kb)) - 1u) : 0u;
+  return prefix_mask | (tree_bits & rows_mask);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -366,80 +384,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      // s_full(j) was committed after PV(j-1) was issued, so O and the P
+      // columns of tile j-1 are released by now; this wait returns at once
+      if (j > 0 && !wait_or_abort(&bars->o_done, (j - 1) & 1, bars)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const bool full = key0 + kBN <= T;  // all slots of the tile are prefix
-      // pass 1: masked row max
-      float mt = -INFINITY;
+      // this thread's S row: 128 fp32 in registers (four loads, one wait)
+      uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + c * 32, r);
-        tmem_ld_wait();
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+      tmem_ld_wait();
+      if (!full) {
+        // slots >= T: visible only on the row's ancestor list (and < T + rows)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int slot = key0 + c * 32 + e;
-          bool vis = full;
-          if (!full) {
-            const int k = slot - T;
-            vis = slot < T || (k < p.rows && anc_bit(anc, k));
-          }
-          const float sv = __uint_as_float(r[e]) * p.scale_log2;
-          mt = vis ? fmaxf(mt, sv) : mt;
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t vm = visible32(anc, key0 + 32 * c - T, p.rows);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            sr[32 * c + e] = ((vm >> e) & 1u) ? sr[32 * c + e] : 0xFF800000u;  // -inf
         }
       }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kBN; e += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
+      }
+      // scale_log2 > 0, so the max commutes with the scaling
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
       const float m_new = fmaxf(m, mt);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_use);
-      // O must be final for tile j-1 before it is rescaled or P overwrites S
-      if (j > 0) {
-        if (!wait_or_abort(&bars->o_done, (j - 1) & 1, bars)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_off + c * 32, r);
-            tmem_ld_wait();
-            uint32_t a[16], b[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
-            }
-            tmem_st16(tO + lane_off + c * 32, a);
-            tmem_st16(tO + lane_off + c * 32 + 16, b);
-          }
-        }
-      }
-      // pass 2: P = 2^(s - m), written as bf16 pairs (64 columns)
-      float ls = 0.f;
+      // P = 2^(s * scale_log2 - m) as bf16 pairs, 16 columns per store
+      const float neg_m = -m_use;
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + c * 32, r);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float pv[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int ee = 2 * e + h2;
-            const int slot = key0 + c * 32 + ee;
-            bool vis = full;
-            if (!full) {
-              const int k = slot - T;
-              vis = slot < T || (k < p.rows && anc_bit(anc, k));
-            }
-            pv[h2] = vis ? exp2f(__uint_as_float(r[ee]) * p.scale_log2 - m_use) : 0.f;
-          }
-          ls += pv[0] + pv[1];
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          const float p0 = exp2f(fmaf(__uint_as_float(sr[32 * c + 2 * e]), p.scale_log2, neg_m));
+          const float p1 = exp2f(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), p.scale_log2, neg_m));
+          ls0 += p0;
+          ls1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tP + lane_off + c * 16, pk);
+      }
+      const float ls = ls0 + ls1;
+      // rescale O when the running max grew (O of tile j-1 is final)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + lane_off + c * 32, r);
+          tmem_ld_wait();
+          uint32_t a[16], b[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
+          }
+          tmem_st16(tO + lane_off + c * 32, a);
+          tmem_st16(tO + lane_off + c * 32 + 16, b);
+        }
       }
       tmem_st_wait();
       l = l * alpha + ls;
@@ -457,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.n_split == 1) {
         const float inv = 1.f / l;
         __nv_bfloat16* dst = p.out + (static_cast<size_t>(prow) * p.Hq + head) * kD;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + lane_off + c * 32, r);
@@ -476,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const size_t tile_idx = (static_cast<size_t>(split) * p.Hkv + g) * p.n_qt + qt;
         float* po = p.part_o + (tile_idx * kBM + lrow) * kD;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + lane_off + c * 32, r);
@@ -505,39 +519,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge split partials: one warp per query row, 4 head dims per lane.
+// Merge split partials: one warp per query row, 4 head dims per lane; lane s
+// holds split s's (m, l), so the loads of all splits are issued together.
 __global__ void __launch_bounds__(128) combine_kernel(const Bf16Params p) {
   const int rows_per_cta = 4;
-  const int tile_rows = kBM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int flat = blockIdx.x * rows_per_cta + warp;  // over Hkv * n_qt * 128
-  const int lrow = flat % tile_rows;
-  const int qt = (flat / tile_rows) % p.n_qt;
-  const int g = flat / (tile_rows * p.n_qt);
+  const int lrow = flat % kBM;
+  const int qt = (flat / kBM) % p.n_qt;
+  const int g = flat / (kBM * p.n_qt);
   if (g >= p.Hkv) return;
   const int qrow = qt * kBM + lrow;
   const int hl = qrow / p.Rp, prow = qrow % p.Rp;
   if (hl >= p.G || prow >= p.rows) return;
   const int head = g * p.G + hl;
-  float M = -INFINITY;
-  for (int s = 0; s < p.n_split; ++s) {
-    const size_t ti = (static_cast<size_t>(s) * p.Hkv + g) * p.n_qt + qt;
-    M = fmaxf(M, __ldcg(p.part_ml + (ti * kBM + lrow) * 2));
-  }
+  const size_t split_stride = static_cast<size_t>(p.Hkv) * p.n_qt * kBM;
+  const size_t base = (static_cast<size_t>(g) * p.n_qt + qt) * kBM + lrow;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
-    const size_t ti = (static_cast<size_t>(s) * p.Hkv + g) * p.n_qt + qt;
-    const float ms = __ldcg(p.part_ml + (ti * kBM + lrow) * 2);
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - M);
-    L += w * __ldcg(p.part_ml + (ti * kBM + lrow) * 2 + 1);
-    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (ti * kBM + lrow) * kD) + lane);
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+  float M = -INFINITY;  // max over all splits
+  for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+    const int s = s0 + lane;
+    const float ms = s < p.n_split ? __ldcg(p.part_ml + (s * split_stride + base) * 2) : -INFINITY;
+    float mm = ms;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    M = fmaxf(M, mm);
   }
+  for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+    const int s = s0 + lane;
+    float w = 0.f;
+    if (s < p.n_split) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + s * split_stride + base);
+      w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+      L += w * ml.y;
+    }
+    const int cnt = min(32, p.n_split - s0);
+    float4 o[4];
+    for (int i = 0; i < cnt; i += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + u < cnt)
+          o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + i + u) * split_stride + base) * kD) + lane);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i + u < cnt) {
+          const float wu = __shfl_sync(0xffffffffu, w, i + u);
+          acc.x += wu * o[u].x;
+          acc.y += wu * o[u].y;
+          acc.z += wu * o[u].z;
+          acc.w += wu * o[u].w;
+        }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = 1.f / L;
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
