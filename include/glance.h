@@ -175,6 +175,31 @@ glance_status glance_lmhead_argmax(const void* h, const void* W, glance_dtype dt
                                    float* maxlogit, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/*
+ * LM head that allocates nothing and takes no workspace. The paper has no
+ * counterpart: this is a convenience of the library. It is for callers that
+ * must not allocate device memory or pass scratch space on this path, for
+ * example code that runs while a stream is captured in a mode that forbids
+ * cudaMalloc, or an engine that has reserved all device memory for its own
+ * pool and has none to lend.
+ *
+ * Same computation, arguments and outputs as glance_lmhead_argmax, BF16 only
+ * (d % 64 == 0, V % 8 == 0, 1 <= M <= 512; anything else is rejected with an
+ * error, F32 with GLANCE_ERR_UNSUPPORTED). Its scratch (a merge ticket and the
+ * partial results of at most 160 CTAs, 240 KB in total) is a file-scope device
+ * array of the library, held by every GPU that loads the library until the
+ * process exits. Each call clears the ticket with cudaMemsetAsync on `stream`;
+ * no call makes cudaMalloc, cudaFree or any other allocating call. The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current: make that first call before any stream capture.
+ * All calls on a device share the array, which keeps the last call's
+ * contents, so calls that may overlap on the GPU (other streams or threads)
+ * race with each other: serialise them.
+ */
+glance_status glance_lmhead_argmax_noalloc(const void* h, const void* W, glance_dtype dtype,
+                                           int M, int d, int V, int32_t* argmax, float* gap,
+                                           float* maxlogit, void* stream);
+
 /* ------------------------------------------------------------------ commit */
 
 /* Workspace bytes for glance_accept_commit. */

@@ -10,12 +10,14 @@ The compute lives in ``libglance.so`` (CUDA kernels behind a C ABI declared in
 """
 from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
                        accept_commit_workspace_bytes, build_tree, build_tree_workspace_bytes,
-                       device_status, lib, lmhead_argmax, lmhead_argmax_workspace_bytes,
+                       device_status, lib, lmhead_argmax, lmhead_argmax_noalloc,
+                       lmhead_argmax_workspace_bytes,
                        reset_device_status, tree_attention, tree_attention_workspace_bytes,
                        version, workspace)
 
 __all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
            "accept_commit", "accept_commit_workspace_bytes", "build_tree",
            "build_tree_workspace_bytes", "device_status", "lib", "lmhead_argmax",
+           "lmhead_argmax_noalloc",
            "lmhead_argmax_workspace_bytes", "reset_device_status", "tree_attention",
            "tree_attention_workspace_bytes", "version", "workspace"]

@@ -21,7 +21,7 @@ DEV_STATUS = {0: "ok", 1: "non-finite draft logits", 2: "tree does not fit the c
 EXPORTS = [
     "glance_build_tree_workspace_bytes", "glance_build_tree",
     "glance_tree_attention_workspace_bytes", "glance_tree_attention",
-    "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax",
+    "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax", "glance_lmhead_argmax_noalloc",
     "glance_accept_commit_workspace_bytes", "glance_accept_commit",
     "glance_last_error", "glance_status_string", "glance_device_status",
     "glance_reset_device_status", "glance_version",
@@ -75,6 +75,8 @@ def lib():
     L.glance_lmhead_argmax_workspace_bytes.restype = sz
     L.glance_lmhead_argmax.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     L.glance_lmhead_argmax.restype = st
+    L.glance_lmhead_argmax_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    L.glance_lmhead_argmax_noalloc.restype = st
     L.glance_accept_commit_workspace_bytes.argtypes = [i32]
     L.glance_accept_commit_workspace_bytes.restype = sz
     L.glance_accept_commit.argtypes = [ctypes.POINTER(TreeC), vp, ctypes.POINTER(KVC), i32, vp, vp,
@@ -195,6 +197,16 @@ def lmhead_argmax(h, W, argmax, gap, maxlogit, ws, stream=None):
     _check(lib().glance_lmhead_argmax(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
                                       _ptr(argmax), _ptr(gap), _ptr(maxlogit), _ptr(ws),
                                       ws.numel(), _stream(stream, h.device)))
+
+
+def lmhead_argmax_noalloc(h, W, argmax, gap, maxlogit, stream=None):
+    """LM head + argmax for callers that cannot allocate: no workspace, the
+    scratch lives in the library (calls on one device must not overlap)."""
+    M, d = h.shape
+    assert W.shape[0] == d and h.is_contiguous() and W.is_contiguous() and h.dtype == W.dtype
+    _check(lib().glance_lmhead_argmax_noalloc(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
+                                              _ptr(argmax), _ptr(gap), _ptr(maxlogit),
+                                              _stream(stream, h.device)))
 
 
 def accept_commit_workspace_bytes(n_layers):

@@ -19,6 +19,8 @@
 // warp fills the other accumulator. CTAs write per-row partials; the last CTA
 // (atomic ticket) merges them, one warp per row.
 // fp32 path: CUDA cores, 128 vocabulary columns x 8 rows per CTA.
+#include <mutex>
+
 #include "glance_internal.cuh"
 
 GLANCE_DEFINE_STATUS_WORD(status_lmhead)
@@ -446,6 +448,112 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
     lmhead_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mh, mw, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: launch");
+  }
+  return GLANCE_OK;
+}
+
+// ------------------------------------------------- no-allocation entry point
+//
+// For callers that cannot allocate device memory or hand the library a
+// workspace on this path: for example code that runs while a stream is being
+// captured in a mode that forbids cudaMalloc, or an engine that has reserved
+// all device memory for its own pool. The scratch that glance_lmhead_argmax
+// takes from its workspace (a merge ticket and one partial per CTA and row)
+// lives instead in the file-scope array below. Every GPU that loads this
+// library holds the array (240 KB) until the process exits.
+
+namespace {
+
+constexpr int kNoAllocMaxCtas = 160;
+constexpr size_t kNoAllocScratchBytes =
+    256 + static_cast<size_t>(kNoAllocMaxCtas) * kBM * sizeof(Partial);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current (in host code the array's name is only
+// a stand-in, not a device address).
+glance_status noalloc_scratch(void** out) {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64)
+    return glance::fail(GLANCE_ERR_UNSUPPORTED, "glance_lmhead_argmax_noalloc: device index %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+      return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: cudaGetSymbolAddress");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return GLANCE_OK;
+}
+
+}  // namespace
+
+extern "C" glance_status glance_lmhead_argmax_noalloc(const void* h, const void* W,
+                                                      glance_dtype dtype, int M, int d, int V,
+                                                      int32_t* argmax, float* gap,
+                                                      float* maxlogit, void* stream) {
+  using glance::fail;
+  if (!h || !W || !argmax || !gap)
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax_noalloc: null pointer argument");
+  if (dtype != GLANCE_BF16)
+    return fail(GLANCE_ERR_UNSUPPORTED, "glance_lmhead_argmax_noalloc: only BF16 is supported");
+  if (M < 1 || M > 512 || d < 1 || V < 1)
+    return fail(GLANCE_ERR_INVALID_ARG,
+                "glance_lmhead_argmax_noalloc: need 1 <= M <= 512, d >= 1, V >= 1 (got M=%d)", M);
+  if (d % kBK != 0 || V % 8 != 0)
+    return fail(GLANCE_ERR_UNSUPPORTED,
+                "glance_lmhead_argmax_noalloc: needs d %% 64 == 0 and V %% 8 == 0");
+  if (!glance::aligned16(h) || !glance::aligned16(W))
+    return fail(GLANCE_ERR_INVALID_ARG,
+                "glance_lmhead_argmax_noalloc: h and W must be 16-byte aligned");
+  const int n_tiles = (V + kBN - 1) / kBN;
+  int grid = glance::num_sms();
+  if (grid > n_tiles) grid = n_tiles;
+  if (grid > kNoAllocMaxCtas) grid = kNoAllocMaxCtas;  // the scratch holds this many CTAs
+  void* scratch = nullptr;
+  glance_status st = noalloc_scratch(&scratch);
+  if (st != GLANCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel),
+                                      static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: smem attribute");
+  // the merge ticket must start at zero (the array keeps the last call's contents)
+  e = cudaMemsetAsync(scratch, 0, 256, s);
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: ticket reset");
+  uint32_t* ticket = static_cast<uint32_t*>(scratch);
+  Partial* part = reinterpret_cast<Partial*>(static_cast<char*>(scratch) + 256);
+  CUtensorMap mw;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
+    const uint32_t box[2] = {64, kBK};
+    st = glance::make_map_bf16(&mw, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                               "glance_lmhead_argmax_noalloc: W map");
+    if (st != GLANCE_OK) return st;
+  }
+  for (int r0 = 0; r0 < M; r0 += kBM) {
+    const int mb = M - r0 < kBM ? M - r0 : kBM;
+    const int a_rows = (mb + 7) / 8 * 8;
+    CUtensorMap mh;
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(mb)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
+    st = glance::make_map_bf16(&mh, static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d,
+                               2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                               "glance_lmhead_argmax_noalloc: h map");
+    if (st != GLANCE_OK) return st;
+    Bf16Params p{mb, d, V, n_tiles, a_rows, argmax + r0, gap + r0,
+                 maxlogit ? maxlogit + r0 : nullptr, part, ticket};
+    lmhead_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mh, mw, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: launch");
   }
   return GLANCE_OK;
 }
