@@ -12,19 +12,26 @@
 // of values. T is read from device memory.
 //
 // bf16 / head_dim 128 path (tcgen05):
-//   CTA = (kv head g, q tile of 128 query rows, key split). The 128 query rows
-//   of a tile are (q head, packed row) pairs of the heads that share kv head g
-//   (grouped-query attention), each head's rows padded to a power of two.
-//   Warp 0 issues TMA loads (Q once, then K and V tiles of 128 slots into a
-//   two-stage ring), warp 1 issues the MMAs (S = Q K^T into tensor memory,
-//   then O += P V with P read from tensor memory), warps 4..7 own one query
-//   row per thread: they read S from tensor memory, apply the key mask in
-//   registers (the ancestor words of their row are held in registers), run
-//   the online softmax in base 2, write P as bf16 into its own tensor-memory
-//   columns (so the next tile's S = Q K^T never overwrites a P that the
-//   previous PV has not read yet), and rescale O when the running max grows. Key splits write (O, m, l) partials and a
-//   second kernel merges them; with one split the CTA normalises and writes
-//   bf16 output itself.
+//   CTA = (kv head g, tile of 128 query rows, key split), 384 threads. The 128
+//   query rows of a tile are (q head, packed row) pairs of the heads that share
+//   kv head g (grouped-query attention), each head's rows padded to a power of
+//   two. Warp 0 issues TMA loads (Q once, then K and V tiles of 128 slots into
+//   a three-stage ring); warp 1 issues the MMAs: S = Q K^T into one of two
+//   tensor-memory S buffers, so the next tile's S is computed while this
+//   tile's softmax runs, then O += P V with P read from tensor memory.
+//   Warps 4..11 run the softmax, two threads per query row (one TMEM lane,
+//   64 keys each; the halves exchange their row maxima through shared memory):
+//   they read S with tcgen05.ld, apply the key mask in registers (the row's
+//   ancestor words sit in registers and become one 32-bit visibility word per
+//   32 slots), run the online softmax in base 2, write P as bf16 pairs and
+//   rescale O in tensor memory when the running max grows.
+//   The key range [0, T + N + 1) is split over up to 16 CTAs per (g, q tile)
+//   so that the grid fills the SMs with one CTA each; the launch is
+//   cooperative, so all CTAs are resident at once. Each CTA writes its
+//   unnormalised partial O and (m, l) per row to the workspace (L2-resident),
+//   announces itself on the group's counter (release), waits for the other
+//   splits (acquire, bounded by a timeout that sets the device status), and
+//   merges the rows it owns. One launch per layer.
 // fp32 path (any head_dim multiple of 32 up to 128): plain CUDA cores, one
 //   CTA per (row, q head), keys in chunks of 128 with an online softmax.
 #include "glance_internal.cuh"
@@ -134,20 +141,23 @@ __global__ void __launch_bounds__(kF32Threads) tree_attention_f32_kernel(const F
 constexpr int kD = 128;          // head_dim
 constexpr int kBM = 128;         // query rows per tile (MMA M)
 constexpr int kBN = 128;         // key slots per tile (MMA N of S, K of PV)
-constexpr int kStages = 2;       // K/V ring depth
-constexpr int kThreads = 256;    // 8 warps
-constexpr int kTmemCols = 512;   // S (128) + O (128) + P (64, bf16 pairs), power of two
-constexpr uint32_t kHalfBytes = kBN * 128;          // 64 head dims x 128 slots, bf16
+constexpr int kStages = 3;       // K/V ring depth
+constexpr int kThreads = 384;    // 12 warps: TMA, MMA, TMEM, idle, 2 x 4 softmax
+constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64 used)
+constexpr int kMaxSplit = 16;    // key splits of one (kv head, q tile)
+constexpr uint32_t kHalfBytes = kBN * 128;          // 64 head dims x 128 slots, bf16: 16 KB
 constexpr uint32_t kQBytes = 2 * kBM * 128;         // 32 KB
 constexpr uint32_t kKVStageBytes = 4 * kHalfBytes;  // K and V, two halves each: 64 KB
-constexpr size_t kSmemBytes = 1024 /*align*/ + kQBytes + kStages * kKVStageBytes + 256;
+constexpr uint32_t kRingBytes = kStages * kKVStageBytes;
+constexpr size_t kSmemBytes = 1024 /*align*/ + kQBytes + kRingBytes + 1280;
 
 struct Bf16Params {
   const uint64_t* anc;
   const int32_t* t_len;
   __nv_bfloat16* out;        // [rows][Hq][128]
-  float* part_o;             // [S][Hkv][n_qt][128][128]
-  float* part_ml;            // [S][Hkv][n_qt][128][2]
+  float4* part_o;            // [groups][n_split][32 dim quads][128 rows] unnormalised partial O
+  float2* part_ml;           // [groups][n_split][128] (running max, sum) per row
+  uint32_t* arrive;          // [groups] split arrivals, then [groups] departures
   int rows, Hq, Hkv, G, Rp, n_qt, n_split, W, t_cap;
   int box_rows;              // rows per Q box = min(Rp, 128)
   float scale_log2;          // scale * log2(e)
@@ -157,12 +167,14 @@ struct __align__(8) Bars {
   uint64_t q_full;
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full;
+  uint64_t s_full[2];
   uint64_t p_ready;
   uint64_t o_done;
   uint32_t tmem_base;
   int abort_flag;
+  float xch[2][kBM];         // [half][row]: partial max / sum exchange
 };
+static_assert(sizeof(Bars) <= 1280, "barrier block");
 
 __device__ __forceinline__ void fail_pipeline(Bars* bars) {
   report(GLANCE_DEV_PIPELINE_TIMEOUT);
@@ -206,6 +218,8 @@ __device__ __forceinline__ uint32_t visible32(const uint64_t (&a)[4], int kb, in
   return prefix_mask | (tree_bits & rows_mask);
 }
 
+// One CTA = (kv head g, q tile, key split). The key splits of one (g, q tile)
+// merge their partial results through the workspace once all have arrived.
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attention_bf16_kernel(const __grid_constant__ CUtensorMap map_q,
                                const __grid_constant__ CUtensorMap map_k,
@@ -215,12 +229,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* sQ = smem;
   unsigned char* sKV = smem + kQBytes;
-  Bars* bars = reinterpret_cast<Bars*>(sKV + kStages * kKVStageBytes);
+  Bars* bars = reinterpret_cast<Bars*>(sKV + kRingBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x % p.n_split;
   const int qt = (blockIdx.x / p.n_split) % p.n_qt;
   const int g = blockIdx.x / (p.n_split * p.n_qt);
+
+  // The next kernel in the stream may start its own prologue on free SMs now;
+  // this kernel sets up barriers and tensor memory, then waits until the
+  // previous kernel's writes are visible before it reads any input.
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->o_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  pdl_wait_prior();
 
   const int T = *p.t_len;
   const bool room = T >= 0 && T + p.rows <= p.t_cap;
@@ -231,33 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile1 = static_cast<int>((static_cast<long long>(n_tiles) * (split + 1)) / p.n_split);
   const int my_tiles = tile1 - tile0;
 
-  if (threadIdx.x == 0) {
-    if (!room && blockIdx.x == 0) report(GLANCE_DEV_TREE_CAPACITY);
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_ready, 128);
-    mbar_init(&bars->o_done, 1);
-    bars->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
+  if (threadIdx.x == 0 && !room && blockIdx.x == 0) report(GLANCE_DEV_TREE_CAPACITY);
   // query pieces of this tile that hold no real (head, row): zero them so the
   // MMA reads finite values
   {
     const int pieces = kBM / p.box_rows;
     for (int pc = 0; pc < pieces; ++pc) {
       const int r0 = qt * kBM + pc * p.box_rows;  // first q-row of the piece
-      const int hl = r0 / p.Rp;
-      if (hl >= p.G) {
-        for (int half = 0; half < 2; ++half) {
-          uint4* dst = reinterpret_cast<uint4*>(sQ + half * (kBM * 128) + pc * p.box_rows * 128);
+      if (r0 / p.Rp >= p.G) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint4* dst = reinterpret_cast<uint4*>(sQ + hf * (kBM * 128) + pc * p.box_rows * 128);
           for (int i = threadIdx.x; i < p.box_rows * 8; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
         }
       }
@@ -268,50 +293,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tS = tmem;         // S (fp32, 128 cols)
-  const uint32_t tO = tmem + 128;   // O (fp32, 128 cols)
-  const uint32_t tP = tmem + 256;   // P (bf16 pairs, 64 cols)
+  const uint32_t tS0 = tmem;         // S, double-buffered (fp32, 128 cols each)
+  const uint32_t tO = tmem + 256;    // O (fp32, 128 cols)
+  const uint32_t tP = tmem + 384;    // P (bf16 pairs, 64 cols)
+
+  // softmax-thread state, live until the merge
+  const bool is_sm = warp >= 4;
+  const int half = is_sm ? (warp - 4) >> 2 : 0;  // which 64 keys / 64 output dims
+  const int quarter = warp & 3;                   // TMEM lane quarter
+  const int lrow = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const int qrow = qt * kBM + lrow;  // index within the kv head's query rows
+  const int hl = qrow / p.Rp;
+  const int prow = qrow % p.Rp;
+  const bool valid = hl < p.G && prow < p.rows;
+  const int head = g * p.G + hl;
+  float m = -INFINITY, lh = 0.f;
+  bool ok = true;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && my_tiles > 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      // Q: pieces of box_rows rows; piece pc covers q-rows qt*128 + pc*box_rows ...
       const int pieces = kBM / p.box_rows;
       int n_boxes = 0;
       for (int pc = 0; pc < pieces; ++pc) n_boxes += ((qt * kBM + pc * p.box_rows) / p.Rp < p.G) ? 2 : 0;
       mbar_arrive_expect_tx(&bars->q_full, n_boxes * p.box_rows * 128);
       for (int pc = 0; pc < pieces; ++pc) {
         const int r0 = qt * kBM + pc * p.box_rows;
-        const int hl = r0 / p.Rp;
-        if (hl >= p.G) continue;
-        const int head = g * p.G + hl;
-        const int row0 = r0 % p.Rp;
-        for (int half = 0; half < 2; ++half)
-          tma_load_3d(sQ + half * (kBM * 128) + pc * p.box_rows * 128, &map_q, &bars->q_full,
-                      half * 64, head, row0, pol_q);
+        const int h = r0 / p.Rp;
+        if (h >= p.G) continue;
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(sQ + hf * (kBM * 128) + pc * p.box_rows * 128, &map_q, &bars->q_full,
+                      hf * 64, g * p.G + h, r0 % p.Rp, pol_q);
       }
       int issued = 0;
       for (int j = 0; j < my_tiles; ++j) {
         const int st = j % kStages;
-        if (j >= kStages) {
-          if (!wait_or_abort(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars)) {
-            fail_pipeline(bars);
-            break;
-          }
+        if (j >= kStages && !wait_or_abort(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars)) {
+          fail_pipeline(bars);
+          break;
+        }
+        // every CTA starts with the same burst: let Q and the first tile land
+        // before the rest of the ring is requested, so the first S is early
+        if (j == 1 && !(wait_or_abort(&bars->q_full, 0, bars) && wait_or_abort(&bars->kv_full[0], 0, bars))) {
+          fail_pipeline(bars);
+          break;
         }
         unsigned char* stage = sKV + st * kKVStageBytes;
-        ++issued;
         const int key0 = (tile0 + j) * kBN;
         mbar_arrive_expect_tx(&bars->kv_full[st], kKVStageBytes);
         tma_load_3d(stage + 0 * kHalfBytes, &map_k, &bars->kv_full[st], 0, key0, g, pol_kv);
         tma_load_3d(stage + 1 * kHalfBytes, &map_k, &bars->kv_full[st], 64, key0, g, pol_kv);
         tma_load_3d(stage + 2 * kHalfBytes, &map_v, &bars->kv_full[st], 0, key0, g, pol_kv);
         tma_load_3d(stage + 3 * kHalfBytes, &map_v, &bars->kv_full[st], 64, key0, g, pol_kv);
+        ++issued;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
         // let copies already in flight land before the CTA's smem is released
@@ -326,17 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);
       const uint32_t q_addr = smem_u32(sQ);
-      bool ok = wait_or_abort(&bars->q_full, 0, bars);
-      for (int j = 0; ok && j < my_tiles; ++j) {
+      auto issue_qk = [&](int j) -> bool {
         const int st = j % kStages;
-        if (!wait_or_abort(&bars->kv_full[st], (j / kStages) & 1, bars)) {
-          ok = false;
-          break;
-        }
+        if (!wait_or_abort(&bars->kv_full[st], (j / kStages) & 1, bars)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sKV + st * kKVStageBytes);
-        const uint32_t v_addr = k_addr + 2 * kHalfBytes;
-        // S = Q K^T over head_dim 128 = 8 steps of 16
+        const uint32_t tS = tS0 + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
@@ -344,13 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + offk, 16, 1024),
                       idesc_s, kk > 0);
         }
-        mma_commit(&bars->s_full);
-        // wait for P (and the O rescale) from the softmax warps
+        mma_commit(&bars->s_full[j & 1]);
+        return true;
+      };
+      bool good = wait_or_abort(&bars->q_full, 0, bars) && issue_qk(0);
+      for (int j = 0; good && j < my_tiles; ++j) {
+        // S of the next tile goes into the other buffer while tile j's softmax runs;
+        // that buffer was last read by the softmax of tile j-1, which p_ready(j-1) covered
+        if (j + 1 < my_tiles && !issue_qk(j + 1)) {
+          good = false;
+          break;
+        }
         if (!wait_or_abort(&bars->p_ready, j & 1, bars)) {
-          ok = false;
+          good = false;
           break;
         }
         tc_fence_after();
+        const uint32_t v_addr = smem_u32(sKV + (j % kStages) * kKVStageBytes) + 2 * kHalfBytes;
         // O += P V over 128 key slots = 8 steps of 16 (8 bf16-pair columns of P each)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -358,51 +400,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->o_done);
         // only stages the producer will refill need a release
-        if (j + kStages < my_tiles) mma_commit(&bars->kv_empty[st]);
+        if (j + kStages < my_tiles) mma_commit(&bars->kv_empty[j % kStages]);
       }
-      if (!ok) fail_pipeline(bars);
+      if (!good) fail_pipeline(bars);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------ softmax + epilogue
-    const int quarter = warp - 4;  // TMEM lane quarter
-    const int lrow = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int qrow = qt * kBM + lrow;  // index within the kv head's query rows
-    const int hl = qrow / p.Rp;
-    const int prow = qrow % p.Rp;
-    const bool valid = hl < p.G && prow < p.rows;
-    const int head = g * p.G + hl;
+  } else if (is_sm) {
+    // ------------------------------------------------------------ softmax
     uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int w = 0; w < 4; ++w)
       if (valid && w < p.W) anc[w] = p.anc[prow * p.W + w];
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
+    // Every softmax thread reaches both named barriers of every tile; a failed
+    // wait raises the CTA's abort flag, and all threads leave the loop
+    // together right after the first barrier.
     for (int j = 0; j < my_tiles; ++j) {
       const int key0 = (tile0 + j) * kBN;
-      if (!wait_or_abort(&bars->s_full, j & 1, bars)) {
-        ok = false;
-        break;
-      }
-      // s_full(j) was committed after PV(j-1) was issued, so O and the P
-      // columns of tile j-1 are released by now; this wait returns at once
-      if (j > 0 && !wait_or_abort(&bars->o_done, (j - 1) & 1, bars)) {
-        ok = false;
-        break;
-      }
+      // warp-uniform: tcgen05.ld / st below are warp-collective
+      const bool got_s = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[j & 1], (j >> 1) & 1, bars));
+      if (!got_s) fail_pipeline(bars);
       tc_fence_after();
-      const bool full = key0 + kBN <= T;  // all slots of the tile are prefix
-      // this thread's S row: 128 fp32 in registers (four loads, one wait)
-      uint32_t sr[128];
+      const uint32_t tS = tS0 + (j & 1) * 128;
+      // this thread's 64 keys of the S row
+      uint32_t sr[64];
+      if (got_s) {
+        tmem_ld32(tS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-      tmem_ld_wait();
-      if (!full) {
+        for (int e = 0; e < 64; ++e) sr[e] = 0xFF800000u;
+      }
+      if (key0 + kBN > T) {
         // slots >= T: visible only on the row's ancestor list (and < T + rows)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t vm = visible32(anc, key0 + 32 * c - T, p.rows);
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t vm = visible32(anc, key0 + 64 * half + 32 * c - T, p.rows);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             sr[32 * c + e] = ((vm >> e) & 1u) ? sr[32 * c + e] : 0xFF800000u;  // -inf
@@ -410,105 +442,222 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < kBN; e += 4) {
+      for (int e = 0; e < 64; e += 4) {
         mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
         mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
         mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
         mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
       }
       // scale_log2 > 0, so the max commutes with the scaling
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
-      const float m_new = fmaxf(m, mt);
+      const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+      // the other half of the row holds the other 64 keys
+      bars->xch[half][lrow] = pm;
+      const bool seen = *reinterpret_cast<volatile int*>(&bars->abort_flag) != 0;
+      if (named_bar_or(1, 256, seen || !got_s)) {
+        ok = false;
+        break;  // the barrier's OR gives every softmax thread the same answer
+      }
+      const float mt = fmaxf(pm, bars->xch[half ^ 1][lrow]);
+      named_bar(1, 256);  // both halves have read before the array is reused
+      // The running max only moves when some row of the warp grew by more than
+      // 8 (base 2) or had no max yet: a stale max keeps P <= 2^8, cancels
+      // between O and l, and lets most tiles skip the O rescale. The two warps
+      // that hold the halves of these 32 rows see the same (mt, m) per row, so
+      // their votes, and their maxima, agree.
+      const bool grow = __any_sync(0xffffffffu, mt > m + 8.f);
+      const float m_new = grow ? fmaxf(m, mt) : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_use);
-      // P = 2^(s * scale_log2 - m) as bf16 pairs, 16 columns per store
+      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
       const float neg_m = -m_use;
       float ls0 = 0.f, ls1 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sr[32 * c + 2 * e]), p.scale_log2, neg_m));
-          const float p1 = exp2f(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), p.scale_log2, neg_m));
-          ls0 += p0;
-          ls1 += p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tP + lane_off + c * 16, pk);
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, neg_m));
+        ls0 += p0;
+        ls1 += p1;
+        pk[e] = pack_bf16x2(p0, p1);
       }
-      const float ls = ls0 + ls1;
-      // rescale O when the running max grew (O of tile j-1 is final)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // PV(j-1) must be done with P and O before they are rewritten
+      const bool got_o =
+          __all_sync(0xffffffffu, j == 0 || wait_or_abort(&bars->o_done, (j - 1) & 1, bars));
+      if (!got_o) fail_pipeline(bars);
+      tc_fence_after();
+      if (got_o) {
+        tmem_st16(tP + lane_off + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+        tmem_st16(tP + lane_off + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+        // rescale this half's 64 output dims when the running max grew
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + lane_off + c * 32, r);
-          tmem_ld_wait();
-          uint32_t a[16], b[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tO + lane_off + 64 * half + 32 * c;
+            tmem_ld32(ta, r);
+            tmem_ld_wait();
+            uint32_t a[16], b[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
+            for (int e = 0; e < 16; ++e) {
+              a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
+            }
+            tmem_st16(ta, a);
+            tmem_st16(ta + 16, b);
           }
-          tmem_st16(tO + lane_off + c * 32, a);
-          tmem_st16(tO + lane_off + c * 32 + 16, b);
         }
+        tmem_st_wait();
       }
-      tmem_st_wait();
-      l = l * alpha + ls;
+      lh = lh * alpha + (ls0 + ls1);
       m = m_new;
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
     }
-    if (ok && my_tiles > 0) {
-      if (!wait_or_abort(&bars->o_done, (my_tiles - 1) & 1, bars)) ok = false;
-    }
-    if (!ok) fail_pipeline(bars);
+    const bool last_ok = !ok || my_tiles == 0 || wait_or_abort(&bars->o_done, (my_tiles - 1) & 1, bars);
+    if (!last_ok) fail_pipeline(bars);
+    // one answer for all 256 softmax threads: the epilogue's TMEM loads are
+    // warp-collective
+    ok = !named_bar_or(1, 256, !ok || !last_ok);
     tc_fence_after();
-    // epilogue
-    if (ok && my_tiles > 0) {
-      if (p.n_split == 1) {
-        const float inv = 1.f / l;
-        __nv_bfloat16* dst = p.out + (static_cast<size_t>(prow) * p.Hq + head) * kD;
+  }
+
+  // ---------------------------------------------------------------- output
+  // total l of the row = sum of the two halves' partial sums (same max)
+  float l = 0.f;
+  if (is_sm) {
+    bars->xch[half][lrow] = lh;
+    named_bar(1, 256);
+    l = lh + bars->xch[half ^ 1][lrow];
+  }
+  if (p.n_split == 1) {
+    if (is_sm && ok && my_tiles > 0) {
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = p.out + (static_cast<size_t>(prow) * p.Hq + head) * kD + 64 * half;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + lane_off + c * 32, r);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + lane_off + 64 * half + 32 * c, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  } else {
+    // The key splits of one (g, q tile) are co-resident (cooperative launch).
+    // Each CTA writes its unnormalised partial O and (m, l) per row to the
+    // workspace (L2-resident), publishes its arrival on the group counter with
+    // a release add, waits (bounded) until all splits have arrived, then
+    // merges the rows it owns:
+    //   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+    // The last CTA to leave resets the group's counters to zero.
+    const int S = p.n_split;
+    const int grp = blockIdx.x / S;
+    const int rpo = (kBM + S - 1) / S;  // rows per owner
+    const int own0 = split * rpo;
+    const int own_rows = own0 >= kBM ? 0 : (kBM - own0 < rpo ? kBM - own0 : rpo);
+    if (is_sm) {
+      // column-major (dim quad, row): a warp's store covers 32 consecutive rows
+      float4* po = p.part_o + (static_cast<size_t>(grp) * S + split) * 32 * kBM + lrow;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        if (my_tiles > 0 && ok) {
+          tmem_ld32(tO + lane_off + 64 * half + 32 * c, r);
           tmem_ld_wait();
-          if (valid) {
-            uint32_t pk[16];
+        } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        for (int v4 = 0; v4 < 8; ++v4)
+          po[(16 * half + 8 * c + v4) * kBM] =
+              make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                          __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+      }
+      if (half == 0)
+        p.part_ml[(static_cast<size_t>(grp) * S + split) * kBM + lrow] =
+            make_float2(my_tiles > 0 && ok ? m : -INFINITY, l);
+      named_bar(1, 256);  // this CTA's partial is written (CTA scope)
+      if (threadIdx.x == 128) {
+        uint32_t* arrived = p.arrive + grp;
+        atom_add_release_gpu(arrived, 1u);  // cumulative release of the CTA's writes
+        const uint64_t t0 = globaltimer_ns();
+        bool done = false;
+        for (uint32_t i = 0;; ++i) {
+          if (ld_acquire_gpu(arrived) >= static_cast<uint32_t>(S)) {
+            done = true;
+            break;
+          }
+          if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
+        }
+        if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
+        // the last split to leave resets both counters for the next call
+        uint32_t* departed = p.arrive + p.Hkv * p.n_qt + grp;
+        if (atomicAdd(departed, 1u) == static_cast<uint32_t>(S - 1)) {
+          *arrived = 0u;
+          *departed = 0u;
+        }
+      }
+      named_bar(1, 256);  // all splits' partials are visible (acquired above)
+      // this CTA owns tile rows [own0, own0 + own_rows): (row, 8 dims) per
+      // item, rows fastest so that neighbouring threads read neighbouring rows
+      const int t = threadIdx.x - 128;
+      const size_t grp_base = static_cast<size_t>(grp) * S * kBM;
+      for (int item = t; item < own_rows * 16; item += 256) {
+        const int c8 = item / own_rows, rr = item - c8 * own_rows;
+        const int orow = own0 + rr;
+        float2 mlr[kMaxSplit];
+#pragma unroll
+        for (int sx = 0; sx < kMaxSplit; ++sx)
+          mlr[sx] = sx < S ? __ldcg(p.part_ml + grp_base + static_cast<size_t>(sx) * kBM + orow)
+                           : make_float2(-INFINITY, 0.f);
+        float M = -INFINITY;
+#pragma unroll
+        for (int sx = 0; sx < kMaxSplit; ++sx) M = fmaxf(M, mlr[sx].x);
+        float Lt = 0.f, wts[kMaxSplit];
+#pragma unroll
+        for (int sx = 0; sx < kMaxSplit; ++sx) {
+          wts[sx] = mlr[sx].x == -INFINITY ? 0.f : exp2f(mlr[sx].x - M);
+          Lt += wts[sx] * mlr[sx].y;
+        }
+        const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sx = 0; sx < kMaxSplit; ++sx) {
+          if (sx < S && wts[sx] != 0.f) {
+            const float4* src =
+                p.part_o + ((static_cast<size_t>(grp) * S + sx) * 32 + 2 * c8) * kBM + orow;
+            const float4 a = __ldcg(src), b = __ldcg(src + kBM);
+            const float w = wts[sx] * inv;
+            acc[0] += w * a.x;
+            acc[1] += w * a.y;
+            acc[2] += w * a.z;
+            acc[3] += w * a.w;
+            acc[4] += w * b.x;
+            acc[5] += w * b.y;
+            acc[6] += w * b.z;
+            acc[7] += w * b.w;
           }
         }
-      } else {
-        const size_t tile_idx = (static_cast<size_t>(split) * p.Hkv + g) * p.n_qt + qt;
-        float* po = p.part_o + (tile_idx * kBM + lrow) * kD;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + lane_off + c * 32, r);
-          tmem_ld_wait();
-          float4* d4 = reinterpret_cast<float4*>(po + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            d4[v4] = make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                                 __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+        const int oq = qt * kBM + orow;
+        const int ohl = oq / p.Rp, oprow = oq % p.Rp;
+        if (ohl < p.G && oprow < p.rows) {
+          uint4 v;
+          v.x = pack_bf16x2(acc[0], acc[1]);
+          v.y = pack_bf16x2(acc[2], acc[3]);
+          v.z = pack_bf16x2(acc[4], acc[5]);
+          v.w = pack_bf16x2(acc[6], acc[7]);
+          *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(oprow) * p.Hq + g * p.G + ohl) * kD +
+                                    8 * c8) = v;
         }
-        p.part_ml[(tile_idx * kBM + lrow) * 2 + 0] = m;
-        p.part_ml[(tile_idx * kBM + lrow) * 2 + 1] = l;
       }
-    } else if (p.n_split > 1) {
-      // empty split (or failure): a partial that contributes nothing
-      const size_t tile_idx = (static_cast<size_t>(split) * p.Hkv + g) * p.n_qt + qt;
-      p.part_ml[(tile_idx * kBM + lrow) * 2 + 0] = -INFINITY;
-      p.part_ml[(tile_idx * kBM + lrow) * 2 + 1] = 0.f;
     }
   }
   tc_fence_before();
@@ -517,68 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// Merge split partials: one warp per query row, 4 head dims per lane; lane s
-// holds split s's (m, l), so the loads of all splits are issued together.
-__global__ void __launch_bounds__(128) combine_kernel(const Bf16Params p) {
-  const int rows_per_cta = 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int flat = blockIdx.x * rows_per_cta + warp;  // over Hkv * n_qt * 128
-  const int lrow = flat % kBM;
-  const int qt = (flat / kBM) % p.n_qt;
-  const int g = flat / (kBM * p.n_qt);
-  if (g >= p.Hkv) return;
-  const int qrow = qt * kBM + lrow;
-  const int hl = qrow / p.Rp, prow = qrow % p.Rp;
-  if (hl >= p.G || prow >= p.rows) return;
-  const int head = g * p.G + hl;
-  const size_t split_stride = static_cast<size_t>(p.Hkv) * p.n_qt * kBM;
-  const size_t base = (static_cast<size_t>(g) * p.n_qt + qt) * kBM + lrow;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
-  float M = -INFINITY;  // max over all splits
-  for (int s0 = 0; s0 < p.n_split; s0 += 32) {
-    const int s = s0 + lane;
-    const float ms = s < p.n_split ? __ldcg(p.part_ml + (s * split_stride + base) * 2) : -INFINITY;
-    float mm = ms;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    M = fmaxf(M, mm);
-  }
-  for (int s0 = 0; s0 < p.n_split; s0 += 32) {
-    const int s = s0 + lane;
-    float w = 0.f;
-    if (s < p.n_split) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + s * split_stride + base);
-      w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-      L += w * ml.y;
-    }
-    const int cnt = min(32, p.n_split - s0);
-    float4 o[4];
-    for (int i = 0; i < cnt; i += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i + u < cnt)
-          o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + i + u) * split_stride + base) * kD) + lane);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i + u < cnt) {
-          const float wu = __shfl_sync(0xffffffffu, w, i + u);
-          acc.x += wu * o[u].x;
-          acc.y += wu * o[u].y;
-          acc.z += wu * o[u].z;
-          acc.w += wu * o[u].w;
-        }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  const float inv = 1.f / L;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *(reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(prow) * p.Hq + head) * kD) + lane) = pk;
 }
 
 int next_pow2_at_least(int x, int lo) {
@@ -597,16 +684,16 @@ Geometry geometry(int rows, int Hq, int Hkv) {
   gm.Rp = next_pow2_at_least(rows, 32);
   gm.box_rows = gm.Rp < kBM ? gm.Rp : kBM;
   gm.n_qt = (gm.G * gm.Rp + kBM - 1) / kBM;
-  int s = glance::num_sms() / (Hkv * gm.n_qt);
-  gm.n_split = s < 1 ? 1 : (s > 64 ? 64 : s);
+  // one CTA per SM and every CTA resident at once (cooperative launch)
+  int sp = glance::num_sms() / (Hkv * gm.n_qt);
+  gm.n_split = sp < 1 ? 1 : (sp > kMaxSplit ? kMaxSplit : sp);
   return gm;
 }
 
-size_t bf16_ws_bytes(int rows, int Hq, int Hkv) {
-  const Geometry gm = geometry(rows, Hq, Hkv);
+size_t bf16_ws_bytes(const Geometry& gm, int Hkv) {
   if (gm.n_split == 1) return 256;
-  const size_t tiles = static_cast<size_t>(gm.n_split) * Hkv * gm.n_qt;
-  return (tiles * kBM * kD * sizeof(float) + 255) / 256 * 256 + tiles * kBM * 2 * sizeof(float) + 256;
+  const size_t slots = static_cast<size_t>(Hkv) * gm.n_qt * gm.n_split * kBM;
+  return 256 + slots * kD * sizeof(float) + slots * sizeof(float2);
 }
 
 glance_status check_common(const void* q, int n_q_heads, const glance_kv* kv,
@@ -636,8 +723,8 @@ extern "C" size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_head
   if (!kv || n_rows < 1 || n_rows > 256 || kv->n_kv_heads < 1 || n_q_heads < 1 ||
       n_q_heads % kv->n_kv_heads)
     return 0;
-  if (kv->dtype == GLANCE_F32) return 256;
-  return bf16_ws_bytes(n_rows, n_q_heads, kv->n_kv_heads);
+  if (kv->dtype != GLANCE_BF16) return 256;
+  return bf16_ws_bytes(geometry(n_rows, n_q_heads, kv->n_kv_heads), kv->n_kv_heads);
 }
 
 extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, const glance_kv* kv,
@@ -688,14 +775,16 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
                 "glance_tree_attention: q/k/v/out must be 16-byte aligned with 16-byte strides");
   if (kv->t_cap > (1 << 30))
     return fail(GLANCE_ERR_UNSUPPORTED, "glance_tree_attention: t_cap too large");
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(tree_attention_bf16_kernel),
+                                      static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: smem attribute");
   const Geometry gm = geometry(rows, n_q_heads, kv->n_kv_heads);
-  const size_t need = bf16_ws_bytes(rows, n_q_heads, kv->n_kv_heads);
+  const size_t need = bf16_ws_bytes(gm, kv->n_kv_heads);
   if (!workspace || workspace_bytes < need)
     return fail(GLANCE_ERR_CAPACITY, "glance_tree_attention: workspace %zu bytes < %zu needed",
                 workspace_bytes, need);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return fail(GLANCE_ERR_INVALID_ARG, "glance_tree_attention: workspace must be 256-byte aligned");
-
   CUtensorMap mq, mk, mv;
   {
     const uint64_t dims[3] = {kD, static_cast<uint64_t>(n_q_heads), static_cast<uint64_t>(rows)};
@@ -722,10 +811,14 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
   p.anc = tree->anc;
   p.t_len = kv->t_len;
   p.out = static_cast<__nv_bfloat16*>(out);
-  const size_t tiles = static_cast<size_t>(gm.n_split) * kv->n_kv_heads * gm.n_qt;
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       (tiles * kBM * kD * sizeof(float) + 255) / 256 * 256);
+  {
+    // [256 B counters][partial O][partial (m, l)]
+    const size_t slots = static_cast<size_t>(kv->n_kv_heads) * gm.n_qt * gm.n_split * kBM;
+    char* ws = static_cast<char*>(workspace);
+    p.arrive = reinterpret_cast<uint32_t*>(ws);
+    p.part_o = reinterpret_cast<float4*>(ws + 256);
+    p.part_ml = reinterpret_cast<float2*>(ws + 256 + slots * kD * sizeof(float));
+  }
   p.rows = rows;
   p.Hq = n_q_heads;
   p.Hkv = kv->n_kv_heads;
@@ -737,17 +830,22 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
   p.t_cap = kv->t_cap;
   p.box_rows = gm.box_rows;
   p.scale_log2 = scale * kLog2e;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(tree_attention_bf16_kernel), static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: smem attribute");
-  const int grid = kv->n_kv_heads * gm.n_qt * gm.n_split;
-  tree_attention_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kv->n_kv_heads * gm.n_qt * gm.n_split);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  // the key splits of a group wait for each other: every CTA must be resident
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  // may start while the previous kernel in the stream finishes (the kernel
+  // waits for it with griddepcontrol.wait before reading its inputs)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, tree_attention_bf16_kernel, mq, mk, mv, p);
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: launch");
-  if (gm.n_split > 1) {
-    const int total_rows = kv->n_kv_heads * gm.n_qt * kBM;
-    combine_kernel<<<(total_rows + 3) / 4, 128, 0, s>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: combine launch");
-  }
   return GLANCE_OK;
 }
