@@ -56,12 +56,16 @@ struct BuildParams {
 constexpr int kBuckets = 2048;      // first-pass buckets of the gap to the max
 constexpr float kBucketsPerNat = 64.f;
 
+constexpr int kBoundary = 512;  // boundary-bucket items resolved by counting
+
 struct SelectSmem {
   uint32_t hist[kBuckets];
   uint32_t warp_tot[kThreads / 32];
   int bstar;
   uint32_t above, cnt;
   uint32_t digit, above2, cnt2;
+  uint32_t nb;
+  unsigned long long bnd[kBoundary];
 };
 
 __device__ __forceinline__ float inv_ord_key(uint32_t k) {
@@ -100,11 +104,17 @@ __device__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
 // Selects the `want` best items (by unique 64-bit key) of kPerThread items per
 // thread and writes their keys, in any order, to out[0..want). item(e, v, x, k)
 // gives item e's validity, logit and key; m is the maximum valid logit.
+// Pass 1 histograms the gap to m in 1/64-nat buckets; the buckets above the
+// boundary bucket are taken whole in pass 2, which also collects the boundary
+// bucket's items; those (normally a handful) are ranked by counting. Only a
+// boundary bucket of more than kBoundary items (massive exact ties) falls back
+// to a radix select over the items.
 template <typename Item>
 __device__ void select_top(Item item, uint32_t want, float m, unsigned long long* out,
                            SelectSmem& sm) {
   if (want == 0) return;  // uniform across the block
   for (int i = threadIdx.x; i < kBuckets; i += kThreads) sm.hist[i] = 0;
+  if (threadIdx.x == 0) sm.nb = 0;
   __syncthreads();
 #pragma unroll
   for (int e = 0; e < kPerThread; ++e) {
@@ -136,64 +146,100 @@ __device__ void select_top(Item item, uint32_t want, float m, unsigned long long
   }
   __syncthreads();
   const int bstar = sm.bstar;
-  const uint32_t need = want - sm.above;
+  const uint32_t above = sm.above;
+  const uint32_t need = want - above;
   const bool whole = sm.cnt == need;
-  // inside the boundary bucket: radix select on the full keys
-  unsigned long long prefix = 0, mask = 0;
-  if (!whole) {
-    uint32_t krem = need;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      sm.hist[threadIdx.x] = 0;
-      __syncthreads();
+  const bool small = sm.cnt <= static_cast<uint32_t>(kBoundary);
+  // pass 2: buckets above the boundary (and the boundary when it is taken
+  // whole) go straight to out; boundary items go to the shared list
+  uint32_t c1 = 0;
 #pragma unroll
-      for (int e = 0; e < kPerThread; ++e) {
-        bool v;
-        float x;
-        unsigned long long k;
-        item(e, v, x, k);
-        if (v && bucket_of(m, x) == bstar && (k & mask) == prefix)
-          atomicAdd(&sm.hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      // thread t holds digit d = 255 - t; the scan gives the count of digits >= d
-      const uint32_t d = 255u - threadIdx.x;
-      const uint32_t hv = sm.hist[d];
-      const uint32_t in2 = block_incl_scan(hv, sm.warp_tot);
-      const uint32_t ex2 = in2 - hv;
-      if (ex2 < krem && in2 >= krem) {
-        sm.digit = d;
-        sm.above2 = ex2;
-        sm.cnt2 = hv;
-      }
-      __syncthreads();
-      prefix |= static_cast<unsigned long long>(sm.digit) << shift;
-      mask |= 0xFFull << shift;
-      krem -= sm.above2;
-      const bool done = sm.cnt2 == krem;
-      __syncthreads();
-      if (done) break;
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    const int b = v ? bucket_of(m, x) : kBuckets;
+    c1 += (b < bstar || (whole && b == bstar));
+  }
+  uint32_t pos = block_incl_scan(c1, sm.warp_tot) - c1;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    const int b = v ? bucket_of(m, x) : kBuckets;
+    if (b < bstar || (whole && b == bstar)) {
+      out[pos++] = k;
+    } else if (b == bstar && small) {
+      sm.bnd[atomicAdd(&sm.nb, 1u)] = k;
     }
   }
-  // compaction
-  uint32_t cntl = 0;
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    bool v;
-    float x;
-    unsigned long long k;
-    item(e, v, x, k);
-    const int b = v ? bucket_of(m, x) : kBuckets;
-    cntl += v && (b < bstar || (b == bstar && (whole || (k & mask) >= prefix)));
+  if (whole) return;  // uniform: `whole` is read from shared memory
+  __syncthreads();
+  if (small) {
+    // rank of each boundary item among the boundary items (unique keys)
+    const uint32_t nb = sm.nb;
+    for (uint32_t i = threadIdx.x; i < nb; i += kThreads) {
+      const unsigned long long k = sm.bnd[i];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < nb; ++j) rank += sm.bnd[j] > k;
+      if (rank < need) out[above + rank] = k;
+    }
+    return;
   }
-  uint32_t pos = block_incl_scan(cntl, sm.warp_tot) - cntl;
-#pragma unroll
+  // fallback: radix select on the full keys inside the boundary bucket
+  unsigned long long prefix = 0, mask = 0;
+  uint32_t krem = need;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    sm.hist[threadIdx.x] = 0;
+    __syncthreads();
+#pragma unroll 2
+    for (int e = 0; e < kPerThread; ++e) {
+      bool v;
+      float x;
+      unsigned long long k;
+      item(e, v, x, k);
+      if (v && bucket_of(m, x) == bstar && (k & mask) == prefix)
+        atomicAdd(&sm.hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    // thread t holds digit d = 255 - t; the scan gives the count of digits >= d
+    const uint32_t d = 255u - threadIdx.x;
+    const uint32_t hv = sm.hist[d];
+    const uint32_t in2 = block_incl_scan(hv, sm.warp_tot);
+    const uint32_t ex2 = in2 - hv;
+    if (ex2 < krem && in2 >= krem) {
+      sm.digit = d;
+      sm.above2 = ex2;
+      sm.cnt2 = hv;
+    }
+    __syncthreads();
+    prefix |= static_cast<unsigned long long>(sm.digit) << shift;
+    mask |= 0xFFull << shift;
+    krem -= sm.above2;
+    const bool done = sm.cnt2 == krem;
+    __syncthreads();
+    if (done) break;
+  }
+  uint32_t c2 = 0;
+#pragma unroll 2
   for (int e = 0; e < kPerThread; ++e) {
     bool v;
     float x;
     unsigned long long k;
     item(e, v, x, k);
-    const int b = v ? bucket_of(m, x) : kBuckets;
-    if (v && (b < bstar || (b == bstar && (whole || (k & mask) >= prefix)))) out[pos++] = k;
+    c2 += v && bucket_of(m, x) == bstar && (k & mask) >= prefix;
+  }
+  uint32_t pos2 = above + block_incl_scan(c2, sm.warp_tot) - c2;
+#pragma unroll 2
+  for (int e = 0; e < kPerThread; ++e) {
+    bool v;
+    float x;
+    unsigned long long k;
+    item(e, v, x, k);
+    if (v && bucket_of(m, x) == bstar && (k & mask) >= prefix) out[pos2++] = k;
   }
 }
 
@@ -222,18 +268,18 @@ __device__ __forceinline__ bool tie_less(uint32_t da, unsigned long long ha, uns
   return la < lb;
 }
 
+// One popped node: 32 bytes, written with two 16-byte stores.
+struct __align__(16) PopRec {
+  float score;   // log plug-in score
+  float pscore;  // parent's score (0 at depth 1)
+  int dep;       // depth
+  int par;       // parent's pop index, -1 at depth 1
+  unsigned long long hi, lo;  // rank bytes of the path
+};
+
 struct TreeSmem {
-  // frontier slots (slot s is owned by lane s % 32)
-  float f_score[256], f_pscore[256];
-  unsigned long long f_hi[256], f_lo[256];
-  int16_t f_par[256];
-  uint8_t f_dep[256];
-  // popped nodes, in pop order
-  float p_score[kMaxN];
-  unsigned long long p_hi[kMaxN], p_lo[kMaxN];
-  int16_t p_parent[kMaxN];
+  PopRec pop[kMaxN];
   int16_t p_pos[kMaxN];
-  uint8_t p_dep[kMaxN];
 };
 
 __device__ __forceinline__ void set_reg(uint32_t (&a)[kSlotsPerLane], int i, uint32_t v) {
@@ -241,12 +287,22 @@ __device__ __forceinline__ void set_reg(uint32_t (&a)[kSlotsPerLane], int i, uin
   for (int t = 0; t < kSlotsPerLane; ++t)
     if (t == i) a[t] = v;
 }
+__device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlotsPerLane], int i) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int t = 0; t < kSlotsPerLane; ++t)
+    if (t == i) v = a[t];
+  return v;
+}
+
+constexpr uint32_t kRootChild = 0xFFFFu;  // code of the first node (rank 0 at offset 1)
 
 __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
   float* s_logq = reinterpret_cast<float*>(dyn);
   int* s_tok = reinterpret_cast<int*>(dyn + sizeof(float) * p.L * p.K);
-  TreeSmem& ts = *reinterpret_cast<TreeSmem*>(dyn + 8 * ((sizeof(float) * 2 * p.L * p.K + 7) / 8));
+  TreeSmem& ts = *reinterpret_cast<TreeSmem*>(
+      dyn + 16 * ((sizeof(float) * 2 * p.L * p.K + 15) / 16));
   const int LK = p.L * p.K;
   for (int i = threadIdx.x; i < LK; i += kThreads) {
     s_logq[i] = __ldcg(p.top_logq + i);
@@ -256,20 +312,21 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   const int N = p.N, L = p.L, K = p.K;
 
   if (threadIdx.x < 32) {
+    // Lane-owned frontier slots (slot s = lane + 32 i): a 32-bit score key
+    // (0 = empty) and a code: (k << 1) = first child of pop k, (k << 1) | 1 =
+    // next sibling of pop k. A node's path, depth, parent and parent score
+    // follow from pop k's record, so a slot carries no other data.
     const int lane = threadIdx.x;
-    uint32_t ko[kSlotsPerLane];  // score keys of this lane's slots; 0 = empty
+    uint32_t ko[kSlotsPerLane], kc[kSlotsPerLane];
 #pragma unroll
-    for (int i = 0; i < kSlotsPerLane; ++i) ko[i] = 0;
-    if (lane == 0) {  // first frontier entry: rank 0 at offset 1
-      ts.f_score[0] = s_logq[0];
-      ts.f_pscore[0] = 0.f;
-      ts.f_hi[0] = 0ull;
-      ts.f_lo[0] = 0ull;
-      ts.f_par[0] = -1;
-      ts.f_dep[0] = 1;
-      ko[0] = ord_key(s_logq[0]);
+    for (int i = 0; i < kSlotsPerLane; ++i) {
+      ko[i] = 0;
+      kc[i] = 0;
     }
-    __syncwarp();
+    if (lane == 0) {
+      ko[0] = ord_key(s_logq[0]);
+      kc[0] = kRootChild;
+    }
     int cnt = 1;
     for (int k = 0; k < N; ++k) {
       uint32_t bo = 0;
@@ -293,87 +350,107 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
       }
       const unsigned cand = __ballot_sync(0xffffffffu, bo == mmax);
       const bool slow = __popc(cand) > 1 || __ballot_sync(0xffffffffu, bo == mmax && dup) != 0;
-      int ws;
+      int ws;       // winning slot
+      uint32_t wc;  // its code
+      // node data of a code (all lanes compute it for the same code)
+      auto node_of = [&](uint32_t code, uint32_t key, PopRec& nd) {
+        if (code == kRootChild) {
+          nd.score = s_logq[0];
+          nd.pscore = 0.f;
+          nd.dep = 1;
+          nd.par = -1;
+          nd.hi = nd.lo = 0ull;
+          return;
+        }
+        const PopRec g = ts.pop[code >> 1];
+        nd.score = __uint_as_float(key);  // placeholder, replaced by the caller
+        if ((code & 1u) == 0) {  // first child: rank 0 appended (a zero byte)
+          nd.pscore = g.score;
+          nd.dep = g.dep + 1;
+          nd.par = static_cast<int>(code >> 1);
+          nd.hi = g.hi;
+          nd.lo = g.lo;
+        } else {  // next sibling: the last rank + 1
+          nd.pscore = g.pscore;
+          nd.dep = g.dep;
+          nd.par = g.par;
+          nd.hi = g.hi;
+          nd.lo = g.lo;
+          set_rank(nd.hi, nd.lo, g.dep - 1, get_rank(g.hi, g.lo, g.dep - 1) + 1);
+        }
+      };
       if (!slow) {
-        ws = __shfl_sync(0xffffffffu, bi * 32 + lane, __ffs(cand) - 1);
+        const int win = __ffs(cand) - 1;
+        ws = __shfl_sync(0xffffffffu, bi * 32 + lane, win);
+        wc = __shfl_sync(0xffffffffu, get_reg(kc, bi), win);
       } else {
         // exact score tie: least (depth, rank vector) among slots with key mmax
         int my = -1;
-        uint32_t md = 0;
+        uint32_t mc = 0, md = 0;
         unsigned long long mh = 0, ml = 0;
 #pragma unroll
         for (int i = 0; i < kSlotsPerLane; ++i) {
           if (ko[i] == mmax) {
-            const int sl = i * 32 + lane;
-            const uint32_t d = ts.f_dep[sl];
-            const unsigned long long h = ts.f_hi[sl], l = ts.f_lo[sl];
-            if (my < 0 || tie_less(d, h, l, md, mh, ml)) {
-              my = sl;
-              md = d;
-              mh = h;
-              ml = l;
+            PopRec nd;
+            node_of(kc[i], ko[i], nd);
+            if (my < 0 || tie_less(nd.dep, nd.hi, nd.lo, md, mh, ml)) {
+              my = i * 32 + lane;
+              mc = kc[i];
+              md = nd.dep;
+              mh = nd.hi;
+              ml = nd.lo;
             }
           }
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
           const int oy = __shfl_xor_sync(0xffffffffu, my, o);
+          const uint32_t oc = __shfl_xor_sync(0xffffffffu, mc, o);
           const uint32_t od = __shfl_xor_sync(0xffffffffu, md, o);
           const unsigned long long oh = __shfl_xor_sync(0xffffffffu, mh, o);
           const unsigned long long ol = __shfl_xor_sync(0xffffffffu, ml, o);
           if (oy >= 0 && (my < 0 || tie_less(od, oh, ol, md, mh, ml))) {
             my = oy;
+            mc = oc;
             md = od;
             mh = oh;
             ml = ol;
           }
         }
         ws = my;
+        wc = mc;
       }
-      const uint32_t d = ts.f_dep[ws];
-      const unsigned long long hi = ts.f_hi[ws], lo = ts.f_lo[ws];
-      const int par = ts.f_par[ws];
-      const float pscore = ts.f_pscore[ws];
-      const float score = ts.f_score[ws];
-      const uint32_t r = get_rank(hi, lo, d - 1);
+      PopRec nd;
+      node_of(wc, mmax, nd);
+      nd.score = inv_ord_key(mmax);
+      const uint32_t d = static_cast<uint32_t>(nd.dep);
+      const uint32_t r = get_rank(nd.hi, nd.lo, d - 1);
       const bool has_child = static_cast<int>(d) < L;
       const bool has_sib = static_cast<int>(r) + 1 < K;
       // successors: first child (rank 0 at offset d+1), next sibling (rank r+1)
-      const float c_score = has_child ? score + s_logq[d * K] : 0.f;
-      const float s_score = has_sib ? pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
-      const int ns = cnt;
+      const float c_score = has_child ? nd.score + s_logq[d * K] : 0.f;
+      const float s_score = has_sib ? nd.pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
       if (lane == 0) {
-        ts.p_score[k] = score;
-        ts.p_hi[k] = hi;
-        ts.p_lo[k] = lo;
-        ts.p_parent[k] = static_cast<int16_t>(par);
-        ts.p_dep[k] = static_cast<uint8_t>(d);
-        unsigned long long ch = hi, cl = lo, sh = hi, sl = lo;
-        set_rank(ch, cl, d, 0);
-        set_rank(sh, sl, d - 1, r + 1);
-        if (has_child) {
-          ts.f_score[ws] = c_score;
-          ts.f_pscore[ws] = score;
-          ts.f_hi[ws] = ch;
-          ts.f_lo[ws] = cl;
-          ts.f_par[ws] = static_cast<int16_t>(k);
-          ts.f_dep[ws] = static_cast<uint8_t>(d + 1);
-        }
-        const int sslot = has_child ? ns : ws;
-        if (has_sib) {
-          ts.f_score[sslot] = s_score;
-          ts.f_pscore[sslot] = pscore;
-          ts.f_hi[sslot] = sh;
-          ts.f_lo[sslot] = sl;
-          ts.f_par[sslot] = static_cast<int16_t>(par);
-          ts.f_dep[sslot] = static_cast<uint8_t>(d);
-        }
+        uint4* dst = reinterpret_cast<uint4*>(&ts.pop[k]);
+        dst[0] = make_uint4(__float_as_uint(nd.score), __float_as_uint(nd.pscore),
+                            static_cast<uint32_t>(nd.dep), static_cast<uint32_t>(nd.par));
+        dst[1] = make_uint4(static_cast<uint32_t>(nd.hi), static_cast<uint32_t>(nd.hi >> 32),
+                            static_cast<uint32_t>(nd.lo), static_cast<uint32_t>(nd.lo >> 32));
       }
+      // the popped slot takes the child (else the sibling); a new slot takes
+      // the sibling when both exist
       const uint32_t k_ws = has_child ? ord_key(c_score) : (has_sib ? ord_key(s_score) : 0u);
-      if (lane == (ws & 31)) set_reg(ko, ws >> 5, k_ws);
+      const uint32_t c_ws = (static_cast<uint32_t>(k) << 1) | (has_child ? 0u : 1u);
+      if (lane == (ws & 31)) {
+        set_reg(ko, ws >> 5, k_ws);
+        set_reg(kc, ws >> 5, c_ws);
+      }
       if (has_child && has_sib) {
-        if (lane == (ns & 31)) set_reg(ko, ns >> 5, ord_key(s_score));
-        ++cnt;
+        const int ns = cnt++;
+        if (lane == (ns & 31)) {
+          set_reg(ko, ns >> 5, ord_key(s_score));
+          set_reg(kc, ns >> 5, (static_cast<uint32_t>(k) << 1) | 1u);
+        }
       }
       __syncwarp();
     }
@@ -384,11 +461,12 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   const int T = *p.t_len;
   const int W = p.tree.mask_words;
   for (int kk = threadIdx.x; kk < N; kk += kThreads) {
-    const uint32_t dk = ts.p_dep[kk];
-    const unsigned long long hk = ts.p_hi[kk], lk = ts.p_lo[kk];
+    const uint32_t dk = ts.pop[kk].dep;
+    const unsigned long long hk = ts.pop[kk].hi, lk = ts.pop[kk].lo;
     int pos = 1;
 #pragma unroll 4
-    for (int j = 0; j < N; ++j) pos += tie_less(ts.p_dep[j], ts.p_hi[j], ts.p_lo[j], dk, hk, lk);
+    for (int j = 0; j < N; ++j)
+      pos += tie_less(ts.pop[j].dep, ts.pop[j].hi, ts.pop[j].lo, dk, hk, lk);
     ts.p_pos[kk] = static_cast<int16_t>(pos);
   }
   __syncthreads();
@@ -403,17 +481,17 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
       continue;
     }
     const int row = ts.p_pos[kk];
-    const int d = ts.p_dep[kk];
-    const uint32_t r = get_rank(ts.p_hi[kk], ts.p_lo[kk], d - 1);
-    const int par = ts.p_parent[kk];
+    const int d = ts.pop[kk].dep;
+    const uint32_t r = get_rank(ts.pop[kk].hi, ts.pop[kk].lo, d - 1);
+    const int par = ts.pop[kk].par;
     p.tree.token[row] = s_tok[(d - 1) * K + r];
     p.tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
     p.tree.depth[row] = d;
     p.tree.pos_id[row] = T + d;
-    p.tree.score[row] = ts.p_score[kk];
+    p.tree.score[row] = ts.pop[kk].score;
     unsigned long long words[4] = {1ull, 0ull, 0ull, 0ull};
     words[row >> 6] |= 1ull << (row & 63);
-    for (int u = par; u >= 0; u = ts.p_parent[u]) {
+    for (int u = par; u >= 0; u = ts.pop[u].par) {
       const int pr = ts.p_pos[u];
       words[pr >> 6] |= 1ull << (pr & 63);
     }
@@ -513,14 +591,19 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildPara
   for (int o = 16; o; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
   if (lane == 0) red_d[warp] = sd;
 
-  // ---- chunk top-K
+  // ---- chunk top-K. The logits move to shared memory (item e of thread t at
+  // e * 256 + t, conflict-free) so the selection passes re-read them instead
+  // of holding 32 values, keys and buckets live in registers.
+  float* xs = reinterpret_cast<float*>(dyn);
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) xs[e * kThreads + threadIdx.x] = x[e];
   const int kc = min(p.K, n_valid);
   unsigned long long* my_cand = p.cand + (static_cast<size_t>(row) * p.C + chunk) * p.K;
   select_top(
       [&](int e, bool& v, float& xv, unsigned long long& k) {
         v = valid_of(e);
-        xv = x[e];
-        k = make_key(x[e], static_cast<uint32_t>(id_of(e)));
+        xv = xs[e * kThreads + threadIdx.x];
+        k = make_key(xv, static_cast<uint32_t>(id_of(e)));
       },
       static_cast<uint32_t>(kc), m, my_cand, sm);
   if (threadIdx.x == 0) {
@@ -555,23 +638,17 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildPara
       red_f[0] = static_cast<float>(M);
     }
   }
-  // candidates: flat index f = c * K + i, valid when i < min(K, chunk size)
-  unsigned long long keys[kPerThread];
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int f = threadIdx.x + kThreads * e;
-    const int c = f / p.K, i = f - c * p.K;
-    keys[e] = 0ull;
-    if (c < p.C) {
-      const int kc_c = min(p.K, min(kChunk, p.V - c * kChunk));
-      if (i < kc_c) keys[e] = __ldcg(p.cand + (static_cast<size_t>(row) * p.C + c) * p.K + i);
-    }
-  }
   __syncthreads();
   const float row_max = red_f[0];
+  // candidates (read from L2 on each pass): flat index f = c * K + i, valid
+  // when i < min(K, chunk size)
+  const unsigned long long* row_cand = p.cand + static_cast<size_t>(row) * p.C * p.K;
   select_top(
       [&](int e, bool& v, float& xv, unsigned long long& k) {
-        k = keys[e];
+        const int f = threadIdx.x + kThreads * e;
+        const int c = f / p.K, i = f - c * p.K;
+        k = 0ull;
+        if (c < p.C && i < min(p.K, min(kChunk, p.V - c * kChunk))) k = __ldcg(row_cand + f);
         v = k != 0ull;
         xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
       },
@@ -699,7 +776,9 @@ extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtyp
   p.top_tok = reinterpret_cast<int32_t*>(ws + w.top_tok);
   p.top_logq = reinterpret_cast<float*>(ws + w.top_logq);
 
-  const size_t dyn = 8 * ((sizeof(float) * 2 * L * p.K + 7) / 8) + sizeof(TreeSmem);
+  // dynamic smem: the chunk's logits during selection, the tree search after
+  size_t dyn = 16 * ((sizeof(float) * 2 * L * p.K + 15) / 16) + sizeof(TreeSmem);
+  if (dyn < sizeof(float) * kChunk) dyn = sizeof(float) * kChunk;
   const bool vec = p.is_bf16 ? (V % 4 == 0 && glance::aligned16(draft_logits))
                              : (V % 4 == 0 && glance::aligned16(draft_logits));
   void (*kern)(const BuildParams);

@@ -335,12 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail_pipeline(bars);
           break;
         }
-        // every CTA starts with the same burst: let Q and the first tile land
-        // before the rest of the ring is requested, so the first S is early
-        if (j == 1 && !(wait_or_abort(&bars->q_full, 0, bars) && wait_or_abort(&bars->kv_full[0], 0, bars))) {
-          fail_pipeline(bars);
-          break;
-        }
         unsigned char* stage = sKV + st * kKVStageBytes;
         const int key0 = (tile0 + j) * kBN;
         mbar_arrive_expect_tx(&bars->kv_full[st], kKVStageBytes);
