@@ -43,6 +43,47 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the full36 workload. A figure holds only for the kernel
+# sources it was taken on: `digest` is the first 16 hex digits of the sha256 of
+# the listed files, and a changed source reports traffic null.
+CSRC = os.path.join("tree_verified_block_gb300", "csrc")
+NCU_TRAFFIC = {
+    "glance_tree_attention": dict(bytes=17_889_792, digest="8673c360cd2cd1fc",
+                                  files=["tree_attention.cu", "glance_internal.cuh"],
+                                  profile="profiles/tree_attention_full36.md"),
+    "glance_lmhead_argmax": dict(bytes=1_245_328_000 + 2_759_424, digest="25ca914779b9aa6c",
+                                 files=["lmhead.cu", "glance_internal.cuh"],
+                                 profile="profiles/lmhead_argmax_full36.md"),
+}
+
+
+def source_digest(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    e = NCU_TRAFFIC.get(kernel)
+    if e is None or source_digest(e["files"]) != e["digest"]:
+        return None
+    return e["bytes"]
+
+
+def workload_config(cfg, world=1):
+    return {"workload": f"{cfg['name']}: Qwen3-VL-8B verify round, T={cfg['T']}, N={cfg['N']}, "
+                        f"L={cfg['L']}, V={cfg['V']}, d={cfg['d']}, {cfg['n_layers']} layers, "
+                        f"{cfg['Hq']}/{cfg['Hkv']} heads x {cfg['D']}",
+            "T": cfg["T"], "N": cfg["N"], "L": cfg["L"], "V": cfg["V"], "d": cfg["d"],
+            "n_layers": cfg["n_layers"], "parallelism": f"replicas x{world}",
+            "l2": "no flush: each step streams ~1.9 GB of distinct inputs (> 129 MB L2)",
+            "cuda_graph": True}
+
+
 # ------------------------------------------------------------------ workload
 
 class Workload:
@@ -139,10 +180,9 @@ class Workload:
                         self.new_root, self.ws_c)
 
     def launches_per_step(self):
-        split = self.g.tree_attention_workspace_bytes(self.R, self.cfg["Hq"], self.layers[0]) > 256
-        attn = self.cfg["n_layers"] * (2 if split else 1)
-        lm = (self.R + 127) // 128
-        return 1 + attn + lm + 1
+        # one launch per ABI call: build_tree, tree_attention per layer,
+        # lmhead_argmax, accept_commit (the t_len reset is a torch copy)
+        return 1 + self.cfg["n_layers"] + 1 + 1
 
     def algorithmic_bytes(self):
         c = self.cfg
@@ -160,20 +200,75 @@ class Workload:
 
 # ------------------------------------------------------------------ clocks
 
+class _NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries), for the device torch calls `dev`; matched by PCI bus id."""
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+            0x4: "sw_power_cap"}
+
+    def __init__(self, dev):
+        import ctypes
+        import torch
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        pr = torch.cuda.get_device_properties(dev)
+        bus = getattr(pr, "pci_bus_id", None)
+        ok = -1
+        if bus is not None:
+            bid = f"{getattr(pr, 'pci_domain_id', 0):08x}:{bus:02x}:{getattr(pr, 'pci_device_id', 0):02x}.0"
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bid.encode(), ctypes.byref(self.h))
+        if ok != 0:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev.index or 0), ctypes.byref(self.h))
+        if ok != 0:
+            raise RuntimeError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+
+    def sample(self):
+        c = self.c
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn(self.h, c.byref(rs)) != 0:
+            rs.value = 0
+        return float(mhz.value), [n for b, n in self.BITS.items() if rs.value & b]
+
+
 class ClockSampler:
+    """SM clocks and throttle reasons sampled during the timed region: NVML
+    every 5 ms from a host thread, else `nvidia-smi -lms 200`."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
+    def __init__(self, dev):
+        self.dev = dev
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []
+        self.stop = threading.Event()
 
     def __enter__(self):
         try:
+            self.nvml = _NvmlClocks(self.dev)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.dev.index or 0), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -183,11 +278,21 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            s = self.nvml.sample()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(0.005)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.nvml is not None:
+            self.thread.join(timeout=2)
         if self.proc:
             self.proc.terminate()
             try:
@@ -197,21 +302,28 @@ class ClockSampler:
 
     def summary(self):
         sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+        if self.nvml is not None:
+            for mhz, rs in self.samples:
+                sm.append(mhz)
+                reasons.update(rs)
+            mx = self.nvml.max_mhz
+            src = "nvml 5 ms"
+        else:
+            for ln in self.lines:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(self.NAMES, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            src = "nvidia-smi 200 ms"
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "sampler": src}
 
 
 # ------------------------------------------------------------------ timing
@@ -308,7 +420,7 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev) as clk:
         start.record(stream)
         for _ in range(args.steps):
             graph.replay()
@@ -326,18 +438,19 @@ def run_gpu(args):
     pk = peaks()
     attn_total = st["attention_36"]
     dominant = "lmhead" if st["lmhead"] >= attn_total else "attention"
+    kernel = "glance_lmhead_argmax" if dominant == "lmhead" else "glance_tree_attention"
     if dominant == "lmhead":
         dur = st["lmhead"]
         achieved = bytes_["lmhead"] / (dur * 1e-6) / 1e9
-        traffic = None
     else:
         dur = st["attention_layer"]
         achieved = bytes_["attn_layer"] / (dur * 1e-6) / 1e9
-        traffic = None
-    roofline = {"bound": "hbm", "kernel": "glance_lmhead_argmax" if dominant == "lmhead" else "glance_tree_attention",
+    roofline = {"bound": "hbm", "kernel": kernel,
                 "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm"], 4), "traffic": traffic,
-                "peak_source": pk["src"], "launch_us": round(dur, 2)}
+                "frac": round(achieved / pk["hbm"], 4), "traffic": profiled_traffic(kernel),
+                "algorithmic_bytes": bytes_["lmhead" if dominant == "lmhead" else "attn_layer"],
+                "peak_source": pk["src"] + " copy (burst; the kernel is timed alone)",
+                "launch_us": round(dur, 2)}
     lm_tflops = wl.flops()["lmhead"] / (st["lmhead"] * 1e-6) / 1e12
     stages = {k: round(v, 2) for k, v in st.items()}
     stages["lmhead_tensor_tflops"] = round(lm_tflops, 1)
@@ -353,13 +466,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{cfg['name']}: Qwen3-VL-8B verify round, T={cfg['T']}, N={cfg['N']}, "
-                               f"L={cfg['L']}, V={cfg['V']}, d={cfg['d']}, {cfg['n_layers']} layers, "
-                               f"{cfg['Hq']}/{cfg['Hkv']} heads x {cfg['D']}",
-                   "T": cfg["T"], "N": cfg["N"], "L": cfg["L"], "V": cfg["V"], "d": cfg["d"],
-                   "n_layers": cfg["n_layers"], "parallelism": f"replicas x{world}",
-                   "l2": "no flush: each step streams ~1.9 GB of distinct inputs (> 129 MB L2)",
-                   "cuda_graph": True},
+        "config": workload_config(cfg, world),
         "roofline": roofline,
         "stages_us": stages,
         "e2e": e2e,
@@ -504,8 +611,7 @@ def run_reference(args):
            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": f"{cfg['name']}: Qwen3-VL-8B verify round, T={cfg['T']}, N={cfg['N']}, "
-                                  f"L={cfg['L']}, V={cfg['V']}, d={cfg['d']}, {cfg['n_layers']} layers"},
+           "config": workload_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
            "cpu_baseline": {"value": round(value, 5), "unit": "rounds/s",
                             "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 5), "unit": "rounds/s", "h2d_bytes_per_step": 0,
@@ -516,7 +622,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="glance", choices=["glance", "reference"])
     ap.add_argument("--workload", default="full36", choices=["full36", "small"])

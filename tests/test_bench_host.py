@@ -43,3 +43,17 @@ def test_single_process_value():
     import bench
     assert bench.max_over_ranks(12.5, None, "cpu") == 12.5
     assert bench.job_value(1, 50, 1000.0) == pytest.approx(50.0)
+
+
+def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    for name, e in bench.NCU_TRAFFIC.items():
+        assert os.path.exists(os.path.join(ROOT, e["profile"])), name
+        got = bench.profiled_traffic(name)
+        assert got in (None, e["bytes"])
+        assert (got is not None) == (bench.source_digest(e["files"]) == e["digest"])
+    e = dict(bench.NCU_TRAFFIC["glance_tree_attention"], digest="0" * 16)
+    monkeypatch.setitem(bench.NCU_TRAFFIC, "glance_tree_attention", e)
+    assert bench.profiled_traffic("glance_tree_attention") is None
+    assert bench.profiled_traffic("no_such_kernel") is None
