@@ -155,7 +155,7 @@ struct Bf16Params {
   const uint64_t* anc;
   const int32_t* t_len;
   __nv_bfloat16* out;        // [rows][Hq][128]
-  float4* part_o;            // [groups][n_split][32 dim quads][128 rows] unnormalised partial O
+  uint4* part_o;             // [groups][n_split][16 dim octets][128 rows] partial O / l, bf16
   float2* part_ml;           // [groups][n_split][128] (running max, sum) per row
   uint32_t* arrive;          // [groups] split arrivals, then [groups] departures
   int rows, Hq, Hkv, G, Rp, n_qt, n_split, W, t_cap;
@@ -165,7 +165,8 @@ struct Bf16Params {
 
 struct __align__(8) Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_ready;
@@ -243,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
     mbar_init(&bars->s_full[0], 1);
@@ -263,6 +265,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   pdl_wait_prior();
+
+  // Q does not depend on T: its copy goes out before T is read, so the two
+  // round trips overlap. The thread that issues it initialised the barriers.
+  if (threadIdx.x == 0) {
+    const uint64_t pol_q = policy_evict_last();
+    const int pieces = kBM / p.box_rows;
+    int n_boxes = 0;
+    for (int pc = 0; pc < pieces; ++pc) n_boxes += ((qt * kBM + pc * p.box_rows) / p.Rp < p.G) ? 2 : 0;
+    mbar_arrive_expect_tx(&bars->q_full, n_boxes * p.box_rows * 128);
+    for (int pc = 0; pc < pieces; ++pc) {
+      const int r0 = qt * kBM + pc * p.box_rows;
+      const int h = r0 / p.Rp;
+      if (h >= p.G) continue;
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(sQ + hf * (kBM * 128) + pc * p.box_rows * 128, &map_q, &bars->q_full,
+                    hf * 64, g * p.G + h, r0 % p.Rp, pol_q);
+    }
+  }
 
   const int T = *p.t_len;
   const bool room = T >= 0 && T + p.rows <= p.t_cap;
@@ -313,42 +333,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    if (lane == 0 && my_tiles == 0) {
+      // Q was issued before T was known: let it land before the CTA exits
+      (void)mbar_wait(&bars->q_full, 0, 50000000ull);
+    }
     if (lane == 0 && my_tiles > 0) {
       const uint64_t pol_kv = policy_evict_first();
-      const uint64_t pol_q = policy_evict_last();
-      const int pieces = kBM / p.box_rows;
-      int n_boxes = 0;
-      for (int pc = 0; pc < pieces; ++pc) n_boxes += ((qt * kBM + pc * p.box_rows) / p.Rp < p.G) ? 2 : 0;
-      mbar_arrive_expect_tx(&bars->q_full, n_boxes * p.box_rows * 128);
-      for (int pc = 0; pc < pieces; ++pc) {
-        const int r0 = qt * kBM + pc * p.box_rows;
-        const int h = r0 / p.Rp;
-        if (h >= p.G) continue;
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(sQ + hf * (kBM * 128) + pc * p.box_rows * 128, &map_q, &bars->q_full,
-                      hf * 64, g * p.G + h, r0 % p.Rp, pol_q);
-      }
       int issued = 0;
       for (int j = 0; j < my_tiles; ++j) {
         const int st = j % kStages;
+        // Every CTA of the grid starts at once: the first tile of all of them
+        // goes out alone, so that Q and K/V of tile 0 land (and the first MMA
+        // starts) before the rest of the ring competes for DRAM.
+        if (j == 1 && !wait_or_abort(&bars->k_full[0], 0, bars)) {
+          fail_pipeline(bars);
+          break;
+        }
         if (j >= kStages && !wait_or_abort(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars)) {
           fail_pipeline(bars);
           break;
         }
         unsigned char* stage = sKV + st * kKVStageBytes;
         const int key0 = (tile0 + j) * kBN;
-        mbar_arrive_expect_tx(&bars->kv_full[st], kKVStageBytes);
-        tma_load_3d(stage + 0 * kHalfBytes, &map_k, &bars->kv_full[st], 0, key0, g, pol_kv);
-        tma_load_3d(stage + 1 * kHalfBytes, &map_k, &bars->kv_full[st], 64, key0, g, pol_kv);
-        tma_load_3d(stage + 2 * kHalfBytes, &map_v, &bars->kv_full[st], 0, key0, g, pol_kv);
-        tma_load_3d(stage + 3 * kHalfBytes, &map_v, &bars->kv_full[st], 64, key0, g, pol_kv);
+        // K and V of a tile complete separately: QK^T needs only K, and V
+        // lands while the tile's softmax runs
+        mbar_arrive_expect_tx(&bars->k_full[st], 2 * kHalfBytes);
+        tma_load_3d(stage + 0 * kHalfBytes, &map_k, &bars->k_full[st], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 1 * kHalfBytes, &map_k, &bars->k_full[st], 64, key0, g, pol_kv);
+        mbar_arrive_expect_tx(&bars->v_full[st], 2 * kHalfBytes);
+        tma_load_3d(stage + 2 * kHalfBytes, &map_v, &bars->v_full[st], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 3 * kHalfBytes, &map_v, &bars->v_full[st], 64, key0, g, pol_kv);
         ++issued;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
         // let copies already in flight land before the CTA's smem is released
         (void)mbar_wait(&bars->q_full, 0, 50000000ull);
         for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-          (void)mbar_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, 50000000ull);
+        {
+          (void)mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, 50000000ull);
+          (void)mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, 50000000ull);
+        }
       }
     }
   } else if (warp == 1) {
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(sQ);
       auto issue_qk = [&](int j) -> bool {
         const int st = j % kStages;
-        if (!wait_or_abort(&bars->kv_full[st], (j / kStages) & 1, bars)) return false;
+        if (!wait_or_abort(&bars->k_full[st], (j / kStages) & 1, bars)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sKV + st * kKVStageBytes);
         const uint32_t tS = tS0 + (j & 1) * 128;
@@ -381,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           good = false;
           break;
         }
-        if (!wait_or_abort(&bars->p_ready, j & 1, bars)) {
+        if (!wait_or_abort(&bars->p_ready, j & 1, bars) ||
+            !wait_or_abort(&bars->v_full[j % kStages], (j / kStages) & 1, bars)) {
           good = false;
           break;
         }
@@ -545,11 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // The key splits of one (g, q tile) are co-resident (cooperative launch).
-    // Each CTA writes its unnormalised partial O and (m, l) per row to the
-    // workspace (L2-resident), publishes its arrival on the group counter with
-    // a release add, waits (bounded) until all splits have arrived, then
+    // Each CTA writes its partial O_s / l_s (bf16) and (m_s, l_s) per row to
+    // the workspace (L2-resident), publishes its arrival on the group counter
+    // with a release add, waits (bounded) until all splits have arrived, then
     // merges the rows it owns:
-    //   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+    //   O = sum_s w_s l_s (O_s / l_s) / sum_s w_s l_s,  w_s = 2^(m_s - M).
     // The last CTA to leave resets the group's counters to zero.
     const int S = p.n_split;
     const int grp = blockIdx.x / S;
@@ -557,8 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int own0 = split * rpo;
     const int own_rows = own0 >= kBM ? 0 : (kBM - own0 < rpo ? kBM - own0 : rpo);
     if (is_sm) {
-      // column-major (dim quad, row): a warp's store covers 32 consecutive rows
-      float4* po = p.part_o + (static_cast<size_t>(grp) * S + split) * 32 * kBM + lrow;
+      // column-major (dim octet, row): a warp's store covers 32 consecutive rows
+      uint4* po = p.part_o + (static_cast<size_t>(grp) * S + split) * 16 * kBM + lrow;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
@@ -570,10 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4)
-          po[(16 * half + 8 * c + v4) * kBM] =
-              make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                          __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+        for (int v8 = 0; v8 < 4; ++v8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[8 * v8 + 2 * e]) * inv_l,
+                               __uint_as_float(r[8 * v8 + 2 * e + 1]) * inv_l);
+          po[(8 * half + 4 * c + v8) * kBM] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       if (half == 0)
         p.part_ml[(static_cast<size_t>(grp) * S + split) * kBM + lrow] =
@@ -607,37 +637,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = t; item < own_rows * 16; item += 256) {
         const int c8 = item / own_rows, rr = item - c8 * own_rows;
         const int orow = own0 + rr;
+        // every split's (m, l) and partial of this item, loaded together
         float2 mlr[kMaxSplit];
+        uint4 pv[kMaxSplit];
 #pragma unroll
-        for (int sx = 0; sx < kMaxSplit; ++sx)
+        for (int sx = 0; sx < kMaxSplit; ++sx) {
           mlr[sx] = sx < S ? __ldcg(p.part_ml + grp_base + static_cast<size_t>(sx) * kBM + orow)
                            : make_float2(-INFINITY, 0.f);
+          pv[sx] = sx < S ? __ldcg(p.part_o + ((static_cast<size_t>(grp) * S + sx) * 16 + c8) * kBM + orow)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
         float M = -INFINITY;
 #pragma unroll
         for (int sx = 0; sx < kMaxSplit; ++sx) M = fmaxf(M, mlr[sx].x);
         float Lt = 0.f, wts[kMaxSplit];
 #pragma unroll
         for (int sx = 0; sx < kMaxSplit; ++sx) {
-          wts[sx] = mlr[sx].x == -INFINITY ? 0.f : exp2f(mlr[sx].x - M);
-          Lt += wts[sx] * mlr[sx].y;
+          wts[sx] = mlr[sx].x == -INFINITY ? 0.f : exp2f(mlr[sx].x - M) * mlr[sx].y;
+          Lt += wts[sx];
         }
         const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int sx = 0; sx < kMaxSplit; ++sx) {
           if (sx < S && wts[sx] != 0.f) {
-            const float4* src =
-                p.part_o + ((static_cast<size_t>(grp) * S + sx) * 32 + 2 * c8) * kBM + orow;
-            const float4 a = __ldcg(src), b = __ldcg(src + kBM);
             const float w = wts[sx] * inv;
-            acc[0] += w * a.x;
-            acc[1] += w * a.y;
-            acc[2] += w * a.z;
-            acc[3] += w * a.w;
-            acc[4] += w * b.x;
-            acc[5] += w * b.y;
-            acc[6] += w * b.z;
-            acc[7] += w * b.w;
+            const uint32_t av[4] = {pv[sx].x, pv[sx].y, pv[sx].z, pv[sx].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[2 * e] += w * __uint_as_float(av[e] << 16);
+              acc[2 * e + 1] += w * __uint_as_float(av[e] & 0xFFFF0000u);
+            }
           }
         }
         const int oq = qt * kBM + orow;
@@ -687,7 +717,7 @@ Geometry geometry(int rows, int Hq, int Hkv) {
 size_t bf16_ws_bytes(const Geometry& gm, int Hkv) {
   if (gm.n_split == 1) return 256;
   const size_t slots = static_cast<size_t>(Hkv) * gm.n_qt * gm.n_split * kBM;
-  return 256 + slots * kD * sizeof(float) + slots * sizeof(float2);
+  return 256 + slots * kD * sizeof(__nv_bfloat16) + slots * sizeof(float2);
 }
 
 glance_status check_common(const void* q, int n_q_heads, const glance_kv* kv,
@@ -810,8 +840,8 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
     const size_t slots = static_cast<size_t>(kv->n_kv_heads) * gm.n_qt * gm.n_split * kBM;
     char* ws = static_cast<char*>(workspace);
     p.arrive = reinterpret_cast<uint32_t*>(ws);
-    p.part_o = reinterpret_cast<float4*>(ws + 256);
-    p.part_ml = reinterpret_cast<float2*>(ws + 256 + slots * kD * sizeof(float));
+    p.part_o = reinterpret_cast<uint4*>(ws + 256);
+    p.part_ml = reinterpret_cast<float2*>(ws + 256 + slots * kD * sizeof(__nv_bfloat16));
   }
   p.rows = rows;
   p.Hq = n_q_heads;
