@@ -14,6 +14,12 @@
  *   glance_accept_commit   acceptance walk A(S), KV commit, bonus root
  *                          (Definition 1; Appendix B.1 proof of Theorem 1)
  *
+ * Each step also has a batched form (glance_*_batched) that runs the rounds
+ * of B <= 16 independent requests in one launch: same L, V, N and head
+ * geometry, but each request has its own draft logits, root, prefix length T
+ * (ragged) and KV caches. The LM head needs no batched form: the B requests'
+ * rows are stacked into one h of M = B (N + 1) <= 512 rows.
+ *
  * Conventions shared by every call
  * --------------------------------
  * - Memory: every array argument is a DEVICE pointer unless its comment says
@@ -168,7 +174,8 @@ size_t glance_lmhead_argmax_workspace_bytes(int M, int d, int V, glance_dtype dt
  * maxima; gap[i] = max logit - largest logit of any other token (0 on an
  * exact tie); maxlogit[i] the max logit (nullable).
  * Supported: BF16 with d % 64 == 0, V % 8 == 0, 1 <= M <= 512; F32 with any
- * d, V and M <= 512.
+ * d, V and M <= 512. BF16 runs as one launch that streams W once for all M
+ * rows (M > 128: all row blocks of a vocabulary tile share each W stage).
  */
 glance_status glance_lmhead_argmax(const void* h, const void* W, glance_dtype dtype, int M,
                                    int d, int V, int32_t* argmax, float* gap,
@@ -225,6 +232,68 @@ glance_status glance_accept_commit(const glance_tree* tree, const int32_t* argma
                                    const glance_kv* layers, int n_layers, int32_t* n_accepted,
                                    int32_t* accepted_tok, int32_t* new_root, void* workspace,
                                    size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------- batched */
+
+/*
+ * B requests in one launch per step (1 <= B <= 16). These calls compute, for
+ * every request r, exactly what the single-request call computes on request
+ * r's arguments; the paper defines one round per request (Definition 1), and
+ * a batch is B independent rounds.
+ *
+ * Layout: per-request device arrays are stacked along a leading B axis
+ * (draft_logits [B][L][V], root_token [B], q and out [B][N+1][n_q_heads][128],
+ * argmax [B][N+1], n_accepted [B], accepted_tok [B][L], new_root [B]).
+ * Per-request descriptors are HOST arrays: trees [B] (all sized for the same
+ * N and L), and the KV views described at each call.
+ */
+
+/* Workspace bytes for glance_build_tree_batched (0 on bad sizes). */
+size_t glance_build_tree_batched_workspace_bytes(int B, int L, int V, int N);
+
+/*
+ * glance_build_tree for B requests. t_len: device int32 [B], request r's T.
+ * Same limits as glance_build_tree.
+ */
+glance_status glance_build_tree_batched(const void* draft_logits, glance_dtype dtype, int B,
+                                        int L, int V, int N, const int32_t* root_token,
+                                        const int32_t* t_len, const glance_tree* trees,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for glance_tree_attention_batched (0 on bad sizes); the
+ * split of the key range over CTAs depends on every request's t_cap, so pass
+ * the same kv array as to the call. */
+size_t glance_tree_attention_batched_workspace_bytes(int B, int n_rows, int n_q_heads,
+                                                     const glance_kv* kv);
+
+/*
+ * glance_tree_attention for B requests of one layer. kv: host array [B],
+ * request r's cache of this layer (its own k, v, t_cap, strides and t_len;
+ * n_kv_heads and head_dim shared). BF16 with head_dim 128 only (F32 returns
+ * GLANCE_ERR_UNSUPPORTED). The key range of request r is split over about
+ * t_cap_r / (work per CTA) CTAs; the split that finishes a (request, kv head,
+ * query tile) last merges it, so no CTA waits for another.
+ */
+glance_status glance_tree_attention_batched(const void* q, int n_q_heads, const glance_kv* kv,
+                                            const glance_tree* trees, int B, float scale,
+                                            void* out, void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/* Workspace bytes for glance_accept_commit_batched (0 on bad sizes). */
+size_t glance_accept_commit_batched_workspace_bytes(int B, int n_layers);
+
+/*
+ * glance_accept_commit for B requests. layers: host array [B][n_layers],
+ * request r's views at layers[r * n_layers + l]; all layers of a request share
+ * its geometry and t_len, and no two requests share a t_len. Limits:
+ * 1 <= n_layers <= 128, B * n_layers <= 1024.
+ */
+glance_status glance_accept_commit_batched(const glance_tree* trees, int B,
+                                           const int32_t* argmax, const glance_kv* layers,
+                                           int n_layers, int32_t* n_accepted,
+                                           int32_t* accepted_tok, int32_t* new_root,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream);
 
 /* ------------------------------------------------------------------ status */
 

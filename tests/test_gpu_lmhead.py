@@ -35,7 +35,7 @@ def compare(got, ref, tol):
 
 
 @pytest.mark.parametrize("M,d,V", [(1, 64, 8), (16, 128, 1000), (64, 256, 5000),
-                                   (128, 512, 4104), (200, 256, 3000), (64, 192, 136),
+                                   (128, 512, 4104), (200, 256, 3000), (64, 192, 136), (384, 256, 4104), (129, 64, 520),
                                    (512, 128, 2048)])
 def test_bf16_shapes(dev, clean_status, M, d, V):
     gen = W.rng(M, d, V)

@@ -7,17 +7,24 @@ The compute lives in ``libglance.so`` (CUDA kernels behind a C ABI declared in
 * ``tree_attention``  ancestor-masked GQA attention of the packed rows
 * ``lmhead_argmax``   LM head with fused per-row argmax and top-2 gap
 * ``accept_commit``   acceptance walk A(S), KV commit, new root
+
+``*_batched`` forms run B independent requests (ragged prefix lengths) in one
+launch per step; the LM head takes the B requests' rows stacked.
 """
 from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
-                       accept_commit_workspace_bytes, build_tree, build_tree_workspace_bytes,
+                       accept_commit_batched, accept_commit_batched_workspace_bytes,
+                       accept_commit_workspace_bytes, build_tree, build_tree_batched,
+                       build_tree_batched_workspace_bytes, build_tree_workspace_bytes,
                        device_status, lib, lmhead_argmax, lmhead_argmax_noalloc,
-                       lmhead_argmax_workspace_bytes,
-                       reset_device_status, tree_attention, tree_attention_workspace_bytes,
-                       version, workspace)
+                       lmhead_argmax_workspace_bytes, reset_device_status, tree_attention,
+                       tree_attention_batched, tree_attention_batched_workspace_bytes,
+                       tree_attention_workspace_bytes, version, workspace)
 
 __all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
-           "accept_commit", "accept_commit_workspace_bytes", "build_tree",
-           "build_tree_workspace_bytes", "device_status", "lib", "lmhead_argmax",
-           "lmhead_argmax_noalloc",
-           "lmhead_argmax_workspace_bytes", "reset_device_status", "tree_attention",
-           "tree_attention_workspace_bytes", "version", "workspace"]
+           "accept_commit", "accept_commit_batched", "accept_commit_batched_workspace_bytes",
+           "accept_commit_workspace_bytes", "build_tree", "build_tree_batched",
+           "build_tree_batched_workspace_bytes", "build_tree_workspace_bytes", "device_status",
+           "lib", "lmhead_argmax", "lmhead_argmax_noalloc", "lmhead_argmax_workspace_bytes",
+           "reset_device_status", "tree_attention", "tree_attention_batched",
+           "tree_attention_batched_workspace_bytes", "tree_attention_workspace_bytes", "version",
+           "workspace"]

@@ -23,6 +23,9 @@ EXPORTS = [
     "glance_tree_attention_workspace_bytes", "glance_tree_attention",
     "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax", "glance_lmhead_argmax_noalloc",
     "glance_accept_commit_workspace_bytes", "glance_accept_commit",
+    "glance_build_tree_batched_workspace_bytes", "glance_build_tree_batched",
+    "glance_tree_attention_batched_workspace_bytes", "glance_tree_attention_batched",
+    "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
     "glance_reset_device_status", "glance_version",
 ]
@@ -82,6 +85,21 @@ def lib():
     L.glance_accept_commit.argtypes = [ctypes.POINTER(TreeC), vp, ctypes.POINTER(KVC), i32, vp, vp,
                                        vp, vp, sz, vp]
     L.glance_accept_commit.restype = st
+    L.glance_build_tree_batched_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.glance_build_tree_batched_workspace_bytes.restype = sz
+    L.glance_build_tree_batched.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp,
+                                            ctypes.POINTER(TreeC), vp, sz, vp]
+    L.glance_build_tree_batched.restype = st
+    L.glance_tree_attention_batched_workspace_bytes.argtypes = [i32, i32, i32, ctypes.POINTER(KVC)]
+    L.glance_tree_attention_batched_workspace_bytes.restype = sz
+    L.glance_tree_attention_batched.argtypes = [vp, i32, ctypes.POINTER(KVC), ctypes.POINTER(TreeC),
+                                                i32, ctypes.c_float, vp, vp, sz, vp]
+    L.glance_tree_attention_batched.restype = st
+    L.glance_accept_commit_batched_workspace_bytes.argtypes = [i32, i32]
+    L.glance_accept_commit_batched_workspace_bytes.restype = sz
+    L.glance_accept_commit_batched.argtypes = [ctypes.POINTER(TreeC), i32, vp, ctypes.POINTER(KVC),
+                                               i32, vp, vp, vp, vp, sz, vp]
+    L.glance_accept_commit_batched.restype = st
     L.glance_last_error.argtypes = []
     L.glance_last_error.restype = ctypes.c_char_p
     L.glance_status_string.argtypes = [st]
@@ -218,6 +236,60 @@ def accept_commit(tree, argmax, layers, n_accepted, accepted_tok, new_root, ws, 
     _check(lib().glance_accept_commit(ctypes.byref(tree.c), _ptr(argmax), arr, len(layers),
                                       _ptr(n_accepted), _ptr(accepted_tok), _ptr(new_root),
                                       _ptr(ws), ws.numel(), _stream(stream, argmax.device)))
+
+
+# ------------------------------------------------------------ batched calls
+
+def _trees(trees):
+    return (TreeC * len(trees))(*[t.c for t in trees])
+
+
+def _kvs(kvs):
+    return (KVC * len(kvs))(*[k.c for k in kvs])
+
+
+def build_tree_batched_workspace_bytes(B, L, V, N):
+    return lib().glance_build_tree_batched_workspace_bytes(B, L, V, N)
+
+
+def build_tree_batched(draft_logits, N, root_token, t_len, trees, ws, stream=None):
+    """draft_logits [B][L][V]; root_token, t_len int32 [B]; trees: B Tree objects."""
+    B, L, V = draft_logits.shape
+    assert draft_logits.is_contiguous() and len(trees) == B
+    _check(lib().glance_build_tree_batched(_ptr(draft_logits), _dtype_code(draft_logits), B, L, V,
+                                           N, _ptr(root_token), _ptr(t_len), _trees(trees),
+                                           _ptr(ws), ws.numel(),
+                                           _stream(stream, draft_logits.device)))
+
+
+def tree_attention_batched_workspace_bytes(rows, n_q_heads, kvs):
+    return lib().glance_tree_attention_batched_workspace_bytes(len(kvs), rows, n_q_heads, _kvs(kvs))
+
+
+def tree_attention_batched(q, kvs, trees, scale, out, ws, stream=None):
+    """q, out [B][N+1][Hq][128] bf16; kvs: B KVLayer views of this layer."""
+    B = q.shape[0]
+    assert q.is_contiguous() and out.is_contiguous() and q.shape == out.shape
+    assert len(kvs) == B and len(trees) == B
+    _check(lib().glance_tree_attention_batched(_ptr(q), q.shape[2], _kvs(kvs), _trees(trees), B,
+                                               float(scale), _ptr(out), _ptr(ws), ws.numel(),
+                                               _stream(stream, q.device)))
+
+
+def accept_commit_batched_workspace_bytes(B, n_layers):
+    return lib().glance_accept_commit_batched_workspace_bytes(B, n_layers)
+
+
+def accept_commit_batched(trees, argmax, layers, n_accepted, accepted_tok, new_root, ws,
+                          stream=None):
+    """layers[r][l]: KVLayer of request r, layer l; argmax [B][N+1]; outputs [B], [B][L], [B]."""
+    B = len(trees)
+    n_layers = len(layers[0])
+    flat = [layers[r][l] for r in range(B) for l in range(n_layers)]
+    _check(lib().glance_accept_commit_batched(_trees(trees), B, _ptr(argmax), _kvs(flat), n_layers,
+                                              _ptr(n_accepted), _ptr(accepted_tok),
+                                              _ptr(new_root), _ptr(ws), ws.numel(),
+                                              _stream(stream, argmax.device)))
 
 
 def device_status():

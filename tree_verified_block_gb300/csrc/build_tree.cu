@@ -36,21 +36,24 @@ constexpr int kPerThread = 32;
 constexpr int kChunk = kThreads * kPerThread;  // logits per CTA
 constexpr int kMaxL = 16;
 constexpr int kMaxN = 255;
+constexpr int kMaxB = 16;       // requests of one batched call
+constexpr int kTicketsPerReq = 32;  // [0, L): row tickets, [kMaxL]: request ticket
 constexpr int kSlotsPerLane = 8;  // frontier capacity 256 >= N + 1
 
+// B requests (blockIdx.y); "global row" = request * L + offset row.
 struct BuildParams {
-  const void* logits;
+  const void* logits;           // [B][L][V]
   int is_bf16;
-  int L, V, N, K, C;
-  const int32_t* root_token;
-  const int32_t* t_len;
-  glance_tree tree;
-  uint32_t* tickets;            // [kMaxL] row tickets, [kMaxL] global ticket
-  double* chunk_m;              // [L][C] chunk max
-  double* chunk_s;              // [L][C] chunk sum exp(x - m)
-  unsigned long long* cand;     // [L][C][K]
-  int32_t* top_tok;             // [L][K]
-  float* top_logq;              // [L][K]
+  int B, L, V, N, K, C;
+  const int32_t* root_token;    // [B]
+  const int32_t* t_len;         // [B]
+  uint32_t* tickets;            // [B][kTicketsPerReq]
+  double* chunk_m;              // [B * L][C] chunk max
+  double* chunk_s;              // [B * L][C] chunk sum exp(x - m)
+  unsigned long long* cand;     // [B * L][C][K]
+  int32_t* top_tok;             // [B * L][K]
+  float* top_logq;              // [B * L][K]
+  glance_tree tree[kMaxB];
 };
 
 constexpr int kBuckets = 2048;      // first-pass buckets of the gap to the max
@@ -297,16 +300,17 @@ __device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlotsPerLane], 
 
 constexpr uint32_t kRootChild = 0xFFFFu;  // code of the first node (rank 0 at offset 1)
 
-__device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
+__device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int req) {
   // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
   float* s_logq = reinterpret_cast<float*>(dyn);
   int* s_tok = reinterpret_cast<int*>(dyn + sizeof(float) * p.L * p.K);
   TreeSmem& ts = *reinterpret_cast<TreeSmem*>(
       dyn + 16 * ((sizeof(float) * 2 * p.L * p.K + 15) / 16));
   const int LK = p.L * p.K;
+  const size_t lk0 = static_cast<size_t>(req) * LK;
   for (int i = threadIdx.x; i < LK; i += kThreads) {
-    s_logq[i] = __ldcg(p.top_logq + i);
-    s_tok[i] = __ldcg(p.top_tok + i);
+    s_logq[i] = __ldcg(p.top_logq + lk0 + i);
+    s_tok[i] = __ldcg(p.top_tok + lk0 + i);
   }
   __syncthreads();
   const int N = p.N, L = p.L, K = p.K;
@@ -458,8 +462,9 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   __syncthreads();
 
   // canonical position: 1 + number of nodes before it in (depth, rank vector)
-  const int T = *p.t_len;
-  const int W = p.tree.mask_words;
+  const int T = p.t_len[req];
+  const glance_tree& tree = p.tree[req];
+  const int W = tree.mask_words;
   for (int kk = threadIdx.x; kk < N; kk += kThreads) {
     const uint32_t dk = ts.pop[kk].dep;
     const unsigned long long hk = ts.pop[kk].hi, lk = ts.pop[kk].lo;
@@ -472,37 +477,37 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn) {
   __syncthreads();
   for (int kk = threadIdx.x; kk <= N; kk += kThreads) {
     if (kk == N) {  // root row
-      p.tree.token[0] = *p.root_token;
-      p.tree.parent[0] = -1;
-      p.tree.depth[0] = 0;
-      p.tree.pos_id[0] = T;
-      p.tree.score[0] = 0.f;
-      for (int w = 0; w < W; ++w) p.tree.anc[w] = (w == 0) ? 1ull : 0ull;
+      tree.token[0] = p.root_token[req];
+      tree.parent[0] = -1;
+      tree.depth[0] = 0;
+      tree.pos_id[0] = T;
+      tree.score[0] = 0.f;
+      for (int w = 0; w < W; ++w) tree.anc[w] = (w == 0) ? 1ull : 0ull;
       continue;
     }
     const int row = ts.p_pos[kk];
     const int d = ts.pop[kk].dep;
     const uint32_t r = get_rank(ts.pop[kk].hi, ts.pop[kk].lo, d - 1);
     const int par = ts.pop[kk].par;
-    p.tree.token[row] = s_tok[(d - 1) * K + r];
-    p.tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
-    p.tree.depth[row] = d;
-    p.tree.pos_id[row] = T + d;
-    p.tree.score[row] = ts.pop[kk].score;
+    tree.token[row] = s_tok[(d - 1) * K + r];
+    tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
+    tree.depth[row] = d;
+    tree.pos_id[row] = T + d;
+    tree.score[row] = ts.pop[kk].score;
     unsigned long long words[4] = {1ull, 0ull, 0ull, 0ull};
     words[row >> 6] |= 1ull << (row & 63);
     for (int u = par; u >= 0; u = ts.pop[u].par) {
       const int pr = ts.p_pos[u];
       words[pr >> 6] |= 1ull << (pr & 63);
     }
-    for (int w = 0; w < W; ++w) p.tree.anc[row * W + w] = words[w];
+    for (int w = 0; w < W; ++w) tree.anc[row * W + w] = words[w];
   }
 }
 
 // ------------------------------------------------------------------- kernel
 
 template <bool kBF16, bool kVec>
-__global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildParams p) {
+__global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_constant__ BuildParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ SelectSmem sm;
   __shared__ double red_d[kThreads / 32];
@@ -511,8 +516,11 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildPara
   __shared__ unsigned long long sel[256];
   __shared__ double s_lse;
 
-  const int row = blockIdx.x / p.C;
+  const int req = blockIdx.y;
+  const int row = req * p.L + blockIdx.x / p.C;  // global row
   const int chunk = blockIdx.x % p.C;
+  uint32_t* const tickets = p.tickets + req * kTicketsPerReq;
+  const int orow = blockIdx.x / p.C;               // offset row within the request
   const int base = chunk * kChunk;
   const int n_valid = min(kChunk, p.V - base);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -616,11 +624,11 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildPara
   // ---- 2. last CTA of this row merges
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_ticket = atomicAdd(&p.tickets[row], 1u);
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&tickets[orow], 1u);
   __syncthreads();
   if (s_ticket != static_cast<uint32_t>(p.C - 1)) return;
   __threadfence();
-  if (threadIdx.x == 0) p.tickets[row] = 0;  // ready for the next call
+  if (threadIdx.x == 0) tickets[orow] = 0;  // ready for the next call
 
   // row log-sum-exp and max from the chunks' (max, sum) pairs, in fp64
   if (warp == 0) {
@@ -669,12 +677,12 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const BuildPara
   // ---- 3. last row-merger builds the tree
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_ticket = atomicAdd(&p.tickets[kMaxL], 1u);
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&tickets[kMaxL], 1u);
   __syncthreads();
   if (s_ticket != static_cast<uint32_t>(p.L - 1)) return;
   __threadfence();
-  if (threadIdx.x == 0) p.tickets[kMaxL] = 0;
-  tree_phase(p, dyn);
+  if (threadIdx.x == 0) tickets[kMaxL] = 0;
+  tree_phase(p, dyn, req);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -683,23 +691,24 @@ struct WsLayout {
   size_t tickets, chunk_m, chunk_s, cand, top_tok, top_logq, total;
 };
 
-WsLayout ws_layout(int L, int V, int N) {
+WsLayout ws_layout(int B, int L, int V, int N) {
   const int K = N < V ? N : V;
   const int C = (V + kChunk - 1) / kChunk;
+  const size_t rows = static_cast<size_t>(B) * L;
   WsLayout w;
   size_t o = 0;
   w.tickets = o;
-  o = align_up(o + sizeof(uint32_t) * (2 * kMaxL), 256);
+  o = align_up(o + sizeof(uint32_t) * kTicketsPerReq * B, 256);
   w.chunk_m = o;
-  o = align_up(o + sizeof(double) * L * C, 256);
+  o = align_up(o + sizeof(double) * rows * C, 256);
   w.chunk_s = o;
-  o = align_up(o + sizeof(double) * L * C, 256);
+  o = align_up(o + sizeof(double) * rows * C, 256);
   w.cand = o;
-  o = align_up(o + sizeof(unsigned long long) * static_cast<size_t>(L) * C * K, 256);
+  o = align_up(o + sizeof(unsigned long long) * rows * C * K, 256);
   w.top_tok = o;
-  o = align_up(o + sizeof(int32_t) * L * K, 256);
+  o = align_up(o + sizeof(int32_t) * rows * K, 256);
   w.top_logq = o;
-  o = align_up(o + sizeof(float) * L * K, 256);
+  o = align_up(o + sizeof(float) * rows * K, 256);
   w.total = o;
   return w;
 }
@@ -720,46 +729,44 @@ bool sizes_ok(int L, int V, int N) {
   return total >= N;
 }
 
-}  // namespace
-
-extern "C" size_t glance_build_tree_workspace_bytes(int L, int V, int N) {
-  if (!sizes_ok(L, V, N)) return 0;
-  return ws_layout(L, V, N).total;
-}
-
-extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtype dtype, int L,
-                                           int V, int N, const int32_t* root_token,
-                                           const int32_t* t_len, const glance_tree* tree,
-                                           void* workspace, size_t workspace_bytes,
-                                           void* stream) {
+glance_status launch_build(const char* who, const void* draft_logits, glance_dtype dtype, int B,
+                           int L, int V, int N, const int32_t* root_token, const int32_t* t_len,
+                           const glance_tree* trees, void* workspace, size_t workspace_bytes,
+                           void* stream) {
   using glance::fail;
-  if (!draft_logits || !root_token || !t_len || !tree || !workspace)
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: null pointer argument");
+  if (!draft_logits || !root_token || !t_len || !trees || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (B < 1 || B > kMaxB)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= B <= %d (got %d)", who, kMaxB, B);
   if (dtype != GLANCE_F32 && dtype != GLANCE_BF16)
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: dtype must be F32 or BF16");
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: dtype must be F32 or BF16", who);
   if (!sizes_ok(L, V, N))
     return fail(GLANCE_ERR_INVALID_ARG,
-                "glance_build_tree: need 1<=L<=16, 2<=V<=262144, 1<=N<=255, N <= #strings, "
+                "%s: need 1<=L<=16, 2<=V<=262144, 1<=N<=255, N <= #strings, "
                 "ceil(V/8192)*min(N,V) <= 8192 (got L=%d V=%d N=%d)",
-                L, V, N);
-  if (tree->n != N || tree->L != L || tree->mask_words != (N + 1 + 63) / 64)
-    return fail(GLANCE_ERR_INVALID_ARG,
-                "glance_build_tree: tree struct sized for n=%d L=%d mask_words=%d, call has "
-                "N=%d L=%d (mask_words must be %d)",
-                tree->n, tree->L, tree->mask_words, N, L, (N + 64) / 64);
-  if (!tree->token || !tree->parent || !tree->depth || !tree->pos_id || !tree->score ||
-      !tree->anc)
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: null tree array");
-  const WsLayout w = ws_layout(L, V, N);
+                who, L, V, N);
+  for (int r = 0; r < B; ++r) {
+    const glance_tree* tree = trees + r;
+    if (tree->n != N || tree->L != L || tree->mask_words != (N + 1 + 63) / 64)
+      return fail(GLANCE_ERR_INVALID_ARG,
+                  "%s: tree %d sized for n=%d L=%d mask_words=%d, call has N=%d L=%d "
+                  "(mask_words must be %d)",
+                  who, r, tree->n, tree->L, tree->mask_words, N, L, (N + 64) / 64);
+    if (!tree->token || !tree->parent || !tree->depth || !tree->pos_id || !tree->score ||
+        !tree->anc)
+      return fail(GLANCE_ERR_INVALID_ARG, "%s: null array in tree %d", who, r);
+  }
+  const WsLayout w = ws_layout(B, L, V, N);
   if (workspace_bytes < w.total)
-    return fail(GLANCE_ERR_CAPACITY, "glance_build_tree: workspace %zu bytes < %zu needed",
+    return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who,
                 workspace_bytes, w.total);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_build_tree: workspace must be 256-byte aligned");
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
 
   BuildParams p;
   p.logits = draft_logits;
   p.is_bf16 = dtype == GLANCE_BF16;
+  p.B = B;
   p.L = L;
   p.V = V;
   p.N = N;
@@ -767,7 +774,7 @@ extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtyp
   p.C = (V + kChunk - 1) / kChunk;
   p.root_token = root_token;
   p.t_len = t_len;
-  p.tree = *tree;
+  for (int r = 0; r < kMaxB; ++r) p.tree[r] = trees[r < B ? r : 0];
   char* ws = static_cast<char*>(workspace);
   p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets);
   p.chunk_m = reinterpret_cast<double*>(ws + w.chunk_m);
@@ -779,17 +786,47 @@ extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtyp
   // dynamic smem: the chunk's logits during selection, the tree search after
   size_t dyn = 16 * ((sizeof(float) * 2 * L * p.K + 15) / 16) + sizeof(TreeSmem);
   if (dyn < sizeof(float) * kChunk) dyn = sizeof(float) * kChunk;
-  const bool vec = p.is_bf16 ? (V % 4 == 0 && glance::aligned16(draft_logits))
-                             : (V % 4 == 0 && glance::aligned16(draft_logits));
+  const bool vec = V % 4 == 0 && glance::aligned16(draft_logits);
   void (*kern)(const BuildParams);
   if (p.is_bf16)
     kern = vec ? build_tree_kernel<true, true> : build_tree_kernel<true, false>;
   else
     kern = vec ? build_tree_kernel<false, true> : build_tree_kernel<false, false>;
   cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(kern), static_cast<int>(dyn));
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_build_tree: smem attribute");
-  kern<<<L * p.C, kThreads, dyn, static_cast<cudaStream_t>(stream)>>>(p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  kern<<<dim3(L * p.C, B), kThreads, dyn, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_build_tree: launch");
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
+}
+
+}  // namespace
+
+extern "C" size_t glance_build_tree_workspace_bytes(int L, int V, int N) {
+  if (!sizes_ok(L, V, N)) return 0;
+  return ws_layout(1, L, V, N).total;
+}
+
+extern "C" glance_status glance_build_tree(const void* draft_logits, glance_dtype dtype, int L,
+                                           int V, int N, const int32_t* root_token,
+                                           const int32_t* t_len, const glance_tree* tree,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  return launch_build("glance_build_tree", draft_logits, dtype, 1, L, V, N, root_token, t_len,
+                      tree, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t glance_build_tree_batched_workspace_bytes(int B, int L, int V, int N) {
+  if (B < 1 || B > kMaxB || !sizes_ok(L, V, N)) return 0;
+  return ws_layout(B, L, V, N).total;
+}
+
+extern "C" glance_status glance_build_tree_batched(const void* draft_logits, glance_dtype dtype,
+                                                   int B, int L, int V, int N,
+                                                   const int32_t* root_token,
+                                                   const int32_t* t_len, const glance_tree* trees,
+                                                   void* workspace, size_t workspace_bytes,
+                                                   void* stream) {
+  return launch_build("glance_build_tree_batched", draft_logits, dtype, B, L, V, N, root_token,
+                      t_len, trees, workspace, workspace_bytes, stream);
 }

@@ -156,34 +156,53 @@ __global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p)
 // ------------------------------------------------------------------ bf16 path
 
 constexpr int kBM = 128;   // rows per MMA (M), padded with zero rows
-constexpr int kBN = 256;   // vocabulary columns per tile (N)
 constexpr int kBK = 64;    // one 128-byte swizzle atom of K
-constexpr int kStages = 4;
 constexpr int kThreads = 256;
-constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
-constexpr uint32_t kBBytes = kBK * kBN * 2;  // 32 KB
+constexpr uint32_t kABytes = kBM * kBK * 2;    // one row block's K slice: 16 KB
 constexpr uint32_t kWBoxBytes = kBK * 64 * 2;  // one 64 x 64 box of W: 8 KB
-constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256;
+
+// Tile shapes by the number NB of 128-row blocks of h (M <= 128 * NB): every
+// vocabulary tile of BN columns is multiplied by all NB row blocks from the
+// same W stage, so W streams from HBM once whatever M is. The NB x BN fp32
+// accumulators of a tile take NB * BN TMEM columns; with NBUF = 2 the MMA
+// warp fills one set while the epilogue drains the other.
+//   NB = 1: BN 256, 4 stages of 48 KB, 2 accumulator sets
+//   NB = 2: BN 128, 4 stages of 48 KB, 2 sets
+//   NB = 3: BN 128, 3 stages of 64 KB, 1 set
+//   NB = 4: BN 128, 2 stages of 80 KB, 1 set
+template <int NB>
+struct Shape {
+  static constexpr int BN = NB == 1 ? 256 : 128;
+  static constexpr int STAGES = NB <= 2 ? 4 : (NB == 3 ? 3 : 2);
+  static constexpr int NBUF = NB <= 2 ? 2 : 1;
+  static constexpr uint32_t kBBytes = kBK * BN * 2;
+  static constexpr uint32_t kStageBytes = NB * kABytes + kBBytes;
+  static constexpr size_t kSmem = 1024 + STAGES * kStageBytes + 256;
+  static_assert(NB * BN * NBUF <= 512, "tensor memory");
+  static_assert(kSmem <= 232448, "shared memory");
+};
 
 struct Bf16Params {
-  int M, d, V, n_tiles, a_rows;
+  int M, d, V, n_tiles, a_rows;  // a_rows: rows a TMA box of h writes (NB = 1)
   int32_t* argmax;
   float* gap;
   float* maxlogit;
-  Partial* part;  // [grid][kBM]
+  Partial* part;  // [grid][NB * 128]
   uint32_t* ticket;
 };
 
+template <int STAGES>
 struct __align__(8) Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
+template <typename BarsT>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, BarsT* bars) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -195,20 +214,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
-__device__ __forceinline__ void fail_pipeline(Bars* bars) {
+template <typename BarsT>
+__device__ __forceinline__ void fail_pipeline(BarsT* bars) {
   report(GLANCE_DEV_PIPELINE_TIMEOUT);
   atomicExch(&bars->abort_flag, 1);
 }
 
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_bf16_kernel(const __grid_constant__ CUtensorMap map_h,
                        const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
+  using Sh = Shape<NB>;
+  constexpr int BN = Sh::BN, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char* sA = smem;
-  unsigned char* sB = smem + kStages * kABytes;
-  Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kBBytes);
+  // stage s: NB A slices (16 KB each), then the W slice
+  Bars<STAGES>* bars = reinterpret_cast<Bars<STAGES>*>(smem + STAGES * Sh::kStageBytes);
   __shared__ uint32_t s_ticket;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -232,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  // rows a_rows..127 of every A stage stay zero (TMA only writes a_rows rows)
-  if (p.a_rows < kBM) {
-    for (int s = 0; s < kStages; ++s) {
-      uint4* dst = reinterpret_cast<uint4*>(sA + s * kABytes + p.a_rows * 128);
+  // NB = 1: rows a_rows..127 of every A stage stay zero (TMA only writes a_rows rows)
+  if (NB == 1 && p.a_rows < kBM) {
+    for (int s = 0; s < STAGES; ++s) {
+      uint4* dst = reinterpret_cast<uint4*>(smem + s * Sh::kStageBytes + p.a_rows * 128);
       for (int i = threadIdx.x; i < (kBM - p.a_rows) * 8; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -251,61 +273,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_w);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
-      const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBK * 2;
+      // NB > 1: boxes of 128 rows; rows past M are filled with zeros by TMA
+      const uint32_t a_bytes = NB == 1 ? static_cast<uint32_t>(p.a_rows) * kBK * 2 : NB * kABytes;
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
-        const int v0 = (blockIdx.x + i * gridDim.x) * kBN;
+        const int v0 = (blockIdx.x + i * gridDim.x) * BN;
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
-          const int st = it % kStages;
-          if (it >= kStages && !wait_or_abort(&bars->empty[st], ((it / kStages) - 1) & 1, bars)) {
+          const int st = it % STAGES;
+          if (it >= STAGES && !wait_or_abort(&bars->empty[st], ((it / STAGES) - 1) & 1, bars)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->full[st], a_bytes + kBBytes);
-          tma_load_2d(sA + st * kABytes, &map_h, &bars->full[st], kb * kBK, 0, pol_h);
+          unsigned char* stage = smem + st * Sh::kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], a_bytes + Sh::kBBytes);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            tma_load_2d(sB + st * kBBytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
+          for (int b = 0; b < NB; ++b)
+            tma_load_2d(stage + b * kABytes, &map_h, &bars->full[st], kb * kBK, b * kBM, pol_h);
+#pragma unroll
+          for (int q = 0; q < BN / 64; ++q)
+            tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
                         kb * kBK, pol_w);
         }
       }
       if (!ok) {
         fail_pipeline(bars);
-        for (int j = it > kStages ? it - kStages : 0; j < it; ++j)
-          (void)mbar_wait(&bars->full[j % kStages], (j / kStages) & 1, 50000000ull);
+        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+          (void)mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1, 50000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, true);
-      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, true);
+      const uint32_t s0 = smem_u32(smem);
       int it = 0;
       bool ok = true;
       const int total_it = my_tiles * n_kb;
       for (int i = 0; ok && i < my_tiles; ++i) {
-        const int buf = i & 1;
-        if (i >= 2 && !wait_or_abort(&bars->acc_empty[buf], ((i >> 1) - 1) & 1, bars)) {
+        const int buf = NBUF == 2 ? (i & 1) : 0;
+        const int use = NBUF == 2 ? (i >> 1) : i;  // earlier uses of this accumulator set
+        if (use >= 1 && !wait_or_abort(&bars->acc_empty[buf], (use - 1) & 1, bars)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kBN;
+        const uint32_t d_tmem = tmem + buf * (NB * BN);
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
-          const int st = it % kStages;
-          if (!wait_or_abort(&bars->full[st], (it / kStages) & 1, bars)) {
+          const int st = it % STAGES;
+          if (!wait_or_abort(&bars->full[st], (it / STAGES) & 1, bars)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = a0 + st * kABytes, b_addr = b0 + st * kBBytes;
+          const uint32_t st_addr = s0 + st * Sh::kStageBytes;
+          const uint32_t b_addr = st_addr + NB * kABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                        sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
-                        (kb > 0 || k > 0) ? 1u : 0u);
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_ss(d_tmem + b * BN, sdesc_sw128(st_addr + b * kABytes + k * 32, 16, 1024),
+                          sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
           // only stages the producer will refill need a release
-          if (it + kStages < total_it) mma_commit(&bars->empty[st]);
+          if (it + STAGES < total_it) mma_commit(&bars->empty[st]);
         }
         if (!ok) break;
         mma_commit(&bars->acc_full[buf]);
@@ -316,38 +346,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp - 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m1 = -INFINITY, m2 = -INFINITY;
-    int i1 = 0x7FFFFFFF;
+    float m1[NB], m2[NB];
+    int i1[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      m1[b] = -INFINITY;
+      m2[b] = -INFINITY;
+      i1[b] = 0x7FFFFFFF;
+    }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
-      const int buf = i & 1;
-      if (!wait_or_abort(&bars->acc_full[buf], (i >> 1) & 1, bars)) {
+      const int buf = NBUF == 2 ? (i & 1) : 0;
+      const int use = NBUF == 2 ? (i >> 1) : i;
+      if (!wait_or_abort(&bars->acc_full[buf], use & 1, bars)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int v0 = (blockIdx.x + i * gridDim.x) * kBN;
-      const uint32_t t_acc = tmem + buf * kBN + lane_off;
+      const int v0 = (blockIdx.x + i * gridDim.x) * BN;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint32_t t_acc = tmem + buf * (NB * BN) + b * BN + lane_off;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_acc + c * 32, r);
-        tmem_ld_wait();
-        const int col0 = v0 + c * 32;
-        if (col0 + 32 <= p.V) {
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_acc + c * 32, r);
+          tmem_ld_wait();
+          const int col0 = v0 + c * 32;
+          if (col0 + 32 <= p.V) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1, i1, m2);
-        } else {
+            for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1, i1, m2);
+            for (int e = 0; e < 32; ++e)
+              if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[buf]);
     }
     if (!ok) fail_pipeline(bars);
-    if (row < p.M) p.part[static_cast<size_t>(blockIdx.x) * kBM + row] = Partial{m1, i1, m2};
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (b * kBM + row < p.M)
+        p.part[static_cast<size_t>(blockIdx.x) * (NB * kBM) + b * kBM + row] = Partial{m1[b], i1[b], m2[b]};
   }
   tc_fence_before();
   __syncthreads();
@@ -362,13 +405,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
-  merge_partials(p.part, gridDim.x, kBM, p.M, p.argmax, p.gap, p.maxlogit);
+  merge_partials(p.part, gridDim.x, NB * kBM, p.M, p.argmax, p.gap, p.maxlogit);
 }
 
+int row_blocks(int M) { return (M + kBM - 1) / kBM; }
+
 size_t ws_bytes_bf16(int M) {
-  (void)M;
   const int grid = glance::num_sms();
-  return 256 + (static_cast<size_t>(grid) * kBM * sizeof(Partial) + 255) / 256 * 256;
+  return 256 + (static_cast<size_t>(grid) * row_blocks(M) * kBM * sizeof(Partial) + 255) / 256 * 256;
+}
+
+template <int NB>
+glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
+                          float* gap, float* maxlogit, Partial* part, uint32_t* ticket, int max_grid,
+                          cudaStream_t s, const char* who) {
+  using Sh = Shape<NB>;
+  const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
+  int grid = glance::num_sms();
+  if (grid > n_tiles) grid = n_tiles;
+  if (grid > max_grid) grid = max_grid;
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel<NB>),
+                                      static_cast<int>(Sh::kSmem));
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  CUtensorMap mw, mh;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
+    const uint32_t box[2] = {64, kBK};
+    glance_status st = glance::make_map_bf16(&mw, W, 2, dims, strides, box,
+                                             CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  const int a_rows = NB == 1 ? (M + 7) / 8 * 8 : kBM;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
+    glance_status st = glance::make_map_bf16(&mh, h, 2, dims, strides, box,
+                                             CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket};
+  lmhead_bf16_kernel<NB><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
 }
 
 size_t ws_bytes_f32(int M, int V) {
@@ -417,39 +498,21 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
   if (workspace_bytes < ws_bytes_bf16(M))
     return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace %zu bytes < %zu needed",
                 workspace_bytes, ws_bytes_bf16(M));
-  const int n_tiles = (V + kBN - 1) / kBN;
-  int grid = glance::num_sms();
-  if (grid > n_tiles) grid = n_tiles;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel), static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: smem attribute");
-  CUtensorMap mw;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
-    const uint32_t box[2] = {64, kBK};
-    glance_status st = glance::make_map_bf16(&mw, W, 2, dims, strides, box,
-                                             CU_TENSOR_MAP_SWIZZLE_128B, "glance_lmhead_argmax: W map");
-    if (st != GLANCE_OK) return st;
+  // one launch: W streams once for all rows
+  switch (row_blocks(M)) {
+    case 1:
+      return launch_bf16<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
+                            "glance_lmhead_argmax");
+    case 2:
+      return launch_bf16<2>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
+                            "glance_lmhead_argmax");
+    case 3:
+      return launch_bf16<3>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
+                            "glance_lmhead_argmax");
+    default:
+      return launch_bf16<4>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
+                            "glance_lmhead_argmax");
   }
-  // rows in blocks of 128: each block streams W once
-  for (int r0 = 0; r0 < M; r0 += kBM) {
-    const int mb = M - r0 < kBM ? M - r0 : kBM;
-    const int a_rows = (mb + 7) / 8 * 8;
-    CUtensorMap mh;
-    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(mb)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
-    glance_status st = glance::make_map_bf16(
-        &mh, static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, 2, dims, strides, box,
-        CU_TENSOR_MAP_SWIZZLE_128B, "glance_lmhead_argmax: h map");
-    if (st != GLANCE_OK) return st;
-    Bf16Params p{mb, d, V, n_tiles, a_rows, argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr,
-                 part, ticket};
-    lmhead_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mh, mw, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax: launch");
-  }
-  return GLANCE_OK;
 }
 
 // ------------------------------------------------- no-allocation entry point
@@ -513,47 +576,23 @@ extern "C" glance_status glance_lmhead_argmax_noalloc(const void* h, const void*
   if (!glance::aligned16(h) || !glance::aligned16(W))
     return fail(GLANCE_ERR_INVALID_ARG,
                 "glance_lmhead_argmax_noalloc: h and W must be 16-byte aligned");
-  const int n_tiles = (V + kBN - 1) / kBN;
-  int grid = glance::num_sms();
-  if (grid > n_tiles) grid = n_tiles;
-  if (grid > kNoAllocMaxCtas) grid = kNoAllocMaxCtas;  // the scratch holds this many CTAs
   void* scratch = nullptr;
   glance_status st = noalloc_scratch(&scratch);
   if (st != GLANCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel),
-                                      static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: smem attribute");
   // the merge ticket must start at zero (the array keeps the last call's contents)
-  e = cudaMemsetAsync(scratch, 0, 256, s);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 256, s);
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: ticket reset");
   uint32_t* ticket = static_cast<uint32_t*>(scratch);
   Partial* part = reinterpret_cast<Partial*>(static_cast<char*>(scratch) + 256);
-  CUtensorMap mw;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
-    const uint32_t box[2] = {64, kBK};
-    st = glance::make_map_bf16(&mw, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                               "glance_lmhead_argmax_noalloc: W map");
-    if (st != GLANCE_OK) return st;
-  }
+  // rows in blocks of 128, one launch each (the scratch holds the partials of
+  // one block for at most kNoAllocMaxCtas CTAs)
   for (int r0 = 0; r0 < M; r0 += kBM) {
     const int mb = M - r0 < kBM ? M - r0 : kBM;
-    const int a_rows = (mb + 7) / 8 * 8;
-    CUtensorMap mh;
-    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(mb)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
-    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
-    st = glance::make_map_bf16(&mh, static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d,
-                               2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                               "glance_lmhead_argmax_noalloc: h map");
+    st = launch_bf16<1>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb, d, V,
+                        argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr, part, ticket,
+                        kNoAllocMaxCtas, s, "glance_lmhead_argmax_noalloc");
     if (st != GLANCE_OK) return st;
-    Bf16Params p{mb, d, V, n_tiles, a_rows, argmax + r0, gap + r0,
-                 maxlogit ? maxlogit + r0 : nullptr, part, ticket};
-    lmhead_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(mh, mw, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: launch");
   }
   return GLANCE_OK;
 }

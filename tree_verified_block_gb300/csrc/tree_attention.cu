@@ -145,22 +145,42 @@ constexpr int kStages = 3;       // K/V ring depth
 constexpr int kThreads = 384;    // 12 warps: TMA, MMA, TMEM, idle, 2 x 4 softmax
 constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64 used)
 constexpr int kMaxSplit = 16;    // key splits of one (kv head, q tile)
+constexpr int kMaxB = 16;        // requests of one batched call
 constexpr uint32_t kHalfBytes = kBN * 128;          // 64 head dims x 128 slots, bf16: 16 KB
 constexpr uint32_t kQBytes = 2 * kBM * 128;         // 32 KB
 constexpr uint32_t kKVStageBytes = 4 * kHalfBytes;  // K and V, two halves each: 64 KB
 constexpr uint32_t kRingBytes = kStages * kKVStageBytes;
 constexpr size_t kSmemBytes = 1024 /*align*/ + kQBytes + kRingBytes + 1280;
 
+// B requests, CTAs request-major: request r owns CTAs [cta0[r], cta0[r+1]),
+// (kv head g, q tile qt, split) with the split fastest. A group is one
+// (request, g, qt); its n_split[r] CTAs cover the request's key range.
+// NB: capacity of the per-request arrays (1 for single-request calls, so
+// that their parameter block stays small).
+template <int NB>
 struct Bf16Params {
-  const uint64_t* anc;
-  const int32_t* t_len;
-  __nv_bfloat16* out;        // [rows][Hq][128]
-  uint4* part_o;             // [groups][n_split][16 dim octets][128 rows] partial O / l, bf16
-  float2* part_ml;           // [groups][n_split][128] (running max, sum) per row
+  const uint64_t* anc[NB];
+  const int32_t* t_len[NB];
+  int t_cap[NB];
+  int cta0[NB + 1];
+  int n_split[NB];
+  int slot0[NB];             // first partial slot of the request's groups
+  __nv_bfloat16* out;        // [B][rows][Hq][128]
+  uint4* part_o;             // [slots][16 dim octets][128 rows] partial O / l, bf16
+  float2* part_ml;           // [slots][128] (running max, sum) per row
   uint32_t* arrive;          // [groups] split arrivals, then [groups] departures
-  int rows, Hq, Hkv, G, Rp, n_qt, n_split, W, t_cap;
+  int B, rows, Hq, Hkv, G, Rp, n_qt, W;
   int box_rows;              // rows per Q box = min(Rp, 128)
+  int ticket_merge;          // 1: the last split CTA of a group merges it (any grid);
+                             // 0: all splits wait for each other (cooperative launch)
   float scale_log2;          // scale * log2(e)
+};
+
+// K and V tensor maps of every request's cache of this layer
+template <int NB>
+struct KVMaps {
+  CUtensorMap k[NB];
+  CUtensorMap v[NB];
 };
 
 struct __align__(8) Bars {
@@ -221,10 +241,11 @@ __device__ __forceinline__ uint32_t visible32(const uint64_t (&a)[4], int kb, in
 
 // One CTA = (kv head g, q tile, key split). The key splits of one (g, q tile)
 // merge their partial results through the workspace once all have arrived.
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attention_bf16_kernel(const __grid_constant__ CUtensorMap map_q,
-                               const __grid_constant__ CUtensorMap map_k,
-                               const __grid_constant__ CUtensorMap map_v, const Bf16Params p) {
+                               const __grid_constant__ KVMaps<NB> maps,
+                               const __grid_constant__ Bf16Params<NB> p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,9 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(sKV + kRingBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x % p.n_split;
-  const int qt = (blockIdx.x / p.n_split) % p.n_qt;
-  const int g = blockIdx.x / (p.n_split * p.n_qt);
+  int req = 0;
+  while (req + 1 < p.B && static_cast<int>(blockIdx.x) >= p.cta0[req + 1]) ++req;
+  const int n_split = p.n_split[req];
+  const int local = blockIdx.x - p.cta0[req];
+  const int split = local % n_split;
+  const int grp_local = local / n_split;  // g * n_qt + qt
+  const int qt = grp_local % p.n_qt;
+  const int g = grp_local / p.n_qt;
+  const int grp = req * p.Hkv * p.n_qt + grp_local;
+  const CUtensorMap* map_k = &maps.k[req];
+  const CUtensorMap* map_v = &maps.v[req];
+  const int q_row0 = req * p.rows;  // this request's first row in q and out
 
   // The next kernel in the stream may start its own prologue on free SMs now;
   // this kernel sets up barriers and tensor memory, then waits until the
@@ -257,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_q);
-    tma_prefetch_desc(&map_k);
-    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(map_k);
+    tma_prefetch_desc(map_v);
   }
   if (warp == 2) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -280,20 +310,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (h >= p.G) continue;
       for (int hf = 0; hf < 2; ++hf)
         tma_load_3d(sQ + hf * (kBM * 128) + pc * p.box_rows * 128, &map_q, &bars->q_full,
-                    hf * 64, g * p.G + h, r0 % p.Rp, pol_q);
+                    hf * 64, g * p.G + h, q_row0 + r0 % p.Rp, pol_q);
     }
   }
 
-  const int T = *p.t_len;
-  const bool room = T >= 0 && T + p.rows <= p.t_cap;
+  const int T = *p.t_len[req];
+  const bool room = T >= 0 && T + p.rows <= p.t_cap[req];
   // key tiles of this split over slots [0, T + rows)
   const int n_keys = room ? T + p.rows : 0;
   const int n_tiles = (n_keys + kBN - 1) / kBN;
-  const int tile0 = static_cast<int>((static_cast<long long>(n_tiles) * split) / p.n_split);
-  const int tile1 = static_cast<int>((static_cast<long long>(n_tiles) * (split + 1)) / p.n_split);
+  const int tile0 = static_cast<int>((static_cast<long long>(n_tiles) * split) / n_split);
+  const int tile1 = static_cast<int>((static_cast<long long>(n_tiles) * (split + 1)) / n_split);
   const int my_tiles = tile1 - tile0;
 
-  if (threadIdx.x == 0 && !room && blockIdx.x == 0) report(GLANCE_DEV_TREE_CAPACITY);
+  if (threadIdx.x == 0 && !room && local == 0) report(GLANCE_DEV_TREE_CAPACITY);
   // query pieces of this tile that hold no real (head, row): zero them so the
   // MMA reads finite values
   {
@@ -358,11 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K and V of a tile complete separately: QK^T needs only K, and V
         // lands while the tile's softmax runs
         mbar_arrive_expect_tx(&bars->k_full[st], 2 * kHalfBytes);
-        tma_load_3d(stage + 0 * kHalfBytes, &map_k, &bars->k_full[st], 0, key0, g, pol_kv);
-        tma_load_3d(stage + 1 * kHalfBytes, &map_k, &bars->k_full[st], 64, key0, g, pol_kv);
+        tma_load_3d(stage + 0 * kHalfBytes, map_k, &bars->k_full[st], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 1 * kHalfBytes, map_k, &bars->k_full[st], 64, key0, g, pol_kv);
         mbar_arrive_expect_tx(&bars->v_full[st], 2 * kHalfBytes);
-        tma_load_3d(stage + 2 * kHalfBytes, &map_v, &bars->v_full[st], 0, key0, g, pol_kv);
-        tma_load_3d(stage + 3 * kHalfBytes, &map_v, &bars->v_full[st], 64, key0, g, pol_kv);
+        tma_load_3d(stage + 2 * kHalfBytes, map_v, &bars->v_full[st], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 3 * kHalfBytes, map_v, &bars->v_full[st], 64, key0, g, pol_kv);
         ++issued;
       }
       if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
@@ -428,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t anc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      if (valid && w < p.W) anc[w] = p.anc[prow * p.W + w];
+      if (valid && w < p.W) anc[w] = p.anc[req][prow * p.W + w];
     // Every softmax thread reaches both named barriers of every tile; a failed
     // wait raises the CTA's abort flag, and all threads leave the loop
     // together right after the first barrier.
@@ -547,10 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(1, 256);
     l = lh + bars->xch[half ^ 1][lrow];
   }
-  if (p.n_split == 1) {
+  if (n_split == 1) {
     if (is_sm && ok && my_tiles > 0) {
       const float inv = 1.f / l;
-      __nv_bfloat16* dst = p.out + (static_cast<size_t>(prow) * p.Hq + head) * kD + 64 * half;
+      __nv_bfloat16* dst = p.out + (static_cast<size_t>(q_row0 + prow) * p.Hq + head) * kD + 64 * half;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
@@ -569,21 +599,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // The key splits of one (g, q tile) are co-resident (cooperative launch).
-    // Each CTA writes its partial O_s / l_s (bf16) and (m_s, l_s) per row to
-    // the workspace (L2-resident), publishes its arrival on the group counter
-    // with a release add, waits (bounded) until all splits have arrived, then
-    // merges the rows it owns:
-    //   O = sum_s w_s l_s (O_s / l_s) / sum_s w_s l_s,  w_s = 2^(m_s - M).
-    // The last CTA to leave resets the group's counters to zero.
-    const int S = p.n_split;
-    const int grp = blockIdx.x / S;
-    const int rpo = (kBM + S - 1) / S;  // rows per owner
-    const int own0 = split * rpo;
-    const int own_rows = own0 >= kBM ? 0 : (kBM - own0 < rpo ? kBM - own0 : rpo);
+    // Each split CTA writes its partial O_s / l_s (bf16) and (m_s, l_s) per
+    // row to the workspace (L2-resident) and publishes it on the group
+    // counter with a release add. The group is then merged as
+    //   O = sum_s w_s l_s (O_s / l_s) / sum_s w_s l_s,  w_s = 2^(m_s - M):
+    // * cooperative mode: every split waits (acquire loads, bounded) until
+    //   all have arrived and merges 1/S of the rows; the last to leave resets
+    //   both counters;
+    // * ticket mode: the split whose add completes the count acquires the
+    //   others' partials, merges all rows and resets the counter; nobody waits.
+    const int S = n_split;
+    const int slot = p.slot0[req] + grp_local * S;  // first partial slot of the group
+    int own0, own_rows;
     if (is_sm) {
       // column-major (dim octet, row): a warp's store covers 32 consecutive rows
-      uint4* po = p.part_o + (static_cast<size_t>(grp) * S + split) * 16 * kBM + lrow;
+      uint4* po = p.part_o + (static_cast<size_t>(slot) + split) * 16 * kBM + lrow;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
@@ -606,34 +636,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (half == 0)
-        p.part_ml[(static_cast<size_t>(grp) * S + split) * kBM + lrow] =
+        p.part_ml[(static_cast<size_t>(slot) + split) * kBM + lrow] =
             make_float2(my_tiles > 0 && ok ? m : -INFINITY, l);
       named_bar(1, 256);  // this CTA's partial is written (CTA scope)
       if (threadIdx.x == 128) {
         uint32_t* arrived = p.arrive + grp;
-        atom_add_release_gpu(arrived, 1u);  // cumulative release of the CTA's writes
-        const uint64_t t0 = globaltimer_ns();
-        bool done = false;
-        for (uint32_t i = 0;; ++i) {
-          if (ld_acquire_gpu(arrived) >= static_cast<uint32_t>(S)) {
-            done = true;
-            break;
+        if (p.ticket_merge) {
+          const uint32_t before = atom_add_acq_rel_gpu(arrived, 1u);
+          const bool last = before == static_cast<uint32_t>(S - 1);
+          if (last) *arrived = 0u;  // every split has added: ready for the next call
+          bars->xch[0][0] = last ? 1.f : 0.f;
+        } else {
+          atom_add_release_gpu(arrived, 1u);  // cumulative release of the CTA's writes
+          const uint64_t t0 = globaltimer_ns();
+          bool done = false;
+          for (uint32_t i = 0;; ++i) {
+            if (ld_acquire_gpu(arrived) >= static_cast<uint32_t>(S)) {
+              done = true;
+              break;
+            }
+            if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
           }
-          if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
-        }
-        if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
-        // the last split to leave resets both counters for the next call
-        uint32_t* departed = p.arrive + p.Hkv * p.n_qt + grp;
-        if (atomicAdd(departed, 1u) == static_cast<uint32_t>(S - 1)) {
-          *arrived = 0u;
-          *departed = 0u;
+          if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
+          // the last split to leave resets both counters for the next call
+          uint32_t* departed = p.arrive + p.B * p.Hkv * p.n_qt + grp;
+          if (atomicAdd(departed, 1u) == static_cast<uint32_t>(S - 1)) {
+            *arrived = 0u;
+            *departed = 0u;
+          }
         }
       }
       named_bar(1, 256);  // all splits' partials are visible (acquired above)
-      // this CTA owns tile rows [own0, own0 + own_rows): (row, 8 dims) per
+      if (p.ticket_merge) {
+        own0 = 0;
+        own_rows = bars->xch[0][0] != 0.f ? kBM : 0;
+      } else {
+        const int rpo = (kBM + S - 1) / S;  // rows per owner
+        own0 = split * rpo;
+        own_rows = own0 >= kBM ? 0 : (kBM - own0 < rpo ? kBM - own0 : rpo);
+      }
+      // this CTA merges tile rows [own0, own0 + own_rows): (row, 8 dims) per
       // item, rows fastest so that neighbouring threads read neighbouring rows
       const int t = threadIdx.x - 128;
-      const size_t grp_base = static_cast<size_t>(grp) * S * kBM;
+      const size_t grp_base = static_cast<size_t>(slot) * kBM;
       for (int item = t; item < own_rows * 16; item += 256) {
         const int c8 = item / own_rows, rr = item - c8 * own_rows;
         const int orow = own0 + rr;
@@ -644,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sx = 0; sx < kMaxSplit; ++sx) {
           mlr[sx] = sx < S ? __ldcg(p.part_ml + grp_base + static_cast<size_t>(sx) * kBM + orow)
                            : make_float2(-INFINITY, 0.f);
-          pv[sx] = sx < S ? __ldcg(p.part_o + ((static_cast<size_t>(grp) * S + sx) * 16 + c8) * kBM + orow)
+          pv[sx] = sx < S ? __ldcg(p.part_o + ((static_cast<size_t>(slot) + sx) * 16 + c8) * kBM + orow)
                           : make_uint4(0u, 0u, 0u, 0u);
         }
         float M = -INFINITY;
@@ -678,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.y = pack_bf16x2(acc[2], acc[3]);
           v.z = pack_bf16x2(acc[4], acc[5]);
           v.w = pack_bf16x2(acc[6], acc[7]);
-          *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(oprow) * p.Hq + g * p.G + ohl) * kD +
-                                    8 * c8) = v;
+          *reinterpret_cast<uint4*>(
+              p.out + (static_cast<size_t>(q_row0 + oprow) * p.Hq + g * p.G + ohl) * kD + 8 * c8) = v;
         }
       }
     }
@@ -698,26 +743,63 @@ int next_pow2_at_least(int x, int lo) {
   return r;
 }
 
-struct Geometry {
-  int G, Rp, n_qt, box_rows, n_split;
+// Launch plan of one bf16 call over B requests.
+struct Plan {
+  int G, Rp, n_qt, box_rows;
+  int n_split[kMaxB];
+  int cta0[kMaxB + 1];
+  int slot0[kMaxB];
+  int ticket;            // merge mode (see Bf16Params::ticket_merge)
+  size_t counters_bytes; // arrival / departure counters
+  size_t slots;          // partial slots of 128 rows
+  size_t ws_bytes;
 };
 
-Geometry geometry(int rows, int Hq, int Hkv) {
-  Geometry gm;
-  gm.G = Hq / Hkv;
-  gm.Rp = next_pow2_at_least(rows, 32);
-  gm.box_rows = gm.Rp < kBM ? gm.Rp : kBM;
-  gm.n_qt = (gm.G * gm.Rp + kBM - 1) / kBM;
-  // one CTA per SM and every CTA resident at once (cooperative launch)
-  int sp = glance::num_sms() / (Hkv * gm.n_qt);
-  gm.n_split = sp < 1 ? 1 : (sp > kMaxSplit ? kMaxSplit : sp);
-  return gm;
-}
-
-size_t bf16_ws_bytes(const Geometry& gm, int Hkv) {
-  if (gm.n_split == 1) return 256;
-  const size_t slots = static_cast<size_t>(Hkv) * gm.n_qt * gm.n_split * kBM;
-  return 256 + slots * kD * sizeof(__nv_bfloat16) + slots * sizeof(float2);
+// B == 1: one wave, one CTA per SM: S = SMs / groups key splits per group,
+// cooperative merge. B > 1: ticket merge and any number of waves; request
+// r's groups get S_r = ceil(tiles_r / tau) splits, tiles_r its key tiles at
+// full capacity (t_cap), tau chosen so that the grid is about two waves.
+Plan make_plan(int B, int rows, int Hq, const glance_kv* kv) {
+  Plan pl;
+  const int Hkv = kv[0].n_kv_heads;
+  pl.G = Hq / Hkv;
+  pl.Rp = next_pow2_at_least(rows, 32);
+  pl.box_rows = pl.Rp < kBM ? pl.Rp : kBM;
+  pl.n_qt = (pl.G * pl.Rp + kBM - 1) / kBM;
+  const int gpr = Hkv * pl.n_qt;  // groups per request
+  const int sms = glance::num_sms();
+  if (B == 1) {
+    const int sp = sms / gpr;
+    pl.n_split[0] = sp < 1 ? 1 : (sp > kMaxSplit ? kMaxSplit : sp);
+    pl.ticket = 0;
+  } else {
+    long long units = 0;
+    for (int r = 0; r < B; ++r) units += static_cast<long long>(gpr) * ((kv[r].t_cap + kBN - 1) / kBN);
+    long long tau = (units + 2ll * sms - 1) / (2ll * sms);
+    if (tau < 4) tau = 4;
+    for (int r = 0; r < B; ++r) {
+      const long long tiles = (kv[r].t_cap + kBN - 1) / kBN;
+      long long sp = (tiles + tau - 1) / tau;
+      pl.n_split[r] = static_cast<int>(sp < 1 ? 1 : (sp > kMaxSplit ? kMaxSplit : sp));
+    }
+    pl.ticket = 1;
+  }
+  pl.cta0[0] = 0;
+  size_t slots = 0;
+  for (int r = 0; r < B; ++r) {
+    pl.cta0[r + 1] = pl.cta0[r] + gpr * pl.n_split[r];
+    pl.slot0[r] = static_cast<int>(slots);
+    if (pl.n_split[r] > 1) slots += static_cast<size_t>(gpr) * pl.n_split[r];
+  }
+  for (int r = B; r < kMaxB; ++r) {
+    pl.n_split[r] = 1;
+    pl.cta0[r + 1] = pl.cta0[B];
+    pl.slot0[r] = static_cast<int>(slots);
+  }
+  pl.slots = slots;
+  pl.counters_bytes = (2ull * B * gpr * sizeof(uint32_t) + 255) / 256 * 256;
+  pl.ws_bytes = pl.counters_bytes + slots * kBM * (kD * sizeof(__nv_bfloat16) + sizeof(float2));
+  return pl;
 }
 
 glance_status check_common(const void* q, int n_q_heads, const glance_kv* kv,
@@ -740,6 +822,153 @@ glance_status check_common(const void* q, int n_q_heads, const glance_kv* kv,
   return GLANCE_OK;
 }
 
+// Checks shared by the bf16 single and batched calls.
+glance_status check_bf16(const char* who, const void* q, int n_q_heads, const glance_kv* kv,
+                         const glance_tree* trees, int B, const void* out) {
+  using glance::fail;
+  if (!q || !kv || !trees || !out)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (B < 1 || B > kMaxB) return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= B <= %d", who, kMaxB);
+  const int rows = trees[0].n + 1;
+  for (int r = 0; r < B; ++r) {
+    const glance_kv& x = kv[r];
+    const glance_tree& t = trees[r];
+    if (!x.k || !x.v || !x.t_len || !t.anc)
+      return fail(GLANCE_ERR_INVALID_ARG, "%s: null kv/tree array (request %d)", who, r);
+    if (t.n + 1 != rows || rows < 1 || rows > 256 || t.mask_words != (rows + 63) / 64)
+      return fail(GLANCE_ERR_INVALID_ARG,
+                  "%s: every tree needs the same N, 1 <= N+1 <= 256 and mask_words = "
+                  "ceil((N+1)/64) (request %d)", who, r);
+    if (x.dtype != GLANCE_BF16)
+      return fail(r == 0 && B == 1 ? GLANCE_ERR_INVALID_ARG : GLANCE_ERR_UNSUPPORTED,
+                  "%s: dtype must be BF16 here (request %d)", who, r);
+    if (x.head_dim != kD) return fail(GLANCE_ERR_UNSUPPORTED, "%s: bf16 needs head_dim 128", who);
+    if (x.n_kv_heads != kv[0].n_kv_heads || x.n_kv_heads < 1 || n_q_heads < 1 ||
+        n_q_heads % x.n_kv_heads != 0)
+      return fail(GLANCE_ERR_INVALID_ARG,
+                  "%s: n_q_heads must be a positive multiple of n_kv_heads, the same for every "
+                  "request (request %d)", who, r);
+    if (x.t_cap < rows || x.row_stride < x.head_dim ||
+        x.head_stride < static_cast<int64_t>(x.t_cap) * x.row_stride)
+      return fail(GLANCE_ERR_INVALID_ARG, "%s: bad kv geometry (request %d)", who, r);
+    if (!glance::aligned16(x.k) || !glance::aligned16(x.v) || (x.row_stride * 2) % 16 ||
+        (x.head_stride * 2) % 16)
+      return fail(GLANCE_ERR_INVALID_ARG,
+                  "%s: k/v must be 16-byte aligned with 16-byte strides (request %d)", who, r);
+    if (x.t_cap > (1 << 30)) return fail(GLANCE_ERR_UNSUPPORTED, "%s: t_cap too large", who);
+  }
+  const int G = n_q_heads / kv[0].n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: bf16 needs n_q_heads / n_kv_heads in {1, 2, 4, 8}",
+                who);
+  if (!glance::aligned16(q) || !glance::aligned16(out))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: q and out must be 16-byte aligned", who);
+  return GLANCE_OK;
+}
+
+template <int NB>
+glance_status launch_bf16(const char* who, const void* q, int n_q_heads, const glance_kv* kv,
+                          const glance_tree* trees, int B, float scale, void* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  using glance::fail;
+  glance_status st = check_bf16(who, q, n_q_heads, kv, trees, B, out);
+  if (st != GLANCE_OK) return st;
+  const int rows = trees[0].n + 1;
+  if (B > NB) return fail(GLANCE_ERR_INVALID_ARG, "%s: B too large", who);
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(tree_attention_bf16_kernel<NB>),
+                                      static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  const Plan pl = make_plan(B, rows, n_q_heads, kv);
+  if (!workspace || workspace_bytes < pl.ws_bytes)
+    return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                pl.ws_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  CUtensorMap mq;
+  KVMaps<NB> maps;
+  {
+    // all requests' rows stacked: [B * rows][Hq][128]
+    const uint64_t dims[3] = {kD, static_cast<uint64_t>(n_q_heads),
+                              static_cast<uint64_t>(B) * rows};
+    const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(n_q_heads) * kD * 2ull};
+    const uint32_t box[3] = {64, 1, static_cast<uint32_t>(pl.box_rows)};
+    st = glance::make_map_bf16(&mq, q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  for (int r = 0; r < NB; ++r) {
+    const glance_kv& x = kv[r < B ? r : 0];
+    const uint64_t dims[3] = {kD, static_cast<uint64_t>(x.t_cap),
+                              static_cast<uint64_t>(x.n_kv_heads)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(x.row_stride) * 2ull,
+                                 static_cast<uint64_t>(x.head_stride) * 2ull};
+    const uint32_t box[3] = {64, kBN, 1};
+    if (r >= B) {
+      maps.k[r] = maps.k[0];
+      maps.v[r] = maps.v[0];
+      continue;
+    }
+    st = glance::make_map_bf16(&maps.k[r], x.k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                               who);
+    if (st != GLANCE_OK) return st;
+    st = glance::make_map_bf16(&maps.v[r], x.v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                               who);
+    if (st != GLANCE_OK) return st;
+  }
+  Bf16Params<NB> p;
+  for (int r = 0; r < NB; ++r) {
+    const int rr = r < B ? r : 0;
+    p.anc[r] = trees[rr].anc;
+    p.t_len[r] = kv[rr].t_len;
+    p.t_cap[r] = kv[rr].t_cap;
+    p.n_split[r] = pl.n_split[r];
+    p.slot0[r] = pl.slot0[r];
+  }
+  for (int r = 0; r <= NB; ++r) p.cta0[r] = pl.cta0[r];
+  p.out = static_cast<__nv_bfloat16*>(out);
+  {
+    // [counters][partial O][partial (m, l)]
+    char* ws = static_cast<char*>(workspace);
+    p.arrive = reinterpret_cast<uint32_t*>(ws);
+    p.part_o = reinterpret_cast<uint4*>(ws + pl.counters_bytes);
+    p.part_ml = reinterpret_cast<float2*>(ws + pl.counters_bytes +
+                                          pl.slots * kBM * kD * sizeof(__nv_bfloat16));
+  }
+  p.B = B;
+  p.rows = rows;
+  p.Hq = n_q_heads;
+  p.Hkv = kv[0].n_kv_heads;
+  p.G = pl.G;
+  p.Rp = pl.Rp;
+  p.n_qt = pl.n_qt;
+  p.W = trees[0].mask_words;
+  p.box_rows = pl.box_rows;
+  p.ticket_merge = pl.ticket;
+  p.scale_log2 = scale * kLog2e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.cta0[B]);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
+  // may start while the previous kernel in the stream finishes (the kernel
+  // waits for it with griddepcontrol.wait before reading its inputs)
+  attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+  ++n_attr;
+  if (!pl.ticket) {
+    // the key splits of a group wait for each other: every CTA must be resident
+    attr[n_attr].id = cudaLaunchAttributeCooperative;
+    attr[n_attr].val.cooperative = 1;
+    ++n_attr;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n_attr;
+  e = cudaLaunchKernelEx(&cfg, tree_attention_bf16_kernel<NB>, mq, maps, p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
+
 }  // namespace
 
 extern "C" size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_heads,
@@ -748,7 +977,7 @@ extern "C" size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_head
       n_q_heads % kv->n_kv_heads)
     return 0;
   if (kv->dtype != GLANCE_BF16) return 256;
-  return bf16_ws_bytes(geometry(n_rows, n_q_heads, kv->n_kv_heads), kv->n_kv_heads);
+  return make_plan(1, n_rows, n_q_heads, kv).ws_bytes;
 }
 
 extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, const glance_kv* kv,
@@ -787,89 +1016,25 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
   }
   if (kv->dtype != GLANCE_BF16)
     return fail(GLANCE_ERR_INVALID_ARG, "glance_tree_attention: dtype must be F32 or BF16");
-  if (kv->head_dim != kD)
-    return fail(GLANCE_ERR_UNSUPPORTED, "glance_tree_attention: bf16 needs head_dim 128");
-  const int G = n_q_heads / kv->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8)
-    return fail(GLANCE_ERR_UNSUPPORTED,
-                "glance_tree_attention: bf16 needs n_q_heads / n_kv_heads in {1, 2, 4, 8}");
-  if (!glance::aligned16(q) || !glance::aligned16(kv->k) || !glance::aligned16(kv->v) ||
-      !glance::aligned16(out) || (kv->row_stride * 2) % 16 || (kv->head_stride * 2) % 16)
-    return fail(GLANCE_ERR_INVALID_ARG,
-                "glance_tree_attention: q/k/v/out must be 16-byte aligned with 16-byte strides");
-  if (kv->t_cap > (1 << 30))
-    return fail(GLANCE_ERR_UNSUPPORTED, "glance_tree_attention: t_cap too large");
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(tree_attention_bf16_kernel),
-                                      static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: smem attribute");
-  const Geometry gm = geometry(rows, n_q_heads, kv->n_kv_heads);
-  const size_t need = bf16_ws_bytes(gm, kv->n_kv_heads);
-  if (!workspace || workspace_bytes < need)
-    return fail(GLANCE_ERR_CAPACITY, "glance_tree_attention: workspace %zu bytes < %zu needed",
-                workspace_bytes, need);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_tree_attention: workspace must be 256-byte aligned");
-  CUtensorMap mq, mk, mv;
-  {
-    const uint64_t dims[3] = {kD, static_cast<uint64_t>(n_q_heads), static_cast<uint64_t>(rows)};
-    const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(n_q_heads) * kD * 2ull};
-    const uint32_t box[3] = {64, 1, static_cast<uint32_t>(gm.box_rows)};
-    st = glance::make_map_bf16(&mq, q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                               "glance_tree_attention: q map");
-    if (st != GLANCE_OK) return st;
-  }
-  {
-    const uint64_t dims[3] = {kD, static_cast<uint64_t>(kv->t_cap),
-                              static_cast<uint64_t>(kv->n_kv_heads)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(kv->row_stride) * 2ull,
-                                 static_cast<uint64_t>(kv->head_stride) * 2ull};
-    const uint32_t box[3] = {64, kBN, 1};
-    st = glance::make_map_bf16(&mk, kv->k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                               "glance_tree_attention: k map");
-    if (st != GLANCE_OK) return st;
-    st = glance::make_map_bf16(&mv, kv->v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                               "glance_tree_attention: v map");
-    if (st != GLANCE_OK) return st;
-  }
-  Bf16Params p;
-  p.anc = tree->anc;
-  p.t_len = kv->t_len;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  {
-    // [256 B counters][partial O][partial (m, l)]
-    const size_t slots = static_cast<size_t>(kv->n_kv_heads) * gm.n_qt * gm.n_split * kBM;
-    char* ws = static_cast<char*>(workspace);
-    p.arrive = reinterpret_cast<uint32_t*>(ws);
-    p.part_o = reinterpret_cast<uint4*>(ws + 256);
-    p.part_ml = reinterpret_cast<float2*>(ws + 256 + slots * kD * sizeof(__nv_bfloat16));
-  }
-  p.rows = rows;
-  p.Hq = n_q_heads;
-  p.Hkv = kv->n_kv_heads;
-  p.G = gm.G;
-  p.Rp = gm.Rp;
-  p.n_qt = gm.n_qt;
-  p.n_split = gm.n_split;
-  p.W = tree->mask_words;
-  p.t_cap = kv->t_cap;
-  p.box_rows = gm.box_rows;
-  p.scale_log2 = scale * kLog2e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kv->n_kv_heads * gm.n_qt * gm.n_split);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  // the key splits of a group wait for each other: every CTA must be resident
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  // may start while the previous kernel in the stream finishes (the kernel
-  // waits for it with griddepcontrol.wait before reading its inputs)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, tree_attention_bf16_kernel, mq, mk, mv, p);
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_tree_attention: launch");
-  return GLANCE_OK;
+  return launch_bf16<1>("glance_tree_attention", q, n_q_heads, kv, tree, 1, scale, out,
+                        workspace, workspace_bytes, s);
+}
+
+extern "C" size_t glance_tree_attention_batched_workspace_bytes(int B, int n_rows, int n_q_heads,
+                                                                const glance_kv* kv) {
+  if (!kv || B < 1 || B > kMaxB || n_rows < 1 || n_rows > 256 || n_q_heads < 1) return 0;
+  for (int r = 0; r < B; ++r)
+    if (kv[r].n_kv_heads != kv[0].n_kv_heads || kv[r].n_kv_heads < 1 ||
+        n_q_heads % kv[r].n_kv_heads || kv[r].dtype != GLANCE_BF16 || kv[r].t_cap < 1)
+      return 0;
+  return make_plan(B, n_rows, n_q_heads, kv).ws_bytes;
+}
+
+extern "C" glance_status glance_tree_attention_batched(const void* q, int n_q_heads,
+                                                       const glance_kv* kv,
+                                                       const glance_tree* trees, int B,
+                                                       float scale, void* out, void* workspace,
+                                                       size_t workspace_bytes, void* stream) {
+  return launch_bf16<kMaxB>("glance_tree_attention_batched", q, n_q_heads, kv, trees, B, scale,
+                            out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
