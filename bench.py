@@ -32,6 +32,8 @@ FULL36 = dict(name="full36", T=4096, N=63, L=15, V=151936, d=4096, n_layers=36, 
               D=128, path_depth=(3, 15))
 SMALL = dict(name="small", T=512, N=31, L=15, V=16384, d=512, n_layers=4, Hq=32, Hkv=8, D=128,
              path_depth=(3, 15))
+RAGGED8 = dict(name="ragged8", B=8, T_range=(512, 8192), entropy=(0.3, 1.5, 4.0), N=63, L=15,
+               V=151936, d=4096, n_layers=36, Hq=32, Hkv=8, D=128, path_depth=(3, 15))
 
 
 def peaks():
@@ -49,7 +51,7 @@ def peaks():
 # the listed files, and a changed source reports traffic null.
 CSRC = os.path.join("tree_verified_block_gb300", "csrc")
 NCU_TRAFFIC = {
-    "glance_tree_attention": dict(bytes=17_889_792, digest="8673c360cd2cd1fc",
+    "glance_tree_attention": dict(bytes=17_895_424, digest="0373385bf58664ae",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
     "glance_lmhead_argmax": dict(bytes=1_245_328_000 + 2_759_424, digest="25ca914779b9aa6c",
@@ -196,6 +198,117 @@ class Workload:
         c = self.cfg
         lm = 2 * self.R * c["d"] * c["V"]
         return dict(lmhead=lm)
+
+
+class BatchedWorkload:
+    """B concurrent requests with ragged prefix lengths T ~ U{512..8192}, each
+    with its own draft marginals (entropy 0.3 / 1.5 / 4.0 nats cycled), root,
+    N = 63 tree and per-request KV caches; one launch per step over the batch
+    and the LM head over the B x 64 stacked rows.
+
+    host=True draws every input with the seeded numpy generators (the oracle
+    can recompute from the host copies); host=False draws q, K, V and W with a
+    seeded torch generator on the device (same distributions; for timing,
+    where 36 layers of ragged caches would take minutes to draw on the host).
+    """
+
+    def __init__(self, cfg, dev, seed=5000, host=True, n_layers=None):
+        import torch
+        import tree_verified_block_gb300 as g
+        c = dict(cfg)
+        if n_layers is not None:
+            c["n_layers"] = n_layers
+        self.cfg, self.dev, self.g, self.host = c, dev, g, host
+        B, R, D = c["B"], c["N"] + 1, c["D"]
+        self.B, self.R = B, R
+        gen = W.rng(seed)
+        lo, hi = c["T_range"]
+        self.T = [int(t) for t in gen.integers(lo, hi + 1, size=B)]
+        self.t_cap = [t + R + 64 for t in self.T]
+        self.x = np.stack([W.draft_logits_entropy(c["L"], c["V"], c["entropy"][r % len(c["entropy"])],
+                                                  seed=seed + 1 + r) for r in range(B)])
+        bf = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+        if host:
+            self.q_bits = [W.normal_bf16(gen, (B, R, c["Hq"], D)) for _ in range(c["n_layers"])]
+            self.k_bits = [[W.normal_bf16(gen, (c["Hkv"], self.t_cap[r], D)) for r in range(B)]
+                           for _ in range(c["n_layers"])]
+            self.v_bits = [[W.normal_bf16(gen, (c["Hkv"], self.t_cap[r], D)) for r in range(B)]
+                           for _ in range(c["n_layers"])]
+            self.W_bits = W.normal_bf16(gen, (c["d"], c["V"]), std=0.02)
+            self.q = [bf(b) for b in self.q_bits]
+            self.k = [[bf(b) for b in kl] for kl in self.k_bits]
+            self.v = [[bf(b) for b in vl] for vl in self.v_bits]
+            self.W = bf(self.W_bits)
+            h = gen.standard_normal((B * R, c["d"]), dtype=np.float32)
+            self.h_f32 = torch.from_numpy(h).to(dev)
+        else:
+            tg = torch.Generator(device=dev)
+            tg.manual_seed(seed)
+            rn = lambda *shape, std=1.0: (torch.randn(*shape, generator=tg, device=dev) * std).to(torch.bfloat16)
+            self.q = [rn(B, R, c["Hq"], D) for _ in range(c["n_layers"])]
+            self.k = [[rn(c["Hkv"], self.t_cap[r], D) for r in range(B)] for _ in range(c["n_layers"])]
+            self.v = [[rn(c["Hkv"], self.t_cap[r], D) for r in range(B)] for _ in range(c["n_layers"])]
+            self.W = rn(c["d"], c["V"], std=0.02)
+            self.h_f32 = torch.randn(B * R, c["d"], generator=tg, device=dev)
+            self.q_bits = self.k_bits = self.v_bits = self.W_bits = None
+        self.x_dev = torch.from_numpy(self.x.astype(np.float32)).to(dev)
+        self.t0 = torch.tensor(self.T, dtype=torch.int32, device=dev)
+        self.t_len = self.t0.clone()
+        self.root = torch.from_numpy(gen.integers(0, c["V"], size=B).astype(np.int32)).to(dev)
+        # layers[l][r] for attention, by_req[r][l] for the commit
+        self.layers = [[g.KVLayer(self.k[l][r], self.v[l][r], self.t_len[r:r + 1]) for r in range(B)]
+                       for l in range(c["n_layers"])]
+        self.by_req = [[self.layers[l][r] for l in range(c["n_layers"])] for r in range(B)]
+        self.trees = [g.Tree(c["N"], c["L"], dev) for _ in range(B)]
+        self.out = [torch.empty_like(q) for q in self.q]
+        M = B * R
+        self.argmax = torch.empty(M, dtype=torch.int32, device=dev)
+        self.gap = torch.empty(M, dtype=torch.float32, device=dev)
+        self.maxlogit = torch.empty(M, dtype=torch.float32, device=dev)
+        self.n_acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.acc_tok = torch.zeros((B, c["L"]), dtype=torch.int32, device=dev)
+        self.new_root = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.ws_tree = g.workspace(g.build_tree_batched_workspace_bytes(B, c["L"], c["V"], c["N"]), dev)
+        self.ws_attn = g.workspace(g.tree_attention_batched_workspace_bytes(R, c["Hq"], self.layers[0]), dev)
+        self.ws_lm = g.workspace(g.lmhead_argmax_workspace_bytes(M, c["d"], c["V"], torch.bfloat16), dev)
+        self.ws_c = g.workspace(g.accept_commit_batched_workspace_bytes(B, c["n_layers"]), dev)
+        # h: each request's rows planted so that its walk follows its best chain
+        g.build_tree_batched(self.x_dev, c["N"], self.root, self.t_len, self.trees, self.ws_tree)
+        self.tree_host = [t.to_host() for t in self.trees]
+        self.path_rows, self.path_tokens = [], []
+        hp = self.h_f32.clone()
+        for r in range(B):
+            rows, toks = Workload._chain(self, self.tree_host[r], gen)
+            self.path_rows.append(rows)
+            self.path_tokens.append(toks)
+            for u, t in zip(rows, toks):
+                col = self.W[:, t].double()
+                hp[r * R + u] += (10.0 * col / (col @ col)).float()
+        self.h = hp.to(torch.bfloat16)
+        self.h_bits = self.h.view(torch.int16).cpu().numpy().view(np.uint16) if host else None
+
+    def step(self):
+        g, c = self.g, self.cfg
+        self.t_len.copy_(self.t0)
+        g.build_tree_batched(self.x_dev, c["N"], self.root, self.t_len, self.trees, self.ws_tree)
+        scale = c["D"] ** -0.5
+        for l in range(c["n_layers"]):
+            g.tree_attention_batched(self.q[l], self.layers[l], self.trees, scale, self.out[l],
+                                     self.ws_attn)
+        g.lmhead_argmax(self.h, self.W, self.argmax, self.gap, self.maxlogit, self.ws_lm)
+        g.accept_commit_batched(self.trees, self.argmax, self.by_req, self.n_acc, self.acc_tok,
+                                self.new_root, self.ws_c)
+
+    def algorithmic_bytes(self):
+        c = self.cfg
+        R = self.R
+        attn = sum((t + R) * c["Hkv"] * c["D"] * 2 * 2 for t in self.T) + 2 * self.B * R * c["Hq"] * c["D"] * 2
+        return dict(tree=self.B * c["L"] * c["V"] * 4, attn_layer=attn,
+                    lmhead=c["d"] * c["V"] * 2 + self.B * R * c["d"] * 2)
+
+    def flops(self):
+        c = self.cfg
+        return dict(lmhead=2 * self.B * self.R * c["d"] * c["V"])
 
 
 # ------------------------------------------------------------------ clocks
@@ -374,6 +487,82 @@ def stage_times(wl, reps=20):
     return res
 
 
+def run_batched(dev, reps=10):
+    """The ragged8 batched round (secondary measurement): whole round and
+    per-stage device times from CUDA-graph replays, with each stage's
+    fraction of its roof."""
+    bw = BatchedWorkload(RAGGED8, dev, seed=5000, host=False)
+    g, c = bw.g, bw.cfg
+    import torch
+    for _ in range(3):
+        bw.step()
+    torch.cuda.synchronize()
+    scale = c["D"] ** -0.5
+    st = {"round": graph_time_us(bw.step, reps)}
+
+    def tree():
+        bw.t_len.copy_(bw.t0)
+        g.build_tree_batched(bw.x_dev, c["N"], bw.root, bw.t_len, bw.trees, bw.ws_tree)
+    st["tree"] = graph_time_us(tree, reps)
+    st["attention_36"] = graph_time_us(
+        lambda: [g.tree_attention_batched(bw.q[l], bw.layers[l], bw.trees, scale, bw.out[l], bw.ws_attn)
+                 for l in range(c["n_layers"])], reps)
+    st["attention_layer"] = graph_time_us(
+        lambda: g.tree_attention_batched(bw.q[0], bw.layers[0], bw.trees, scale, bw.out[0], bw.ws_attn),
+        reps * 5)
+    st["lmhead_m512"] = graph_time_us(
+        lambda: g.lmhead_argmax(bw.h, bw.W, bw.argmax, bw.gap, bw.maxlogit, bw.ws_lm), reps)
+
+    def commit():
+        bw.t_len.copy_(bw.t0)
+        g.accept_commit_batched(bw.trees, bw.argmax, bw.by_req, bw.n_acc, bw.acc_tok, bw.new_root,
+                                bw.ws_c)
+    st["commit"] = graph_time_us(commit, reps)
+    pk = peaks()
+    by, fl = bw.algorithmic_bytes(), bw.flops()
+    lm_tf = fl["lmhead"] / (st["lmhead_m512"] * 1e-6) / 1e12
+    out = {"workload": f"ragged8: {c['B']} requests, T in {bw.T}, N={c['N']}, L={c['L']}, "
+                       f"V={c['V']}, d={c['d']}, {c['n_layers']} layers, LM head M={bw.B * bw.R}",
+           "rounds_per_s": round(1e6 / st["round"], 2),
+           "request_rounds_per_s": round(bw.B * 1e6 / st["round"], 2),
+           "stages_us": {k: round(v, 2) for k, v in st.items()},
+           "attention_layer_hbm_frac": round(by["attn_layer"] / (st["attention_layer"] * 1e-6) / 1e9 / pk["hbm"], 4),
+           "lmhead_m512_tflops": round(lm_tf, 1),
+           "lmhead_m512_tensor_frac": round(lm_tf / pk["bf16"], 4),
+           "lmhead_m512_hbm_frac": round(by["lmhead"] / (st["lmhead_m512"] * 1e-6) / 1e9 / pk["hbm"], 4),
+           "data": "synthetic, q/K/V/W drawn on the device (seeded torch generator)"}
+    return out
+
+
+def run_case(args):
+    """One kernel alone on a small case (a few GB on the device), launched
+    warmup + steps times, for profiler captures; prints its graph-timed
+    duration. lmhead512: the LM head over 512 stacked rows, [512, 4096] x
+    [4096, 151936], inputs drawn on the device."""
+    import torch
+    import tree_verified_block_gb300 as g
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    M, d, V = 512, 4096, 151936
+    tg = torch.Generator(device=dev)
+    tg.manual_seed(7)
+    h = torch.randn(M, d, generator=tg, device=dev).to(torch.bfloat16)
+    Wt = (torch.randn(d, V, generator=tg, device=dev) * 0.02).to(torch.bfloat16)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    gap = torch.empty(M, dtype=torch.float32, device=dev)
+    mx = torch.empty(M, dtype=torch.float32, device=dev)
+    ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.bfloat16), dev)
+    fn = lambda: g.lmhead_argmax(h, Wt, am, gap, mx, ws)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    us = graph_time_us(fn, 10)
+    tf = 2 * M * d * V / (us * 1e-6) / 1e12
+    pk = peaks()
+    print(json.dumps({"case": args.case, "us": round(us, 2), "tflops": round(tf, 1),
+                      "tensor_frac": round(tf / pk["bf16"], 4)}), flush=True)
+
+
 def max_over_ranks(ms, dist, device):
     """Slowest rank's time: the job's time (replicas run independent rounds)."""
     if dist is None:
@@ -460,6 +649,7 @@ def run_gpu(args):
     stages["tree_hbm_frac"] = round(bytes_["tree"] / (st["tree"] * 1e-6) / 1e9 / pk["hbm"], 4)
 
     e2e = run_e2e(wl, args.steps)
+    batched = run_batched(dev) if (args.batched and rank == 0) else None
     code, text = g.device_status()
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": world,
@@ -474,6 +664,8 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "device_status": code,
     }
+    if batched is not None:
+        out["ragged8"] = batched
     if rank == 0:
         if args.cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(cfg, wl)
@@ -627,10 +819,16 @@ def main():
     ap.add_argument("--impl", default="glance", choices=["glance", "reference"])
     ap.add_argument("--workload", default="full36", choices=["full36", "small"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--case", default=None, choices=["lmhead512"],
+                    help="run one kernel alone on a small case (for profiler captures)")
+    ap.add_argument("--no-batched", dest="batched", action="store_false",
+                    help="skip the secondary ragged8 batched-round measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -9,15 +9,17 @@
 // equal maxima), gap = max - (largest logit of any other id), max. The logits
 // never leave the chip.
 //
-// bf16 path (tcgen05): persistent CTAs, one per SM, each walking vocabulary
-// tiles of 256 columns. Warp 0 streams h (K-major, 128-byte swizzle) and W
+// bf16 path (tcgen05), M <= 128: persistent CTAs, one per SM, each walking
+// vocabulary tiles of 256 columns. Warp 0 streams h (K-major, 128-byte swizzle) and W
 // ([d][V] row-major, so V is the MN-major side of the B operand) through a
 // 4-stage TMA ring; warp 1 issues M=128 x N=256 x K=16 MMAs into one of two
 // tensor-memory accumulators; warps 4..7 each own one row (one TMEM lane),
 // read the tile's 256 fp32 logits and fold them into a running
 // (max, argmax, second max) held in registers across tiles, while the MMA
 // warp fills the other accumulator. CTAs write per-row partials; the last CTA
-// (atomic ticket) merges them, one warp per row.
+// (atomic ticket) merges them, one warp per row. M > 128 (rows of several
+// requests stacked, up to 512): clusters of two CTAs split the rows and share
+// each W tile through TMA multicast, one launch, W read from HBM once.
 // fp32 path: CUDA cores, 128 vocabulary columns x 8 rows per CTA.
 #include <mutex>
 
@@ -161,15 +163,11 @@ constexpr int kThreads = 256;
 constexpr uint32_t kABytes = kBM * kBK * 2;    // one row block's K slice: 16 KB
 constexpr uint32_t kWBoxBytes = kBK * 64 * 2;  // one 64 x 64 box of W: 8 KB
 
-// Tile shapes by the number NB of 128-row blocks of h (M <= 128 * NB): every
-// vocabulary tile of BN columns is multiplied by all NB row blocks from the
-// same W stage, so W streams from HBM once whatever M is. The NB x BN fp32
-// accumulators of a tile take NB * BN TMEM columns; with NBUF = 2 the MMA
-// warp fills one set while the epilogue drains the other.
-//   NB = 1: BN 256, 4 stages of 48 KB, 2 accumulator sets
-//   NB = 2: BN 128, 4 stages of 48 KB, 2 sets
-//   NB = 3: BN 128, 3 stages of 64 KB, 1 set
-//   NB = 4: BN 128, 2 stages of 80 KB, 1 set
+// Tile shape of the single-CTA kernel by the number NB of 128-row blocks of
+// h it multiplies with each W stage (the library launches it with NB = 1, M
+// <= 128: BN 256, 4 stages of 48 KB, two accumulator sets of 256 columns so
+// the epilogue drains one while the MMA warp fills the other; larger M runs
+// on CTA pairs, below).
 template <int NB>
 struct Shape {
   static constexpr int BN = NB == 1 ? 256 : 128;
@@ -408,6 +406,216 @@ __global__ void __launch_bounds__(kThreads, 1)
   merge_partials(p.part, gridDim.x, NB * kBM, p.M, p.argmax, p.gap, p.maxlogit);
 }
 
+// ---------------------------------------------- bf16, M > 128: CTA pairs
+//
+// Rows 0..M-1 are split over the two CTAs of a cluster (rank 0: the first
+// NB * 128 rows, rank 1: the next NB * 128); both walk the same vocabulary
+// tiles of 256 columns in lockstep. Each loads its own rows of h and one half
+// of the W tile, which it multicasts to both CTAs, so every W byte leaves L2
+// once per pair and each SM requests NB * 16 + 16 KB per K slice instead of
+// NB * 32 + 32 KB. A stage is refilled only when both CTAs' MMAs are done with
+// it: the MMA warps' commits arrive on the stage's empty barrier in both CTAs.
+//   NB = 1 (M <= 256): 4 stages of 48 KB, 2 accumulator sets of 256 columns
+//   NB = 2 (M <= 512): 3 stages of 64 KB, 1 accumulator set of 2 x 256
+template <int NB>
+struct PairShape {
+  static constexpr int BN = 256;
+  static constexpr int STAGES = NB == 1 ? 4 : 3;
+  static constexpr int NBUF = NB == 1 ? 2 : 1;
+  static constexpr uint32_t kBBytes = kBK * BN * 2;
+  static constexpr uint32_t kStageBytes = NB * kABytes + kBBytes;
+  static constexpr size_t kSmem = 1024 + STAGES * kStageBytes + 256;
+  static_assert(NB * BN * NBUF <= 512, "tensor memory");
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_h,
+                            const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
+  using Sh = PairShape<NB>;
+  constexpr int BN = Sh::BN, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
+  constexpr uint16_t kBoth = 0x3;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars<STAGES>* bars = reinterpret_cast<Bars<STAGES>*>(smem + STAGES * Sh::kStageBytes);
+  __shared__ uint32_t s_ticket;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int row0 = rank * NB * kBM;  // this CTA's first row of h
+  const int n_kb = p.d / kBK;
+  const int my_tiles = (p.n_tiles - pair + n_pairs - 1) / n_pairs;  // same for both CTAs
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 2);  // both CTAs' MMA warps release a stage
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 128);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  // both CTAs' barriers exist before either multicasts into the other
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&map_h);
+      tma_prefetch_desc(&map_w);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int v0 = (pair + i * n_pairs) * BN;
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % STAGES;
+          if (it >= STAGES && !wait_or_abort(&bars->empty[st], ((it / STAGES) - 1) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          unsigned char* stage = smem + st * Sh::kStageBytes;
+          // own rows of h (rows past M read as zeros) + the whole W slice, half of
+          // which the peer multicasts here
+          mbar_arrive_expect_tx(&bars->full[st], NB * kABytes + Sh::kBBytes);
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+            tma_load_2d(stage + b * kABytes, &map_h, &bars->full[st], kb * kBK, row0 + b * kBM, pol_h);
+#pragma unroll
+          for (int q = 2 * rank; q < 2 * rank + 2; ++q)
+            tma_load_2d_mcast(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[st],
+                              v0 + 64 * q, kb * kBK, kBoth, pol_w);
+        }
+      }
+      if (!ok) {
+        fail_pipeline(bars);
+        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+          (void)mbar_wait(&bars->full[j % STAGES], (j / STAGES) & 1, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, true);
+      const uint32_t s0 = smem_u32(smem);
+      int it = 0;
+      bool ok = true;
+      const int total_it = my_tiles * n_kb;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int buf = NBUF == 2 ? (i & 1) : 0;
+        const int use = NBUF == 2 ? (i >> 1) : i;
+        if (use >= 1 && !wait_or_abort(&bars->acc_empty[buf], (use - 1) & 1, bars)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * (NB * BN);
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int st = it % STAGES;
+          if (!wait_or_abort(&bars->full[st], (it / STAGES) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st_addr = s0 + st * Sh::kStageBytes;
+          const uint32_t b_addr = st_addr + NB * kABytes;
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_ss(d_tmem + b * BN, sdesc_sw128(st_addr + b * kABytes + k * 32, 16, 1024),
+                          sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+          // stages that will be refilled: release them in both CTAs
+          if (it + STAGES < total_it) mma_commit_mcast(&bars->empty[st], kBoth);
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full[buf]);
+      }
+      if (!ok) fail_pipeline(bars);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m1[NB], m2[NB];
+    int i1[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      m1[b] = -INFINITY;
+      m2[b] = -INFINITY;
+      i1[b] = 0x7FFFFFFF;
+    }
+    bool ok = true;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int buf = NBUF == 2 ? (i & 1) : 0;
+      const int use = NBUF == 2 ? (i >> 1) : i;
+      if (!wait_or_abort(&bars->acc_full[buf], use & 1, bars)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int v0 = (pair + i * n_pairs) * BN;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint32_t t_acc = tmem + buf * (NB * BN) + b * BN + lane_off;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_acc + c * 32, r);
+          tmem_ld_wait();
+          const int col0 = v0 + c * 32;
+          if (col0 + 32 <= p.V) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[buf]);
+    }
+    if (!ok) fail_pipeline(bars);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int grow = row0 + b * kBM + row;
+      if (grow < p.M) p.part[static_cast<size_t>(pair) * (2 * NB * kBM) + grow] = Partial{m1[b], i1[b], m2[b]};
+    }
+  }
+  tc_fence_before();
+  // neither CTA leaves while the other may still touch its shared memory
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(p.ticket, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
+  __threadfence();
+  if (threadIdx.x == 0) *p.ticket = 0;
+  merge_partials(p.part, n_pairs, 2 * NB * kBM, p.M, p.argmax, p.gap, p.maxlogit);
+}
+
 int row_blocks(int M) { return (M + kBM - 1) / kBM; }
 
 size_t ws_bytes_bf16(int M) {
@@ -457,6 +665,83 @@ size_t ws_bytes_f32(int M, int V) {
   return 256 + (static_cast<size_t>(colblks) * M * sizeof(Partial) + 255) / 256 * 256;
 }
 
+// Clusters of 2 that can be resident at once with this kernel's shared
+// memory, per device (queried once).
+template <int NB>
+int max_pairs() {
+  static int cached[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * glance::num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairShape<NB>::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_bf16_pair_kernel<NB>, &cfg) != cudaSuccess || n < 1)
+      n = -1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int NB>
+glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
+                          float* gap, float* maxlogit, Partial* part, uint32_t* ticket,
+                          cudaStream_t s, const char* who) {
+  using Sh = PairShape<NB>;
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_pair_kernel<NB>),
+                                      static_cast<int>(Sh::kSmem));
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
+  int pairs = max_pairs<NB>();
+  if (pairs < 1) return glance::fail(GLANCE_ERR_CUDA, "%s: no resident CTA pair fits", who);
+  if (pairs > n_tiles) pairs = n_tiles;
+  if (2 * pairs > glance::num_sms()) pairs = glance::num_sms() / 2;
+  CUtensorMap mw, mh;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(d)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(V) * 2ull};
+    const uint32_t box[2] = {64, kBK};
+    glance_status st = glance::make_map_bf16(&mw, W, 2, dims, strides, box,
+                                             CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2ull};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(kBM)};
+    glance_status st = glance::make_map_bf16(&mh, h, 2, dims, strides, box,
+                                             CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  Bf16Params p{M, d, V, n_tiles, kBM, argmax, gap, maxlogit, part, ticket};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Sh::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_pair_kernel<NB>, mh, mw, p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
+
 }  // namespace
 
 extern "C" size_t glance_lmhead_argmax_workspace_bytes(int M, int d, int V, glance_dtype dtype) {
@@ -499,20 +784,14 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
     return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace %zu bytes < %zu needed",
                 workspace_bytes, ws_bytes_bf16(M));
   // one launch: W streams once for all rows
-  switch (row_blocks(M)) {
-    case 1:
-      return launch_bf16<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
-                            "glance_lmhead_argmax");
-    case 2:
-      return launch_bf16<2>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
-                            "glance_lmhead_argmax");
-    case 3:
-      return launch_bf16<3>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
-                            "glance_lmhead_argmax");
-    default:
-      return launch_bf16<4>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
-                            "glance_lmhead_argmax");
-  }
+  if (M <= kBM)
+    return launch_bf16<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
+                          "glance_lmhead_argmax");
+  if (M <= 2 * kBM)
+    return launch_pair<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, s,
+                          "glance_lmhead_argmax");
+  return launch_pair<2>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, s,
+                        "glance_lmhead_argmax");
 }
 
 // ------------------------------------------------- no-allocation entry point
