@@ -319,6 +319,21 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
       "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
       : "memory");
 }
+// Bulk copy global -> this CTA's shared memory (16-byte aligned addresses, a
+// multiple of 16 bytes), counted on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Orders this thread's earlier generic-proxy view of global memory (including
+// what it acquired from other threads) before its later async-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

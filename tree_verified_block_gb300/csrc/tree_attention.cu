@@ -191,6 +191,7 @@ struct __align__(8) Bars {
   uint64_t s_full[2];
   uint64_t p_ready;
   uint64_t o_done;
+  uint64_t merge_full;       // ticket-mode merge: partials staged in shared memory
   uint32_t tmem_base;
   int abort_flag;
   float xch[2][kBM];         // [half][row]: partial max / sum exchange
@@ -239,6 +240,101 @@ __device__ __forceinline__ uint32_t visible32(const uint64_t (&a)[4], int kb, in
   return prefix_mask | (tree_bits & rows_mask);
 }
 
+// Ticket mode: the last split of a group merges all 128 rows from shared
+// memory (the K/V ring and Q area are idle by now). The splits' (m, l) go
+// first, then their partials (O_s / l_s, bf16, 32 KB per split, contiguous in
+// the workspace) in chunks of kMergeChunk splits, one bulk copy each. Called
+// by the 256 softmax threads; thread (lrow, half) owns 64 output dims of row
+// lrow.
+constexpr int kMergeMlBytes = kMaxSplit * kBM * 8;  // [S][128] float2
+constexpr int kMergeWBytes = kMaxSplit * kBM * 4;   // [S][128] weights
+constexpr int kMergeChunk =
+    static_cast<int>((kQBytes + kRingBytes - kMergeMlBytes - kMergeWBytes) / (kBM * kD * 2));
+
+template <typename P>
+__device__ void ticket_merge(const P& p, Bars* bars, unsigned char* area, int slot, int S, int qt,
+                             int g, int q_row0, int half, int lrow) {
+  const float2* s_ml = reinterpret_cast<const float2*>(area);
+  float* s_w = reinterpret_cast<float*>(area + kMergeMlBytes);
+  unsigned char* s_o = area + kMergeMlBytes + kMergeWBytes;
+  const int n_chunks = (S + kMergeChunk - 1) / kMergeChunk;
+  if (threadIdx.x == 128) {
+    // the other splits' partials were acquired through the group counter
+    // (generic proxy); the bulk copies read them through the async proxy
+    fence_proxy_async_global();
+    const int c0 = S < kMergeChunk ? S : kMergeChunk;
+    mbar_arrive_expect_tx(&bars->merge_full,
+                          static_cast<uint32_t>(S * kBM * 8 + c0 * kBM * kD * 2));
+    bulk_copy_g2s(area, p.part_ml + static_cast<size_t>(slot) * kBM,
+                  static_cast<uint32_t>(S * kBM * 8), &bars->merge_full);
+    bulk_copy_g2s(s_o, p.part_o + static_cast<size_t>(slot) * 16 * kBM,
+                  static_cast<uint32_t>(c0 * kBM * kD * 2), &bars->merge_full);
+  }
+  const bool got = mbar_wait(&bars->merge_full, 0, 2000000000ull);
+  if (half == 0) {
+    float M = -INFINITY;
+    for (int sx = 0; sx < S; ++sx) M = fmaxf(M, s_ml[sx * kBM + lrow].x);
+    float Lt = 0.f;
+    for (int sx = 0; sx < S; ++sx) {
+      const float2 ml = s_ml[sx * kBM + lrow];
+      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M) * ml.y;
+      s_w[sx * kBM + lrow] = w;
+      Lt += w;
+    }
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    for (int sx = 0; sx < S; ++sx) s_w[sx * kBM + lrow] *= inv;
+  }
+  // one answer for all 256 threads, so that they leave the loop together
+  bool bad = named_bar_or(1, 256, !got);
+  float acc[64];
+#pragma unroll
+  for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+  for (int k = 0; k < n_chunks && !bad; ++k) {
+    const int base = k * kMergeChunk;
+    const int cnt = S - base < kMergeChunk ? S - base : kMergeChunk;
+    if (k > 0) {
+      named_bar(1, 256);  // every thread is done with the previous chunk
+      if (threadIdx.x == 128) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars->merge_full, static_cast<uint32_t>(cnt * kBM * kD * 2));
+        bulk_copy_g2s(s_o, p.part_o + static_cast<size_t>(slot + base) * 16 * kBM,
+                      static_cast<uint32_t>(cnt * kBM * kD * 2), &bars->merge_full);
+      }
+      bad = named_bar_or(1, 256, !mbar_wait(&bars->merge_full, k & 1, 2000000000ull));
+      if (bad) break;
+    }
+    for (int sx = 0; sx < cnt; ++sx) {
+      const float w = s_w[(base + sx) * kBM + lrow];
+      if (w == 0.f) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(s_o) + (sx * 16 + 8 * half) * kBM + lrow;
+#pragma unroll
+      for (int o = 0; o < 8; ++o) {
+        const uint4 v = src[o * kBM];
+        const uint32_t av[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[8 * o + 2 * e] += w * __uint_as_float(av[e] << 16);
+          acc[8 * o + 2 * e + 1] += w * __uint_as_float(av[e] & 0xFFFF0000u);
+        }
+      }
+    }
+  }
+  if (bad) {
+    report(GLANCE_DEV_PIPELINE_TIMEOUT);
+    return;
+  }
+  const int oq = qt * kBM + lrow;
+  const int ohl = oq / p.Rp, oprow = oq % p.Rp;
+  if (ohl < p.G && oprow < p.rows) {
+    uint4* dst = reinterpret_cast<uint4*>(
+        p.out + (static_cast<size_t>(q_row0 + oprow) * p.Hq + g * p.G + ohl) * kD + 64 * half);
+#pragma unroll
+    for (int o = 0; o < 8; ++o)
+      dst[o] = make_uint4(pack_bf16x2(acc[8 * o], acc[8 * o + 1]), pack_bf16x2(acc[8 * o + 2], acc[8 * o + 3]),
+                          pack_bf16x2(acc[8 * o + 4], acc[8 * o + 5]), pack_bf16x2(acc[8 * o + 6], acc[8 * o + 7]));
+  }
+}
+
 // One CTA = (kv head g, q tile, key split). The key splits of one (g, q tile)
 // merge their partial results through the workspace once all have arrived.
 template <int NB>
@@ -282,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->merge_full, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -669,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(1, 256);  // all splits' partials are visible (acquired above)
       if (p.ticket_merge) {
         own0 = 0;
-        own_rows = bars->xch[0][0] != 0.f ? kBM : 0;
+        own_rows = 0;
+        if (bars->xch[0][0] != 0.f) ticket_merge(p, bars, sQ, slot, S, qt, g, q_row0, half, lrow);
       } else {
         const int rpo = (kBM + S - 1) / S;  // rows per owner
         own0 = split * rpo;
