@@ -41,3 +41,31 @@ def lmhead_argmax(h, W, chunk=8192):
 
 def logits(h, W):
     return np.asarray(h, dtype=np.float64) @ np.asarray(W, dtype=np.float64)
+
+
+def next_token_entropy(h, W, chunk=8192):
+    """Entropy in nats of softmax(logits[i]) for each row i.
+
+    The target's next-token entropy H at the round root ("Vision Is Not
+    Overhead ...", Section 6 and Equation 2; Proposition 1 in Appendix B):
+    the packed root row of a round carries the target's distribution
+    p(. | x, b), and H = -sum_w p(w) log p(w) = logsumexp(l) - sum_w p(w) l_w.
+    Two passes in float64: the row maxima, then sum exp(l - m) and
+    sum exp(l - m) l over column chunks.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    M = h.shape[0]
+    V = W.shape[1]
+    m = np.full(M, -np.inf)
+    for c0 in range(0, V, chunk):
+        lg = h @ np.asarray(W[:, c0:c0 + chunk], dtype=np.float64)
+        m = np.maximum(m, lg.max(axis=1))
+    s = np.zeros(M)
+    el = np.zeros(M)
+    for c0 in range(0, V, chunk):
+        lg = h @ np.asarray(W[:, c0:c0 + chunk], dtype=np.float64)
+        e = np.exp(lg - m[:, None])
+        s += e.sum(axis=1)
+        el += (e * lg).sum(axis=1)
+    lse = m + np.log(s)
+    return lse - el / s

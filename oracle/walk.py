@@ -42,6 +42,41 @@ def walk(tree, argmax, L=None):
     return a, path, acc, int(argmax[u])
 
 
+def walk_gated(tree, argmax, gap, L, threshold):
+    """Walk with the tie-aware gate ("Vision Is Not Overhead ...", Section 4.2
+    and the end of the proof of Theorem 1 in Appendix B.1): a visited row whose
+    top-2 logit margin is below `threshold` is a near-tie, where reduced
+    precision may reorder the target's top two tokens, so the round defers to
+    the target's own token there. The walk stops at the first such row and
+    reports gated = True; that row's packed argmax is then not trusted as the
+    next token (the caller recomputes it). Returns (a, path, accepted tokens,
+    new_root, gated); without a near-tie on the path this is walk().
+    """
+    token, parent, depth = tree["token"], tree["parent"], tree["depth"]
+    rows = len(token)
+    u = 0
+    path = [0]
+    gated = False
+    while True:
+        if gap[u] < threshold:
+            gated = True
+            break
+        if depth[u] >= L:
+            break
+        target = int(argmax[u])
+        nxt = None
+        for c in range(rows):
+            if parent[c] == u and token[c] == target:
+                nxt = c
+                break
+        if nxt is None:
+            break
+        u = nxt
+        path.append(u)
+    a = len(path) - 1
+    return a, path, [int(token[r]) for r in path[1:]], int(argmax[u]), gated
+
+
 def tree_strings(tree):
     """The set S as token tuples (root excluded)."""
     token, parent = tree["token"], tree["parent"]

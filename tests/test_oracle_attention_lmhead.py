@@ -133,3 +133,42 @@ def test_lmhead_exact_ties_lowest_id_gap_zero():
     for chunk in (2, 4, 10):
         arg, gap, mx = lmhead_argmax(h, W, chunk=chunk)
         assert arg[0] == 3 and gap[0] == 0.0 and mx[0] == 1.0
+
+
+# ------------------------------------------------------- next-token entropy
+
+def test_entropy_uniform_logits_is_log_V():
+    from oracle.lmhead import next_token_entropy
+    d, V = 16, 1000
+    H = next_token_entropy(np.ones((3, d)), np.zeros((d, V)), chunk=300)
+    assert np.allclose(H, np.log(V), atol=1e-12)
+
+
+def test_entropy_one_raised_logit_closed_form():
+    # logits c on one token and 0 on the other V - 1: p = e^c / (e^c + V - 1),
+    # H = -p ln p - (1 - p) ln((1 - p) / (V - 1))
+    from oracle.lmhead import next_token_entropy
+    V = 513
+    for c in (0.5, 4.0, 20.0):
+        W = np.zeros((1, V))
+        W[0, 77] = c
+        H = next_token_entropy(np.ones((1, 1)), W, chunk=100)[0]
+        p = np.exp(c) / (np.exp(c) + V - 1)
+        want = -p * np.log(p) - (1 - p) * np.log((1 - p) / (V - 1))
+        assert abs(H - want) < 1e-12
+
+
+def test_entropy_matches_scipy_and_is_shift_invariant():
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    from oracle.lmhead import next_token_entropy
+    g = np.random.default_rng(5)
+    h = g.standard_normal((6, 24))
+    W = g.standard_normal((24, 700)) * 0.7
+    H = next_token_entropy(h, W, chunk=128)
+    lg = h @ W
+    assert np.allclose(H, entropy(softmax(lg, axis=1), axis=1), atol=1e-10)
+    # an extra input column of ones with a constant W row shifts every logit
+    h2 = np.concatenate([h, np.ones((6, 1))], axis=1)
+    W2 = np.concatenate([W, np.full((1, 700), 9.0)], axis=0)
+    assert np.allclose(next_token_entropy(h2, W2, chunk=50), H, atol=1e-10)
