@@ -183,6 +183,22 @@ glance_status glance_lmhead_argmax(const void* h, const void* W, glance_dtype dt
                                    void* stream);
 
 /*
+ * glance_lmhead_argmax plus each row's next-token entropy (Section 6 and
+ * Equation 2: the law that sets the accepted length is keyed on the target's
+ * next-token entropy H at the round root; Proposition 1 in Appendix B). For
+ * row i, entropy[i] = -sum_v p_v ln p_v in nats with p = softmax(logits[i]),
+ * accumulated in the same pass over the logit tiles as the argmax (fp32 sums
+ * relative to the running maximum), so row 0 of each request's packed tree
+ * gives its round's root entropy. BF16 only (F32 returns
+ * GLANCE_ERR_UNSUPPORTED); same workspace size and limits as
+ * glance_lmhead_argmax. entropy: device float [M], required.
+ */
+glance_status glance_lmhead_argmax_entropy(const void* h, const void* W, glance_dtype dtype, int M,
+                                           int d, int V, int32_t* argmax, float* gap,
+                                           float* maxlogit, float* entropy, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/*
  * LM head that allocates nothing and takes no workspace. The paper has no
  * counterpart: this is a convenience of the library. It is for callers that
  * must not allocate device memory or pass scratch space on this path, for
@@ -294,6 +310,34 @@ glance_status glance_accept_commit_batched(const glance_tree* trees, int B,
                                            int32_t* accepted_tok, int32_t* new_root,
                                            void* workspace, size_t workspace_bytes,
                                            void* stream);
+
+/*
+ * glance_accept_commit with the tie-aware gate (Section 4.2; the end of the
+ * proof of Theorem 1 in Appendix B.1): gap: device float [N+1] (batched:
+ * [B][N+1]), the rows' top-2 logit margins from the LM head. The walk stops
+ * at the first visited row whose margin is below gate_threshold, a near-tie
+ * where reduced precision may reorder the target's two best tokens; the round
+ * commits the path up to that row and sets gated (device int32, [B] when
+ * batched) to 1, meaning that row's packed argmax (reported as new_root) is
+ * not trusted and the caller recomputes the target's own token there.
+ * Otherwise gated = 0 and the result equals glance_accept_commit's. The pages
+ * print no threshold value; a threshold <= 0 never gates. Same workspace as
+ * the ungated calls.
+ */
+glance_status glance_accept_commit_gated(const glance_tree* tree, const int32_t* argmax,
+                                         const float* gap, float gate_threshold,
+                                         const glance_kv* layers, int n_layers,
+                                         int32_t* n_accepted, int32_t* accepted_tok,
+                                         int32_t* new_root, int32_t* gated, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+glance_status glance_accept_commit_gated_batched(const glance_tree* trees, int B,
+                                                 const int32_t* argmax, const float* gap,
+                                                 float gate_threshold, const glance_kv* layers,
+                                                 int n_layers, int32_t* n_accepted,
+                                                 int32_t* accepted_tok, int32_t* new_root,
+                                                 int32_t* gated, void* workspace,
+                                                 size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------ status */
 

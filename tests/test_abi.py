@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(glib):
 
 
 def test_version_and_status_strings(glib):
-    assert glib.glance_version() == 200
+    assert glib.glance_version() == 300
     assert glib.glance_status_string(0) == b"GLANCE_OK"
     assert glib.glance_status_string(3) == b"GLANCE_ERR_CAPACITY"
 

@@ -133,3 +133,97 @@ def test_capacity_error_leaves_T(dev):
     code, _ = g.device_status()
     g.reset_device_status()
     assert code == 2 and int(t_len.item()) == 30
+
+
+# ---------------------------------------------------------- tie-aware gate
+
+def _gated_case(seed, near_tie_depth, L=15, N=63, V=40):
+    from test_gpu_attention import random_tree
+    ref = random_tree(N, L, 1000, seed)
+    gen = W.rng(seed, 5)
+    am, _ = planted_argmax(ref, 15, V, gen)
+    gap = gen.uniform(0.5, 3.0, size=N + 1).astype(np.float32)
+    # walk the planted chain to place a near-tie at the requested depth
+    u, chain = 0, [0]
+    while True:
+        kids = [c for c in range(N + 1) if ref["parent"][c] == u and ref["token"][c] == am[u]]
+        if not kids or ref["depth"][u] >= L:
+            break
+        u = kids[0]
+        chain.append(u)
+    if near_tie_depth is not None and near_tie_depth < len(chain):
+        gap[chain[near_tie_depth]] = 1e-4
+    off_path = [r for r in range(N + 1) if r not in chain][:4]
+    gap[off_path] = 0.0
+    return ref, am, gap, chain
+
+
+@pytest.mark.parametrize("near_tie_depth,thr", [(None, 1e-3), (0, 1e-3), (2, 1e-3), (2, 1e-5),
+                                                (3, 0.0)])
+def test_gated_commit_matches_oracle(dev, clean_status, near_tie_depth, thr):
+    import tree_verified_block_gb300 as g
+    from oracle.walk import walk_gated
+    L, n_layers, Hkv, D, T = 15, 2, 8, 128, 1000
+    ref, am, gap, chain = _gated_case(11, near_tie_depth)
+    t_cap = T + len(ref["token"]) + 8
+    gen = W.rng(12)
+    ks = [W.normal_bf16(gen, (Hkv, t_cap, D)) for _ in range(n_layers)]
+    vs = [W.normal_bf16(gen, (Hkv, t_cap, D)) for _ in range(n_layers)]
+    t_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    layers = [g.KVLayer(bf16_tensor(k, dev), bf16_tensor(v, dev), t_len) for k, v in zip(ks, vs)]
+    tree = upload_tree(ref, L, dev)
+    n_acc = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    acc = torch.full((L,), -1, dtype=torch.int32, device=dev)
+    nr = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    gated = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    ws = g.workspace(g.accept_commit_workspace_bytes(n_layers), dev)
+    g.accept_commit_gated(tree, torch.from_numpy(am.astype(np.int32)).to(dev),
+                          torch.from_numpy(gap).to(dev), thr, layers, n_acc, acc, nr, gated, ws)
+    a, path, toks, new_root, want_gated = walk_gated(ref, am, gap, L, thr)
+    assert int(n_acc.item()) == a and acc.cpu().numpy()[:a].tolist() == toks
+    assert int(nr.item()) == new_root and int(gated.item()) == int(want_gated)
+    if near_tie_depth is not None and thr > 1e-4 and near_tie_depth < len(chain):
+        assert want_gated and a == near_tie_depth
+    assert int(t_len.item()) == T + a + 1
+    for l in range(n_layers):
+        kk, vv = ks[l].copy(), vs[l].copy()
+        o_commit(kk, vv, T, path)
+        assert np.array_equal(layers[l].k.view(torch.int16).cpu().numpy().view(np.uint16), kk)
+        assert np.array_equal(layers[l].v.view(torch.int16).cpu().numpy().view(np.uint16), vv)
+
+
+def test_gated_batched_matches_oracle(dev, clean_status):
+    import tree_verified_block_gb300 as g
+    from oracle.walk import walk_gated
+    L, n_layers, Hkv, D, B = 15, 2, 2, 128, 3
+    cases = [_gated_case(20 + r, [None, 1, 0][r]) for r in range(B)]
+    Ts = [700, 64, 3000]
+    t_lens = torch.tensor(Ts, dtype=torch.int32, device=dev)
+    gen = W.rng(13)
+    trees, layers, host = [], [], []
+    for r, (ref, am, gap, chain) in enumerate(cases):
+        t_cap = Ts[r] + len(ref["token"]) + 3
+        ks = [W.normal_bf16(gen, (Hkv, t_cap, D)) for _ in range(n_layers)]
+        vs = [W.normal_bf16(gen, (Hkv, t_cap, D)) for _ in range(n_layers)]
+        host.append((ks, vs))
+        trees.append(upload_tree(ref, L, dev))
+        layers.append([g.KVLayer(bf16_tensor(k, dev), bf16_tensor(v, dev), t_lens[r:r + 1])
+                       for k, v in zip(ks, vs)])
+    amt = torch.from_numpy(np.stack([c[1] for c in cases]).astype(np.int32)).to(dev)
+    gapt = torch.from_numpy(np.stack([c[2] for c in cases])).to(dev)
+    n_acc = torch.full((B,), -1, dtype=torch.int32, device=dev)
+    acc = torch.full((B, L), -1, dtype=torch.int32, device=dev)
+    nr = torch.full((B,), -1, dtype=torch.int32, device=dev)
+    gated = torch.full((B,), -1, dtype=torch.int32, device=dev)
+    ws = g.workspace(g.accept_commit_batched_workspace_bytes(B, n_layers), dev)
+    g.accept_commit_gated_batched(trees, amt, gapt, 1e-3, layers, n_acc, acc, nr, gated, ws)
+    n_acc, acc, nr, gated, newT = (t.cpu().numpy() for t in (n_acc, acc, nr, gated, t_lens))
+    for r, (ref, am, gap, chain) in enumerate(cases):
+        a, path, toks, new_root, want_gated = walk_gated(ref, am, gap, L, 1e-3)
+        assert n_acc[r] == a and acc[r][:a].tolist() == toks and nr[r] == new_root
+        assert gated[r] == int(want_gated) and newT[r] == Ts[r] + a + 1
+        for l in range(n_layers):
+            kk, vv = host[r][0][l].copy(), host[r][1][l].copy()
+            o_commit(kk, vv, Ts[r], path)
+            assert np.array_equal(layers[r][l].k.view(torch.int16).cpu().numpy().view(np.uint16), kk)
+    assert [bool(x) for x in gated] == [False, True, True]

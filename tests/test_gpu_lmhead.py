@@ -97,3 +97,64 @@ def test_fp32(dev, clean_status, M, d, V):
     g.lmhead_argmax(torch.from_numpy(h).to(dev), torch.from_numpy(Wm).to(dev), am, gap, mx, ws)
     ref = o_lmhead(h, Wm)
     compare((am.cpu().numpy(), gap.cpu().numpy(), mx.cpu().numpy()), ref, 1e-5)
+
+
+# ------------------------------------------------------- next-token entropy
+# Tolerance: |dH| <= max|dl| * E_p|l - E_p l| for a logit perturbation dl;
+# bf16-input logits agree with fp64 to ~1e-3 and fp32 sums over V terms add
+# ~1e-4 relative, so 1e-2 absolute bounds the difference with margin.
+
+def run_entropy(hb, Wb, dev):
+    import tree_verified_block_gb300 as g
+    M, d = hb.shape
+    V = Wb.shape[1]
+    h, Wt = bf16_tensor(hb, dev), bf16_tensor(Wb, dev)
+    out = [torch.full((M,), -1, dtype=torch.int32, device=dev)] + \
+          [torch.full((M,), float("nan"), dtype=torch.float32, device=dev) for _ in range(3)]
+    ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.bfloat16), dev)
+    g.lmhead_argmax_entropy(h, Wt, out[0], out[1], out[2], out[3], ws)
+    plain = [torch.empty_like(t) for t in out[:3]]
+    g.lmhead_argmax(h, Wt, plain[0], plain[1], plain[2], ws)
+    got = [t.cpu().numpy() for t in out]
+    for a, b in zip(got[:3], plain):
+        assert np.array_equal(a, b.cpu().numpy())  # same fold, same answer
+    return got
+
+
+@pytest.mark.parametrize("M,d,V", [(16, 128, 1000), (64, 256, 5000), (129, 64, 520),
+                                   (200, 256, 3000), (512, 128, 2048)])
+def test_bf16_entropy_shapes(dev, clean_status, M, d, V):
+    from oracle.lmhead import next_token_entropy
+    gen = W.rng(M, d, V, 5)
+    hb = W.normal_bf16(gen, (M, d))
+    Wb = W.normal_bf16(gen, (d, V), std=0.05)
+    am, gap, mx, H = run_entropy(hb, Wb, dev)
+    compare((am, gap, mx), o_lmhead(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb)), 2e-2)
+    want = next_token_entropy(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb))
+    assert np.abs(H - want).max() < 1e-2
+
+
+def test_bf16_entropy_qwen_vocab_across_temperatures(dev, clean_status):
+    # rows scaled from near-uniform to near-deterministic next-token distributions
+    from oracle.lmhead import next_token_entropy
+    M, d, V = 64, 4096, 151936
+    gen = W.rng(41)
+    Wb = W.normal_bf16(gen, (d, V), std=0.02)
+    h = gen.standard_normal((M, d), dtype=np.float32)
+    h *= np.geomspace(0.05, 40.0, M, dtype=np.float32)[:, None]
+    hb = W.to_bf16_bits(h)
+    am, gap, mx, H = run_entropy(hb, Wb, dev)
+    want = next_token_entropy(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb))
+    assert want.max() > 11.0 and want.min() < 0.5   # the sweep spans the range
+    assert np.abs(H - want).max() < 1e-2
+
+
+def test_entropy_rejects_f32(dev):
+    import tree_verified_block_gb300 as g
+    h = torch.zeros((4, 32), device=dev)
+    Wt = torch.zeros((32, 64), device=dev)
+    out = torch.zeros(4, dtype=torch.int32, device=dev)
+    f = torch.zeros(4, device=dev)
+    ws = g.workspace(1 << 16, dev)
+    with pytest.raises(g.GlanceError):
+        g.lmhead_argmax_entropy(h, Wt, out, f, f, f, ws)

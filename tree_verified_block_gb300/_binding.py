@@ -26,6 +26,8 @@ EXPORTS = [
     "glance_build_tree_batched_workspace_bytes", "glance_build_tree_batched",
     "glance_tree_attention_batched_workspace_bytes", "glance_tree_attention_batched",
     "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
+    "glance_lmhead_argmax_entropy", "glance_accept_commit_gated",
+    "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
     "glance_reset_device_status", "glance_version",
 ]
@@ -100,6 +102,15 @@ def lib():
     L.glance_accept_commit_batched.argtypes = [ctypes.POINTER(TreeC), i32, vp, ctypes.POINTER(KVC),
                                                i32, vp, vp, vp, vp, sz, vp]
     L.glance_accept_commit_batched.restype = st
+    L.glance_lmhead_argmax_entropy.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    L.glance_lmhead_argmax_entropy.restype = st
+    L.glance_accept_commit_gated.argtypes = [ctypes.POINTER(TreeC), vp, vp, ctypes.c_float,
+                                             ctypes.POINTER(KVC), i32, vp, vp, vp, vp, vp, sz, vp]
+    L.glance_accept_commit_gated.restype = st
+    L.glance_accept_commit_gated_batched.argtypes = [ctypes.POINTER(TreeC), i32, vp, vp,
+                                                     ctypes.c_float, ctypes.POINTER(KVC), i32, vp,
+                                                     vp, vp, vp, vp, sz, vp]
+    L.glance_accept_commit_gated_batched.restype = st
     L.glance_last_error.argtypes = []
     L.glance_last_error.restype = ctypes.c_char_p
     L.glance_status_string.argtypes = [st]
@@ -227,6 +238,16 @@ def lmhead_argmax_noalloc(h, W, argmax, gap, maxlogit, stream=None):
                                               _stream(stream, h.device)))
 
 
+def lmhead_argmax_entropy(h, W, argmax, gap, maxlogit, entropy, ws, stream=None):
+    """lmhead_argmax plus each row's next-token entropy (nats), bf16."""
+    M, d = h.shape
+    assert W.shape[0] == d and h.is_contiguous() and W.is_contiguous() and h.dtype == W.dtype
+    _check(lib().glance_lmhead_argmax_entropy(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
+                                              _ptr(argmax), _ptr(gap), _ptr(maxlogit),
+                                              _ptr(entropy), _ptr(ws), ws.numel(),
+                                              _stream(stream, h.device)))
+
+
 def accept_commit_workspace_bytes(n_layers):
     return lib().glance_accept_commit_workspace_bytes(n_layers)
 
@@ -236,6 +257,16 @@ def accept_commit(tree, argmax, layers, n_accepted, accepted_tok, new_root, ws, 
     _check(lib().glance_accept_commit(ctypes.byref(tree.c), _ptr(argmax), arr, len(layers),
                                       _ptr(n_accepted), _ptr(accepted_tok), _ptr(new_root),
                                       _ptr(ws), ws.numel(), _stream(stream, argmax.device)))
+
+
+def accept_commit_gated(tree, argmax, gap, threshold, layers, n_accepted, accepted_tok, new_root,
+                        gated, ws, stream=None):
+    """accept_commit with the tie-aware gate on the rows' top-2 margins."""
+    arr = (KVC * len(layers))(*[l.c for l in layers])
+    _check(lib().glance_accept_commit_gated(ctypes.byref(tree.c), _ptr(argmax), _ptr(gap),
+                                            float(threshold), arr, len(layers), _ptr(n_accepted),
+                                            _ptr(accepted_tok), _ptr(new_root), _ptr(gated),
+                                            _ptr(ws), ws.numel(), _stream(stream, argmax.device)))
 
 
 # ------------------------------------------------------------ batched calls
@@ -290,6 +321,18 @@ def accept_commit_batched(trees, argmax, layers, n_accepted, accepted_tok, new_r
                                               _ptr(n_accepted), _ptr(accepted_tok),
                                               _ptr(new_root), _ptr(ws), ws.numel(),
                                               _stream(stream, argmax.device)))
+
+
+def accept_commit_gated_batched(trees, argmax, gap, threshold, layers, n_accepted, accepted_tok,
+                                new_root, gated, ws, stream=None):
+    B = len(trees)
+    n_layers = len(layers[0])
+    flat = [layers[r][l] for r in range(B) for l in range(n_layers)]
+    _check(lib().glance_accept_commit_gated_batched(_trees(trees), B, _ptr(argmax), _ptr(gap),
+                                                    float(threshold), _kvs(flat), n_layers,
+                                                    _ptr(n_accepted), _ptr(accepted_tok),
+                                                    _ptr(new_root), _ptr(gated), _ptr(ws),
+                                                    ws.numel(), _stream(stream, argmax.device)))
 
 
 def device_status():

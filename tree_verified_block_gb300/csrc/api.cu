@@ -130,6 +130,6 @@ glance_status glance_reset_device_status(void) {
   return read_all_status(&dummy, true);
 }
 
-int glance_version(void) { return 200; }
+int glance_version(void) { return 300; }
 
 }  // extern "C"

@@ -17,6 +17,12 @@
 // destination is written. The last CTA of a request to finish (atomic ticket;
 // all others have read T by then) writes a, the accepted tokens and the new
 // root of that request, and advances its T by a + 1.
+//
+// Tie-aware gate (Section 4.2; the end of the proof of Theorem 1 in Appendix
+// B.1), when the rows' top-2 margins are given: the walk stops at the first
+// visited row whose margin is below the threshold (a near-tie, where reduced
+// precision may reorder the target's top two tokens) and flags the request;
+// its new root is then the caller's to recompute.
 #include "glance_internal.cuh"
 
 GLANCE_DEFINE_STATUS_WORD(status_commit)
@@ -50,6 +56,9 @@ struct ReqInfo {
 template <int kEntries>
 struct CommitParams {
   const int32_t* argmax;      // [B][rows]
+  const float* gap;           // [B][rows] top-2 margins, or null (no gate)
+  float gate;                 // margin threshold of the gate
+  int32_t* gated;             // [B], or null
   int rows, L, B;
   int n_layers, n_kv_heads, row_bytes;
   int32_t* n_accepted;        // [B]
@@ -68,6 +77,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ __align__(16) unsigned char stage[kMaxPath * kMaxRowBytes];
   __shared__ uint32_t s_ticket;
   __shared__ int s_tok[256], s_par[256], s_dep[256], s_arg[256];
+  __shared__ float s_gap[256];
+  __shared__ int s_gated;
 
   // slice: blockIdx.x = ((request * n_layers + layer) * 2 + kv) * n_kv_heads + head
   const int per_req = p.n_layers * 2 * p.n_kv_heads;
@@ -79,14 +90,20 @@ __global__ void __launch_bounds__(kThreads)
     s_par[i] = __ldg(rq.parent + i);
     s_dep[i] = __ldg(rq.depth + i);
     s_arg[i] = __ldg(p.argmax + req * p.rows + i);
+    s_gap[i] = p.gap ? __ldg(p.gap + req * p.rows + i) : INFINITY;
   }
   if (threadIdx.x == 0) s_T = *rq.t_len;
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int u = 0, a = 0;
+    bool gated = false;
     if (lane == 0) s_path[0] = 0;
-    for (int step = 0; step < p.L; ++step) {
+    for (int step = 0; step <= p.L; ++step) {
+      if (s_gap[u] < p.gate) {  // near-tie on the path: defer (never true without margins)
+        gated = true;
+        break;
+      }
       if (s_dep[u] >= p.L) break;
       const int target = s_arg[u];
       int found = -1;
@@ -107,6 +124,7 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) {
       s_a = a;
       s_newroot = s_arg[u];
+      s_gated = gated ? 1 : 0;
     }
   }
   __syncthreads();
@@ -148,6 +166,7 @@ __global__ void __launch_bounds__(kThreads)
     p.ticket[req] = 0;
     p.n_accepted[req] = a;
     p.new_root[req] = s_newroot;
+    if (p.gated) p.gated[req] = s_gated;
     if (room) *rq.t_len = T + a + 1;
   }
   if (threadIdx.x >= 1 && threadIdx.x <= a)
@@ -156,13 +175,15 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int kEntries>
 glance_status fill_and_launch(const char* who, const glance_tree* trees, int B,
-                              const int32_t* argmax, const glance_kv* layers, int n_layers,
-                              int32_t* n_accepted, int32_t* accepted_tok, int32_t* new_root,
-                              void* workspace, int row_bytes, int esize, void* stream);
+                              const int32_t* argmax, const float* gap, float gate, int32_t* gated,
+                              const glance_kv* layers, int n_layers, int32_t* n_accepted,
+                              int32_t* accepted_tok, int32_t* new_root, void* workspace,
+                              int row_bytes, int esize, void* stream);
 
 // layers: [B][n_layers] cache views, argmax [B][rows]; outputs per request.
 glance_status launch_commit(const char* who, const glance_tree* trees, int B,
-                            const int32_t* argmax, const glance_kv* layers, int n_layers,
+                            const int32_t* argmax, const float* gap, float gate,
+                            int32_t* gated, const glance_kv* layers, int n_layers,
                             int32_t* n_accepted, int32_t* accepted_tok, int32_t* new_root,
                             void* workspace, size_t workspace_bytes, void* stream) {
   using glance::fail;
@@ -185,18 +206,20 @@ glance_status launch_commit(const char* who, const glance_tree* trees, int B,
                 "%s: head_dim * element size must be a multiple of 16 and <= %d bytes", who,
                 kMaxRowBytes);
   if (B * n_layers <= kSmallEntries)
-    return fill_and_launch<kSmallEntries>(who, trees, B, argmax, layers, n_layers, n_accepted,
-                                          accepted_tok, new_root, workspace, row_bytes, esize,
-                                          stream);
-  return fill_and_launch<kMaxEntries>(who, trees, B, argmax, layers, n_layers, n_accepted,
-                                      accepted_tok, new_root, workspace, row_bytes, esize, stream);
+    return fill_and_launch<kSmallEntries>(who, trees, B, argmax, gap, gate, gated, layers,
+                                          n_layers, n_accepted, accepted_tok, new_root, workspace,
+                                          row_bytes, esize, stream);
+  return fill_and_launch<kMaxEntries>(who, trees, B, argmax, gap, gate, gated, layers, n_layers,
+                                      n_accepted, accepted_tok, new_root, workspace, row_bytes,
+                                      esize, stream);
 }
 
 template <int kEntries>
 glance_status fill_and_launch(const char* who, const glance_tree* trees, int B,
-                              const int32_t* argmax, const glance_kv* layers, int n_layers,
-                              int32_t* n_accepted, int32_t* accepted_tok, int32_t* new_root,
-                              void* workspace, int row_bytes, int esize, void* stream) {
+                              const int32_t* argmax, const float* gap, float gate, int32_t* gated,
+                              const glance_kv* layers, int n_layers, int32_t* n_accepted,
+                              int32_t* accepted_tok, int32_t* new_root, void* workspace,
+                              int row_bytes, int esize, void* stream) {
   using glance::fail;
   const glance_kv& l0 = layers[0];
   CommitParams<kEntries> p;
@@ -245,6 +268,9 @@ glance_status fill_and_launch(const char* who, const glance_tree* trees, int B,
   }
   for (int r = B; r < kMaxB; ++r) p.req[r] = p.req[0];
   p.argmax = argmax;
+  p.gap = gap;
+  p.gate = gate;
+  p.gated = gated;
   p.rows = n + 1;
   p.L = L;
   p.B = B;
@@ -273,8 +299,9 @@ extern "C" glance_status glance_accept_commit(const glance_tree* tree, const int
                                               int32_t* n_accepted, int32_t* accepted_tok,
                                               int32_t* new_root, void* workspace,
                                               size_t workspace_bytes, void* stream) {
-  return launch_commit("glance_accept_commit", tree, 1, argmax, layers, n_layers, n_accepted,
-                       accepted_tok, new_root, workspace, workspace_bytes, stream);
+  return launch_commit("glance_accept_commit", tree, 1, argmax, nullptr, 0.f, nullptr, layers,
+                       n_layers, n_accepted, accepted_tok, new_root, workspace, workspace_bytes,
+                       stream);
 }
 
 extern "C" size_t glance_accept_commit_batched_workspace_bytes(int B, int n_layers) {
@@ -290,6 +317,33 @@ extern "C" glance_status glance_accept_commit_batched(const glance_tree* trees, 
                                                       int32_t* n_accepted, int32_t* accepted_tok,
                                                       int32_t* new_root, void* workspace,
                                                       size_t workspace_bytes, void* stream) {
-  return launch_commit("glance_accept_commit_batched", trees, B, argmax, layers, n_layers,
-                       n_accepted, accepted_tok, new_root, workspace, workspace_bytes, stream);
+  return launch_commit("glance_accept_commit_batched", trees, B, argmax, nullptr, 0.f, nullptr,
+                       layers, n_layers, n_accepted, accepted_tok, new_root, workspace,
+                       workspace_bytes, stream);
+}
+
+extern "C" glance_status glance_accept_commit_gated(const glance_tree* tree, const int32_t* argmax,
+                                                    const float* gap, float gate_threshold,
+                                                    const glance_kv* layers, int n_layers,
+                                                    int32_t* n_accepted, int32_t* accepted_tok,
+                                                    int32_t* new_root, int32_t* gated,
+                                                    void* workspace, size_t workspace_bytes,
+                                                    void* stream) {
+  if (!gap || !gated)
+    return glance::fail(GLANCE_ERR_INVALID_ARG, "glance_accept_commit_gated: null gap or gated");
+  return launch_commit("glance_accept_commit_gated", tree, 1, argmax, gap, gate_threshold, gated,
+                       layers, n_layers, n_accepted, accepted_tok, new_root, workspace,
+                       workspace_bytes, stream);
+}
+
+extern "C" glance_status glance_accept_commit_gated_batched(
+    const glance_tree* trees, int B, const int32_t* argmax, const float* gap, float gate_threshold,
+    const glance_kv* layers, int n_layers, int32_t* n_accepted, int32_t* accepted_tok,
+    int32_t* new_root, int32_t* gated, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!gap || !gated)
+    return glance::fail(GLANCE_ERR_INVALID_ARG,
+                        "glance_accept_commit_gated_batched: null gap or gated");
+  return launch_commit("glance_accept_commit_gated_batched", trees, B, argmax, gap,
+                       gate_threshold, gated, layers, n_layers, n_accepted, accepted_tok, new_root,
+                       workspace, workspace_bytes, stream);
 }

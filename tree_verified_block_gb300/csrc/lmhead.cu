@@ -58,6 +58,93 @@ __device__ __forceinline__ void merge(Partial& a, const Partial& b) {
   }
 }
 
+// With the entropy: s = sum_v exp(l_v - m1) and u = sum_v exp(l_v - m1) (l_v - m1)
+// over the columns seen, relative to the running maximum m1; the row's entropy
+// is then H = log s - u / s.
+struct PartialH {
+  float m1;
+  int i1;
+  float m2;
+  float s;
+  float u;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Re-expresses (s, u) relative to a new maximum M >= m.
+__device__ __forceinline__ void rebase(float m, float M, float& s, float& u) {
+  if (m == -INFINITY) {
+    s = 0.f;
+    u = 0.f;
+    return;
+  }
+  const float f = expf(m - M);
+  u = f * (u + s * (m - M));
+  s *= f;
+}
+
+__device__ __forceinline__ void merge(PartialH& a, const PartialH& b) {
+  const float M = fmaxf(a.m1, b.m1);
+  float sa = a.s, ua = a.u, sb = b.s, ub = b.u;
+  rebase(a.m1, M, sa, ua);
+  rebase(b.m1, M, sb, ub);
+  Partial pa{a.m1, a.i1, a.m2};
+  merge(pa, Partial{b.m1, b.i1, b.m2});
+  a = PartialH{pa.m1, pa.i1, pa.m2, sa + sb, ua + ub};
+}
+
+// Folds one chunk of 32 logits (columns col0.., valid below V) into the
+// entropy sums; m is the running maximum after this chunk, hm the maximum the
+// sums are relative to.
+__device__ __forceinline__ void entropy_chunk(const uint32_t (&r)[32], int col0, int V, float m,
+                                              float& hm, float& hs, float& hu) {
+  if (m > hm) {
+    if (hm != -INFINITY) {
+      const float f = ex2_approx((hm - m) * kLog2e);
+      hu = f * (hu + hs * (hm - m));
+      hs *= f;
+    }
+    hm = m;
+  }
+  const int n = V - col0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    if (e < n) {
+      const float dx = __uint_as_float(r[e]) - hm;
+      const float pe = ex2_approx(dx * kLog2e);
+      hs += pe;
+      hu = fmaf(pe, dx, hu);
+    }
+  }
+}
+
+// Last CTA: one warp per row merges every CTA's partial for that row.
+__device__ void merge_partials_h(const PartialH* part, int n_parts, int part_stride, int M,
+                                 int32_t* argmax, float* gap, float* maxlogit, float* entropy) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int r = warp; r < M; r += nwarps) {
+    PartialH a{-INFINITY, 0x7FFFFFFF, -INFINITY, 0.f, 0.f};
+    for (int c = lane; c < n_parts; c += 32) {
+      const PartialH* q = part + static_cast<size_t>(c) * part_stride + r;
+      merge(a, PartialH{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2), __ldcg(&q->s), __ldcg(&q->u)});
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      PartialH b{__shfl_xor_sync(0xffffffffu, a.m1, o), __shfl_xor_sync(0xffffffffu, a.i1, o),
+                 __shfl_xor_sync(0xffffffffu, a.m2, o), __shfl_xor_sync(0xffffffffu, a.s, o),
+                 __shfl_xor_sync(0xffffffffu, a.u, o)};
+      merge(a, b);
+    }
+    if (lane == 0) {
+      argmax[r] = a.i1;
+      gap[r] = a.m1 - a.m2;
+      if (maxlogit) maxlogit[r] = a.m1;
+      entropy[r] = logf(a.s) - a.u / a.s;
+    }
+  }
+}
+
 // Last CTA: one warp per row merges every CTA's partial for that row.
 __device__ void merge_partials(const Partial* part, int n_parts, int part_stride, int M,
                                int32_t* argmax, float* gap, float* maxlogit) {
@@ -185,8 +272,9 @@ struct Bf16Params {
   int32_t* argmax;
   float* gap;
   float* maxlogit;
-  Partial* part;  // [grid][NB * 128]
+  void* part;       // [grid][rows] Partial, or PartialH with the entropy
   uint32_t* ticket;
+  float* entropy;   // [M], written by the kH kernels
 };
 
 template <int STAGES>
@@ -218,7 +306,7 @@ __device__ __forceinline__ void fail_pipeline(BarsT* bars) {
   atomicExch(&bars->abort_flag, 1);
 }
 
-template <int NB>
+template <int NB, bool kH>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_bf16_kernel(const __grid_constant__ CUtensorMap map_h,
                        const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
@@ -344,13 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp - 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m1[NB], m2[NB];
+    float m1[NB], m2[NB], hm[NB], hs[NB], hu[NB];
     int i1[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       m1[b] = -INFINITY;
       m2[b] = -INFINITY;
       i1[b] = 0x7FFFFFFF;
+      hm[b] = -INFINITY;
+      hs[b] = 0.f;
+      hu[b] = 0.f;
     }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -379,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
           }
+          if (kH) entropy_chunk(r, col0, p.V, m1[b], hm[b], hs[b], hu[b]);
         }
       }
       tc_fence_before();
@@ -387,8 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) fail_pipeline(bars);
 #pragma unroll
     for (int b = 0; b < NB; ++b)
-      if (b * kBM + row < p.M)
-        p.part[static_cast<size_t>(blockIdx.x) * (NB * kBM) + b * kBM + row] = Partial{m1[b], i1[b], m2[b]};
+      if (b * kBM + row < p.M) {
+        const size_t at = static_cast<size_t>(blockIdx.x) * (NB * kBM) + b * kBM + row;
+        if (kH)
+          static_cast<PartialH*>(p.part)[at] = PartialH{m1[b], i1[b], m2[b], hs[b], hu[b]};
+        else
+          static_cast<Partial*>(p.part)[at] = Partial{m1[b], i1[b], m2[b]};
+      }
   }
   tc_fence_before();
   __syncthreads();
@@ -403,7 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
-  merge_partials(p.part, gridDim.x, NB * kBM, p.M, p.argmax, p.gap, p.maxlogit);
+  if (kH)
+    merge_partials_h(static_cast<const PartialH*>(p.part), gridDim.x, NB * kBM, p.M, p.argmax, p.gap,
+                     p.maxlogit, p.entropy);
+  else
+    merge_partials(static_cast<const Partial*>(p.part), gridDim.x, NB * kBM, p.M, p.argmax, p.gap,
+                   p.maxlogit);
 }
 
 // ---------------------------------------------- bf16, M > 128: CTA pairs
@@ -429,7 +531,7 @@ struct PairShape {
   static_assert(kSmem <= 232448, "shared memory");
 };
 
-template <int NB>
+template <int NB, bool kH>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_h,
                             const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
@@ -551,13 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp - 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m1[NB], m2[NB];
+    float m1[NB], m2[NB], hm[NB], hs[NB], hu[NB];
     int i1[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       m1[b] = -INFINITY;
       m2[b] = -INFINITY;
       i1[b] = 0x7FFFFFFF;
+      hm[b] = -INFINITY;
+      hs[b] = 0.f;
+      hu[b] = 0.f;
     }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -586,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
           }
+          if (kH) entropy_chunk(r, col0, p.V, m1[b], hm[b], hs[b], hu[b]);
         }
       }
       tc_fence_before();
@@ -595,7 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const int grow = row0 + b * kBM + row;
-      if (grow < p.M) p.part[static_cast<size_t>(pair) * (2 * NB * kBM) + grow] = Partial{m1[b], i1[b], m2[b]};
+      if (grow < p.M) {
+        const size_t at = static_cast<size_t>(pair) * (2 * NB * kBM) + grow;
+        if (kH)
+          static_cast<PartialH*>(p.part)[at] = PartialH{m1[b], i1[b], m2[b], hs[b], hu[b]};
+        else
+          static_cast<Partial*>(p.part)[at] = Partial{m1[b], i1[b], m2[b]};
+      }
     }
   }
   tc_fence_before();
@@ -613,26 +725,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
-  merge_partials(p.part, n_pairs, 2 * NB * kBM, p.M, p.argmax, p.gap, p.maxlogit);
+  if (kH)
+    merge_partials_h(static_cast<const PartialH*>(p.part), n_pairs, 2 * NB * kBM, p.M, p.argmax,
+                     p.gap, p.maxlogit, p.entropy);
+  else
+    merge_partials(static_cast<const Partial*>(p.part), n_pairs, 2 * NB * kBM, p.M, p.argmax,
+                   p.gap, p.maxlogit);
 }
 
 int row_blocks(int M) { return (M + kBM - 1) / kBM; }
 
 size_t ws_bytes_bf16(int M) {
   const int grid = glance::num_sms();
-  return 256 + (static_cast<size_t>(grid) * row_blocks(M) * kBM * sizeof(Partial) + 255) / 256 * 256;
+  // large enough for the partials with the entropy sums
+  return 256 + (static_cast<size_t>(grid) * row_blocks(M) * kBM * sizeof(PartialH) + 255) / 256 * 256;
 }
 
-template <int NB>
+template <int NB, bool kH>
 glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
-                          float* gap, float* maxlogit, Partial* part, uint32_t* ticket, int max_grid,
-                          cudaStream_t s, const char* who) {
+                          float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
+                          int max_grid, cudaStream_t s, const char* who) {
   using Sh = Shape<NB>;
   const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
   int grid = glance::num_sms();
   if (grid > n_tiles) grid = n_tiles;
   if (grid > max_grid) grid = max_grid;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel<NB>),
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel<NB, kH>),
                                       static_cast<int>(Sh::kSmem));
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   CUtensorMap mw, mh;
@@ -653,8 +771,8 @@ glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int
                                              CU_TENSOR_MAP_SWIZZLE_128B, who);
     if (st != GLANCE_OK) return st;
   }
-  Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket};
-  lmhead_bf16_kernel<NB><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
+  Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket, entropy};
+  lmhead_bf16_kernel<NB, kH><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
@@ -687,19 +805,20 @@ int max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, lmhead_bf16_pair_kernel<NB>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_bf16_pair_kernel<NB, false>, &cfg) != cudaSuccess ||
+        n < 1)
       n = -1;
     cached[dev] = n;
   }
   return cached[dev];
 }
 
-template <int NB>
+template <int NB, bool kH>
 glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
-                          float* gap, float* maxlogit, Partial* part, uint32_t* ticket,
+                          float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
                           cudaStream_t s, const char* who) {
   using Sh = PairShape<NB>;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_pair_kernel<NB>),
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_pair_kernel<NB, kH>),
                                       static_cast<int>(Sh::kSmem));
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
@@ -724,7 +843,7 @@ glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int
                                              CU_TENSOR_MAP_SWIZZLE_128B, who);
     if (st != GLANCE_OK) return st;
   }
-  Bf16Params p{M, d, V, n_tiles, kBM, argmax, gap, maxlogit, part, ticket};
+  Bf16Params p{M, d, V, n_tiles, kBM, argmax, gap, maxlogit, part, ticket, entropy};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kThreads);
@@ -737,8 +856,36 @@ glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_pair_kernel<NB>, mh, mw, p);
+  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_pair_kernel<NB, kH>, mh, mw, p);
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
+
+// bf16 LM head, one launch (W streams once for all rows): one CTA per SM for
+// M <= 128, CTA pairs above. entropy == nullptr skips the entropy sums.
+template <bool kH>
+glance_status lmhead_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
+                          float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
+                          cudaStream_t s, const char* who) {
+  if (M <= kBM)
+    return launch_bf16<1, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, 1 << 30,
+                              s, who);
+  if (M <= 2 * kBM)
+    return launch_pair<1, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s, who);
+  return launch_pair<2, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s, who);
+}
+
+glance_status check_bf16_call(const char* who, const void* h, const void* W, int M, int d, int V,
+                              void* workspace, size_t workspace_bytes) {
+  using glance::fail;
+  if (d % kBK != 0 || V % 8 != 0)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: bf16 needs d %% 64 == 0 and V %% 8 == 0", who);
+  if (!glance::aligned16(h) || !glance::aligned16(W))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: h and W must be 16-byte aligned", who);
+  if (workspace_bytes < ws_bytes_bf16(M))
+    return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                ws_bytes_bf16(M));
+  (void)workspace;
   return GLANCE_OK;
 }
 
@@ -776,22 +923,32 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
   }
   if (dtype != GLANCE_BF16)
     return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: dtype must be F32 or BF16");
-  if (d % kBK != 0 || V % 8 != 0)
-    return fail(GLANCE_ERR_UNSUPPORTED, "glance_lmhead_argmax: bf16 needs d %% 64 == 0 and V %% 8 == 0");
-  if (!glance::aligned16(h) || !glance::aligned16(W))
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_lmhead_argmax: h and W must be 16-byte aligned");
-  if (workspace_bytes < ws_bytes_bf16(M))
-    return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace %zu bytes < %zu needed",
-                workspace_bytes, ws_bytes_bf16(M));
-  // one launch: W streams once for all rows
-  if (M <= kBM)
-    return launch_bf16<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, 1 << 30, s,
-                          "glance_lmhead_argmax");
-  if (M <= 2 * kBM)
-    return launch_pair<1>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, s,
-                          "glance_lmhead_argmax");
-  return launch_pair<2>(h, W, M, d, V, argmax, gap, maxlogit, part, ticket, s,
-                        "glance_lmhead_argmax");
+  glance_status st =
+      check_bf16_call("glance_lmhead_argmax", h, W, M, d, V, workspace, workspace_bytes);
+  if (st != GLANCE_OK) return st;
+  return lmhead_bf16<false>(h, W, M, d, V, argmax, gap, maxlogit, nullptr, part, ticket, s,
+                            "glance_lmhead_argmax");
+}
+
+extern "C" glance_status glance_lmhead_argmax_entropy(const void* h, const void* W,
+                                                      glance_dtype dtype, int M, int d, int V,
+                                                      int32_t* argmax, float* gap, float* maxlogit,
+                                                      float* entropy, void* workspace,
+                                                      size_t workspace_bytes, void* stream) {
+  using glance::fail;
+  const char* who = "glance_lmhead_argmax_entropy";
+  if (!h || !W || !argmax || !gap || !entropy || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (M < 1 || M > 512 || d < 1 || V < 1)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= M <= 512, d >= 1, V >= 1", who);
+  if (dtype != GLANCE_BF16) return fail(GLANCE_ERR_UNSUPPORTED, "%s: BF16 only", who);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  glance_status st = check_bf16_call(who, h, W, M, d, V, workspace, workspace_bytes);
+  if (st != GLANCE_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  return lmhead_bf16<true>(h, W, M, d, V, argmax, gap, maxlogit, entropy, ws + 256,
+                           reinterpret_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream), who);
 }
 
 // ------------------------------------------------- no-allocation entry point
@@ -868,9 +1025,10 @@ extern "C" glance_status glance_lmhead_argmax_noalloc(const void* h, const void*
   // one block for at most kNoAllocMaxCtas CTAs)
   for (int r0 = 0; r0 < M; r0 += kBM) {
     const int mb = M - r0 < kBM ? M - r0 : kBM;
-    st = launch_bf16<1>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb, d, V,
-                        argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr, part, ticket,
-                        kNoAllocMaxCtas, s, "glance_lmhead_argmax_noalloc");
+    st = launch_bf16<1, false>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb,
+                               d, V, argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr,
+                               nullptr, part, ticket, kNoAllocMaxCtas, s,
+                               "glance_lmhead_argmax_noalloc");
     if (st != GLANCE_OK) return st;
   }
   return GLANCE_OK;
