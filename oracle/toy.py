@@ -8,6 +8,10 @@ Follows "Vision Is Not Overhead ..." (arXiv 2609.00355):
     commit, bonus token as the next root.
   * Theorem 1 (Section 4.2; full statement and proof in Appendix B.1): for any
     tree the rounds emit exactly the greedy autoregressive sequence.
+  * Section 5.4: under sampling every committed token is a draw from the
+    target's own verified row. With `pick` = a sampler whose noise is keyed by
+    the predicted token's absolute position (oracle.sampling), the rounds emit
+    exactly the sampled autoregressive sequence of the same seed.
 
 The pages do not describe the toy target; it is a plain pre-norm decoder:
 token embedding; per layer RMSNorm -> GQA attention with rotate-half RoPE
@@ -19,6 +23,7 @@ default, float32 for the fp32 form of Theorem 1).
 import numpy as np
 
 from .lmhead import lmhead_argmax
+from .sampling import lmhead_sample
 from .tree import build_tree
 from .walk import walk
 
@@ -90,38 +95,59 @@ class ToyTarget:
         return h @ self.Wlm
 
 
-def greedy_ar(target, prompt, n_tokens):
-    """Plain greedy autoregression: returns (tokens, min top-2 gap seen)."""
+def greedy_pick(target):
+    """Token choice of greedy decoding: (argmax, top-2 gap) of each row."""
+    def pick(h, pos):
+        arg, gap, _ = lmhead_argmax(h, target.Wlm)
+        return arg, gap
+    return pick
+
+
+def sample_pick(target, inv_temp, seed, seq=0):
+    """Token choice of sampled decoding: a Gumbel-max draw from softmax(l / T)
+    keyed by the absolute position of the predicted token."""
+    def pick(h, pos):
+        return lmhead_sample(h, target.Wlm, inv_temp, seed, pos, np.full(len(pos), seq))
+    return pick
+
+
+def greedy_ar(target, prompt, n_tokens, pick=None):
+    """Plain autoregression (greedy unless `pick` says otherwise): returns
+    (tokens, min top-2 gap seen). pick(h, pos) returns (tokens, gaps) for rows
+    h whose predicted tokens sit at absolute positions pos."""
+    pick = pick or greedy_pick(target)
     P = len(prompt)
     cache = target.new_cache(P + n_tokens + 1)
     slots = np.arange(P)
     h = target.forward(prompt, np.arange(P), slots, [np.arange(i + 1) for i in range(P)], cache)
-    arg, gap, _ = lmhead_argmax(h[-1:], target.Wlm)
+    arg, gap = pick(h[-1:], np.array([P]))
     out = [int(arg[0])]
     min_gap = float(gap[0])
     t = P
     while len(out) < n_tokens:
         h = target.forward([out[-1]], [t], [t], [np.arange(t + 1)], cache)
-        arg, gap, _ = lmhead_argmax(h, target.Wlm)
+        arg, gap = pick(h, np.array([t + 1]))
         out.append(int(arg[0]))
         min_gap = min(min_gap, float(gap[0]))
         t += 1
     return out, min_gap
 
 
-def glance_decode(target, prompt, n_tokens, N, L, draft_fn, tree_override=None):
+def glance_decode(target, prompt, n_tokens, N, L, draft_fn, tree_override=None, pick=None):
     """GLANCE rounds on the toy target.
 
     draft_fn(r) returns the (L, V) draft logits of the round whose root is
     emitted token r. tree_override(r, root, T) may return a tree dict to use in
     place of the built one (Theorem 1 holds for any tree). Returns (tokens,
-    per-round accepted lengths, min top-2 gap over visited rows).
+    per-round accepted lengths, min top-2 gap over visited rows). pick as in
+    greedy_ar (greedy by default).
     """
+    pick = pick or greedy_pick(target)
     P = len(prompt)
     cap = P + n_tokens + N + 2
     cache = target.new_cache(cap)
     h = target.forward(prompt, np.arange(P), np.arange(P), [np.arange(i + 1) for i in range(P)], cache)
-    arg, gap, _ = lmhead_argmax(h[-1:], target.Wlm)
+    arg, gap = pick(h[-1:], np.array([P]))
     out = [int(arg[0])]
     min_gap = float(gap[0])
     T = P
@@ -137,7 +163,7 @@ def glance_decode(target, prompt, n_tokens, N, L, draft_fn, tree_override=None):
             anc_rows = [k for k in range(rows) if (int(tree["anc"][i, k // 64]) >> (k % 64)) & 1]
             visible.append(np.concatenate([np.arange(T), T + np.asarray(anc_rows)]))
         h = target.forward(tree["token"], tree["pos_id"], slots, visible, cache)
-        arg, gap, _ = lmhead_argmax(h, target.Wlm)
+        arg, gap = pick(h, np.asarray(tree["pos_id"]) + 1)
         a, path, acc, new_root = walk(tree, arg, L)
         min_gap = min([min_gap] + [float(gap[p]) for p in path])
         for Kc, Vc in cache:
