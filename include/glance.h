@@ -199,6 +199,28 @@ glance_status glance_lmhead_argmax_entropy(const void* h, const void* W, glance_
                                            size_t workspace_bytes, void* stream);
 
 /*
+ * Sampling-mode LM head (Section 5.4: under sampling the committed token is a
+ * draw from the target's own verified row, so the walk of Definition 1 runs
+ * unchanged on these tokens and preserves the target's distribution).
+ * tokens[i] = argmax_v (l_iv * inv_temperature + g_iv), a draw from
+ * softmax(l_i / T); g_iv = -ln(-ln u) with u from Philox4x32-10 (Salmon et
+ * al., SC 2011): counter (v / 4, position[i], seq ? seq[i] : 0, 0), key (seed
+ * low 32 bits, seed high 32 bits), output word v % 4, u = (top 23 bits of the
+ * word + 1/2) / 2^23. position[i] (device int32 [M], required) is the
+ * absolute sequence position of the token row i predicts (a packed row's
+ * pos_id + 1); seq (device int32 [M], nullable) separates streams, e.g. the
+ * requests of a batch. Noise keyed by position makes tree rounds reproduce
+ * sampled autoregression of the same seed token for token. gap[i] is the
+ * top-2 margin of the perturbed values. F32 or BF16, same limits and
+ * workspace as glance_lmhead_argmax; inv_temperature must be finite and > 0.
+ */
+glance_status glance_lmhead_sample(const void* h, const void* W, glance_dtype dtype, int M, int d,
+                                   int V, float inv_temperature, uint64_t seed,
+                                   const int32_t* position, const int32_t* seq, int32_t* tokens,
+                                   float* gap, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
  * LM head that allocates nothing and takes no workspace. The paper has no
  * counterpart: this is a convenience of the library. It is for callers that
  * must not allocate device memory or pass scratch space on this path, for

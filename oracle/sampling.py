@@ -12,7 +12,8 @@ uniforms come from the counter-based generator Philox4x32-10 (Salmon, Moraes,
 Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011): for
 the row that predicts the token at absolute sequence position `pos` of stream
 `seq`, column v uses counter (v // 4, pos, seq, 0), key (seed mod 2^32,
-seed div 2^32), output word v mod 4, and u = (floor(word / 2^8) + 1/2) / 2^24.
+seed div 2^32), output word v mod 4, and u = (floor(word / 2^9) + 1/2) / 2^23
+(the top 23 bits, centred: exact in float32, never 0 or 1).
 Keying the noise by the predicted token's position (not by the round) makes
 speculative sampling reproduce autoregressive sampling with the same seed
 token for token, by the argument of Theorem 1 applied to the perturbed
@@ -47,9 +48,9 @@ def philox4x32_10(ctr, key):
 
 
 def uniforms(words):
-    """(0, 1) uniforms from 32-bit words: the top 24 bits, centred."""
-    w = np.asarray(words, dtype=np.uint64) >> np.uint64(8)
-    return (w.astype(np.float64) + 0.5) / float(1 << 24)
+    """(0, 1) uniforms from 32-bit words: the top 23 bits, centred."""
+    w = np.asarray(words, dtype=np.uint64) >> np.uint64(9)
+    return (w.astype(np.float64) + 0.5) / float(1 << 23)
 
 
 def gumbel_noise(seed, seq, pos, V):

@@ -50,7 +50,7 @@ def test_philox_counters_give_distinct_blocks_and_avalanche():
 
 
 def test_uniform_range_and_gumbel_moments():
-    u = uniforms(np.array([0, 255, (1 << 32) - 1], dtype=np.uint64))
+    u = uniforms(np.array([0, 511, (1 << 32) - 1], dtype=np.uint64))
     assert u[0] > 0 and u[-1] < 1 and u[0] == u[1]
     g = np.concatenate([gumbel_noise(99, 0, p, 4096) for p in range(40)])
     assert abs(g.mean() - np.euler_gamma) < 0.02

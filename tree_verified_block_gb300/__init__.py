@@ -14,6 +14,7 @@ launch per step; the LM head takes the B requests' rows stacked.
 from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
                        accept_commit_batched, accept_commit_batched_workspace_bytes,
                        accept_commit_gated, accept_commit_gated_batched, lmhead_argmax_entropy,
+                       lmhead_sample,
                        accept_commit_workspace_bytes, build_tree, build_tree_batched,
                        build_tree_batched_workspace_bytes, build_tree_workspace_bytes,
                        device_status, lib, lmhead_argmax, lmhead_argmax_noalloc,
@@ -24,6 +25,7 @@ from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree,
 __all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
            "accept_commit", "accept_commit_batched", "accept_commit_batched_workspace_bytes",
            "accept_commit_gated", "accept_commit_gated_batched", "lmhead_argmax_entropy",
+           "lmhead_sample",
            "accept_commit_workspace_bytes", "build_tree", "build_tree_batched",
            "build_tree_batched_workspace_bytes", "build_tree_workspace_bytes", "device_status",
            "lib", "lmhead_argmax", "lmhead_argmax_noalloc", "lmhead_argmax_workspace_bytes",

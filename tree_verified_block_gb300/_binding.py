@@ -26,7 +26,7 @@ EXPORTS = [
     "glance_build_tree_batched_workspace_bytes", "glance_build_tree_batched",
     "glance_tree_attention_batched_workspace_bytes", "glance_tree_attention_batched",
     "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
-    "glance_lmhead_argmax_entropy", "glance_accept_commit_gated",
+    "glance_lmhead_argmax_entropy", "glance_lmhead_sample", "glance_accept_commit_gated",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
     "glance_reset_device_status", "glance_version",
@@ -104,6 +104,9 @@ def lib():
     L.glance_accept_commit_batched.restype = st
     L.glance_lmhead_argmax_entropy.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     L.glance_lmhead_argmax_entropy.restype = st
+    L.glance_lmhead_sample.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint64,
+                                       vp, vp, vp, vp, vp, sz, vp]
+    L.glance_lmhead_sample.restype = st
     L.glance_accept_commit_gated.argtypes = [ctypes.POINTER(TreeC), vp, vp, ctypes.c_float,
                                              ctypes.POINTER(KVC), i32, vp, vp, vp, vp, vp, sz, vp]
     L.glance_accept_commit_gated.restype = st
@@ -246,6 +249,17 @@ def lmhead_argmax_entropy(h, W, argmax, gap, maxlogit, entropy, ws, stream=None)
                                               _ptr(argmax), _ptr(gap), _ptr(maxlogit),
                                               _ptr(entropy), _ptr(ws), ws.numel(),
                                               _stream(stream, h.device)))
+
+
+def lmhead_sample(h, W, inv_temperature, seed, position, seq, tokens, gap, ws, stream=None):
+    """Sampling-mode LM head: tokens[i] is a Gumbel-max draw from
+    softmax(l_i / T), the noise keyed by (seed, position[i], seq[i])."""
+    M, d = h.shape
+    assert W.shape[0] == d and h.is_contiguous() and W.is_contiguous() and h.dtype == W.dtype
+    _check(lib().glance_lmhead_sample(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
+                                      float(inv_temperature), int(seed) & ((1 << 64) - 1),
+                                      _ptr(position), _ptr(seq), _ptr(tokens), _ptr(gap), _ptr(ws),
+                                      ws.numel(), _stream(stream, h.device)))
 
 
 def accept_commit_workspace_bytes(n_layers):

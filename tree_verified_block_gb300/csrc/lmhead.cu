@@ -21,6 +21,16 @@
 // requests stacked, up to 512): clusters of two CTAs split the rows and share
 // each W tile through TMA multicast, one launch, W read from HBM once.
 // fp32 path: CUDA cores, 128 vocabulary columns x 8 rows per CTA.
+//
+// Sampling mode (Section 5.4: under sampling the committed token is a draw
+// from the target's own verified row): the same kernels fold l / T + g
+// instead of l, g = -ln(-ln u) Gumbel noise from the counter-based generator
+// Philox4x32-10 (Salmon et al., SC 2011). Column v of the row predicting
+// absolute position pos of stream seq uses counter (v / 4, pos, seq, 0), key
+// (seed low, seed high) and output word v % 4; u = (top 23 bits + 1/2) / 2^23.
+// The argmax is then a draw from softmax(l / T), and since the noise depends
+// on the predicted position only, tree rounds reproduce sampled
+// autoregression of the same seed.
 #include <mutex>
 
 #include "glance_internal.cuh"
@@ -70,6 +80,50 @@ struct PartialH {
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// What the bf16 kernels fold per row.
+constexpr int kGreedy = 0;   // argmax, gap, max of the logits
+constexpr int kEntropy = 1;  // ... and the softmax entropy
+constexpr int kSample = 2;   // argmax and gap of l / T + Gumbel noise
+
+// Philox4x32-10: ten rounds of two 32x32 -> 64-bit products; the key advances
+// by the Weyl increments (2^32 / golden ratio, 2^32 (sqrt 3 - 1)) per round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint32_t lo0 = c.x * kM0, hi0 = __umulhi(c.x, kM0);
+    const uint32_t lo1 = c.z * kM1, hi1 = __umulhi(c.z, kM1);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Gumbel noise from one 32-bit word: u = (top 23 bits + 1/2) / 2^23 in (0, 1).
+__device__ __forceinline__ float gumbel_of(uint32_t w) {
+  const float u = (static_cast<float>(w >> 9) + 0.5f) * (1.0f / 8388608.0f);
+  return -logf(-logf(u));
+}
+
+// Replaces the 32 logits of columns col0.. (col0 % 4 == 0) of one row by
+// l / T + g (sampling mode).
+__device__ __forceinline__ void perturb_chunk(uint32_t (&r)[32], int col0, float inv_temp,
+                                              uint32_t pos, uint32_t seq, uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(col0 / 4 + q), pos, seq, 0u), k0, k1);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      r[4 * q + j] = __float_as_uint(fmaf(__uint_as_float(r[4 * q + j]), inv_temp, gumbel_of(ws[j])));
+  }
+}
 
 // Re-expresses (s, u) relative to a new maximum M >= m.
 __device__ __forceinline__ void rebase(float m, float M, float& s, float& u) {
@@ -186,6 +240,11 @@ struct F32Params {
   float* maxlogit;
   Partial* part;  // [n_colblk][M]
   uint32_t* ticket;
+  // sampling mode when position != null: fold l / T + Gumbel noise
+  const int32_t* position;
+  const int32_t* seq;
+  float inv_temp;
+  uint32_t seed_lo, seed_hi;
 };
 
 __global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p) {
@@ -215,6 +274,19 @@ __global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p)
     }
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.position && v < p.V) {
+#pragma unroll
+    for (int r = 0; r < kF32Rows; ++r) {
+      if (r0 + r < p.M) {
+        const uint32_t pos = static_cast<uint32_t>(p.position[r0 + r]);
+        const uint32_t sq = p.seq ? static_cast<uint32_t>(p.seq[r0 + r]) : 0u;
+        const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(v / 4), pos, sq, 0u),
+                                      p.seed_lo, p.seed_hi);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        acc[r] = fmaf(acc[r], p.inv_temp, gumbel_of(ws[v & 3]));
+      }
+    }
+  }
 #pragma unroll
   for (int r = 0; r < kF32Rows; ++r) {
     Partial a{v < p.V ? acc[r] : -INFINITY, v < p.V ? v : 0x7FFFFFFF, -INFINITY};
@@ -274,7 +346,12 @@ struct Bf16Params {
   float* maxlogit;
   void* part;       // [grid][rows] Partial, or PartialH with the entropy
   uint32_t* ticket;
-  float* entropy;   // [M], written by the kH kernels
+  float* entropy;   // [M], written by the kMode == kEntropy kernels
+  // sampling mode
+  float inv_temp;
+  uint32_t seed_lo, seed_hi;
+  const int32_t* position;  // [M] absolute position of the token each row predicts
+  const int32_t* seq;       // [M] stream of each row, or null (0)
 };
 
 template <int STAGES>
@@ -306,12 +383,13 @@ __device__ __forceinline__ void fail_pipeline(BarsT* bars) {
   atomicExch(&bars->abort_flag, 1);
 }
 
-template <int NB, bool kH>
+template <int NB, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_bf16_kernel(const __grid_constant__ CUtensorMap map_h,
                        const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
   using Sh = Shape<NB>;
   constexpr int BN = Sh::BN, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
+  constexpr bool kH = kMode == kEntropy, kS = kMode == kSample;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -443,6 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       hs[b] = 0.f;
       hu[b] = 0.f;
     }
+    // sampling: each of this thread's rows' predicted position and stream
+    uint32_t spos[NB], sseq[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int gr = b * kBM + row;
+      spos[b] = (kS && gr < p.M) ? static_cast<uint32_t>(p.position[gr]) : 0u;
+      sseq[b] = (kS && gr < p.M && p.seq) ? static_cast<uint32_t>(p.seq[gr]) : 0u;
+    }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = NBUF == 2 ? (i & 1) : 0;
@@ -462,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_acc + c * 32, r);
           tmem_ld_wait();
           const int col0 = v0 + c * 32;
+          if (kS) perturb_chunk(r, col0, p.inv_temp, spos[b], sseq[b], p.seed_lo, p.seed_hi);
           if (col0 + 32 <= p.V) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
@@ -531,13 +618,14 @@ struct PairShape {
   static_assert(kSmem <= 232448, "shared memory");
 };
 
-template <int NB, bool kH>
+template <int NB, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_h,
                             const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
   using Sh = PairShape<NB>;
   constexpr int BN = Sh::BN, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
   constexpr uint16_t kBoth = 0x3;
+  constexpr bool kH = kMode == kEntropy, kS = kMode == kSample;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -664,6 +752,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       hs[b] = 0.f;
       hu[b] = 0.f;
     }
+    // sampling: each of this thread's rows' predicted position and stream
+    uint32_t spos[NB], sseq[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int gr = row0 + b * kBM + row;
+      spos[b] = (kS && gr < p.M) ? static_cast<uint32_t>(p.position[gr]) : 0u;
+      sseq[b] = (kS && gr < p.M && p.seq) ? static_cast<uint32_t>(p.seq[gr]) : 0u;
+    }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = NBUF == 2 ? (i & 1) : 0;
@@ -683,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_acc + c * 32, r);
           tmem_ld_wait();
           const int col0 = v0 + c * 32;
+          if (kS) perturb_chunk(r, col0, p.inv_temp, spos[b], sseq[b], p.seed_lo, p.seed_hi);
           if (col0 + 32 <= p.V) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
@@ -741,16 +838,33 @@ size_t ws_bytes_bf16(int M) {
   return 256 + (static_cast<size_t>(grid) * row_blocks(M) * kBM * sizeof(PartialH) + 255) / 256 * 256;
 }
 
-template <int NB, bool kH>
+// Sampling-mode arguments (unused by the other modes).
+struct SampleArgs {
+  float inv_temp = 1.f;
+  uint64_t seed = 0;
+  const int32_t* position = nullptr;
+  const int32_t* seq = nullptr;
+};
+
+void set_sample(Bf16Params& p, const SampleArgs& sa) {
+  p.inv_temp = sa.inv_temp;
+  p.seed_lo = static_cast<uint32_t>(sa.seed & 0xFFFFFFFFull);
+  p.seed_hi = static_cast<uint32_t>(sa.seed >> 32);
+  p.position = sa.position;
+  p.seq = sa.seq;
+}
+
+template <int NB, int kMode>
 glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
                           float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
-                          int max_grid, cudaStream_t s, const char* who) {
+                          int max_grid, cudaStream_t s, const char* who,
+                          const SampleArgs& sa = SampleArgs()) {
   using Sh = Shape<NB>;
   const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
   int grid = glance::num_sms();
   if (grid > n_tiles) grid = n_tiles;
   if (grid > max_grid) grid = max_grid;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel<NB, kH>),
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_kernel<NB, kMode>),
                                       static_cast<int>(Sh::kSmem));
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   CUtensorMap mw, mh;
@@ -772,7 +886,8 @@ glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int
     if (st != GLANCE_OK) return st;
   }
   Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket, entropy};
-  lmhead_bf16_kernel<NB, kH><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
+  set_sample(p, sa);
+  lmhead_bf16_kernel<NB, kMode><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
@@ -784,8 +899,9 @@ size_t ws_bytes_f32(int M, int V) {
 }
 
 // Clusters of 2 that can be resident at once with this kernel's shared
-// memory, per device (queried once).
-template <int NB>
+// memory, per device (queried once, after the kernel's shared-memory
+// attribute is set).
+template <int NB, int kMode>
 int max_pairs() {
   static int cached[64] = {0};
   static std::mutex mu;
@@ -805,7 +921,7 @@ int max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, lmhead_bf16_pair_kernel<NB, false>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_bf16_pair_kernel<NB, kMode>, &cfg) != cudaSuccess ||
         n < 1)
       n = -1;
     cached[dev] = n;
@@ -813,16 +929,16 @@ int max_pairs() {
   return cached[dev];
 }
 
-template <int NB, bool kH>
+template <int NB, int kMode>
 glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
                           float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
-                          cudaStream_t s, const char* who) {
+                          cudaStream_t s, const char* who, const SampleArgs& sa = SampleArgs()) {
   using Sh = PairShape<NB>;
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_pair_kernel<NB, kH>),
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(lmhead_bf16_pair_kernel<NB, kMode>),
                                       static_cast<int>(Sh::kSmem));
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
-  int pairs = max_pairs<NB>();
+  int pairs = max_pairs<NB, kMode>();
   if (pairs < 1) return glance::fail(GLANCE_ERR_CUDA, "%s: no resident CTA pair fits", who);
   if (pairs > n_tiles) pairs = n_tiles;
   if (2 * pairs > glance::num_sms()) pairs = glance::num_sms() / 2;
@@ -844,6 +960,7 @@ glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int
     if (st != GLANCE_OK) return st;
   }
   Bf16Params p{M, d, V, n_tiles, kBM, argmax, gap, maxlogit, part, ticket, entropy};
+  set_sample(p, sa);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kThreads);
@@ -856,23 +973,25 @@ glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_pair_kernel<NB, kH>, mh, mw, p);
+  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_pair_kernel<NB, kMode>, mh, mw, p);
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
 }
 
 // bf16 LM head, one launch (W streams once for all rows): one CTA per SM for
 // M <= 128, CTA pairs above. entropy == nullptr skips the entropy sums.
-template <bool kH>
+template <int kMode>
 glance_status lmhead_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
                           float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
-                          cudaStream_t s, const char* who) {
+                          cudaStream_t s, const char* who, const SampleArgs& sa = SampleArgs()) {
   if (M <= kBM)
-    return launch_bf16<1, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, 1 << 30,
-                              s, who);
+    return launch_bf16<1, kMode>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket,
+                                 1 << 30, s, who, sa);
   if (M <= 2 * kBM)
-    return launch_pair<1, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s, who);
-  return launch_pair<2, kH>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s, who);
+    return launch_pair<1, kMode>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s,
+                                 who, sa);
+  return launch_pair<2, kMode>(h, W, M, d, V, argmax, gap, maxlogit, entropy, part, ticket, s, who,
+                               sa);
 }
 
 glance_status check_bf16_call(const char* who, const void* h, const void* W, int M, int d, int V,
@@ -914,7 +1033,7 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
     if (workspace_bytes < ws_bytes_f32(M, V))
       return fail(GLANCE_ERR_CAPACITY, "glance_lmhead_argmax: workspace too small");
     F32Params p{static_cast<const float*>(h), static_cast<const float*>(W), M, d, V, argmax, gap,
-                maxlogit, part, ticket};
+                maxlogit, part, ticket, nullptr, nullptr, 1.f, 0u, 0u};
     dim3 grid((V + kF32Cols - 1) / kF32Cols, (M + kF32Rows - 1) / kF32Rows);
     lmhead_f32_kernel<<<grid, kF32Cols, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
@@ -926,8 +1045,8 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
   glance_status st =
       check_bf16_call("glance_lmhead_argmax", h, W, M, d, V, workspace, workspace_bytes);
   if (st != GLANCE_OK) return st;
-  return lmhead_bf16<false>(h, W, M, d, V, argmax, gap, maxlogit, nullptr, part, ticket, s,
-                            "glance_lmhead_argmax");
+  return lmhead_bf16<kGreedy>(h, W, M, d, V, argmax, gap, maxlogit, nullptr, part, ticket, s,
+                              "glance_lmhead_argmax");
 }
 
 extern "C" glance_status glance_lmhead_argmax_entropy(const void* h, const void* W,
@@ -947,8 +1066,50 @@ extern "C" glance_status glance_lmhead_argmax_entropy(const void* h, const void*
   glance_status st = check_bf16_call(who, h, W, M, d, V, workspace, workspace_bytes);
   if (st != GLANCE_OK) return st;
   char* ws = static_cast<char*>(workspace);
-  return lmhead_bf16<true>(h, W, M, d, V, argmax, gap, maxlogit, entropy, ws + 256,
-                           reinterpret_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream), who);
+  return lmhead_bf16<kEntropy>(h, W, M, d, V, argmax, gap, maxlogit, entropy, ws + 256,
+                               reinterpret_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream),
+                               who);
+}
+
+extern "C" glance_status glance_lmhead_sample(const void* h, const void* W, glance_dtype dtype,
+                                              int M, int d, int V, float inv_temperature,
+                                              uint64_t seed, const int32_t* position,
+                                              const int32_t* seq, int32_t* tokens, float* gap,
+                                              void* workspace, size_t workspace_bytes,
+                                              void* stream) {
+  using glance::fail;
+  const char* who = "glance_lmhead_sample";
+  if (!h || !W || !position || !tokens || !gap || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (M < 1 || M > 512 || d < 1 || V < 1)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= M <= 512, d >= 1, V >= 1", who);
+  if (!(inv_temperature > 0.f) || !isfinite(inv_temperature))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: inv_temperature must be finite and > 0", who);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* ticket = static_cast<uint32_t*>(workspace);
+  char* part = static_cast<char*>(workspace) + 256;
+  if (dtype == GLANCE_F32) {
+    if (workspace_bytes < ws_bytes_f32(M, V)) return fail(GLANCE_ERR_CAPACITY, "%s: workspace too small", who);
+    F32Params p{static_cast<const float*>(h), static_cast<const float*>(W), M, d, V, tokens, gap,
+                nullptr, reinterpret_cast<Partial*>(part), ticket, position, seq, inv_temperature,
+                static_cast<uint32_t>(seed & 0xFFFFFFFFull), static_cast<uint32_t>(seed >> 32)};
+    dim3 grid((V + kF32Cols - 1) / kF32Cols, (M + kF32Rows - 1) / kF32Rows);
+    lmhead_f32_kernel<<<grid, kF32Cols, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return glance::cuda_fail(e, who);
+    return GLANCE_OK;
+  }
+  if (dtype != GLANCE_BF16) return fail(GLANCE_ERR_INVALID_ARG, "%s: dtype must be F32 or BF16", who);
+  glance_status st = check_bf16_call(who, h, W, M, d, V, workspace, workspace_bytes);
+  if (st != GLANCE_OK) return st;
+  SampleArgs sa;
+  sa.inv_temp = inv_temperature;
+  sa.seed = seed;
+  sa.position = position;
+  sa.seq = seq;
+  return lmhead_bf16<kSample>(h, W, M, d, V, tokens, gap, nullptr, nullptr, part, ticket, s, who, sa);
 }
 
 // ------------------------------------------------- no-allocation entry point
@@ -1025,7 +1186,7 @@ extern "C" glance_status glance_lmhead_argmax_noalloc(const void* h, const void*
   // one block for at most kNoAllocMaxCtas CTAs)
   for (int r0 = 0; r0 < M; r0 += kBM) {
     const int mb = M - r0 < kBM ? M - r0 : kBM;
-    st = launch_bf16<1, false>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb,
+    st = launch_bf16<1, kGreedy>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb,
                                d, V, argmax + r0, gap + r0, maxlogit ? maxlogit + r0 : nullptr,
                                nullptr, part, ticket, kNoAllocMaxCtas, s,
                                "glance_lmhead_argmax_noalloc");
