@@ -54,7 +54,7 @@ NCU_TRAFFIC = {
     "glance_tree_attention": dict(bytes=17_895_424, digest="0373385bf58664ae",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
-    "glance_lmhead_argmax": dict(bytes=1_245_328_000 + 2_759_424, digest="25ca914779b9aa6c",
+    "glance_lmhead_argmax": dict(bytes=1_245_326_000 + 2_963_968, digest="2aaa31d6b85ac4fd",
                                  files=["lmhead.cu", "glance_internal.cuh"],
                                  profile="profiles/lmhead_argmax_full36.md"),
 }

@@ -47,17 +47,6 @@ struct Partial {
   float m2;
 };
 
-__device__ __forceinline__ void fold(float x, int col, float& m1, int& i1, float& m2) {
-  // columns arrive in increasing order: a later equal maximum keeps the lower id
-  if (x > m1) {
-    m2 = m1;
-    m1 = x;
-    i1 = col;
-  } else if (x > m2) {
-    m2 = x;
-  }
-}
-
 __device__ __forceinline__ void merge(Partial& a, const Partial& b) {
   if (b.m1 > a.m1 || (b.m1 == a.m1 && b.i1 < a.i1)) {
     a.m2 = fmaxf(b.m2, a.m1);
@@ -105,9 +94,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 // Gumbel noise from one 32-bit word: u = (top 23 bits + 1/2) / 2^23 in (0, 1).
+// The inner log needs full relative accuracy near u = 1, where -ln u is tiny
+// and decides the largest noise values; the outer one only absolute accuracy.
 __device__ __forceinline__ float gumbel_of(uint32_t w) {
   const float u = (static_cast<float>(w >> 9) + 0.5f) * (1.0f / 8388608.0f);
-  return -logf(-logf(u));
+  return -__logf(-logf(u));
 }
 
 // Replaces the 32 logits of columns col0.. (col0 % 4 == 0) of one row by
@@ -161,14 +152,66 @@ __device__ __forceinline__ void entropy_chunk(const uint32_t (&r)[32], int col0,
     hm = m;
   }
   const int n = V - col0;
+  // independent terms, summed as a tree (the epilogue runs one warp per
+  // scheduler, so long dependent chains would be latency-bound)
+  float ps[32], pu[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
-    if (e < n) {
-      const float dx = __uint_as_float(r[e]) - hm;
-      const float pe = ex2_approx(dx * kLog2e);
-      hs += pe;
-      hu = fmaf(pe, dx, hu);
+    const bool ok = e < n;
+    const float dx = ok ? __uint_as_float(r[e]) - hm : 0.f;
+    const float pe = ok ? ex2_approx(dx * kLog2e) : 0.f;
+    ps[e] = pe;
+    pu[e] = pe * dx;
+  }
+#pragma unroll
+  for (int w = 16; w; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) {
+      ps[e] += ps[e + w];
+      pu[e] += pu[e + w];
     }
+  hs += ps[0];
+  hu += pu[0];
+}
+
+// Folds 32 logits of columns col0.. (valid below V) into the running
+// (max, argmax, second max). The chunk is reduced as a tree first: its max,
+// the lowest column holding it, and the largest other value; then merged
+// (columns arrive in increasing order, so an equal maximum keeps the earlier
+// id).
+__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, float& m1,
+                                           int& i1, float& m2) {
+  const int n = V - col0;
+  float x[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) x[e] = e < n ? __uint_as_float(r[e]) : -INFINITY;
+  float t[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) t[e] = fmaxf(x[e], x[e + 16]);
+#pragma unroll
+  for (int w = 8; w; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+  const float cm = t[0];
+  if (!(cm > m2)) return;  // nothing in the chunk changes the top two
+  uint32_t hit = 0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) hit |= (x[e] == cm ? 1u : 0u) << e;
+  const int ci = __ffs(static_cast<int>(hit)) - 1;
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    t[e] = fmaxf(e == ci ? -INFINITY : x[e], e + 16 == ci ? -INFINITY : x[e + 16]);
+#pragma unroll
+  for (int w = 8; w; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+  const float c2 = t[0];
+  if (cm > m1) {
+    m2 = fmaxf(m1, c2);
+    m1 = cm;
+    i1 = col0 + ci;
+  } else {
+    m2 = fmaxf(m2, cm);
   }
 }
 
@@ -549,14 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           const int col0 = v0 + c * 32;
           if (kS) perturb_chunk(r, col0, p.inv_temp, spos[b], sseq[b], p.seed_lo, p.seed_hi);
-          if (col0 + 32 <= p.V) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
-          }
+          fold_chunk(r, col0, p.V, m1[b], i1[b], m2[b]);
           if (kH) entropy_chunk(r, col0, p.V, m1[b], hm[b], hs[b], hu[b]);
         }
       }
@@ -780,14 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           const int col0 = v0 + c * 32;
           if (kS) perturb_chunk(r, col0, p.inv_temp, spos[b], sseq[b], p.seed_lo, p.seed_hi);
-          if (col0 + 32 <= p.V) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (col0 + e < p.V) fold(__uint_as_float(r[e]), col0 + e, m1[b], i1[b], m2[b]);
-          }
+          fold_chunk(r, col0, p.V, m1[b], i1[b], m2[b]);
           if (kH) entropy_chunk(r, col0, p.V, m1[b], hm[b], hs[b], hu[b]);
         }
       }
