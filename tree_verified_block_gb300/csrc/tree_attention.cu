@@ -252,7 +252,7 @@ constexpr int kMergeChunk =
     static_cast<int>((kQBytes + kRingBytes - kMergeMlBytes - kMergeWBytes) / (kBM * kD * 2));
 
 template <typename P>
-__device__ void ticket_merge(const P& p, Bars* bars, unsigned char* area, int slot, int S, int qt,
+__device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char* area, int slot, int S, int qt,
                              int g, int q_row0, int half, int lrow) {
   const float2* s_ml = reinterpret_cast<const float2*>(area);
   float* s_w = reinterpret_cast<float*>(area + kMergeMlBytes);
