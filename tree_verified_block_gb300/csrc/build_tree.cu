@@ -17,7 +17,8 @@
 //     logits rank by ascending id;
 //  2. the last CTA of each row (atomic ticket, no spinning) selects the K best
 //     of the row's chunk candidates the same way, ranks them by counting and
-//     writes (token, log q) using the row's log-sum-exp (accumulated in fp64);
+//     writes (token, log q) using the row's log-sum-exp (fp32: each chunk's
+//     sum is relative to its own max, so every term is at most 8192);
 //  3. the last row-merger overall runs the best-first search in one warp
 //     (frontier slots in shared memory, their 32-bit score keys in registers,
 //     8 slots per lane, one warp max-reduction per pop; exact score ties take
@@ -48,8 +49,8 @@ struct BuildParams {
   const int32_t* root_token;    // [B]
   const int32_t* t_len;         // [B]
   uint32_t* tickets;            // [B][kTicketsPerReq]
-  double* chunk_m;              // [B * L][C] chunk max
-  double* chunk_s;              // [B * L][C] chunk sum exp(x - m)
+  float* chunk_m;               // [B * L][C] chunk max
+  float* chunk_s;               // [B * L][C] chunk sum exp(x - m)
   unsigned long long* cand;     // [B * L][C][K]
   int32_t* top_tok;             // [B * L][K]
   float* top_logq;              // [B * L][K]
@@ -510,11 +511,11 @@ template <bool kBF16, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_constant__ BuildParams p) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ SelectSmem sm;
-  __shared__ double red_d[kThreads / 32];
+  __shared__ float red_d[kThreads / 32];
   __shared__ float red_f[kThreads / 32];
   __shared__ uint32_t s_ticket;
   __shared__ unsigned long long sel[256];
-  __shared__ double s_lse;
+  __shared__ float s_lse;
 
   const int req = blockIdx.y;
   const int row = req * p.L + blockIdx.x / p.C;  // global row
@@ -594,10 +595,9 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
 #pragma unroll
   for (int e = 0; e < kPerThread; ++e)
     if (valid_of(e)) s += expf(x[e] - m);
-  double sd = s;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
-  if (lane == 0) red_d[warp] = sd;
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) red_d[warp] = s;
 
   // ---- chunk top-K. The logits move to shared memory (item e of thread t at
   // e * 256 + t, conflict-free) so the selection passes re-read them instead
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
       },
       static_cast<uint32_t>(kc), m, my_cand, sm);
   if (threadIdx.x == 0) {
-    double tot = 0.0;
+    float tot = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) tot += red_d[w];
     p.chunk_m[row * p.C + chunk] = m;
     p.chunk_s[row * p.C + chunk] = tot;
@@ -630,33 +630,43 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
   __threadfence();
   if (threadIdx.x == 0) tickets[orow] = 0;  // ready for the next call
 
-  // row log-sum-exp and max from the chunks' (max, sum) pairs, in fp64
+  // The row's candidate keys move to shared memory first (one coalesced
+  // pass; the selection passes then read them there): flat index f = c * K
+  // + i, zero where i >= min(K, chunk size).
+  unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(dyn);
+  const unsigned long long* row_cand = p.cand + static_cast<size_t>(row) * p.C * p.K;
+  const int n_cand = p.C * p.K;
+  for (int f = threadIdx.x; f < n_cand; f += kThreads) {
+    const int c = f / p.K, i = f - c * p.K;
+    s_cand[f] = i < min(p.K, min(kChunk, p.V - c * kChunk)) ? __ldcg(row_cand + f) : 0ull;
+  }
+  // row log-sum-exp and max from the chunks' (max, sum) pairs: every sum is
+  // relative to its chunk's max, so the fp32 terms are at most 8192 each
   if (warp == 0) {
-    double M = -INFINITY;
-    for (int c = lane; c < p.C; c += 32) M = fmax(M, __ldcg(p.chunk_m + row * p.C + c));
+    float cm[2], cs[2];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmax(M, __shfl_xor_sync(0xffffffffu, M, o));
-    double S = 0.0;
-    for (int c = lane; c < p.C; c += 32)
-      S += __ldcg(p.chunk_s + row * p.C + c) * exp(__ldcg(p.chunk_m + row * p.C + c) - M);
+    for (int q = 0; q < 2; ++q) {  // C <= 64
+      const int c = lane + 32 * q;
+      cm[q] = c < p.C ? __ldcg(p.chunk_m + row * p.C + c) : -INFINITY;
+      cs[q] = c < p.C ? __ldcg(p.chunk_s + row * p.C + c) : 0.f;
+    }
+    float M = fmaxf(cm[0], cm[1]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float S = cs[0] * expf(cm[0] - M) + cs[1] * expf(cm[1] - M);
 #pragma unroll
     for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
     if (lane == 0) {
-      s_lse = M + log(S);
-      red_f[0] = static_cast<float>(M);
+      s_lse = M + logf(S);
+      red_f[0] = M;
     }
   }
   __syncthreads();
   const float row_max = red_f[0];
-  // candidates (read from L2 on each pass): flat index f = c * K + i, valid
-  // when i < min(K, chunk size)
-  const unsigned long long* row_cand = p.cand + static_cast<size_t>(row) * p.C * p.K;
   select_top(
       [&](int e, bool& v, float& xv, unsigned long long& k) {
         const int f = threadIdx.x + kThreads * e;
-        const int c = f / p.K, i = f - c * p.K;
-        k = 0ull;
-        if (c < p.C && i < min(p.K, min(kChunk, p.V - c * kChunk))) k = __ldcg(row_cand + f);
+        k = f < n_cand ? s_cand[f] : 0ull;
         v = k != 0ull;
         xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
       },
@@ -671,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
     const float xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
     const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
     p.top_tok[row * p.K + rank] = static_cast<int32_t>(id);
-    p.top_logq[row * p.K + rank] = static_cast<float>(static_cast<double>(xv) - s_lse);
+    p.top_logq[row * p.K + rank] = xv - s_lse;
   }
 
   // ---- 3. last row-merger builds the tree
@@ -700,9 +710,9 @@ WsLayout ws_layout(int B, int L, int V, int N) {
   w.tickets = o;
   o = align_up(o + sizeof(uint32_t) * kTicketsPerReq * B, 256);
   w.chunk_m = o;
-  o = align_up(o + sizeof(double) * rows * C, 256);
+  o = align_up(o + sizeof(float) * rows * C, 256);
   w.chunk_s = o;
-  o = align_up(o + sizeof(double) * rows * C, 256);
+  o = align_up(o + sizeof(float) * rows * C, 256);
   w.cand = o;
   o = align_up(o + sizeof(unsigned long long) * rows * C * K, 256);
   w.top_tok = o;
@@ -777,15 +787,19 @@ glance_status launch_build(const char* who, const void* draft_logits, glance_dty
   for (int r = 0; r < kMaxB; ++r) p.tree[r] = trees[r < B ? r : 0];
   char* ws = static_cast<char*>(workspace);
   p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets);
-  p.chunk_m = reinterpret_cast<double*>(ws + w.chunk_m);
-  p.chunk_s = reinterpret_cast<double*>(ws + w.chunk_s);
+  p.chunk_m = reinterpret_cast<float*>(ws + w.chunk_m);
+  p.chunk_s = reinterpret_cast<float*>(ws + w.chunk_s);
   p.cand = reinterpret_cast<unsigned long long*>(ws + w.cand);
   p.top_tok = reinterpret_cast<int32_t*>(ws + w.top_tok);
   p.top_logq = reinterpret_cast<float*>(ws + w.top_logq);
 
   // dynamic smem: the chunk's logits during selection, the tree search after
+  // dynamic smem: the chunk's logits during selection, the row's candidate
+  // keys during the row merge, the tree search after
   size_t dyn = 16 * ((sizeof(float) * 2 * L * p.K + 15) / 16) + sizeof(TreeSmem);
   if (dyn < sizeof(float) * kChunk) dyn = sizeof(float) * kChunk;
+  const size_t cand_bytes = sizeof(unsigned long long) * static_cast<size_t>(p.C) * p.K;
+  if (dyn < cand_bytes) dyn = cand_bytes;
   const bool vec = V % 4 == 0 && glance::aligned16(draft_logits);
   void (*kern)(const BuildParams);
   if (p.is_bf16)
