@@ -298,6 +298,33 @@ glance_status glance_build_tree_batched(const void* draft_logits, glance_dtype d
                                         const int32_t* t_len, const glance_tree* trees,
                                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes for glance_build_tree_shared (0 on bad sizes). */
+size_t glance_build_tree_shared_workspace_bytes(int B, int L, int V, int N_max);
+
+/*
+ * Trees of B rounds under one shared verifier budget (Appendix B.5,
+ * Propositions 4-6: the allocation maximising total expected committed length
+ * is global best-first over all rounds' nodes, the law keying each round's
+ * node masses by its root entropy, Equation 5). Node s of request r has mass
+ * w_r * pi_hat_r(s); the N_total nodes of highest mass are kept, at most N_max
+ * per request (its tree capacity). w_r = p_m (1 - p_m^L) with logit p_m =
+ * law_b0 - law_b1 * H_r (Equation 2, the geometric mean truncated at L) when
+ * root_entropy (device float [B], e.g. row 0 of the previous round's
+ * glance_lmhead_argmax_entropy) is given, else 1. Request r keeps the best
+ * n_r = n_active[r] (device int32 [B]) nodes of its own best-first order,
+ * packed canonically in rows 1..n_r; rows n_r+1..N_max are inactive (token
+ * -1, parent -1, depth 0, pos_id T, score -inf, ancestor mask = the row
+ * itself) and the walk never reaches them. Equal masses go to the lower
+ * request. Trees are sized for N = N_max; other arguments and limits as
+ * glance_build_tree_batched. Two launches (search, then allocate and pack).
+ */
+glance_status glance_build_tree_shared(const void* draft_logits, glance_dtype dtype, int B, int L,
+                                       int V, int N_max, int N_total, const int32_t* root_token,
+                                       const int32_t* t_len, const float* root_entropy,
+                                       float law_b0, float law_b1, const glance_tree* trees,
+                                       int32_t* n_active, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
 /* Workspace bytes for glance_tree_attention_batched (0 on bad sizes); the
  * split of the key range over CTAs depends on every request's t_cap, so pass
  * the same kv array as to the call. */

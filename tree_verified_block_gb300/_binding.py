@@ -27,6 +27,7 @@ EXPORTS = [
     "glance_tree_attention_batched_workspace_bytes", "glance_tree_attention_batched",
     "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
     "glance_lmhead_argmax_entropy", "glance_lmhead_sample", "glance_accept_commit_gated",
+    "glance_build_tree_shared_workspace_bytes", "glance_build_tree_shared",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
     "glance_reset_device_status", "glance_version",
@@ -104,6 +105,12 @@ def lib():
     L.glance_accept_commit_batched.restype = st
     L.glance_lmhead_argmax_entropy.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     L.glance_lmhead_argmax_entropy.restype = st
+    L.glance_build_tree_shared_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.glance_build_tree_shared_workspace_bytes.restype = sz
+    L.glance_build_tree_shared.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp,
+                                           ctypes.c_float, ctypes.c_float, ctypes.POINTER(TreeC),
+                                           vp, vp, sz, vp]
+    L.glance_build_tree_shared.restype = st
     L.glance_lmhead_sample.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint64,
                                        vp, vp, vp, vp, vp, sz, vp]
     L.glance_lmhead_sample.restype = st
@@ -305,6 +312,23 @@ def build_tree_batched(draft_logits, N, root_token, t_len, trees, ws, stream=Non
                                            N, _ptr(root_token), _ptr(t_len), _trees(trees),
                                            _ptr(ws), ws.numel(),
                                            _stream(stream, draft_logits.device)))
+
+
+def build_tree_shared_workspace_bytes(B, L, V, N_max):
+    return lib().glance_build_tree_shared_workspace_bytes(B, L, V, N_max)
+
+
+def build_tree_shared(draft_logits, N_max, N_total, root_token, t_len, trees, n_active, ws,
+                      root_entropy=None, law_b0=0.0, law_b1=0.0, stream=None):
+    """B trees under a shared budget of N_total nodes (at most N_max each); with
+    root_entropy [B], node masses are keyed by the entropy law."""
+    B, L, V = draft_logits.shape
+    assert draft_logits.is_contiguous() and len(trees) == B
+    _check(lib().glance_build_tree_shared(_ptr(draft_logits), _dtype_code(draft_logits), B, L, V,
+                                          N_max, N_total, _ptr(root_token), _ptr(t_len),
+                                          _ptr(root_entropy), float(law_b0), float(law_b1),
+                                          _trees(trees), _ptr(n_active), _ptr(ws), ws.numel(),
+                                          _stream(stream, draft_logits.device)))
 
 
 def tree_attention_batched_workspace_bytes(rows, n_q_heads, kvs):

@@ -55,6 +55,10 @@ struct BuildParams {
   int32_t* top_tok;             // [B * L][K]
   float* top_logq;              // [B * L][K]
   glance_tree tree[kMaxB];
+  // shared budget (two launches): the search writes its pops here instead of
+  // packing; the pack kernel allocates the budget and packs
+  int search_only;
+  void* pops_out;               // [B][kMaxN] PopRec
 };
 
 constexpr int kBuckets = 2048;      // first-pass buckets of the gap to the max
@@ -301,6 +305,66 @@ __device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlotsPerLane], 
 
 constexpr uint32_t kRootChild = 0xFFFFu;  // code of the first node (rank 0 at offset 1)
 
+// Packs the first n pops of request req (a prefix of the best-first order, so
+// a prefix-closed set) into canonical rows 0..n; rows n+1..N are inactive:
+// token -1, parent -1 (never a child, so the walk never reaches them), depth
+// 0, pos_id T, score -inf, ancestor mask = the row itself.
+__device__ void pack_rows(const BuildParams& p, const int* s_tok, TreeSmem& ts, const int req,
+                          const int n) {
+  const int N = p.N, K = p.K;
+  // canonical position: 1 + number of nodes before it in (depth, rank vector)
+  const int T = p.t_len[req];
+  const glance_tree& tree = p.tree[req];
+  const int W = tree.mask_words;
+  for (int kk = threadIdx.x; kk < n; kk += kThreads) {
+    const uint32_t dk = ts.pop[kk].dep;
+    const unsigned long long hk = ts.pop[kk].hi, lk = ts.pop[kk].lo;
+    int pos = 1;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j)
+      pos += tie_less(ts.pop[j].dep, ts.pop[j].hi, ts.pop[j].lo, dk, hk, lk);
+    ts.p_pos[kk] = static_cast<int16_t>(pos);
+  }
+  __syncthreads();
+  for (int kk = threadIdx.x; kk <= N; kk += kThreads) {
+    if (kk == N) {  // root row
+      tree.token[0] = p.root_token[req];
+      tree.parent[0] = -1;
+      tree.depth[0] = 0;
+      tree.pos_id[0] = T;
+      tree.score[0] = 0.f;
+      for (int w = 0; w < W; ++w) tree.anc[w] = (w == 0) ? 1ull : 0ull;
+      continue;
+    }
+    if (kk >= n) {  // inactive row n + 1 + (kk - n)
+      const int row = kk + 1;
+      tree.token[row] = -1;
+      tree.parent[row] = -1;
+      tree.depth[row] = 0;
+      tree.pos_id[row] = T;
+      tree.score[row] = -INFINITY;
+      for (int w = 0; w < W; ++w) tree.anc[row * W + w] = (w == (row >> 6)) ? (1ull << (row & 63)) : 0ull;
+      continue;
+    }
+    const int row = ts.p_pos[kk];
+    const int d = ts.pop[kk].dep;
+    const uint32_t r = get_rank(ts.pop[kk].hi, ts.pop[kk].lo, d - 1);
+    const int par = ts.pop[kk].par;
+    tree.token[row] = s_tok[(d - 1) * K + r];
+    tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
+    tree.depth[row] = d;
+    tree.pos_id[row] = T + d;
+    tree.score[row] = ts.pop[kk].score;
+    unsigned long long words[4] = {1ull, 0ull, 0ull, 0ull};
+    words[row >> 6] |= 1ull << (row & 63);
+    for (int u = par; u >= 0; u = ts.pop[u].par) {
+      const int pr = ts.p_pos[u];
+      words[pr >> 6] |= 1ull << (pr & 63);
+    }
+    for (int w = 0; w < W; ++w) tree.anc[row * W + w] = words[w];
+  }
+}
+
 __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int req) {
   // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
   float* s_logq = reinterpret_cast<float*>(dyn);
@@ -462,47 +526,13 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
   }
   __syncthreads();
 
-  // canonical position: 1 + number of nodes before it in (depth, rank vector)
-  const int T = p.t_len[req];
-  const glance_tree& tree = p.tree[req];
-  const int W = tree.mask_words;
-  for (int kk = threadIdx.x; kk < N; kk += kThreads) {
-    const uint32_t dk = ts.pop[kk].dep;
-    const unsigned long long hk = ts.pop[kk].hi, lk = ts.pop[kk].lo;
-    int pos = 1;
-#pragma unroll 4
-    for (int j = 0; j < N; ++j)
-      pos += tie_less(ts.pop[j].dep, ts.pop[j].hi, ts.pop[j].lo, dk, hk, lk);
-    ts.p_pos[kk] = static_cast<int16_t>(pos);
+  if (p.search_only) {
+    // shared budget: hand the pops (in best-first order) to the pack kernel
+    PopRec* dst = static_cast<PopRec*>(p.pops_out) + static_cast<size_t>(req) * kMaxN;
+    for (int kk = threadIdx.x; kk < N; kk += kThreads) dst[kk] = ts.pop[kk];
+    return;
   }
-  __syncthreads();
-  for (int kk = threadIdx.x; kk <= N; kk += kThreads) {
-    if (kk == N) {  // root row
-      tree.token[0] = p.root_token[req];
-      tree.parent[0] = -1;
-      tree.depth[0] = 0;
-      tree.pos_id[0] = T;
-      tree.score[0] = 0.f;
-      for (int w = 0; w < W; ++w) tree.anc[w] = (w == 0) ? 1ull : 0ull;
-      continue;
-    }
-    const int row = ts.p_pos[kk];
-    const int d = ts.pop[kk].dep;
-    const uint32_t r = get_rank(ts.pop[kk].hi, ts.pop[kk].lo, d - 1);
-    const int par = ts.pop[kk].par;
-    tree.token[row] = s_tok[(d - 1) * K + r];
-    tree.parent[row] = par < 0 ? 0 : ts.p_pos[par];
-    tree.depth[row] = d;
-    tree.pos_id[row] = T + d;
-    tree.score[row] = ts.pop[kk].score;
-    unsigned long long words[4] = {1ull, 0ull, 0ull, 0ull};
-    words[row >> 6] |= 1ull << (row & 63);
-    for (int u = par; u >= 0; u = ts.pop[u].par) {
-      const int pr = ts.p_pos[u];
-      words[pr >> 6] |= 1ull << (pr & 63);
-    }
-    for (int w = 0; w < W; ++w) tree.anc[row * W + w] = words[w];
-  }
+  pack_rows(p, s_tok, ts, req, N);
 }
 
 // ------------------------------------------------------------------- kernel
@@ -695,6 +725,77 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
   tree_phase(p, dyn, req);
 }
 
+// Shared budget, second launch: one CTA per request. Every CTA ranks its own
+// request's pops (best-first order) among all B x N pops by weighted key
+// log w_r + score (desc; ties to the lower request, then the request's own
+// order), keeps those ranked below N_total (a prefix of its order), and packs
+// them. log w_r = log(p_m (1 - p_m^L)), logit p_m = b0 - b1 H_r, from the
+// root entropies when given, else 0.
+struct SharedArgs {
+  int n_total;
+  const float* root_entropy;  // [B] or null
+  float b0, b1;
+  int32_t* n_active;          // [B]
+};
+
+__global__ void __launch_bounds__(kThreads) shared_pack_kernel(const __grid_constant__ BuildParams p,
+                                                                const SharedArgs sa) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  TreeSmem& ts = *reinterpret_cast<TreeSmem*>(dyn);
+  int* s_tok = reinterpret_cast<int*>(dyn + sizeof(TreeSmem));
+  float* keys = reinterpret_cast<float*>(s_tok + p.L * p.K);  // [B][N]
+  __shared__ float s_logw[kMaxB];
+  __shared__ int s_cnt;
+  const int req = blockIdx.x;
+  const int N = p.N, B = p.B;
+  if (threadIdx.x < B) {
+    float lw = 0.f;
+    if (sa.root_entropy) {
+      const float H = sa.root_entropy[threadIdx.x];
+      const float pm = 1.f / (1.f + expf(-(sa.b0 - sa.b1 * H)));
+      lw = logf(pm) + log1pf(-powf(pm, static_cast<float>(p.L)));
+    }
+    s_logw[threadIdx.x] = lw;
+  }
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const PopRec* pops = static_cast<const PopRec*>(p.pops_out);
+  for (int f = threadIdx.x; f < B * N; f += kThreads) {
+    const int r = f / N, i = f - r * N;
+    keys[f] = s_logw[r] + pops[static_cast<size_t>(r) * kMaxN + i].score;
+  }
+  for (int i = threadIdx.x; i < N; i += kThreads) ts.pop[i] = pops[static_cast<size_t>(req) * kMaxN + i];
+  for (int i = threadIdx.x; i < p.L * p.K; i += kThreads)
+    s_tok[i] = p.top_tok[static_cast<size_t>(req) * p.L * p.K + i];
+  __syncthreads();
+  int mine = 0;
+  for (int i = threadIdx.x; i < N; i += kThreads) {
+    const float k = keys[req * N + i];
+    int rank = i;
+    for (int r = 0; r < B; ++r) {
+      if (r == req) continue;
+      // entries of list r ahead of k form a prefix (the list is non-increasing)
+      const float* lst = keys + r * N;
+      int lo = 0, hi = N;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const bool ahead = r < req ? lst[mid] >= k : lst[mid] > k;
+        if (ahead)
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      rank += lo;
+    }
+    mine += rank < sa.n_total ? 1 : 0;
+  }
+  atomicAdd(&s_cnt, mine);
+  __syncthreads();
+  const int n = s_cnt;
+  if (threadIdx.x == 0) sa.n_active[req] = n;
+  pack_rows(p, s_tok, ts, req, n);
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
@@ -742,7 +843,7 @@ bool sizes_ok(int L, int V, int N) {
 glance_status launch_build(const char* who, const void* draft_logits, glance_dtype dtype, int B,
                            int L, int V, int N, const int32_t* root_token, const int32_t* t_len,
                            const glance_tree* trees, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+                           void* stream, const SharedArgs* shared = nullptr) {
   using glance::fail;
   if (!draft_logits || !root_token || !t_len || !trees || !workspace)
     return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
@@ -767,9 +868,11 @@ glance_status launch_build(const char* who, const void* draft_logits, glance_dty
       return fail(GLANCE_ERR_INVALID_ARG, "%s: null array in tree %d", who, r);
   }
   const WsLayout w = ws_layout(B, L, V, N);
-  if (workspace_bytes < w.total)
+  const size_t pops_at = w.total;  // shared budget: the pops after the regular layout
+  const size_t need = shared ? pops_at + sizeof(PopRec) * kMaxN * B : w.total;
+  if (workspace_bytes < need)
     return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who,
-                workspace_bytes, w.total);
+                workspace_bytes, need);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
 
@@ -792,6 +895,8 @@ glance_status launch_build(const char* who, const void* draft_logits, glance_dty
   p.cand = reinterpret_cast<unsigned long long*>(ws + w.cand);
   p.top_tok = reinterpret_cast<int32_t*>(ws + w.top_tok);
   p.top_logq = reinterpret_cast<float*>(ws + w.top_logq);
+  p.search_only = shared ? 1 : 0;
+  p.pops_out = shared ? static_cast<void*>(ws + pops_at) : nullptr;
 
   // dynamic smem: the chunk's logits during selection, the tree search after
   // dynamic smem: the chunk's logits during selection, the row's candidate
@@ -811,6 +916,14 @@ glance_status launch_build(const char* who, const void* draft_logits, glance_dty
   kern<<<dim3(L * p.C, B), kThreads, dyn, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  if (shared) {
+    const size_t dyn2 = sizeof(TreeSmem) + sizeof(int) * L * p.K + sizeof(float) * B * N;
+    e = glance::ensure_smem(reinterpret_cast<const void*>(shared_pack_kernel), static_cast<int>(dyn2));
+    if (e != cudaSuccess) return glance::cuda_fail(e, who);
+    shared_pack_kernel<<<B, kThreads, dyn2, static_cast<cudaStream_t>(stream)>>>(p, *shared);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  }
   return GLANCE_OK;
 }
 
@@ -843,4 +956,26 @@ extern "C" glance_status glance_build_tree_batched(const void* draft_logits, gla
                                                    void* stream) {
   return launch_build("glance_build_tree_batched", draft_logits, dtype, B, L, V, N, root_token,
                       t_len, trees, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t glance_build_tree_shared_workspace_bytes(int B, int L, int V, int N_max) {
+  if (B < 1 || B > kMaxB || !sizes_ok(L, V, N_max)) return 0;
+  return ws_layout(B, L, V, N_max).total + sizeof(PopRec) * kMaxN * B;
+}
+
+extern "C" glance_status glance_build_tree_shared(const void* draft_logits, glance_dtype dtype,
+                                                  int B, int L, int V, int N_max, int N_total,
+                                                  const int32_t* root_token, const int32_t* t_len,
+                                                  const float* root_entropy, float law_b0,
+                                                  float law_b1, const glance_tree* trees,
+                                                  int32_t* n_active, void* workspace,
+                                                  size_t workspace_bytes, void* stream) {
+  const char* who = "glance_build_tree_shared";
+  if (!n_active) return glance::fail(GLANCE_ERR_INVALID_ARG, "%s: null n_active", who);
+  if (N_total < 0) return glance::fail(GLANCE_ERR_INVALID_ARG, "%s: N_total must be >= 0", who);
+  if (root_entropy && !(isfinite(law_b0) && isfinite(law_b1)))
+    return glance::fail(GLANCE_ERR_INVALID_ARG, "%s: law coefficients must be finite", who);
+  SharedArgs sa{N_total, root_entropy, law_b0, law_b1, n_active};
+  return launch_build(who, draft_logits, dtype, B, L, V, N_max, root_token, t_len, trees,
+                      workspace, workspace_bytes, stream, &sa);
 }
