@@ -1,0 +1,171 @@
+"""Dense verify layers on the GPU vs the oracle (fp64 on the same bf16
+inputs): RMSNorm row scales within 1e-5 relative; projections, SwiGLU,
+q/k with RoPE and the cache rows within 2e-2 * max(1, |ref|); the whole
+layer (with tree attention between) against the oracle's steps with the
+intermediates the library keeps in bf16 rounded there too; cache slots outside the rows'
+untouched."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _util import bf16_tensor
+from oracle.attention import tree_attention as o_attn
+from oracle.bf16 import bf16_bits_to_f64, f32_to_bf16_bits
+from oracle.dense import qkv as o_qkv, residual as o_residual, rms_scale as o_rms
+from oracle.dense import swiglu as o_swiglu
+from test_gpu_attention import random_tree, upload_tree
+
+pytestmark = pytest.mark.gpu
+
+
+def close(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - want) / np.maximum(1.0, np.abs(want))
+    assert err.max() < 2e-2, err.max()
+
+
+def rb16(a):
+    """a rounded to bf16, as the library stores it."""
+    return bf16_bits_to_f64(f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
+
+
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,d", [(64, 4096), (7, 512), (128, 12288)])
+def test_rms_scale(dev, clean_status, M, d):
+    import tree_verified_block_gb300 as g
+    xb = W.normal_bf16(W.rng(M, d), (M, d))
+    r = torch.empty(M, dtype=torch.float32, device=dev)
+    g.rms_scale(bf16_tensor(xb, dev), 1e-6, r)
+    want = o_rms(bf16_bits_to_f64(xb), 1e-6)
+    assert np.all(np.abs(r.cpu().numpy() - want) <= 1e-5 * want)
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 4096, 4096), (17, 12288, 4096), (128, 512, 768), (1, 64, 256)])
+def test_residual_projection(dev, clean_status, M, K, N):
+    import tree_verified_block_gb300 as g
+    gen = W.rng(M, K, N)
+    xb = W.normal_bf16(gen, (M, K))
+    Wb = W.normal_bf16(gen, (K, N), std=0.02)
+    rb = W.normal_bf16(gen, (M, N))
+    res = bf16_tensor(rb, dev)
+    out = torch.full_like(res, float("nan"))
+    ws = g.workspace(g.dense_workspace_bytes(M, K, N), dev)
+    for _ in range(2):  # the grid barrier's counters are reusable
+        g.dense_residual(bf16_tensor(xb, dev), bf16_tensor(Wb, dev), res, out, ws)
+    close(f64(out), o_residual(bf16_bits_to_f64(rb), bf16_bits_to_f64(xb), bf16_bits_to_f64(Wb)))
+    assert int(ws[:256].sum().item()) == 0
+
+
+@pytest.mark.parametrize("M,d,inter", [(64, 4096, 12288), (5, 256, 384)])
+def test_swiglu(dev, clean_status, M, d, inter):
+    import tree_verified_block_gb300 as g
+    gen = W.rng(M, d, inter)
+    hb = W.normal_bf16(gen, (M, d))
+    Gb = W.normal_bf16(gen, (d, inter), std=0.02)
+    Ub = W.normal_bf16(gen, (d, inter), std=0.02)
+    h = bf16_tensor(hb, dev)
+    r = torch.empty(M, dtype=torch.float32, device=dev)
+    g.rms_scale(h, 1e-6, r)
+    act = torch.full((M, inter), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = g.workspace(g.dense_workspace_bytes(M, d, 2 * inter), dev)
+    g.dense_swiglu(h, bf16_tensor(Gb, dev), bf16_tensor(Ub, dev), r, act, ws)
+    want = o_swiglu(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Gb), bf16_bits_to_f64(Ub), 1e-6)
+    close(f64(act), want)
+
+
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_qkv_rope_into_cache(dev, clean_status, qk_norm):
+    import tree_verified_block_gb300 as g
+    M, d, Hq, Hkv, D, T = 64, 4096, 32, 8, 128, 3000
+    t_cap = T + M + 16
+    gen = W.rng(77, int(qk_norm))
+    hb = W.normal_bf16(gen, (M, d))
+    Wb = W.normal_bf16(gen, (d, (Hq + 2 * Hkv) * D), std=0.02)
+    qn = gen.uniform(0.5, 1.5, size=D).astype(np.float32) if qk_norm else None
+    kn = gen.uniform(0.5, 1.5, size=D).astype(np.float32) if qk_norm else None
+    pos = (T + gen.integers(0, 16, size=M)).astype(np.int32)
+    kb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    vb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    t_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    kv = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(vb, dev), t_len)
+    h = bf16_tensor(hb, dev)
+    r = torch.empty(M, dtype=torch.float32, device=dev)
+    g.rms_scale(h, 1e-6, r)
+    q = torch.full((M, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = g.workspace(g.dense_workspace_bytes(M, d, (Hq + 2 * Hkv) * D), dev)
+    tt = lambda a: None if a is None else torch.from_numpy(a).to(dev)
+    g.dense_qkv(h, bf16_tensor(Wb, dev), Hq, r, tt(qn), tt(kn), 1e-6, torch.from_numpy(pos).to(dev),
+                1e6, q, kv, ws)
+    wq, wk, wv = o_qkv(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Wb), Hq, Hkv, D, pos, 1e6, 1e-6,
+                       None if qn is None else qn.astype(np.float64),
+                       None if kn is None else kn.astype(np.float64))
+    close(f64(q), wq)
+    K = f64(kv.k)
+    V = f64(kv.v)
+    close(K[:, T:T + M], wk.transpose(1, 0, 2))
+    close(V[:, T:T + M], wv.transpose(1, 0, 2))
+    # slots outside the rows' are untouched
+    keep = np.r_[0:T, T + M:t_cap]
+    assert np.array_equal(kv.k.view(torch.int16).cpu().numpy().view(np.uint16)[:, keep], kb[:, keep])
+    assert np.array_equal(kv.v.view(torch.int16).cpu().numpy().view(np.uint16)[:, keep], vb[:, keep])
+
+
+def test_full_layer_with_tree_attention(dev, clean_status):
+    import tree_verified_block_gb300 as g
+    M, d, Hq, Hkv, D, I, T = 64, 4096, 32, 8, 128, 12288, 512
+    t_cap = T + M + 8
+    gen = W.rng(2025)
+    ref = random_tree(M - 1, 15, T, 9)
+    xb = W.normal_bf16(gen, (M, d))
+    Wqkv = W.normal_bf16(gen, (d, (Hq + 2 * Hkv) * D), std=0.02)
+    Wo = W.normal_bf16(gen, (Hq * D, d), std=0.02)
+    Wg = W.normal_bf16(gen, (d, I), std=0.02)
+    Wu = W.normal_bf16(gen, (d, I), std=0.02)
+    Wd = W.normal_bf16(gen, (I, d), std=0.02)
+    qn = gen.uniform(0.5, 1.5, size=D).astype(np.float32)
+    kn = gen.uniform(0.5, 1.5, size=D).astype(np.float32)
+    kb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    vb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    pos = ref["pos_id"].astype(np.int32)
+    # GPU layer
+    t_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    kv = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(vb, dev), t_len)
+    tree = upload_tree(ref, 15, dev)
+    x = bf16_tensor(xb, dev)
+    r = torch.empty(M, dtype=torch.float32, device=dev)
+    q = torch.empty((M, Hq, D), dtype=torch.bfloat16, device=dev)
+    att = torch.empty_like(q)
+    x1 = torch.empty_like(x)
+    act = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(x)
+    ws = g.workspace(max(g.dense_workspace_bytes(M, d, 2 * I), g.dense_workspace_bytes(M, I, d),
+                         g.dense_workspace_bytes(M, d, (Hq + 2 * Hkv) * D)), dev)
+    ws_a = g.workspace(g.tree_attention_workspace_bytes(M, Hq, kv), dev)
+    g.rms_scale(x, 1e-6, r)
+    g.dense_qkv(x, bf16_tensor(Wqkv, dev), Hq, r, torch.from_numpy(qn).to(dev), torch.from_numpy(kn).to(dev),
+                1e-6, torch.from_numpy(pos).to(dev), 1e6, q, kv, ws)
+    g.tree_attention(q, kv, tree, D ** -0.5, att, ws_a)
+    g.dense_residual(att.view(M, Hq * D), bf16_tensor(Wo, dev), x, x1, ws)
+    g.rms_scale(x1, 1e-6, r)
+    g.dense_swiglu(x1, bf16_tensor(Wg, dev), bf16_tensor(Wu, dev), r, act, ws)
+    g.dense_residual(act, bf16_tensor(Wd, dev), x1, out, ws)
+    # the oracle's steps on the same bf16 inputs, each intermediate the library
+    # stores as bf16 between calls (q, the cache rows, att, x1, act) rounded
+    # there too; fp64 inside every step
+    Kc, Vc = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
+    x0 = bf16_bits_to_f64(xb)
+    wq, wk, wv = o_qkv(x0, None, bf16_bits_to_f64(Wqkv), Hq, Hkv, D, pos, 1e6, 1e-6,
+                       qn.astype(np.float64), kn.astype(np.float64))
+    Kc[:, T:T + M] = rb16(wk.transpose(1, 0, 2))
+    Vc[:, T:T + M] = rb16(wv.transpose(1, 0, 2))
+    watt = rb16(o_attn(rb16(wq), Kc[:, :T + M], Vc[:, :T + M], T, ref["anc"], D ** -0.5))
+    close(f64(att), watt)
+    wx1 = rb16(o_residual(x0, watt.reshape(M, Hq * D), bf16_bits_to_f64(Wo)))
+    close(f64(x1), wx1)
+    wact = rb16(o_swiglu(wx1, None, bf16_bits_to_f64(Wg), bf16_bits_to_f64(Wu), 1e-6))
+    close(f64(act), wact)
+    close(f64(out), o_residual(wx1, wact, bf16_bits_to_f64(Wd)))

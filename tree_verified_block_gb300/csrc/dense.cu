@@ -1,0 +1,655 @@
+// The target's dense verify layers around tree attention, at the verify
+// width (M <= 128 packed rows).
+//
+// Paper: "Vision Is Not Overhead ..." (arXiv 2609.00355): the verify pass
+// runs the frozen target once over the packed tree rows (Definition 1,
+// Section 4.2) and its forward dominates a round's cost (Table 11 and the
+// round-cost regression of Appendix E). The pages do not describe the layer;
+// this is a Qwen3-shaped pre-norm decoder layer:
+//   x -> RMSNorm -> [q | k | v] = . W_qkv -> per-head RMSNorm of q, k (when
+//   weights are given) -> rotate-half RoPE at the rows' positions -> q out,
+//   K/V into the cache at slots T + row -> (tree attention) -> x + . W_o
+//   -> RMSNorm -> SiLU(. W_gate) * (. W_up) -> x' + . W_down.
+// An RMSNorm's weight is folded into the next projection's rows by the
+// caller; its 1 / rms row scale, which a projection is linear in, is applied
+// to the product (glance_rms_scale computes it).
+//
+// GEMM shape: Y[M x N] = X[M x K] W[K x N], W row-major with N contiguous
+// (the MN-major B operand), bf16 in, fp32 accumulate. At M <= 128 the weights
+// dominate (HBM-bound), and N / 256 output tiles are too few to occupy the
+// SMs, so K is split: unit (tile, split) accumulates its K range in tensor
+// memory and writes an fp32 partial (phase 1); after a grid barrier
+// (cooperative launch) every CTA sums the splits of a share of (tile, 16-row)
+// items and applies the epilogue (phase 2). Phase 1 is the LM head's pipeline:
+// warp 0 streams X and W stages with TMA (4 x 48 KB), warp 1 issues
+// M=128 x N=256 x K=16 MMAs into one of two TMEM accumulators, warps 4..7
+// drain the other one to the partial buffer.
+#include <cstring>
+#include <mutex>
+
+#include "glance_internal.cuh"
+
+GLANCE_DEFINE_STATUS_WORD(status_dense)
+
+using namespace glance_dev;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB
+constexpr uint32_t kBBytes = kBK * kBN * 2;    // 32 KB
+constexpr uint32_t kWBoxBytes = kBK * 64 * 2;  // one 64 x 64 box of W: 8 KB
+constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256;
+constexpr int kItemRows = 16;                  // phase-2 item: 16 rows of a tile
+constexpr int kHeadDim = 128;
+
+enum Mode : int { kResid = 0, kQKV = 1, kSwiGLU = 2 };
+
+struct DenseParams {
+  int M, K, n_tiles, n_split, n_kb, a_rows, mode;
+  float* part;              // [units][a_rows][256] fp32 partials
+  uint32_t* barrier;        // [2] grid barrier: arrivals, departures
+  const float* rscale;      // [M] 1 / rms of the input rows, or null
+  // kResid: out = res + X W, both [M][n_out]
+  const __nv_bfloat16* res;
+  __nv_bfloat16* out;
+  int n_out;
+  // kQKV
+  int Hq, Hkv;
+  const float* q_norm;      // [128] or null
+  const float* k_norm;      // [128] or null
+  float eps;
+  const int32_t* pos;       // [M] position ids
+  float log2_theta;
+  __nv_bfloat16* q_out;     // [M][Hq][128]
+  __nv_bfloat16* k_cache;   // [Hkv][t_cap][128] (strides below)
+  __nv_bfloat16* v_cache;
+  long long head_stride, row_stride;  // elements
+  const int32_t* t_len;
+  int t_cap;
+  // kSwiGLU: act[M][inter] = SiLU(gate) * up
+  __nv_bfloat16* act;
+  int inter;
+};
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fail_pipeline(Bars* bars) {
+  report(GLANCE_DEV_PIPELINE_TIMEOUT);
+  atomicExch(&bars->abort_flag, 1);
+}
+
+// Phase-2 epilogue of one (tile, 16-row) item whose split sum sits in
+// s_sum[16][256] (fp32).
+__device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile, int r0, int T) {
+  const int t = threadIdx.x;
+  if (p.mode == kResid) {
+    // thread: one row, 16 columns
+    const int rr = t / 16, c0 = (t % 16) * 16;
+    const int row = r0 + rr;
+    if (row >= p.M) return;
+    const size_t at = static_cast<size_t>(row) * p.n_out + static_cast<size_t>(tile) * kBN + c0;
+    const uint4* rs = reinterpret_cast<const uint4*>(p.res + at);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + at);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 v = rs[h];
+      const uint32_t rv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(rv[e] << 16) + s_sum[rr * kBN + c0 + 8 * h + 2 * e];
+        const float hi = __uint_as_float(rv[e] & 0xFFFF0000u) + s_sum[rr * kBN + c0 + 8 * h + 2 * e + 1];
+        o[e] = pack_bf16x2(lo, hi);
+      }
+      dst[h] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    return;
+  }
+  if (p.mode == kSwiGLU) {
+    // thread: one row, 8 of the tile's 128 (gate, up) column pairs
+    const int rr = t / 16, j0 = (t % 16) * 8;
+    const int row = r0 + rr;
+    if (row >= p.M) return;
+    const float r = p.rscale ? p.rscale[row] : 1.f;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float a2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + 2 * e + h;
+        const float g = s_sum[rr * kBN + j] * r;
+        const float u = s_sum[rr * kBN + 128 + j] * r;
+        a2[h] = g / (1.f + expf(-g)) * u;
+      }
+      o[e] = pack_bf16x2(a2[0], a2[1]);
+    }
+    *reinterpret_cast<uint4*>(p.act + static_cast<size_t>(row) * p.inter +
+                              static_cast<size_t>(tile) * 128 + j0) = make_uint4(o[0], o[1], o[2], o[3]);
+    return;
+  }
+  // kQKV: the tile is two heads of one segment (q, k or v); eight threads
+  // share a (row, head), each holding dims j0..j0+7 and their RoPE partners
+  // j0+64..j0+71
+  const int rr = t / 16, hh = (t / 8) % 2, sub = t % 8;
+  const int row = r0 + rr;
+  const int col0 = tile * kBN + hh * kHeadDim;  // first column of this head in q|k|v
+  const int qcols = p.Hq * kHeadDim, kcols = p.Hkv * kHeadDim;
+  const int seg = col0 < qcols ? 0 : (col0 < qcols + kcols ? 1 : 2);
+  const int head = seg == 0 ? col0 / kHeadDim
+                            : (seg == 1 ? (col0 - qcols) / kHeadDim : (col0 - qcols - kcols) / kHeadDim);
+  const float r = (p.rscale && row < p.M) ? p.rscale[row] : 1.f;
+  const int j0 = sub * 8;
+  float a[8], b[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    a[e] = s_sum[rr * kBN + hh * kHeadDim + j0 + e] * r;
+    b[e] = s_sum[rr * kBN + hh * kHeadDim + 64 + j0 + e] * r;
+  }
+  const float* gnorm = seg == 0 ? p.q_norm : (seg == 1 ? p.k_norm : nullptr);
+  if (gnorm) {  // per-head RMSNorm over the 128 dims (8 threads, consecutive lanes)
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += a[e] * a[e] + b[e] * b[e];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    const float inv = rsqrtf(ss / kHeadDim + p.eps);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      a[e] *= inv * gnorm[j0 + e];
+      b[e] *= inv * gnorm[64 + j0 + e];
+    }
+  }
+  if (row >= p.M) return;
+  if (seg > 0 && (T < 0 || T + row >= p.t_cap)) {  // the rows' K/V slots must exist
+    report(GLANCE_DEV_TREE_CAPACITY);
+    return;
+  }
+  if (seg < 2) {  // rotate-half RoPE: (a, b) -> (a cos - b sin, b cos + a sin)
+    const float pos = static_cast<float>(p.pos[row]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = j0 + e;
+      const float inv_freq = exp2f(-(2.f * j / kHeadDim) * p.log2_theta);
+      float sn, cs;
+      sincosf(pos * inv_freq, &sn, &cs);
+      const float x = a[e], y = b[e];
+      a[e] = x * cs - y * sn;
+      b[e] = y * cs + x * sn;
+    }
+  }
+  __nv_bfloat16* dst;
+  if (seg == 0) {
+    dst = p.q_out + (static_cast<size_t>(row) * p.Hq + head) * kHeadDim;
+  } else {
+    __nv_bfloat16* base = seg == 1 ? p.k_cache : p.v_cache;
+    dst = base + head * p.head_stride + static_cast<long long>(T + row) * p.row_stride;
+  }
+  uint32_t oa[4], ob[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    oa[e] = pack_bf16x2(a[2 * e], a[2 * e + 1]);
+    ob[e] = pack_bf16x2(b[2 * e], b[2 * e + 1]);
+  }
+  *reinterpret_cast<uint4*>(dst + j0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  *reinterpret_cast<uint4*>(dst + 64 + j0) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dense_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                 const __grid_constant__ CUtensorMap map_b1, const DenseParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kStages * kABytes;
+  Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kBBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = p.n_tiles * p.n_split;
+  const int my_units = (units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+  // K range (in k blocks) of split s
+  auto kb_range = [&](int s, int& kb0, int& kb1) {
+    kb0 = static_cast<int>((static_cast<long long>(p.n_kb) * s) / p.n_split);
+    kb1 = static_cast<int>((static_cast<long long>(p.n_kb) * (s + 1)) / p.n_split);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 128);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  // rows a_rows..127 of every A stage stay zero (TMA only writes a_rows rows)
+  if (p.a_rows < kBM) {
+    for (int s = 0; s < kStages; ++s) {
+      uint4* dst = reinterpret_cast<uint4*>(sA + s * kABytes + p.a_rows * 128);
+      for (int i = threadIdx.x; i < (kBM - p.a_rows) * 8; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  // ------------------------------------------------------------ phase 1
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&map_a);
+      tma_prefetch_desc(&map_b0);
+      tma_prefetch_desc(&map_b1);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBK * 2;
+      int it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < my_units; ++i) {
+        const int u = blockIdx.x + i * gridDim.x;
+        const int tile = u / p.n_split, s = u % p.n_split;
+        int kb0, kb1;
+        kb_range(s, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int st = it % kStages;
+          if (it >= kStages && !wait_or_abort(&bars->empty[st], ((it / kStages) - 1) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[st], a_bytes + kBBytes);
+          tma_load_2d(sA + st * kABytes, &map_a, &bars->full[st], kb * kBK, 0, pol_x);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            unsigned char* dstb = sB + st * kBBytes + q * kWBoxBytes;
+            if (p.mode == kSwiGLU)  // gate columns 128 t.., then up columns 128 t..
+              tma_load_2d(dstb, q < 2 ? &map_b0 : &map_b1, &bars->full[st], tile * 128 + 64 * (q & 1),
+                          kb * kBK, pol_w);
+            else
+              tma_load_2d(dstb, &map_b0, &bars->full[st], tile * kBN + 64 * q, kb * kBK, pol_w);
+          }
+        }
+      }
+      if (!ok) {
+        fail_pipeline(bars);
+        for (int j = it > kStages ? it - kStages : 0; j < it; ++j)
+          (void)mbar_wait(&bars->full[j % kStages], (j / kStages) & 1, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, true);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      int it = 0, total_it = 0;
+      for (int i = 0; i < my_units; ++i) {
+        int kb0, kb1;
+        kb_range((blockIdx.x + i * gridDim.x) % p.n_split, kb0, kb1);
+        total_it += kb1 - kb0;
+      }
+      bool ok = true;
+      for (int i = 0; ok && i < my_units; ++i) {
+        const int u = blockIdx.x + i * gridDim.x;
+        int kb0, kb1;
+        kb_range(u % p.n_split, kb0, kb1);
+        const int buf = i & 1;
+        if (i >= 2 && !wait_or_abort(&bars->acc_empty[buf], ((i >> 1) - 1) & 1, bars)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * kBN;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int st = it % kStages;
+          if (!wait_or_abort(&bars->full[st], (it / kStages) & 1, bars)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = a0 + st * kABytes, b_addr = b0 + st * kBBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                        sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
+                        (kb > kb0 || k > 0) ? 1u : 0u);
+          if (it + kStages < total_it) mma_commit(&bars->empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full[buf]);
+      }
+      if (!ok) fail_pipeline(bars);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp - 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < my_units; ++i) {
+      const int u = blockIdx.x + i * gridDim.x;
+      const int buf = i & 1;
+      if (!wait_or_abort(&bars->acc_full[buf], (i >> 1) & 1, bars)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float4* dst = reinterpret_cast<float4*>(p.part + (static_cast<size_t>(u) * p.a_rows + row) * kBN);
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + buf * kBN + lane_off + c * 32, r);
+        tmem_ld_wait();
+        if (row < p.M) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[c * 8 + v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[buf]);
+    }
+    if (!ok) fail_pipeline(bars);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+
+  // ------------------------------------------------------------ grid barrier
+  // every unit's partial is written (all CTAs are resident: cooperative launch)
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    atom_add_release_gpu(&p.barrier[0], 1u);
+    const uint64_t t0 = globaltimer_ns();
+    bool done = false;
+    for (uint32_t i = 0;; ++i) {
+      if (ld_acquire_gpu(&p.barrier[0]) >= gridDim.x) {
+        done = true;
+        break;
+      }
+      if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
+    }
+    if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
+    s_ok = done ? 1 : 0;
+    // the last CTA to leave resets both counters for the next call
+    if (atomicAdd(&p.barrier[1], 1u) == gridDim.x - 1) {
+      p.barrier[0] = 0u;
+      p.barrier[1] = 0u;
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;
+
+  // ------------------------------------------------------------ phase 2
+  float* s_sum = reinterpret_cast<float*>(smem);  // [16][256], the stage area is free now
+  const int T = p.mode == kQKV ? *p.t_len : 0;
+  const int row_blocks = (p.M + kItemRows - 1) / kItemRows;
+  const int items = p.n_tiles * row_blocks;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int tile = it / row_blocks, r0 = (it % row_blocks) * kItemRows;
+    {
+      // thread: one row, 16 columns; sum over the splits
+      const int rr = threadIdx.x / 16, c0 = (threadIdx.x % 16) * 16;
+      const int row = r0 + rr;
+      float acc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+      if (row < p.M) {
+        for (int s = 0; s < p.n_split; ++s) {
+          const float4* src = reinterpret_cast<const float4*>(
+              p.part + (static_cast<size_t>(tile * p.n_split + s) * p.a_rows + row) * kBN + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float4 x = __ldcg(src + v);
+            acc[4 * v] += x.x;
+            acc[4 * v + 1] += x.y;
+            acc[4 * v + 2] += x.z;
+            acc[4 * v + 3] += x.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s_sum[rr * kBN + c0 + e] = acc[e];
+    }
+    __syncthreads();
+    epilogue_item(p, s_sum, tile, r0, T);
+    __syncthreads();
+  }
+}
+
+// 1 / sqrt(mean(x^2) + eps) per row; one warp per row.
+__global__ void rms_scale_kernel(const __nv_bfloat16* x, int M, int d, float eps, float* r) {
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const __nv_bfloat16* xr = x + static_cast<size_t>(row) * d;
+  float s = 0.f;
+  for (int c = lane * 8; c < d; c += 32 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      s += lo * lo + hi * hi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) r[row] = rsqrtf(s / d + eps);
+}
+
+// Splits per tile so that units = tiles x splits fill about one wave of SMs.
+int choose_split(int n_tiles, int n_kb) {
+  const int sms = glance::num_sms();
+  int s = sms / n_tiles;
+  if (s < 1) s = 1;
+  if (s > n_kb) s = n_kb;
+  return s;
+}
+
+size_t ws_bytes(int M, int K, int n_cols_tiles) {
+  const int n_kb = K / kBK;
+  const int S = choose_split(n_cols_tiles, n_kb);
+  const int a_rows = (M + 7) / 8 * 8;
+  return 256 + static_cast<size_t>(n_cols_tiles) * S * a_rows * kBN * sizeof(float);
+}
+
+glance_status run_dense(const char* who, const void* x, int M, int K, const void* W0, const void* W1,
+                        int w_cols, int n_tiles, DenseParams p, void* workspace,
+                        size_t workspace_bytes, cudaStream_t s) {
+  using glance::fail;
+  if (M < 1 || M > kBM) return fail(GLANCE_ERR_UNSUPPORTED, "%s: need 1 <= M <= 128", who);
+  if (K < kBK || K % kBK) return fail(GLANCE_ERR_UNSUPPORTED, "%s: K must be a multiple of 64", who);
+  if (!glance::aligned16(x) || !glance::aligned16(W0) || !glance::aligned16(W1))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: x and W must be 16-byte aligned", who);
+  const size_t need = ws_bytes(M, K, n_tiles);
+  if (!workspace || workspace_bytes < need)
+    return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(dense_kernel), static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  const int a_rows = (M + 7) / 8 * 8;
+  CUtensorMap ma, mb0, mb1;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2ull};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(a_rows)};
+    glance_status st = glance::make_map_bf16(&ma, x, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(w_cols), static_cast<uint64_t>(K)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(w_cols) * 2ull};
+    const uint32_t box[2] = {64, kBK};
+    glance_status st = glance::make_map_bf16(&mb0, W0, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+    st = glance::make_map_bf16(&mb1, W1, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, who);
+    if (st != GLANCE_OK) return st;
+  }
+  p.M = M;
+  p.K = K;
+  p.n_tiles = n_tiles;
+  p.n_kb = K / kBK;
+  p.n_split = choose_split(n_tiles, p.n_kb);
+  p.a_rows = a_rows;
+  char* ws = static_cast<char*>(workspace);
+  p.barrier = reinterpret_cast<uint32_t*>(ws);
+  p.part = reinterpret_cast<float*>(ws + 256);
+  const int units = n_tiles * p.n_split;
+  int grid = glance::num_sms();
+  if (grid > units) grid = units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  // phase 2 waits for every CTA's phase 1: all CTAs must be resident
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, dense_kernel, ma, mb0, mb1, p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
+
+DenseParams blank_params() {
+  DenseParams p;
+  memset(&p, 0, sizeof(p));
+  return p;
+}
+
+}  // namespace
+
+extern "C" size_t glance_dense_workspace_bytes(int M, int K, int N) {
+  if (M < 1 || M > kBM || K < kBK || K % kBK || N < kBN || N % 128) return 0;
+  // the gate/up projection tiles N = 2 * intermediate in 256-column tiles too
+  return ws_bytes(M, K, (N + kBN - 1) / kBN);
+}
+
+extern "C" glance_status glance_rms_scale(const void* x, int M, int d, float eps, float* r_out,
+                                          void* stream) {
+  using glance::fail;
+  if (!x || !r_out) return fail(GLANCE_ERR_INVALID_ARG, "glance_rms_scale: null pointer argument");
+  if (M < 1 || d < 8 || d % 8 || !glance::aligned16(x))
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_rms_scale: need M >= 1, d % 8 == 0, 16-byte aligned x");
+  rms_scale_kernel<<<(M + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), M, d, eps, r_out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_rms_scale");
+  return GLANCE_OK;
+}
+
+extern "C" glance_status glance_dense_residual(const void* x, const void* W, int M, int K, int N,
+                                               const void* residual, void* out, void* workspace,
+                                               size_t workspace_bytes, void* stream) {
+  using glance::fail;
+  const char* who = "glance_dense_residual";
+  if (!x || !W || !residual || !out) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (N < kBN || N % kBN) return fail(GLANCE_ERR_UNSUPPORTED, "%s: N must be a multiple of 256", who);
+  if (!glance::aligned16(residual) || !glance::aligned16(out))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: residual and out must be 16-byte aligned", who);
+  DenseParams p = blank_params();
+  p.mode = kResid;
+  p.res = static_cast<const __nv_bfloat16*>(residual);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.n_out = N;
+  return run_dense(who, x, M, K, W, W, N, N / kBN, p, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" glance_status glance_dense_swiglu(const void* h, const void* W_gate, const void* W_up,
+                                             int M, int d, int inter, const float* rscale,
+                                             void* act, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  using glance::fail;
+  const char* who = "glance_dense_swiglu";
+  if (!h || !W_gate || !W_up || !act) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (inter < 128 || inter % 128) return fail(GLANCE_ERR_UNSUPPORTED, "%s: inter must be a multiple of 128", who);
+  if (!glance::aligned16(act)) return fail(GLANCE_ERR_INVALID_ARG, "%s: act must be 16-byte aligned", who);
+  DenseParams p = blank_params();
+  p.mode = kSwiGLU;
+  p.rscale = rscale;
+  p.act = static_cast<__nv_bfloat16*>(act);
+  p.inter = inter;
+  return run_dense(who, h, M, d, W_gate, W_up, inter, inter / 128, p, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int M, int d, int n_q_heads,
+                                          const float* rscale, const float* q_norm, const float* k_norm,
+                                          float eps, const int32_t* pos_id, float rope_theta,
+                                          void* q_out, const glance_kv* kv, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  using glance::fail;
+  const char* who = "glance_dense_qkv";
+  if (!h || !W_qkv || !pos_id || !q_out || !kv || !kv->k || !kv->v || !kv->t_len)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (kv->dtype != GLANCE_BF16 || kv->head_dim != kHeadDim)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: bf16 cache with head_dim 128 only", who);
+  const int Hkv = kv->n_kv_heads;
+  if (n_q_heads < 2 || n_q_heads % 2 || Hkv < 2 || Hkv % 2 || n_q_heads % Hkv)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: need even head counts with n_q_heads %% n_kv_heads == 0", who);
+  if (!(rope_theta > 1.f)) return fail(GLANCE_ERR_INVALID_ARG, "%s: rope_theta must be > 1", who);
+  if (!glance::aligned16(q_out) || !glance::aligned16(kv->k) || !glance::aligned16(kv->v) ||
+      kv->row_stride < kHeadDim || (kv->row_stride * 2) % 16 || (kv->head_stride * 2) % 16 ||
+      kv->head_stride < static_cast<int64_t>(kv->t_cap) * kv->row_stride || kv->t_cap < M)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: bad q_out / cache layout", who);
+  DenseParams p = blank_params();
+  p.mode = kQKV;
+  p.rscale = rscale;
+  p.Hq = n_q_heads;
+  p.Hkv = Hkv;
+  p.q_norm = q_norm;
+  p.k_norm = k_norm;
+  p.eps = eps;
+  p.pos = pos_id;
+  p.log2_theta = log2f(rope_theta);
+  p.q_out = static_cast<__nv_bfloat16*>(q_out);
+  p.k_cache = static_cast<__nv_bfloat16*>(kv->k);
+  p.v_cache = static_cast<__nv_bfloat16*>(kv->v);
+  p.head_stride = kv->head_stride;
+  p.row_stride = kv->row_stride;
+  p.t_len = kv->t_len;
+  p.t_cap = kv->t_cap;
+  const int cols = (n_q_heads + 2 * Hkv) * kHeadDim;
+  return run_dense(who, h, M, d, W_qkv, W_qkv, cols, cols / kBN, p, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
