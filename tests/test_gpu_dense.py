@@ -1,8 +1,9 @@
 """Dense verify layers on the GPU vs the oracle (fp64 on the same bf16
 inputs): RMSNorm row scales within 1e-5 relative; projections, SwiGLU,
 q/k with RoPE and the cache rows within 2e-2 * max(1, |ref|); the whole
-layer (with tree attention between) against the oracle's steps with the
-intermediates the library keeps in bf16 rounded there too; cache slots outside the rows'
+layer (with tree attention between) call by call on each call's own bf16
+inputs, and end to end against the fp64 oracle layer within 6e-2 (the bf16
+stores between the calls); cache slots outside the rows'
 untouched."""
 import numpy as np
 import pytest
@@ -11,8 +12,8 @@ import torch
 import workloads as W
 from _util import bf16_tensor
 from oracle.attention import tree_attention as o_attn
-from oracle.bf16 import bf16_bits_to_f64, f32_to_bf16_bits
-from oracle.dense import qkv as o_qkv, residual as o_residual, rms_scale as o_rms
+from oracle.bf16 import bf16_bits_to_f64
+from oracle.dense import dense_layer, qkv as o_qkv, residual as o_residual, rms_scale as o_rms
 from oracle.dense import swiglu as o_swiglu
 from test_gpu_attention import random_tree, upload_tree
 
@@ -23,11 +24,6 @@ def close(got, want):
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - want) / np.maximum(1.0, np.abs(want))
     assert err.max() < 2e-2, err.max()
-
-
-def rb16(a):
-    """a rounded to bf16, as the library stores it."""
-    return bf16_bits_to_f64(f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
 
 
 def f64(t):
@@ -44,8 +40,10 @@ def test_rms_scale(dev, clean_status, M, d):
     assert np.all(np.abs(r.cpu().numpy() - want) <= 1e-5 * want)
 
 
-@pytest.mark.parametrize("M,K,N", [(64, 4096, 4096), (17, 12288, 4096), (128, 512, 768), (1, 64, 256)])
+@pytest.mark.parametrize("M,K,N", [(64, 4096, 4096), (17, 12288, 4096), (64, 12288, 4096), (128, 512, 768),
+                                   (1, 64, 256), (8, 128, 40960)])
 def test_residual_projection(dev, clean_status, M, K, N):
+    # (1, 64, 256): one CTA; (8, 128, 40960): 160 tiles, more clusters than fit at once
     import tree_verified_block_gb300 as g
     gen = W.rng(M, K, N)
     xb = W.normal_bf16(gen, (M, K))
@@ -53,14 +51,16 @@ def test_residual_projection(dev, clean_status, M, K, N):
     rb = W.normal_bf16(gen, (M, N))
     res = bf16_tensor(rb, dev)
     out = torch.full_like(res, float("nan"))
-    ws = g.workspace(g.dense_workspace_bytes(M, K, N), dev)
-    for _ in range(2):  # the grid barrier's counters are reusable
-        g.dense_residual(bf16_tensor(xb, dev), bf16_tensor(Wb, dev), res, out, ws)
-    close(f64(out), o_residual(bf16_bits_to_f64(rb), bf16_bits_to_f64(xb), bf16_bits_to_f64(Wb)))
-    assert int(ws[:256].sum().item()) == 0
+    x, Wt = bf16_tensor(xb, dev), bf16_tensor(Wb, dev)
+    want = o_residual(bf16_bits_to_f64(rb), bf16_bits_to_f64(xb), bf16_bits_to_f64(Wb))
+    g.dense_residual(x, Wt, res, out)
+    close(f64(out), want)
+    g.dense_residual(x, Wt, res, res)  # in place: out aliases the residual
+    close(f64(res), want)
+    assert np.array_equal(res.view(torch.int16).cpu().numpy(), out.view(torch.int16).cpu().numpy())
 
 
-@pytest.mark.parametrize("M,d,inter", [(64, 4096, 12288), (5, 256, 384)])
+@pytest.mark.parametrize("M,d,inter", [(64, 4096, 12288), (5, 256, 384), (128, 1024, 256)])
 def test_swiglu(dev, clean_status, M, d, inter):
     import tree_verified_block_gb300 as g
     gen = W.rng(M, d, inter)
@@ -68,21 +68,18 @@ def test_swiglu(dev, clean_status, M, d, inter):
     Gb = W.normal_bf16(gen, (d, inter), std=0.02)
     Ub = W.normal_bf16(gen, (d, inter), std=0.02)
     h = bf16_tensor(hb, dev)
-    r = torch.empty(M, dtype=torch.float32, device=dev)
-    g.rms_scale(h, 1e-6, r)
     act = torch.full((M, inter), float("nan"), dtype=torch.bfloat16, device=dev)
-    ws = g.workspace(g.dense_workspace_bytes(M, d, 2 * inter), dev)
-    g.dense_swiglu(h, bf16_tensor(Gb, dev), bf16_tensor(Ub, dev), r, act, ws)
+    g.dense_swiglu(h, bf16_tensor(Gb, dev), bf16_tensor(Ub, dev), True, 1e-6, act)
     want = o_swiglu(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Gb), bf16_bits_to_f64(Ub), 1e-6)
     close(f64(act), want)
 
 
-@pytest.mark.parametrize("qk_norm", [False, True])
-def test_qkv_rope_into_cache(dev, clean_status, qk_norm):
+@pytest.mark.parametrize("qk_norm,norm_input", [(False, True), (True, True), (False, False)])
+def test_qkv_rope_into_cache(dev, clean_status, qk_norm, norm_input):
     import tree_verified_block_gb300 as g
     M, d, Hq, Hkv, D, T = 64, 4096, 32, 8, 128, 3000
     t_cap = T + M + 16
-    gen = W.rng(77, int(qk_norm))
+    gen = W.rng(77, int(qk_norm), int(norm_input))
     hb = W.normal_bf16(gen, (M, d))
     Wb = W.normal_bf16(gen, (d, (Hq + 2 * Hkv) * D), std=0.02)
     qn = gen.uniform(0.5, 1.5, size=D).astype(np.float32) if qk_norm else None
@@ -93,16 +90,16 @@ def test_qkv_rope_into_cache(dev, clean_status, qk_norm):
     t_len = torch.tensor([T], dtype=torch.int32, device=dev)
     kv = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(vb, dev), t_len)
     h = bf16_tensor(hb, dev)
-    r = torch.empty(M, dtype=torch.float32, device=dev)
-    g.rms_scale(h, 1e-6, r)
     q = torch.full((M, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
-    ws = g.workspace(g.dense_workspace_bytes(M, d, (Hq + 2 * Hkv) * D), dev)
     tt = lambda a: None if a is None else torch.from_numpy(a).to(dev)
-    g.dense_qkv(h, bf16_tensor(Wb, dev), Hq, r, tt(qn), tt(kn), 1e-6, torch.from_numpy(pos).to(dev),
-                1e6, q, kv, ws)
+    g.dense_qkv(h, bf16_tensor(Wb, dev), Hq, norm_input, tt(qn), tt(kn), 1e-6, torch.from_numpy(pos).to(dev),
+                1e6, q, kv)
     wq, wk, wv = o_qkv(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Wb), Hq, Hkv, D, pos, 1e6, 1e-6,
                        None if qn is None else qn.astype(np.float64),
                        None if kn is None else kn.astype(np.float64))
+    if not norm_input:  # RoPE is linear: without the row norm every output is 1 / r times larger
+        r = o_rms(bf16_bits_to_f64(hb), 1e-6)[:, None, None]
+        wq, wk, wv = wq / r, wk / r, wv / r
     close(f64(q), wq)
     K = f64(kv.k)
     V = f64(kv.v)
@@ -136,36 +133,40 @@ def test_full_layer_with_tree_attention(dev, clean_status):
     kv = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(vb, dev), t_len)
     tree = upload_tree(ref, 15, dev)
     x = bf16_tensor(xb, dev)
-    r = torch.empty(M, dtype=torch.float32, device=dev)
     q = torch.empty((M, Hq, D), dtype=torch.bfloat16, device=dev)
     att = torch.empty_like(q)
     x1 = torch.empty_like(x)
     act = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
     out = torch.empty_like(x)
-    ws = g.workspace(max(g.dense_workspace_bytes(M, d, 2 * I), g.dense_workspace_bytes(M, I, d),
-                         g.dense_workspace_bytes(M, d, (Hq + 2 * Hkv) * D)), dev)
     ws_a = g.workspace(g.tree_attention_workspace_bytes(M, Hq, kv), dev)
-    g.rms_scale(x, 1e-6, r)
-    g.dense_qkv(x, bf16_tensor(Wqkv, dev), Hq, r, torch.from_numpy(qn).to(dev), torch.from_numpy(kn).to(dev),
-                1e-6, torch.from_numpy(pos).to(dev), 1e6, q, kv, ws)
+    g.dense_qkv(x, bf16_tensor(Wqkv, dev), Hq, True, torch.from_numpy(qn).to(dev), torch.from_numpy(kn).to(dev),
+                1e-6, torch.from_numpy(pos).to(dev), 1e6, q, kv)
     g.tree_attention(q, kv, tree, D ** -0.5, att, ws_a)
-    g.dense_residual(att.view(M, Hq * D), bf16_tensor(Wo, dev), x, x1, ws)
-    g.rms_scale(x1, 1e-6, r)
-    g.dense_swiglu(x1, bf16_tensor(Wg, dev), bf16_tensor(Wu, dev), r, act, ws)
-    g.dense_residual(act, bf16_tensor(Wd, dev), x1, out, ws)
-    # the oracle's steps on the same bf16 inputs, each intermediate the library
-    # stores as bf16 between calls (q, the cache rows, att, x1, act) rounded
-    # there too; fp64 inside every step
+    g.dense_residual(att.view(M, Hq * D), bf16_tensor(Wo, dev), x, x1)
+    g.dense_swiglu(x1, bf16_tensor(Wg, dev), bf16_tensor(Wu, dev), True, 1e-6, act)
+    g.dense_residual(act, bf16_tensor(Wd, dev), x1, out)
+    # every call against the oracle's step on that call's own bf16 inputs (the
+    # previous call's stored output); fp64 inside every step
     Kc, Vc = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
     x0 = bf16_bits_to_f64(xb)
     wq, wk, wv = o_qkv(x0, None, bf16_bits_to_f64(Wqkv), Hq, Hkv, D, pos, 1e6, 1e-6,
                        qn.astype(np.float64), kn.astype(np.float64))
-    Kc[:, T:T + M] = rb16(wk.transpose(1, 0, 2))
-    Vc[:, T:T + M] = rb16(wv.transpose(1, 0, 2))
-    watt = rb16(o_attn(rb16(wq), Kc[:, :T + M], Vc[:, :T + M], T, ref["anc"], D ** -0.5))
-    close(f64(att), watt)
-    wx1 = rb16(o_residual(x0, watt.reshape(M, Hq * D), bf16_bits_to_f64(Wo)))
-    close(f64(x1), wx1)
-    wact = rb16(o_swiglu(wx1, None, bf16_bits_to_f64(Wg), bf16_bits_to_f64(Wu), 1e-6))
-    close(f64(act), wact)
-    close(f64(out), o_residual(wx1, wact, bf16_bits_to_f64(Wd)))
+    close(f64(q), wq)
+    K, V = f64(kv.k), f64(kv.v)
+    close(K[:, T:T + M], wk.transpose(1, 0, 2))
+    close(V[:, T:T + M], wv.transpose(1, 0, 2))
+    close(f64(att), o_attn(f64(q), K[:, :T + M], V[:, :T + M], T, ref["anc"], D ** -0.5))
+    close(f64(x1), o_residual(x0, f64(att).reshape(M, Hq * D), bf16_bits_to_f64(Wo)))
+    close(f64(act), o_swiglu(f64(x1), None, bf16_bits_to_f64(Wg), bf16_bits_to_f64(Wu), 1e-6))
+    close(f64(out), o_residual(f64(x1), f64(act), bf16_bits_to_f64(Wd)))
+    # and the whole layer against the fp64 oracle layer: the five bf16 stores
+    # between the calls (q, K/V rows, att, x1, act; each within 2^-9 relative)
+    # move the 12288-term down projection by up to a few 1e-2 at the tails
+    lw = dict(W_qkv=bf16_bits_to_f64(Wqkv), W_o=bf16_bits_to_f64(Wo), W_gate=bf16_bits_to_f64(Wg),
+              W_up=bf16_bits_to_f64(Wu), W_down=bf16_bits_to_f64(Wd), q_norm=qn.astype(np.float64),
+              k_norm=kn.astype(np.float64))
+    want = dense_layer(x0, lw, pos, T, bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), ref["anc"], Hq, Hkv, D,
+                       1e6, 1e-6)
+    got = f64(out)
+    err = np.abs(got - want) / np.maximum(1.0, np.abs(want))
+    assert err.max() < 6e-2 and err.mean() < 5e-3, (err.max(), err.mean())

@@ -28,7 +28,7 @@ EXPORTS = [
     "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
     "glance_lmhead_argmax_entropy", "glance_lmhead_sample", "glance_accept_commit_gated",
     "glance_build_tree_shared_workspace_bytes", "glance_build_tree_shared",
-    "glance_dense_workspace_bytes", "glance_rms_scale", "glance_dense_qkv",
+    "glance_rms_scale", "glance_dense_qkv",
     "glance_dense_residual", "glance_dense_swiglu",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
@@ -113,16 +113,14 @@ def lib():
                                            ctypes.c_float, ctypes.c_float, ctypes.POINTER(TreeC),
                                            vp, vp, sz, vp]
     L.glance_build_tree_shared.restype = st
-    L.glance_dense_workspace_bytes.argtypes = [i32, i32, i32]
-    L.glance_dense_workspace_bytes.restype = sz
     L.glance_rms_scale.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
     L.glance_rms_scale.restype = st
-    L.glance_dense_qkv.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp,
-                                   ctypes.c_float, vp, ctypes.POINTER(KVC), vp, sz, vp]
+    L.glance_dense_qkv.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_float, vp,
+                                   ctypes.c_float, vp, vp, vp]
     L.glance_dense_qkv.restype = st
-    L.glance_dense_residual.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.glance_dense_residual.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     L.glance_dense_residual.restype = st
-    L.glance_dense_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.glance_dense_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp]
     L.glance_dense_swiglu.restype = st
     L.glance_lmhead_sample.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint64,
                                        vp, vp, vp, vp, vp, sz, vp]
@@ -388,40 +386,37 @@ def accept_commit_gated_batched(trees, argmax, gap, threshold, layers, n_accepte
 
 # -------------------------------------------------------------- dense layers
 
-def dense_workspace_bytes(M, K, N):
-    return lib().glance_dense_workspace_bytes(M, K, N)
-
-
 def rms_scale(x, eps, r_out, stream=None):
     M, d = x.shape
     assert x.is_contiguous()
     _check(lib().glance_rms_scale(_ptr(x), M, d, float(eps), _ptr(r_out), _stream(stream, x.device)))
 
 
-def dense_qkv(h, W_qkv, n_q_heads, rscale, q_norm, k_norm, eps, pos_id, rope_theta, q_out, kv, ws,
+def dense_qkv(h, W_qkv, n_q_heads, norm_input, q_norm, k_norm, eps, pos_id, rope_theta, q_out, kv,
               stream=None):
     M, d = h.shape
     assert h.is_contiguous() and W_qkv.is_contiguous() and q_out.is_contiguous()
-    _check(lib().glance_dense_qkv(_ptr(h), _ptr(W_qkv), M, d, n_q_heads, _ptr(rscale),
+    _check(lib().glance_dense_qkv(_ptr(h), _ptr(W_qkv), M, d, n_q_heads, int(bool(norm_input)),
                                   _ptr(q_norm), _ptr(k_norm), float(eps), _ptr(pos_id),
-                                  float(rope_theta), _ptr(q_out), ctypes.byref(kv.c), _ptr(ws),
-                                  ws.numel(), _stream(stream, h.device)))
+                                  float(rope_theta), _ptr(q_out), ctypes.byref(kv.c),
+                                  _stream(stream, h.device)))
 
 
-def dense_residual(x, W, residual, out, ws, stream=None):
+def dense_residual(x, W, residual, out, stream=None):
     M, K = x.shape
     N = W.shape[1]
     assert x.is_contiguous() and W.is_contiguous() and residual.is_contiguous() and out.is_contiguous()
     _check(lib().glance_dense_residual(_ptr(x), _ptr(W), M, K, N, _ptr(residual), _ptr(out),
-                                       _ptr(ws), ws.numel(), _stream(stream, x.device)))
+                                       _stream(stream, x.device)))
 
 
-def dense_swiglu(h, W_gate, W_up, rscale, act, ws, stream=None):
+def dense_swiglu(h, W_gate, W_up, norm_input, eps, act, stream=None):
     M, d = h.shape
     inter = W_gate.shape[1]
     assert h.is_contiguous() and W_gate.is_contiguous() and W_up.is_contiguous() and act.is_contiguous()
-    _check(lib().glance_dense_swiglu(_ptr(h), _ptr(W_gate), _ptr(W_up), M, d, inter, _ptr(rscale),
-                                     _ptr(act), _ptr(ws), ws.numel(), _stream(stream, h.device)))
+    _check(lib().glance_dense_swiglu(_ptr(h), _ptr(W_gate), _ptr(W_up), M, d, inter,
+                                     int(bool(norm_input)), float(eps), _ptr(act),
+                                     _stream(stream, h.device)))
 
 
 def device_status():

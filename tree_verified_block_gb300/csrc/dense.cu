@@ -12,18 +12,22 @@
 //   -> RMSNorm -> SiLU(. W_gate) * (. W_up) -> x' + . W_down.
 // An RMSNorm's weight is folded into the next projection's rows by the
 // caller; its 1 / rms row scale, which a projection is linear in, is applied
-// to the product (glance_rms_scale computes it).
+// to the product, from row sums of squares taken on the input tiles as they
+// stream through shared memory.
 //
 // GEMM shape: Y[M x N] = X[M x K] W[K x N], W row-major with N contiguous
 // (the MN-major B operand), bf16 in, fp32 accumulate. At M <= 128 the weights
-// dominate (HBM-bound), and N / 256 output tiles are too few to occupy the
-// SMs, so K is split: unit (tile, split) accumulates its K range in tensor
-// memory and writes an fp32 partial (phase 1); after a grid barrier
-// (cooperative launch) every CTA sums the splits of a share of (tile, 16-row)
-// items and applies the epilogue (phase 2). Phase 1 is the LM head's pipeline:
-// warp 0 streams X and W stages with TMA (4 x 48 KB), warp 1 issues
-// M=128 x N=256 x K=16 MMAs into one of two TMEM accumulators, warps 4..7
-// drain the other one to the partial buffer.
+// dominate (HBM-bound) and N / 256 output tiles are too few to occupy the
+// SMs, so K is split S ways inside a thread-block cluster of S CTAs: CTA s of
+// the cluster of tile t accumulates K range s in tensor memory (warp 0 streams
+// X and W stages with TMA, 4 x 48 KB; warp 1 issues M=128 x N=256 x K=16 MMAs;
+// warps 4..7 take the input rows' sums of squares from the same stages). Once
+// the whole cluster is done with its stages, warps 4..7 send each row of the
+// fp32 partial to the CTA that owns the row (remote stores into its shared
+// memory); after a second cluster barrier each CTA sums the S partials of its
+// rows and applies the epilogue. No global workspace, no grid-wide barrier. Launches
+// are programmatic dependents of the previous kernel in the stream: the first
+// W stages (which do not depend on it) are in flight before the wait.
 #include <cstring>
 #include <mutex>
 
@@ -43,17 +47,21 @@ constexpr int kThreads = 256;
 constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB
 constexpr uint32_t kBBytes = kBK * kBN * 2;    // 32 KB
 constexpr uint32_t kWBoxBytes = kBK * 64 * 2;  // one 64 x 64 box of W: 8 KB
-constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256;
-constexpr int kItemRows = 16;                  // phase-2 item: 16 rows of a tile
+constexpr uint32_t kStageArea = kStages * (kABytes + kBBytes);
+constexpr int kPartStride = kBN + 4;           // floats per partial row in shared memory
+constexpr int kMaxSplit = 16;
+// received partials: [source rank][owned row][kPartStride], at most M + S - 1 rows
+constexpr uint32_t kRecvBytes = (kBM + kMaxSplit) * kPartStride * 4;
+constexpr int kChunkRows = 16;                 // epilogue: 16 rows at a time
+constexpr size_t kSmemBytes = 1024 + kStageArea + 2048;
 constexpr int kHeadDim = 128;
+static_assert(kRecvBytes + kChunkRows * kBN * 4 <= kStageArea, "partials overlay the stages");
 
 enum Mode : int { kResid = 0, kQKV = 1, kSwiGLU = 2 };
 
 struct DenseParams {
-  int M, K, n_tiles, n_split, n_kb, a_rows, mode;
-  float* part;              // [units][a_rows][256] fp32 partials
-  uint32_t* barrier;        // [2] grid barrier: arrivals, departures
-  const float* rscale;      // [M] 1 / rms of the input rows, or null
+  int M, K, n_kb, a_rows, mode, split, norm_input;
+  float eps;
   // kResid: out = res + X W, both [M][n_out]
   const __nv_bfloat16* res;
   __nv_bfloat16* out;
@@ -62,7 +70,6 @@ struct DenseParams {
   int Hq, Hkv;
   const float* q_norm;      // [128] or null
   const float* k_norm;      // [128] or null
-  float eps;
   const int32_t* pos;       // [M] position ids
   float log2_theta;
   __nv_bfloat16* q_out;     // [M][Hq][128]
@@ -79,10 +86,13 @@ struct DenseParams {
 struct __align__(8) Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full;
+  uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int failed;         // read by the cluster's other CTAs
+  float recv_ss[kBM + kMaxSplit];  // [source rank][owned row]: sums of squares of input rows
+  float r[kChunkRows];
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
@@ -102,21 +112,31 @@ __device__ __forceinline__ void fail_pipeline(Bars* bars) {
   atomicExch(&bars->abort_flag, 1);
 }
 
-// Phase-2 epilogue of one (tile, 16-row) item whose split sum sits in
-// s_sum[16][256] (fp32).
-__device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile, int r0, int T) {
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Epilogue of rows r0 .. min(r0 + 16, r_end) - 1 of one tile, whose summed
+// product sits in s_sum[16][256] (fp32); r (nullable) holds the rows' 1 / rms.
+__device__ void epilogue_rows(const DenseParams& p, const float* s_sum, const float* rs, int tile,
+                              int r0, int r_end, int T) {
   const int t = threadIdx.x;
   if (p.mode == kResid) {
     // thread: one row, 16 columns
     const int rr = t / 16, c0 = (t % 16) * 16;
     const int row = r0 + rr;
-    if (row >= p.M) return;
+    if (row >= r_end) return;
     const size_t at = static_cast<size_t>(row) * p.n_out + static_cast<size_t>(tile) * kBN + c0;
-    const uint4* rs = reinterpret_cast<const uint4*>(p.res + at);
+    const uint4* src = reinterpret_cast<const uint4*>(p.res + at);
     uint4* dst = reinterpret_cast<uint4*>(p.out + at);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint4 v = rs[h];
+      const uint4 v = src[h];
       const uint32_t rv[4] = {v.x, v.y, v.z, v.w};
       uint32_t o[4];
 #pragma unroll
@@ -133,8 +153,8 @@ __device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile
     // thread: one row, 8 of the tile's 128 (gate, up) column pairs
     const int rr = t / 16, j0 = (t % 16) * 8;
     const int row = r0 + rr;
-    if (row >= p.M) return;
-    const float r = p.rscale ? p.rscale[row] : 1.f;
+    if (row >= r_end) return;
+    const float r = rs ? rs[rr] : 1.f;
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -162,7 +182,7 @@ __device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile
   const int seg = col0 < qcols ? 0 : (col0 < qcols + kcols ? 1 : 2);
   const int head = seg == 0 ? col0 / kHeadDim
                             : (seg == 1 ? (col0 - qcols) / kHeadDim : (col0 - qcols - kcols) / kHeadDim);
-  const float r = (p.rscale && row < p.M) ? p.rscale[row] : 1.f;
+  const float r = rs ? rs[rr] : 1.f;
   const int j0 = sub * 8;
   float a[8], b[8];
 #pragma unroll
@@ -185,7 +205,7 @@ __device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile
       b[e] *= inv * gnorm[64 + j0 + e];
     }
   }
-  if (row >= p.M) return;
+  if (row >= r_end) return;
   if (seg > 0 && (T < 0 || T + row >= p.t_cap)) {  // the rows' K/V slots must exist
     report(GLANCE_DEV_TREE_CAPACITY);
     return;
@@ -220,6 +240,9 @@ __device__ void epilogue_item(const DenseParams& p, const float* s_sum, int tile
   *reinterpret_cast<uint4*>(dst + 64 + j0) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
+// Grid: one cluster of p.split CTAs per output tile (blockIdx.x = tile * S +
+// rank). Every wait is bounded; a CTA that gives up still takes part in both
+// cluster barriers, so its peers never wait on it forever.
 __global__ void __launch_bounds__(kThreads, 1)
     dense_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                  const __grid_constant__ CUtensorMap map_b1, const DenseParams p) {
@@ -228,32 +251,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* sA = smem;
   unsigned char* sB = smem + kStages * kABytes;
-  Bars* bars = reinterpret_cast<Bars*>(sB + kStages * kBBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kStageArea);
+  // after phase 1 the stage area receives the cluster's partials of this
+  // CTA's rows, then holds the chunk sums
+  float* s_recv = reinterpret_cast<float*>(smem);
+  float* s_sum = reinterpret_cast<float*>(smem + kRecvBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int units = p.n_tiles * p.n_split;
-  const int my_units = (units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                       static_cast<int>(gridDim.x);
-  // K range (in k blocks) of split s
-  auto kb_range = [&](int s, int& kb0, int& kb1) {
-    kb0 = static_cast<int>((static_cast<long long>(p.n_kb) * s) / p.n_split);
-    kb1 = static_cast<int>((static_cast<long long>(p.n_kb) * (s + 1)) / p.n_split);
-  };
+  const int S = p.split;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int kb0 = static_cast<int>((static_cast<long long>(p.n_kb) * rank) / S);
+  const int kb1 = static_cast<int>((static_cast<long long>(p.n_kb) * (rank + 1)) / S);
+  const int n_it = kb1 - kb0;  // >= 1: S <= n_kb
+  const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBK * 2;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->empty[s], p.norm_input ? 5 : 1);  // the MMA commit (+ warps 4..7)
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->acc_full[b], 1);
-      mbar_init(&bars->acc_empty[b], 128);
-    }
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
+    bars->failed = 0;
     fence_barrier_init();
   }
   if (warp == 2) {
-    tmem_alloc(&bars->tmem_base, 512);
+    tmem_alloc(&bars->tmem_base, kBN);
     tmem_relinquish();
   }
   // rows a_rows..127 of every A stage stay zero (TMA only writes a_rows rows)
@@ -263,48 +289,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = threadIdx.x; i < (kBM - p.a_rows) * 8; i += kThreads) dst[i] = make_uint4(0, 0, 0, 0);
     }
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  auto load_w = [&](int st, int kb, uint64_t pol) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      unsigned char* dstb = sB + st * kBBytes + q * kWBoxBytes;
+      if (p.mode == kSwiGLU)  // gate columns 128 t.., then up columns 128 t..
+        tma_load_2d(dstb, q < 2 ? &map_b0 : &map_b1, &bars->full[st], tile * 128 + 64 * (q & 1), kb * kBK,
+                    pol);
+      else
+        tma_load_2d(dstb, &map_b0, &bars->full[st], tile * kBN + 64 * q, kb * kBK, pol);
+    }
+  };
+  // W does not depend on the previous kernel: its first stages go out now
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b0);
+    tma_prefetch_desc(&map_b1);
+    const uint64_t pol_w = policy_evict_first();
+    for (int it = 0; it < kStages && it < n_it; ++it) {
+      mbar_arrive_expect_tx(&bars->full[it], a_bytes + kBBytes);
+      load_w(it, kb0 + it, pol_w);
+    }
+  }
+  pdl_wait_prior();
+
   // ------------------------------------------------------------ phase 1
+  bool ok = true;
+  float row_ss = 0.f;
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&map_a);
-      tma_prefetch_desc(&map_b0);
-      tma_prefetch_desc(&map_b1);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBK * 2;
       int it = 0;
-      bool ok = true;
-      for (int i = 0; ok && i < my_units; ++i) {
-        const int u = blockIdx.x + i * gridDim.x;
-        const int tile = u / p.n_split, s = u % p.n_split;
-        int kb0, kb1;
-        kb_range(s, kb0, kb1);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int st = it % kStages;
-          if (it >= kStages && !wait_or_abort(&bars->empty[st], ((it / kStages) - 1) & 1, bars)) {
+      for (; it < n_it; ++it) {
+        const int st = it % kStages, kb = kb0 + it;
+        if (it >= kStages) {
+          if (!wait_or_abort(&bars->empty[st], ((it / kStages) - 1) & 1, bars)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&bars->full[st], a_bytes + kBBytes);
-          tma_load_2d(sA + st * kABytes, &map_a, &bars->full[st], kb * kBK, 0, pol_x);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            unsigned char* dstb = sB + st * kBBytes + q * kWBoxBytes;
-            if (p.mode == kSwiGLU)  // gate columns 128 t.., then up columns 128 t..
-              tma_load_2d(dstb, q < 2 ? &map_b0 : &map_b1, &bars->full[st], tile * 128 + 64 * (q & 1),
-                          kb * kBK, pol_w);
-            else
-              tma_load_2d(dstb, &map_b0, &bars->full[st], tile * kBN + 64 * q, kb * kBK, pol_w);
-          }
+          load_w(st, kb, pol_w);
         }
+        tma_load_2d(sA + st * kABytes, &map_a, &bars->full[st], kb * kBK, 0, pol_x);
       }
-      if (!ok) {
+      if (!ok) {  // let the copies in flight land before the stage area is reused
         fail_pipeline(bars);
         for (int j = it > kStages ? it - kStages : 0; j < it; ++j)
           (void)mbar_wait(&bars->full[j % kStages], (j / kStages) & 1, 50000000ull);
@@ -314,128 +349,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, true);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      int it = 0, total_it = 0;
-      for (int i = 0; i < my_units; ++i) {
-        int kb0, kb1;
-        kb_range((blockIdx.x + i * gridDim.x) % p.n_split, kb0, kb1);
-        total_it += kb1 - kb0;
-      }
-      bool ok = true;
-      for (int i = 0; ok && i < my_units; ++i) {
-        const int u = blockIdx.x + i * gridDim.x;
-        int kb0, kb1;
-        kb_range(u % p.n_split, kb0, kb1);
-        const int buf = i & 1;
-        if (i >= 2 && !wait_or_abort(&bars->acc_empty[buf], ((i >> 1) - 1) & 1, bars)) {
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % kStages;
+        if (!wait_or_abort(&bars->full[st], (it / kStages) & 1, bars)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kBN;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int st = it % kStages;
-          if (!wait_or_abort(&bars->full[st], (it / kStages) & 1, bars)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = a0 + st * kABytes, b_addr = b0 + st * kBBytes;
+        const uint32_t a_addr = a0 + st * kABytes, b_addr = b0 + st * kBBytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                        sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024), idesc,
-                        (kb > kb0 || k > 0) ? 1u : 0u);
-          if (it + kStages < total_it) mma_commit(&bars->empty[st]);
-        }
-        if (!ok) break;
-        mma_commit(&bars->acc_full[buf]);
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_bf16_ss(tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 2048, kWBoxBytes, 1024),
+                      idesc, (it > 0 || k > 0) ? 1u : 0u);
+        if (it + kStages < n_it) mma_commit(&bars->empty[st]);
       }
-      if (!ok) fail_pipeline(bars);
+      if (ok) {
+        mma_commit(&bars->acc_full);
+      } else {  // the MMAs issued so far finish before the stage area is reused
+        mma_commit(&bars->drain);
+        (void)mbar_wait(&bars->drain, 0, 50000000ull);
+        fail_pipeline(bars);
+      }
     }
   } else if (warp >= 4) {
+    // one input row per thread: its sum of squares over this K range, from the
+    // A stages (the 128-byte swizzle permutes 16-byte chunks within a row only)
+    const int row = (warp - 4) * 32 + lane;
+    if (p.norm_input) {
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % kStages;
+        const bool got = wait_or_abort(&bars->full[st], (it / kStages) & 1, bars);
+        if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
+          ok = false;
+          break;
+        }
+        if (row < p.M) {
+          const uint4* src = reinterpret_cast<const uint4*>(sA + st * kABytes + row * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = src[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+              row_ss += lo * lo + hi * hi;
+            }
+          }
+        }
+        __syncwarp();  // one arrival per warp, once every lane has read the stage
+        if (lane == 0 && it + kStages < n_it) mbar_arrive(&bars->empty[st]);
+      }
+    }
+    if (ok && !wait_or_abort(&bars->acc_full, 0, bars)) ok = false;
+    if (!ok) fail_pipeline(bars);
+  }
+  // every role is done with its own stage area (or gave up and drained)
+  const bool bad = __syncthreads_or(!ok || *reinterpret_cast<volatile int*>(&bars->abort_flag)) != 0;
+  if (threadIdx.x == 0) bars->failed = bad ? 1 : 0;
+  __syncwarp();
+  cluster_sync_all();  // the whole cluster is done with its stage areas
+  bool peer_bad = false;
+  if (threadIdx.x < S) peer_bad = dsmem_ld_s32(dsmem_addr(&bars->failed, threadIdx.x)) != 0;
+  const bool any_bad = __syncthreads_or(peer_bad) != 0;
+
+  // rows are owned in blocks of rows_per: CTA o of the cluster sums and
+  // finishes rows o * rows_per .. ; each CTA sends its partial of every row
+  // to the row's owner (remote stores into the owner's stage area)
+  const int rows_per = (p.M + S - 1) / S;
+  if (!any_bad && warp >= 4) {
+    tc_fence_after();
     const int quarter = warp - 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    bool ok = true;
-    for (int i = 0; i < my_units; ++i) {
-      const int u = blockIdx.x + i * gridDim.x;
-      const int buf = i & 1;
-      if (!wait_or_abort(&bars->acc_full[buf], (i >> 1) & 1, bars)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float4* dst = reinterpret_cast<float4*>(p.part + (static_cast<size_t>(u) * p.a_rows + row) * kBN);
+    const int owner = row / rows_per, lrow = row - owner * rows_per;
+    const int slot = rank * rows_per + lrow;
+    const uint32_t dst = dsmem_addr(s_recv + slot * kPartStride, row < p.M ? owner : 0);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + buf * kBN + lane_off + c * 32, r);
-        tmem_ld_wait();
-        if (row < p.M) {
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_off + c * 32, r);  // warp-collective: every lane loads
+      tmem_ld_wait();
+      if (row < p.M) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[c * 8 + v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        }
+        for (int v = 0; v < 8; ++v)
+          dsmem_st_f4(dst + (c * 32 + 4 * v) * 4, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       }
-      tc_fence_before();
-      mbar_arrive(&bars->acc_empty[buf]);
     }
-    if (!ok) fail_pipeline(bars);
+    if (p.norm_input && row < p.M) dsmem_st_f32(dsmem_addr(&bars->recv_ss[slot], owner), row_ss);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kBN);
   }
-
-  // ------------------------------------------------------------ grid barrier
-  // every unit's partial is written (all CTAs are resident: cooperative launch)
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    atom_add_release_gpu(&p.barrier[0], 1u);
-    const uint64_t t0 = globaltimer_ns();
-    bool done = false;
-    for (uint32_t i = 0;; ++i) {
-      if (ld_acquire_gpu(&p.barrier[0]) >= gridDim.x) {
-        done = true;
-        break;
-      }
-      if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
-    }
-    if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
-    s_ok = done ? 1 : 0;
-    // the last CTA to leave resets both counters for the next call
-    if (atomicAdd(&p.barrier[1], 1u) == gridDim.x - 1) {
-      p.barrier[0] = 0u;
-      p.barrier[1] = 0u;
-    }
-  }
-  __syncthreads();
-  if (!s_ok) return;
+  __syncwarp();
+  cluster_sync_all();  // every partial has reached its owner
 
   // ------------------------------------------------------------ phase 2
-  float* s_sum = reinterpret_cast<float*>(smem);  // [16][256], the stage area is free now
-  const int T = p.mode == kQKV ? *p.t_len : 0;
-  const int row_blocks = (p.M + kItemRows - 1) / kItemRows;
-  const int items = p.n_tiles * row_blocks;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int tile = it / row_blocks, r0 = (it % row_blocks) * kItemRows;
-    {
-      // thread: one row, 16 columns; sum over the splits
+  if (!any_bad) {
+    const int T = p.mode == kQKV ? *p.t_len : 0;
+    const int r_begin = rank * rows_per;
+    const int r_end = min(p.M, r_begin + rows_per);
+    for (int r0 = r_begin; r0 < r_end; r0 += kChunkRows) {
+      if (p.norm_input && threadIdx.x < kChunkRows) {
+        const int lrow = r0 - r_begin + threadIdx.x;
+        float ss = 0.f;
+        if (r0 + static_cast<int>(threadIdx.x) < r_end)
+          for (int s = 0; s < S; ++s) ss += bars->recv_ss[s * rows_per + lrow];
+        bars->r[threadIdx.x] = rsqrtf(ss / p.K + p.eps);
+      }
+      // thread: one row, 16 columns; sum over the cluster's partials
       const int rr = threadIdx.x / 16, c0 = (threadIdx.x % 16) * 16;
-      const int row = r0 + rr;
+      const int lrow = r0 - r_begin + rr;
       float acc[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-      if (row < p.M) {
-        for (int s = 0; s < p.n_split; ++s) {
-          const float4* src = reinterpret_cast<const float4*>(
-              p.part + (static_cast<size_t>(tile * p.n_split + s) * p.a_rows + row) * kBN + c0);
+      if (r0 + rr < r_end) {
+        for (int s = 0; s < S; ++s) {
+          const float4* src = reinterpret_cast<const float4*>(s_recv + (s * rows_per + lrow) * kPartStride + c0);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const float4 x = __ldcg(src + v);
+            const float4 x = src[v];
             acc[4 * v] += x.x;
             acc[4 * v + 1] += x.y;
             acc[4 * v + 2] += x.z;
@@ -445,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) s_sum[rr * kBN + c0 + e] = acc[e];
+      __syncthreads();
+      epilogue_rows(p, s_sum, p.norm_input ? bars->r : nullptr, tile, r0, r_end, T);
+      __syncthreads();
     }
-    __syncthreads();
-    epilogue_item(p, s_sum, tile, r0, T);
-    __syncthreads();
   }
 }
 
@@ -473,36 +509,70 @@ __global__ void rms_scale_kernel(const __nv_bfloat16* x, int M, int d, float eps
   if (lane == 0) r[row] = rsqrtf(s / d + eps);
 }
 
-// Splits per tile so that units = tiles x splits fill about one wave of SMs.
-int choose_split(int n_tiles, int n_kb) {
-  const int sms = glance::num_sms();
-  int s = sms / n_tiles;
-  if (s < 1) s = 1;
-  if (s > n_kb) s = n_kb;
-  return s;
+// Clusters of `size` CTAs of dense_kernel that fit on the device at once
+// (queried once per device and size, after the shared-memory attribute is set).
+int max_clusters(int size) {
+  static int cached[64][kMaxSplit + 1] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev][size] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(size * glance::num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dense_kernel, &cfg) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = -1;
+    }
+    cached[dev][size] = n;
+  }
+  return cached[dev][size];
 }
 
-size_t ws_bytes(int M, int K, int n_cols_tiles) {
-  const int n_kb = K / kBK;
-  const int S = choose_split(n_cols_tiles, n_kb);
-  const int a_rows = (M + 7) / 8 * 8;
-  return 256 + static_cast<size_t>(n_cols_tiles) * S * a_rows * kBN * sizeof(float);
+// K splits per tile: the largest S (<= 16, <= the K blocks) whose n_tiles
+// clusters all fit on the device at once; 1 when even that takes more than
+// one wave.
+int choose_split(int n_tiles, int n_kb) {
+  int best = 1;
+  for (int s = 2; s <= kMaxSplit && s <= n_kb; ++s)
+    if (max_clusters(s) >= n_tiles) best = s;
+  return best;
+}
+
+cudaError_t ensure_attrs() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dense_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) done[dev] = true;
+  return cudaSuccess;
 }
 
 glance_status run_dense(const char* who, const void* x, int M, int K, const void* W0, const void* W1,
-                        int w_cols, int n_tiles, DenseParams p, void* workspace,
-                        size_t workspace_bytes, cudaStream_t s) {
+                        int w_cols, int n_tiles, DenseParams p, cudaStream_t s) {
   using glance::fail;
   if (M < 1 || M > kBM) return fail(GLANCE_ERR_UNSUPPORTED, "%s: need 1 <= M <= 128", who);
   if (K < kBK || K % kBK) return fail(GLANCE_ERR_UNSUPPORTED, "%s: K must be a multiple of 64", who);
   if (!glance::aligned16(x) || !glance::aligned16(W0) || !glance::aligned16(W1))
     return fail(GLANCE_ERR_INVALID_ARG, "%s: x and W must be 16-byte aligned", who);
-  const size_t need = ws_bytes(M, K, n_tiles);
-  if (!workspace || workspace_bytes < need)
-    return fail(GLANCE_ERR_CAPACITY, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes, need);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
-  cudaError_t e = glance::ensure_smem(reinterpret_cast<const void*>(dense_kernel), static_cast<int>(kSmemBytes));
+  cudaError_t e = ensure_attrs();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   const int a_rows = (M + 7) / 8 * 8;
   CUtensorMap ma, mb0, mb1;
@@ -524,27 +594,23 @@ glance_status run_dense(const char* who, const void* x, int M, int K, const void
   }
   p.M = M;
   p.K = K;
-  p.n_tiles = n_tiles;
   p.n_kb = K / kBK;
-  p.n_split = choose_split(n_tiles, p.n_kb);
+  p.split = choose_split(n_tiles, p.n_kb);
   p.a_rows = a_rows;
-  char* ws = static_cast<char*>(workspace);
-  p.barrier = reinterpret_cast<uint32_t*>(ws);
-  p.part = reinterpret_cast<float*>(ws + 256);
-  const int units = n_tiles * p.n_split;
-  int grid = glance::num_sms();
-  if (grid > units) grid = units;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(n_tiles * p.split);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  // phase 2 waits for every CTA's phase 1: all CTAs must be resident
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, dense_kernel, ma, mb0, mb1, p);
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
@@ -557,12 +623,6 @@ DenseParams blank_params() {
 }
 
 }  // namespace
-
-extern "C" size_t glance_dense_workspace_bytes(int M, int K, int N) {
-  if (M < 1 || M > kBM || K < kBK || K % kBK || N < kBN || N % 128) return 0;
-  // the gate/up projection tiles N = 2 * intermediate in 256-column tiles too
-  return ws_bytes(M, K, (N + kBN - 1) / kBN);
-}
 
 extern "C" glance_status glance_rms_scale(const void* x, int M, int d, float eps, float* r_out,
                                           void* stream) {
@@ -578,8 +638,7 @@ extern "C" glance_status glance_rms_scale(const void* x, int M, int d, float eps
 }
 
 extern "C" glance_status glance_dense_residual(const void* x, const void* W, int M, int K, int N,
-                                               const void* residual, void* out, void* workspace,
-                                               size_t workspace_bytes, void* stream) {
+                                               const void* residual, void* out, void* stream) {
   using glance::fail;
   const char* who = "glance_dense_residual";
   if (!x || !W || !residual || !out) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
@@ -591,14 +650,12 @@ extern "C" glance_status glance_dense_residual(const void* x, const void* W, int
   p.res = static_cast<const __nv_bfloat16*>(residual);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.n_out = N;
-  return run_dense(who, x, M, K, W, W, N, N / kBN, p, workspace, workspace_bytes,
-                   static_cast<cudaStream_t>(stream));
+  return run_dense(who, x, M, K, W, W, N, N / kBN, p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" glance_status glance_dense_swiglu(const void* h, const void* W_gate, const void* W_up,
-                                             int M, int d, int inter, const float* rscale,
-                                             void* act, void* workspace, size_t workspace_bytes,
-                                             void* stream) {
+                                             int M, int d, int inter, int norm_input, float eps,
+                                             void* act, void* stream) {
   using glance::fail;
   const char* who = "glance_dense_swiglu";
   if (!h || !W_gate || !W_up || !act) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
@@ -606,18 +663,17 @@ extern "C" glance_status glance_dense_swiglu(const void* h, const void* W_gate, 
   if (!glance::aligned16(act)) return fail(GLANCE_ERR_INVALID_ARG, "%s: act must be 16-byte aligned", who);
   DenseParams p = blank_params();
   p.mode = kSwiGLU;
-  p.rscale = rscale;
+  p.norm_input = norm_input ? 1 : 0;
+  p.eps = eps;
   p.act = static_cast<__nv_bfloat16*>(act);
   p.inter = inter;
-  return run_dense(who, h, M, d, W_gate, W_up, inter, inter / 128, p, workspace, workspace_bytes,
-                   static_cast<cudaStream_t>(stream));
+  return run_dense(who, h, M, d, W_gate, W_up, inter, inter / 128, p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int M, int d, int n_q_heads,
-                                          const float* rscale, const float* q_norm, const float* k_norm,
+                                          int norm_input, const float* q_norm, const float* k_norm,
                                           float eps, const int32_t* pos_id, float rope_theta,
-                                          void* q_out, const glance_kv* kv, void* workspace,
-                                          size_t workspace_bytes, void* stream) {
+                                          void* q_out, const glance_kv* kv, void* stream) {
   using glance::fail;
   const char* who = "glance_dense_qkv";
   if (!h || !W_qkv || !pos_id || !q_out || !kv || !kv->k || !kv->v || !kv->t_len)
@@ -634,7 +690,7 @@ extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int 
     return fail(GLANCE_ERR_INVALID_ARG, "%s: bad q_out / cache layout", who);
   DenseParams p = blank_params();
   p.mode = kQKV;
-  p.rscale = rscale;
+  p.norm_input = norm_input ? 1 : 0;
   p.Hq = n_q_heads;
   p.Hkv = Hkv;
   p.q_norm = q_norm;
@@ -650,6 +706,5 @@ extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int 
   p.t_len = kv->t_len;
   p.t_cap = kv->t_cap;
   const int cols = (n_q_heads + 2 * Hkv) * kHeadDim;
-  return run_dense(who, h, M, d, W_qkv, W_qkv, cols, cols / kBN, p, workspace, workspace_bytes,
-                   static_cast<cudaStream_t>(stream));
+  return run_dense(who, h, M, d, W_qkv, W_qkv, cols, cols / kBN, p, static_cast<cudaStream_t>(stream));
 }
