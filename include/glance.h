@@ -401,19 +401,24 @@ glance_status glance_accept_commit_gated_batched(const glance_tree* trees, int B
  *   x' -> RMSNorm -> SiLU(. W_gate) * (. W_up) -> x' + . W_down.
  * All bf16 row-major, W as [in][out] (out contiguous), fp32 accumulation.
  * An RMSNorm weight g is folded into the next projection by the caller
- * (W <- diag(g) W); with norm_input != 0 the call scales each product row by
- * 1 / sqrt(mean_k x[row][k]^2 + eps) of its own input row. Each projection is
- * one launch of clusters that split K (no workspace); it is a programmatic
- * dependent of the previous kernel in the stream. The output must not overlap
- * the input x (other CTAs may still be reading it).
+ * (W <- diag(g) W); the 1 / rms row scale is applied to the product. A call
+ * that normalises its input takes the input rows' sums of squares as
+ * in_sumsq [n_sumsq][M] partial sums (row scale 1 / sqrt(sum_t in_sumsq[t][row]
+ * / d + eps); null: no input norm). glance_dense_residual writes them for its
+ * own output (out_sumsq [N / 256][M], nullable), so a layer passes them on;
+ * glance_row_sumsq makes them for rows from anywhere else. Each projection is
+ * one launch of thread-block clusters that split K (no workspace); it is a
+ * programmatic dependent of the previous kernel in the stream. The output must
+ * not overlap the input x (other CTAs may still be reading it).
  */
 
-/* r_out[i] = 1 / sqrt(mean_k x[i][k]^2 + eps) (device float [M]); d % 8 == 0. */
-glance_status glance_rms_scale(const void* x, int M, int d, float eps, float* r_out, void* stream);
+/* sumsq[i] = sum_k x[i][k]^2 (device float [M]; the [1][M] in_sumsq of a
+ * following call); x bf16 [M][d], d % 8 == 0. */
+glance_status glance_row_sumsq(const void* x, int M, int d, float* sumsq, void* stream);
 
 /*
  * QKV projection of h [M][d] with W_qkv [d][(Hq + 2 Hkv) * 128] (q heads,
- * then k heads, then v heads), rows RMS-scaled when norm_input; q and k each
+ * then k heads, then v heads), rows RMS-scaled from in_sumsq; q and k each
  * get a per-head RMSNorm (weights q_norm / k_norm [128], nullable = none,
  * eps) and rotate-half RoPE at pos_id [M] with base rope_theta (dims j and
  * j + 64 rotate by pos * theta^(-2j/128)). q goes to q_out [M][Hq][128]; k
@@ -422,21 +427,24 @@ glance_status glance_rms_scale(const void* x, int M, int d, float eps, float* r_
  * Hq % Hkv == 0, d % 64 == 0.
  */
 glance_status glance_dense_qkv(const void* h, const void* W_qkv, int M, int d, int n_q_heads,
-                               int norm_input, const float* q_norm, const float* k_norm, float eps,
-                               const int32_t* pos_id, float rope_theta, void* q_out,
-                               const glance_kv* kv, void* stream);
+                               const float* in_sumsq, int n_sumsq, const float* q_norm,
+                               const float* k_norm, float eps, const int32_t* pos_id,
+                               float rope_theta, void* q_out, const glance_kv* kv, void* stream);
 
 /* out [M][N] = residual [M][N] + x [M][K] W [K][N] (out may alias residual,
- * not x); K % 64 == 0, N % 256 == 0. The output and down projections. */
+ * not x), and out_sumsq [N / 256][M] (nullable) = per 256-column tile, the
+ * sums of squares of the rows' stored bf16 outputs; K % 64 == 0,
+ * N % 256 == 0. The output and down projections. */
 glance_status glance_dense_residual(const void* x, const void* W, int M, int K, int N,
-                                    const void* residual, void* out, void* stream);
+                                    const void* residual, void* out, float* out_sumsq,
+                                    void* stream);
 
-/* act [M][inter] = SiLU(r h W_gate) * (r h W_up), r the row's RMS scale when
- * norm_input (else 1); W_gate, W_up [d][inter], inter % 128 == 0,
+/* act [M][inter] = SiLU(r h W_gate) * (r h W_up), r the row's RMS scale from
+ * in_sumsq (null: 1); W_gate, W_up [d][inter], inter % 128 == 0,
  * d % 64 == 0. */
 glance_status glance_dense_swiglu(const void* h, const void* W_gate, const void* W_up, int M,
-                                  int d, int inter, int norm_input, float eps, void* act,
-                                  void* stream);
+                                  int d, int inter, const float* in_sumsq, int n_sumsq, float eps,
+                                  void* act, void* stream);
 
 /* ------------------------------------------------------------------ status */
 

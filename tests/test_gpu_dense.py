@@ -1,5 +1,7 @@
 """Dense verify layers on the GPU vs the oracle (fp64 on the same bf16
-inputs): RMSNorm row scales within 1e-5 relative; projections, SwiGLU,
+inputs): RMSNorm row scales from the library's row sums of squares within
+1e-5 relative (row_sumsq, and the residual projections' per-tile sums of
+their own outputs); projections, SwiGLU,
 q/k with RoPE and the cache rows within 2e-2 * max(1, |ref|); the whole
 layer (with tree attention between) call by call on each call's own bf16
 inputs, and end to end against the fp64 oracle layer within 6e-2 (the bf16
@@ -30,14 +32,28 @@ def f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def scale_from_sumsq(parts, d, eps):
+    """1 / rms per row from [n][M] partial sums of squares."""
+    return 1.0 / np.sqrt(parts.reshape(-1, parts.shape[-1]).astype(np.float64).sum(axis=0) / d + eps)
+
+
+def tile_sumsq(xb, width=256):
+    """[d / width][M] fp32 partial row sums of squares of bf16 bits xb [M][d] (test input)."""
+    x = bf16_bits_to_f64(xb)
+    M, d = x.shape
+    return torch.from_numpy(np.ascontiguousarray(
+        (x * x).reshape(M, d // width, width).sum(axis=2).T.astype(np.float32)))
+
+
 @pytest.mark.parametrize("M,d", [(64, 4096), (7, 512), (128, 12288)])
-def test_rms_scale(dev, clean_status, M, d):
+def test_row_sumsq(dev, clean_status, M, d):
     import tree_verified_block_gb300 as g
     xb = W.normal_bf16(W.rng(M, d), (M, d))
-    r = torch.empty(M, dtype=torch.float32, device=dev)
-    g.rms_scale(bf16_tensor(xb, dev), 1e-6, r)
+    ss = torch.empty(M, dtype=torch.float32, device=dev)
+    g.row_sumsq(bf16_tensor(xb, dev), ss)
+    got = scale_from_sumsq(ss.cpu().numpy()[None], d, 1e-6)
     want = o_rms(bf16_bits_to_f64(xb), 1e-6)
-    assert np.all(np.abs(r.cpu().numpy() - want) <= 1e-5 * want)
+    assert np.all(np.abs(got - want) <= 1e-5 * want)
 
 
 @pytest.mark.parametrize("M,K,N", [(64, 4096, 4096), (17, 12288, 4096), (64, 12288, 4096), (128, 512, 768),
@@ -53,8 +69,14 @@ def test_residual_projection(dev, clean_status, M, K, N):
     out = torch.full_like(res, float("nan"))
     x, Wt = bf16_tensor(xb, dev), bf16_tensor(Wb, dev)
     want = o_residual(bf16_bits_to_f64(rb), bf16_bits_to_f64(xb), bf16_bits_to_f64(Wb))
-    g.dense_residual(x, Wt, res, out)
+    ss = torch.full((N // 256, M), float("nan"), dtype=torch.float32, device=dev)
+    g.dense_residual(x, Wt, res, out, ss)
     close(f64(out), want)
+    # the per-tile sums of squares are those of the stored outputs
+    ob = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    got_r = scale_from_sumsq(ss.cpu().numpy(), N, 1e-6)
+    assert np.all(np.abs(got_r - o_rms(bf16_bits_to_f64(ob), 1e-6)) <= 1e-5 * got_r)
+    assert np.allclose(ss.cpu().numpy(), tile_sumsq(ob).numpy(), rtol=1e-5, atol=0)
     g.dense_residual(x, Wt, res, res)  # in place: out aliases the residual
     close(f64(res), want)
     assert np.array_equal(res.view(torch.int16).cpu().numpy(), out.view(torch.int16).cpu().numpy())
@@ -69,7 +91,8 @@ def test_swiglu(dev, clean_status, M, d, inter):
     Ub = W.normal_bf16(gen, (d, inter), std=0.02)
     h = bf16_tensor(hb, dev)
     act = torch.full((M, inter), float("nan"), dtype=torch.bfloat16, device=dev)
-    g.dense_swiglu(h, bf16_tensor(Gb, dev), bf16_tensor(Ub, dev), True, 1e-6, act)
+    # the input's sums of squares in 256-column parts, as a residual projection leaves them
+    g.dense_swiglu(h, bf16_tensor(Gb, dev), bf16_tensor(Ub, dev), tile_sumsq(hb).to(dev), 1e-6, act)
     want = o_swiglu(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Gb), bf16_bits_to_f64(Ub), 1e-6)
     close(f64(act), want)
 
@@ -92,7 +115,11 @@ def test_qkv_rope_into_cache(dev, clean_status, qk_norm, norm_input):
     h = bf16_tensor(hb, dev)
     q = torch.full((M, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
     tt = lambda a: None if a is None else torch.from_numpy(a).to(dev)
-    g.dense_qkv(h, bf16_tensor(Wb, dev), Hq, norm_input, tt(qn), tt(kn), 1e-6, torch.from_numpy(pos).to(dev),
+    ss = None
+    if norm_input:
+        ss = torch.empty(M, dtype=torch.float32, device=dev)
+        g.row_sumsq(h, ss)
+    g.dense_qkv(h, bf16_tensor(Wb, dev), Hq, ss, tt(qn), tt(kn), 1e-6, torch.from_numpy(pos).to(dev),
                 1e6, q, kv)
     wq, wk, wv = o_qkv(bf16_bits_to_f64(hb), None, bf16_bits_to_f64(Wb), Hq, Hkv, D, pos, 1e6, 1e-6,
                        None if qn is None else qn.astype(np.float64),
@@ -139,12 +166,16 @@ def test_full_layer_with_tree_attention(dev, clean_status):
     act = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
     out = torch.empty_like(x)
     ws_a = g.workspace(g.tree_attention_workspace_bytes(M, Hq, kv), dev)
-    g.dense_qkv(x, bf16_tensor(Wqkv, dev), Hq, True, torch.from_numpy(qn).to(dev), torch.from_numpy(kn).to(dev),
+    ss0 = torch.empty(M, dtype=torch.float32, device=dev)
+    ss1 = torch.empty((d // 256, M), dtype=torch.float32, device=dev)
+    ss2 = torch.empty_like(ss1)
+    g.row_sumsq(x, ss0)
+    g.dense_qkv(x, bf16_tensor(Wqkv, dev), Hq, ss0, torch.from_numpy(qn).to(dev), torch.from_numpy(kn).to(dev),
                 1e-6, torch.from_numpy(pos).to(dev), 1e6, q, kv)
     g.tree_attention(q, kv, tree, D ** -0.5, att, ws_a)
-    g.dense_residual(att.view(M, Hq * D), bf16_tensor(Wo, dev), x, x1)
-    g.dense_swiglu(x1, bf16_tensor(Wg, dev), bf16_tensor(Wu, dev), True, 1e-6, act)
-    g.dense_residual(act, bf16_tensor(Wd, dev), x1, out)
+    g.dense_residual(att.view(M, Hq * D), bf16_tensor(Wo, dev), x, x1, ss1)
+    g.dense_swiglu(x1, bf16_tensor(Wg, dev), bf16_tensor(Wu, dev), ss1, 1e-6, act)
+    g.dense_residual(act, bf16_tensor(Wd, dev), x1, out, ss2)  # ss2: the next layer's norm input
     # every call against the oracle's step on that call's own bf16 inputs (the
     # previous call's stored output); fp64 inside every step
     Kc, Vc = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
@@ -159,6 +190,8 @@ def test_full_layer_with_tree_attention(dev, clean_status):
     close(f64(x1), o_residual(x0, f64(att).reshape(M, Hq * D), bf16_bits_to_f64(Wo)))
     close(f64(act), o_swiglu(f64(x1), None, bf16_bits_to_f64(Wg), bf16_bits_to_f64(Wu), 1e-6))
     close(f64(out), o_residual(f64(x1), f64(act), bf16_bits_to_f64(Wd)))
+    got_r = scale_from_sumsq(ss2.cpu().numpy(), d, 1e-6)
+    assert np.all(np.abs(got_r - o_rms(f64(out), 1e-6)) <= 1e-5 * got_r)
     # and the whole layer against the fp64 oracle layer: the five bf16 stores
     # between the calls (q, K/V rows, att, x1, act; each within 2^-9 relative)
     # move the 12288-term down projection by up to a few 1e-2 at the tails

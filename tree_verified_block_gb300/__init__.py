@@ -19,7 +19,7 @@ from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree,
                        build_tree_batched_workspace_bytes, build_tree_shared,
                        build_tree_shared_workspace_bytes, build_tree_workspace_bytes,
                        dense_qkv, dense_residual, dense_swiglu,
-                       device_status, lib, lmhead_argmax, lmhead_argmax_noalloc, rms_scale,
+                       device_status, lib, lmhead_argmax, lmhead_argmax_noalloc, row_sumsq,
                        lmhead_argmax_workspace_bytes, reset_device_status, tree_attention,
                        tree_attention_batched, tree_attention_batched_workspace_bytes,
                        tree_attention_workspace_bytes, version, workspace)
@@ -31,7 +31,7 @@ __all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree
            "accept_commit_workspace_bytes", "build_tree", "build_tree_batched",
            "build_tree_batched_workspace_bytes", "build_tree_shared",
            "build_tree_shared_workspace_bytes", "build_tree_workspace_bytes", "dense_qkv",
-           "dense_residual", "dense_swiglu", "device_status", "rms_scale",
+           "dense_residual", "dense_swiglu", "device_status", "row_sumsq",
            "lib", "lmhead_argmax", "lmhead_argmax_noalloc", "lmhead_argmax_workspace_bytes",
            "reset_device_status", "tree_attention", "tree_attention_batched",
            "tree_attention_batched_workspace_bytes", "tree_attention_workspace_bytes", "version",

@@ -28,7 +28,7 @@ EXPORTS = [
     "glance_accept_commit_batched_workspace_bytes", "glance_accept_commit_batched",
     "glance_lmhead_argmax_entropy", "glance_lmhead_sample", "glance_accept_commit_gated",
     "glance_build_tree_shared_workspace_bytes", "glance_build_tree_shared",
-    "glance_rms_scale", "glance_dense_qkv",
+    "glance_row_sumsq", "glance_dense_qkv",
     "glance_dense_residual", "glance_dense_swiglu",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
@@ -113,14 +113,14 @@ def lib():
                                            ctypes.c_float, ctypes.c_float, ctypes.POINTER(TreeC),
                                            vp, vp, sz, vp]
     L.glance_build_tree_shared.restype = st
-    L.glance_rms_scale.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
-    L.glance_rms_scale.restype = st
-    L.glance_dense_qkv.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_float, vp,
+    L.glance_row_sumsq.argtypes = [vp, i32, i32, vp, vp]
+    L.glance_row_sumsq.restype = st
+    L.glance_dense_qkv.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, ctypes.c_float, vp,
                                    ctypes.c_float, vp, vp, vp]
     L.glance_dense_qkv.restype = st
-    L.glance_dense_residual.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    L.glance_dense_residual.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
     L.glance_dense_residual.restype = st
-    L.glance_dense_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp]
+    L.glance_dense_swiglu.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, ctypes.c_float, vp, vp]
     L.glance_dense_swiglu.restype = st
     L.glance_lmhead_sample.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint64,
                                        vp, vp, vp, vp, vp, sz, vp]
@@ -386,36 +386,48 @@ def accept_commit_gated_batched(trees, argmax, gap, threshold, layers, n_accepte
 
 # -------------------------------------------------------------- dense layers
 
-def rms_scale(x, eps, r_out, stream=None):
+def row_sumsq(x, sumsq, stream=None):
+    """sumsq [M] (float32) = row sums of squares of x [M][d] (bf16)."""
     M, d = x.shape
     assert x.is_contiguous()
-    _check(lib().glance_rms_scale(_ptr(x), M, d, float(eps), _ptr(r_out), _stream(stream, x.device)))
+    _check(lib().glance_row_sumsq(_ptr(x), M, d, _ptr(sumsq), _stream(stream, x.device)))
 
 
-def dense_qkv(h, W_qkv, n_q_heads, norm_input, q_norm, k_norm, eps, pos_id, rope_theta, q_out, kv,
+def _n_parts(in_sumsq, M):
+    if in_sumsq is None:
+        return 0
+    assert in_sumsq.dtype == torch.float32 and in_sumsq.is_contiguous() and in_sumsq.numel() % M == 0
+    return in_sumsq.numel() // M
+
+
+def dense_qkv(h, W_qkv, n_q_heads, in_sumsq, q_norm, k_norm, eps, pos_id, rope_theta, q_out, kv,
               stream=None):
+    """in_sumsq: [n][M] partial row sums of squares of h (None: no input norm)."""
     M, d = h.shape
     assert h.is_contiguous() and W_qkv.is_contiguous() and q_out.is_contiguous()
-    _check(lib().glance_dense_qkv(_ptr(h), _ptr(W_qkv), M, d, n_q_heads, int(bool(norm_input)),
-                                  _ptr(q_norm), _ptr(k_norm), float(eps), _ptr(pos_id),
-                                  float(rope_theta), _ptr(q_out), ctypes.byref(kv.c),
+    _check(lib().glance_dense_qkv(_ptr(h), _ptr(W_qkv), M, d, n_q_heads, _ptr(in_sumsq),
+                                  _n_parts(in_sumsq, M), _ptr(q_norm), _ptr(k_norm), float(eps),
+                                  _ptr(pos_id), float(rope_theta), _ptr(q_out), ctypes.byref(kv.c),
                                   _stream(stream, h.device)))
 
 
-def dense_residual(x, W, residual, out, stream=None):
+def dense_residual(x, W, residual, out, out_sumsq=None, stream=None):
+    """out_sumsq: [N / 256][M] float32 to receive the output rows' sums of squares, or None."""
     M, K = x.shape
     N = W.shape[1]
     assert x.is_contiguous() and W.is_contiguous() and residual.is_contiguous() and out.is_contiguous()
+    if out_sumsq is not None:
+        assert out_sumsq.dtype == torch.float32 and out_sumsq.numel() >= (N // 256) * M
     _check(lib().glance_dense_residual(_ptr(x), _ptr(W), M, K, N, _ptr(residual), _ptr(out),
-                                       _stream(stream, x.device)))
+                                       _ptr(out_sumsq), _stream(stream, x.device)))
 
 
-def dense_swiglu(h, W_gate, W_up, norm_input, eps, act, stream=None):
+def dense_swiglu(h, W_gate, W_up, in_sumsq, eps, act, stream=None):
     M, d = h.shape
     inter = W_gate.shape[1]
     assert h.is_contiguous() and W_gate.is_contiguous() and W_up.is_contiguous() and act.is_contiguous()
-    _check(lib().glance_dense_swiglu(_ptr(h), _ptr(W_gate), _ptr(W_up), M, d, inter,
-                                     int(bool(norm_input)), float(eps), _ptr(act),
+    _check(lib().glance_dense_swiglu(_ptr(h), _ptr(W_gate), _ptr(W_up), M, d, inter, _ptr(in_sumsq),
+                                     _n_parts(in_sumsq, M), float(eps), _ptr(act),
                                      _stream(stream, h.device)))
 
 

@@ -12,16 +12,15 @@
 //   -> RMSNorm -> SiLU(. W_gate) * (. W_up) -> x' + . W_down.
 // An RMSNorm's weight is folded into the next projection's rows by the
 // caller; its 1 / rms row scale, which a projection is linear in, is applied
-// to the product, from row sums of squares taken on the input tiles as they
-// stream through shared memory.
+// to the product. The row sums of squares it needs come from the kernel that
+// wrote the rows: the residual projections emit them per output tile.
 //
 // GEMM shape: Y[M x N] = X[M x K] W[K x N], W row-major with N contiguous
 // (the MN-major B operand), bf16 in, fp32 accumulate. At M <= 128 the weights
 // dominate (HBM-bound) and N / 256 output tiles are too few to occupy the
 // SMs, so K is split S ways inside a thread-block cluster of S CTAs: CTA s of
 // the cluster of tile t accumulates K range s in tensor memory (warp 0 streams
-// X and W stages with TMA, 4 x 48 KB; warp 1 issues M=128 x N=256 x K=16 MMAs;
-// warps 4..7 take the input rows' sums of squares from the same stages). Once
+// X and W stages with TMA, 4 x 48 KB; warp 1 issues M=128 x N=256 x K=16 MMAs). Once
 // the whole cluster is done with its stages, warps 4..7 send each row of the
 // fp32 partial to the CTA that owns the row (remote stores into its shared
 // memory); after a second cluster barrier each CTA sums the S partials of its
@@ -52,16 +51,21 @@ constexpr int kPartStride = kBN + 4;           // floats per partial row in shar
 constexpr int kMaxSplit = 16;
 // received partials: [source rank][owned row][kPartStride], at most M + S - 1 rows
 constexpr uint32_t kRecvBytes = (kBM + kMaxSplit) * kPartStride * 4;
-constexpr int kChunkRows = 16;                 // epilogue: 16 rows at a time
+constexpr int kChunkRows = 16;                 // epilogue: 16 rows at a time (16 threads a row)
 constexpr size_t kSmemBytes = 1024 + kStageArea + 2048;
 constexpr int kHeadDim = 128;
-static_assert(kRecvBytes + kChunkRows * kBN * 4 <= kStageArea, "partials overlay the stages");
+static_assert(kRecvBytes <= kStageArea, "received partials overlay the stages");
 
 enum Mode : int { kResid = 0, kQKV = 1, kSwiGLU = 2 };
 
 struct DenseParams {
-  int M, K, n_kb, a_rows, mode, split, norm_input;
+  int M, K, n_kb, a_rows, mode, split;
   float eps;
+  // input row norm: r[row] = 1 / sqrt(sum_t in_sumsq[t][row] / K + eps) (null: r = 1)
+  const float* in_sumsq;
+  int n_sumsq;
+  // kResid: out_sumsq[tile][row] = sum of squares of the tile's bf16 outputs (nullable)
+  float* out_sumsq;
   // kResid: out = res + X W, both [M][n_out]
   const __nv_bfloat16* res;
   __nv_bfloat16* out;
@@ -91,8 +95,7 @@ struct __align__(8) Bars {
   uint32_t tmem_base;
   int abort_flag;
   int failed;         // read by the cluster's other CTAs
-  float recv_ss[kBM + kMaxSplit];  // [source rank][owned row]: sums of squares of input rows
-  float r[kChunkRows];
+  float r[kBM];       // 1 / rms of the rows this CTA finishes
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
@@ -112,83 +115,96 @@ __device__ __forceinline__ void fail_pipeline(Bars* bars) {
   atomicExch(&bars->abort_flag, 1);
 }
 
-__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 __device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
   int v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
 
-// Epilogue of rows r0 .. min(r0 + 16, r_end) - 1 of one tile, whose summed
-// product sits in s_sum[16][256] (fp32); r (nullable) holds the rows' 1 / rms.
-__device__ void epilogue_rows(const DenseParams& p, const float* s_sum, const float* rs, int tile,
-                              int r0, int r_end, int T) {
+// Columns of a tile that thread t handles in the epilogue: 16 threads per
+// row, each with two groups of 8 columns, a (from column col_a) and b (from
+// col_b). Residual: 16 contiguous columns. SwiGLU: gate column j and its up
+// column 128 + j. QKV: dims j0..j0+7 of one of the tile's two heads and their
+// rotate-half partners j0+64..j0+71 (8 consecutive threads share a head).
+__device__ __forceinline__ void epilogue_cols(int mode, int t, int& col_a, int& col_b) {
+  const int sub = t % 16;
+  if (mode == kResid) {
+    col_a = sub * 16;
+    col_b = col_a + 8;
+  } else if (mode == kSwiGLU) {
+    col_a = sub * 8;
+    col_b = 128 + sub * 8;
+  } else {
+    col_a = (sub / 8) * kHeadDim + (sub % 8) * 8;
+    col_b = col_a + 64;
+  }
+}
+
+// Epilogue of one row's two column groups (summed products a, b, before the
+// row scale r). Every thread of the block calls it (the QKV head norm and the
+// residual's row sums of squares shuffle across lanes); `valid` says whether
+// the row is this thread's.
+__device__ void epilogue_regs(const DenseParams& p, float (&a)[8], float (&b)[8], float r, int tile, int row,
+                              bool valid, int T) {
   const int t = threadIdx.x;
+  int col_a, col_b;
+  epilogue_cols(p.mode, t, col_a, col_b);
   if (p.mode == kResid) {
-    // thread: one row, 16 columns
-    const int rr = t / 16, c0 = (t % 16) * 16;
-    const int row = r0 + rr;
-    if (row >= r_end) return;
-    const size_t at = static_cast<size_t>(row) * p.n_out + static_cast<size_t>(tile) * kBN + c0;
-    const uint4* src = reinterpret_cast<const uint4*>(p.res + at);
-    uint4* dst = reinterpret_cast<uint4*>(p.out + at);
+    float ss = 0.f;
+    if (valid) {
+      const size_t base = static_cast<size_t>(row) * p.n_out + static_cast<size_t>(tile) * kBN;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 v = src[h];
-      const uint32_t rv[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+      for (int h = 0; h < 2; ++h) {
+        const float* v8 = h ? b : a;
+        const size_t at = base + (h ? col_b : col_a);
+        const uint4 v = *reinterpret_cast<const uint4*>(p.res + at);
+        const uint32_t rv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(rv[e] << 16) + s_sum[rr * kBN + c0 + 8 * h + 2 * e];
-        const float hi = __uint_as_float(rv[e] & 0xFFFF0000u) + s_sum[rr * kBN + c0 + 8 * h + 2 * e + 1];
-        o[e] = pack_bf16x2(lo, hi);
+        for (int e = 0; e < 4; ++e) {
+          o[e] = pack_bf16x2(__uint_as_float(rv[e] << 16) + v8[2 * e],
+                             __uint_as_float(rv[e] & 0xFFFF0000u) + v8[2 * e + 1]);
+          const float lo = __uint_as_float(o[e] << 16), hi = __uint_as_float(o[e] & 0xFFFF0000u);
+          ss += lo * lo + hi * hi;  // of the stored (rounded) values
+        }
+        *reinterpret_cast<uint4*>(p.out + at) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      dst[h] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (p.out_sumsq) {  // the row's 16 threads are 16 consecutive lanes
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (valid && t % 16 == 0) p.out_sumsq[static_cast<size_t>(tile) * p.M + row] = ss;
     }
     return;
   }
   if (p.mode == kSwiGLU) {
-    // thread: one row, 8 of the tile's 128 (gate, up) column pairs
-    const int rr = t / 16, j0 = (t % 16) * 8;
-    const int row = r0 + rr;
-    if (row >= r_end) return;
-    const float r = rs ? rs[rr] : 1.f;
+    if (!valid) return;
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float a2[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int j = j0 + 2 * e + h;
-        const float g = s_sum[rr * kBN + j] * r;
-        const float u = s_sum[rr * kBN + 128 + j] * r;
+        const float g = a[2 * e + h] * r, u = b[2 * e + h] * r;
         a2[h] = g / (1.f + expf(-g)) * u;
       }
       o[e] = pack_bf16x2(a2[0], a2[1]);
     }
-    *reinterpret_cast<uint4*>(p.act + static_cast<size_t>(row) * p.inter +
-                              static_cast<size_t>(tile) * 128 + j0) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(p.act + static_cast<size_t>(row) * p.inter + static_cast<size_t>(tile) * 128 +
+                              col_a) = make_uint4(o[0], o[1], o[2], o[3]);
     return;
   }
-  // kQKV: the tile is two heads of one segment (q, k or v); eight threads
-  // share a (row, head), each holding dims j0..j0+7 and their RoPE partners
-  // j0+64..j0+71
-  const int rr = t / 16, hh = (t / 8) % 2, sub = t % 8;
-  const int row = r0 + rr;
+  // kQKV: the tile is two heads of one segment (q, k or v)
+  const int hh = col_a / kHeadDim, j0 = col_a % kHeadDim;
   const int col0 = tile * kBN + hh * kHeadDim;  // first column of this head in q|k|v
   const int qcols = p.Hq * kHeadDim, kcols = p.Hkv * kHeadDim;
   const int seg = col0 < qcols ? 0 : (col0 < qcols + kcols ? 1 : 2);
   const int head = seg == 0 ? col0 / kHeadDim
                             : (seg == 1 ? (col0 - qcols) / kHeadDim : (col0 - qcols - kcols) / kHeadDim);
-  const float r = rs ? rs[rr] : 1.f;
-  const int j0 = sub * 8;
-  float a[8], b[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    a[e] = s_sum[rr * kBN + hh * kHeadDim + j0 + e] * r;
-    b[e] = s_sum[rr * kBN + hh * kHeadDim + 64 + j0 + e] * r;
+    a[e] *= r;
+    b[e] *= r;
   }
   const float* gnorm = seg == 0 ? p.q_norm : (seg == 1 ? p.k_norm : nullptr);
   if (gnorm) {  // per-head RMSNorm over the 128 dims (8 threads, consecutive lanes)
@@ -205,7 +221,7 @@ __device__ void epilogue_rows(const DenseParams& p, const float* s_sum, const fl
       b[e] *= inv * gnorm[64 + j0 + e];
     }
   }
-  if (row >= r_end) return;
+  if (!valid) return;
   if (seg > 0 && (T < 0 || T + row >= p.t_cap)) {  // the rows' K/V slots must exist
     report(GLANCE_DEV_TREE_CAPACITY);
     return;
@@ -253,9 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sB = smem + kStages * kABytes;
   Bars* bars = reinterpret_cast<Bars*>(smem + kStageArea);
   // after phase 1 the stage area receives the cluster's partials of this
-  // CTA's rows, then holds the chunk sums
+  // CTA's rows
   float* s_recv = reinterpret_cast<float*>(smem);
-  float* s_sum = reinterpret_cast<float*>(smem + kRecvBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.split;
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], p.norm_input ? 5 : 1);  // the MMA commit (+ warps 4..7)
+      mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->drain, 1);
@@ -321,7 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------ phase 1
   bool ok = true;
-  float row_ss = 0.f;
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
@@ -372,36 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    // one input row per thread: its sum of squares over this K range, from the
-    // A stages (the 128-byte swizzle permutes 16-byte chunks within a row only)
-    const int row = (warp - 4) * 32 + lane;
-    if (p.norm_input) {
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % kStages;
-        const bool got = wait_or_abort(&bars->full[st], (it / kStages) & 1, bars);
-        if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
-          ok = false;
-          break;
-        }
-        if (row < p.M) {
-          const uint4* src = reinterpret_cast<const uint4*>(sA + st * kABytes + row * 128);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = src[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-              row_ss += lo * lo + hi * hi;
-            }
-          }
-        }
-        __syncwarp();  // one arrival per warp, once every lane has read the stage
-        if (lane == 0 && it + kStages < n_it) mbar_arrive(&bars->empty[st]);
-      }
+    if (!wait_or_abort(&bars->acc_full, 0, bars)) {
+      ok = false;
+      fail_pipeline(bars);
     }
-    if (ok && !wait_or_abort(&bars->acc_full, 0, bars)) ok = false;
-    if (!ok) fail_pipeline(bars);
   }
   // every role is done with its own stage area (or gave up and drained)
   const bool bad = __syncthreads_or(!ok || *reinterpret_cast<volatile int*>(&bars->abort_flag)) != 0;
@@ -436,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       }
     }
-    if (p.norm_input && row < p.M) dsmem_st_f32(dsmem_addr(&bars->recv_ss[slot], owner), row_ss);
   }
   tc_fence_before();
   __syncthreads();
@@ -452,49 +439,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = p.mode == kQKV ? *p.t_len : 0;
     const int r_begin = rank * rows_per;
     const int r_end = min(p.M, r_begin + rows_per);
-    for (int r0 = r_begin; r0 < r_end; r0 += kChunkRows) {
-      if (p.norm_input && threadIdx.x < kChunkRows) {
-        const int lrow = r0 - r_begin + threadIdx.x;
+    if (p.in_sumsq) {
+      for (int lrow = threadIdx.x; lrow < r_end - r_begin; lrow += kThreads) {
         float ss = 0.f;
-        if (r0 + static_cast<int>(threadIdx.x) < r_end)
-          for (int s = 0; s < S; ++s) ss += bars->recv_ss[s * rows_per + lrow];
-        bars->r[threadIdx.x] = rsqrtf(ss / p.K + p.eps);
+        for (int t = 0; t < p.n_sumsq; ++t) ss += p.in_sumsq[static_cast<size_t>(t) * p.M + r_begin + lrow];
+        bars->r[lrow] = rsqrtf(ss / p.K + p.eps);
       }
-      // thread: one row, 16 columns; sum over the cluster's partials
-      const int rr = threadIdx.x / 16, c0 = (threadIdx.x % 16) * 16;
-      const int lrow = r0 - r_begin + rr;
-      float acc[16];
+      __syncthreads();
+    }
+    int col_a, col_b;
+    epilogue_cols(p.mode, threadIdx.x, col_a, col_b);
+    for (int r0 = r_begin; r0 < r_end; r0 += kChunkRows) {
+      // thread: one row, two groups of 8 columns; sum over the cluster's partials
+      const int row = r0 + static_cast<int>(threadIdx.x) / 16;
+      const bool valid = row < r_end;
+      const int lrow = valid ? row - r_begin : 0;
+      float a[8], b[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-      if (r0 + rr < r_end) {
+      for (int e = 0; e < 8; ++e) a[e] = b[e] = 0.f;
+      if (valid) {
         for (int s = 0; s < S; ++s) {
-          const float4* src = reinterpret_cast<const float4*>(s_recv + (s * rows_per + lrow) * kPartStride + c0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float4 x = src[v];
-            acc[4 * v] += x.x;
-            acc[4 * v + 1] += x.y;
-            acc[4 * v + 2] += x.z;
-            acc[4 * v + 3] += x.w;
-          }
+          const float* src = s_recv + (s * rows_per + lrow) * kPartStride;
+          const float4 a0 = *reinterpret_cast<const float4*>(src + col_a);
+          const float4 a1 = *reinterpret_cast<const float4*>(src + col_a + 4);
+          const float4 b0 = *reinterpret_cast<const float4*>(src + col_b);
+          const float4 b1 = *reinterpret_cast<const float4*>(src + col_b + 4);
+          a[0] += a0.x, a[1] += a0.y, a[2] += a0.z, a[3] += a0.w;
+          a[4] += a1.x, a[5] += a1.y, a[6] += a1.z, a[7] += a1.w;
+          b[0] += b0.x, b[1] += b0.y, b[2] += b0.z, b[3] += b0.w;
+          b[4] += b1.x, b[5] += b1.y, b[6] += b1.z, b[7] += b1.w;
         }
       }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) s_sum[rr * kBN + c0 + e] = acc[e];
-      __syncthreads();
-      epilogue_rows(p, s_sum, p.norm_input ? bars->r : nullptr, tile, r0, r_end, T);
-      __syncthreads();
+      const float r = p.in_sumsq && valid ? bars->r[lrow] : 1.f;
+      epilogue_regs(p, a, b, r, tile, row, valid, T);
     }
   }
 }
 
-// 1 / sqrt(mean(x^2) + eps) per row; one warp per row.
-__global__ void rms_scale_kernel(const __nv_bfloat16* x, int M, int d, float eps, float* r) {
+// sumsq[row] = sum_k x[row][k]^2; one warp per row.
+__global__ void row_sumsq_kernel(const __nv_bfloat16* x, int M, int d, float* sumsq) {
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
   const __nv_bfloat16* xr = x + static_cast<size_t>(row) * d;
   float s = 0.f;
+#pragma unroll 4
   for (int c = lane * 8; c < d; c += 32 * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -506,7 +495,7 @@ __global__ void rms_scale_kernel(const __nv_bfloat16* x, int M, int d, float eps
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) r[row] = rsqrtf(s / d + eps);
+  if (lane == 0) sumsq[row] = s;
 }
 
 // Clusters of `size` CTAs of dense_kernel that fit on the device at once
@@ -624,21 +613,21 @@ DenseParams blank_params() {
 
 }  // namespace
 
-extern "C" glance_status glance_rms_scale(const void* x, int M, int d, float eps, float* r_out,
-                                          void* stream) {
+extern "C" glance_status glance_row_sumsq(const void* x, int M, int d, float* sumsq, void* stream) {
   using glance::fail;
-  if (!x || !r_out) return fail(GLANCE_ERR_INVALID_ARG, "glance_rms_scale: null pointer argument");
+  if (!x || !sumsq) return fail(GLANCE_ERR_INVALID_ARG, "glance_row_sumsq: null pointer argument");
   if (M < 1 || d < 8 || d % 8 || !glance::aligned16(x))
-    return fail(GLANCE_ERR_INVALID_ARG, "glance_rms_scale: need M >= 1, d % 8 == 0, 16-byte aligned x");
-  rms_scale_kernel<<<(M + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(x), M, d, eps, r_out);
+    return fail(GLANCE_ERR_INVALID_ARG, "glance_row_sumsq: need M >= 1, d %% 8 == 0, 16-byte aligned x");
+  row_sumsq_kernel<<<(M + 3) / 4, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), M, d, sumsq);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_rms_scale");
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_row_sumsq");
   return GLANCE_OK;
 }
 
 extern "C" glance_status glance_dense_residual(const void* x, const void* W, int M, int K, int N,
-                                               const void* residual, void* out, void* stream) {
+                                               const void* residual, void* out, float* out_sumsq,
+                                               void* stream) {
   using glance::fail;
   const char* who = "glance_dense_residual";
   if (!x || !W || !residual || !out) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
@@ -650,20 +639,23 @@ extern "C" glance_status glance_dense_residual(const void* x, const void* W, int
   p.res = static_cast<const __nv_bfloat16*>(residual);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.n_out = N;
+  p.out_sumsq = out_sumsq;
   return run_dense(who, x, M, K, W, W, N, N / kBN, p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" glance_status glance_dense_swiglu(const void* h, const void* W_gate, const void* W_up,
-                                             int M, int d, int inter, int norm_input, float eps,
-                                             void* act, void* stream) {
+                                             int M, int d, int inter, const float* in_sumsq,
+                                             int n_sumsq, float eps, void* act, void* stream) {
   using glance::fail;
   const char* who = "glance_dense_swiglu";
   if (!h || !W_gate || !W_up || !act) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
   if (inter < 128 || inter % 128) return fail(GLANCE_ERR_UNSUPPORTED, "%s: inter must be a multiple of 128", who);
   if (!glance::aligned16(act)) return fail(GLANCE_ERR_INVALID_ARG, "%s: act must be 16-byte aligned", who);
   DenseParams p = blank_params();
+  if (in_sumsq && n_sumsq < 1) return fail(GLANCE_ERR_INVALID_ARG, "%s: n_sumsq must be >= 1", who);
   p.mode = kSwiGLU;
-  p.norm_input = norm_input ? 1 : 0;
+  p.in_sumsq = in_sumsq;
+  p.n_sumsq = n_sumsq;
   p.eps = eps;
   p.act = static_cast<__nv_bfloat16*>(act);
   p.inter = inter;
@@ -671,7 +663,8 @@ extern "C" glance_status glance_dense_swiglu(const void* h, const void* W_gate, 
 }
 
 extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int M, int d, int n_q_heads,
-                                          int norm_input, const float* q_norm, const float* k_norm,
+                                          const float* in_sumsq, int n_sumsq, const float* q_norm,
+                                          const float* k_norm,
                                           float eps, const int32_t* pos_id, float rope_theta,
                                           void* q_out, const glance_kv* kv, void* stream) {
   using glance::fail;
@@ -688,9 +681,11 @@ extern "C" glance_status glance_dense_qkv(const void* h, const void* W_qkv, int 
       kv->row_stride < kHeadDim || (kv->row_stride * 2) % 16 || (kv->head_stride * 2) % 16 ||
       kv->head_stride < static_cast<int64_t>(kv->t_cap) * kv->row_stride || kv->t_cap < M)
     return fail(GLANCE_ERR_INVALID_ARG, "%s: bad q_out / cache layout", who);
+  if (in_sumsq && n_sumsq < 1) return fail(GLANCE_ERR_INVALID_ARG, "%s: n_sumsq must be >= 1", who);
   DenseParams p = blank_params();
   p.mode = kQKV;
-  p.norm_input = norm_input ? 1 : 0;
+  p.in_sumsq = in_sumsq;
+  p.n_sumsq = n_sumsq;
   p.Hq = n_q_heads;
   p.Hkv = Hkv;
   p.q_norm = q_norm;
