@@ -32,6 +32,8 @@ FULL36 = dict(name="full36", T=4096, N=63, L=15, V=151936, d=4096, n_layers=36, 
               D=128, path_depth=(3, 15))
 SMALL = dict(name="small", T=512, N=31, L=15, V=16384, d=512, n_layers=4, Hq=32, Hkv=8, D=128,
              path_depth=(3, 15))
+FORWARD36 = dict(name="forward36", T=4096, N=63, L=15, V=151936, d=4096, n_layers=36, Hq=32, Hkv=8,
+                 D=128, inter=12288, rope_theta=1e6, eps=1e-6, path_depth=(3, 15))
 RAGGED8 = dict(name="ragged8", B=8, T_range=(512, 8192), entropy=(0.3, 1.5, 4.0), N=63, L=15,
                V=151936, d=4096, n_layers=36, Hq=32, Hkv=8, D=128, path_depth=(3, 15))
 
@@ -439,6 +441,104 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "sampler": src}
 
 
+class ForwardWorkload:
+    """The whole verify forward of one round on a Qwen3-8B-shaped target:
+    tree build, then per layer the dense calls around tree attention (QKV with
+    q/k norm and RoPE into the layer's cache, attention, output projection,
+    SwiGLU, down projection; RMSNorm row scales from the residual projections'
+    row sums of squares), the LM head with argmax on the last layer's rows, and
+    the walk + commit. Weights, input rows and K/V are drawn on the device from
+    a seeded torch generator (N(0, 0.02) weights, N(0, 1) rows and K/V); the
+    RMSNorm gains are taken as already folded into the next projection's rows.
+    The final norm's row scale is left out: a positive per-row scale does not
+    move a row's argmax."""
+
+    def __init__(self, cfg, dev, seed=7000):
+        import torch
+        import tree_verified_block_gb300 as g
+        self.cfg, self.dev, self.g = cfg, dev, g
+        c = cfg
+        R = c["N"] + 1
+        self.R = R
+        t_cap = c["T"] + R + 64
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+
+        def w(k, n):
+            return (torch.randn(k, n, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+
+        d, I, D = c["d"], c["inter"], c["D"]
+        qkv_cols = (c["Hq"] + 2 * c["Hkv"]) * D
+        self.Wqkv = [w(d, qkv_cols) for _ in range(c["n_layers"])]
+        self.Wo = [w(c["Hq"] * D, d) for _ in range(c["n_layers"])]
+        self.Wg = [w(d, I) for _ in range(c["n_layers"])]
+        self.Wu = [w(d, I) for _ in range(c["n_layers"])]
+        self.Wd = [w(I, d) for _ in range(c["n_layers"])]
+        self.W = w(d, c["V"])
+        self.k = [torch.randn(c["Hkv"], t_cap, D, generator=gen, device=dev).to(torch.bfloat16)
+                  for _ in range(c["n_layers"])]
+        self.v = [torch.randn(c["Hkv"], t_cap, D, generator=gen, device=dev).to(torch.bfloat16)
+                  for _ in range(c["n_layers"])]
+        self.x_dev = torch.from_numpy(W.draft_logits_planted(c["L"], c["V"], seed=seed + 1)).to(dev)
+        self.emb = torch.randn(R, d, generator=gen, device=dev).to(torch.bfloat16)
+        self.t0 = torch.tensor([c["T"]], dtype=torch.int32, device=dev)
+        self.t_len = self.t0.clone()
+        self.root = torch.tensor([1234], dtype=torch.int32, device=dev)
+        self.layers = [g.KVLayer(k, v, self.t_len) for k, v in zip(self.k, self.v)]
+        self.tree = g.Tree(c["N"], c["L"], dev)
+        self.xa = torch.empty(R, d, **bf)
+        self.q = torch.empty(R, c["Hq"], D, **bf)
+        self.att = torch.empty(R, c["Hq"], D, **bf)
+        self.act = torch.empty(R, I, **bf)
+        self.ss0 = torch.empty(R, dtype=torch.float32, device=dev)
+        self.ss_a = torch.empty(d // 256, R, dtype=torch.float32, device=dev)
+        self.ss_b = torch.empty(d // 256, R, dtype=torch.float32, device=dev)
+        self.argmax = torch.empty(R, dtype=torch.int32, device=dev)
+        self.gap = torch.empty(R, dtype=torch.float32, device=dev)
+        self.maxlogit = torch.empty(R, dtype=torch.float32, device=dev)
+        self.n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.acc_tok = torch.zeros(c["L"], dtype=torch.int32, device=dev)
+        self.new_root = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws_tree = g.workspace(g.build_tree_workspace_bytes(c["L"], c["V"], c["N"]), dev)
+        self.ws_attn = g.workspace(g.tree_attention_workspace_bytes(R, c["Hq"], self.layers[0]), dev)
+        self.ws_lm = g.workspace(g.lmhead_argmax_workspace_bytes(R, d, c["V"], torch.bfloat16), dev)
+        self.ws_c = g.workspace(g.accept_commit_workspace_bytes(c["n_layers"]), dev)
+
+    def layer(self, l):
+        """One decoder layer over the packed rows (layer 0 reads the input rows)."""
+        g, c = self.g, self.cfg
+        x_in, ss_in = (self.emb, self.ss0) if l == 0 else (self.xa, self.ss_b)
+        g.dense_qkv(x_in, self.Wqkv[l], c["Hq"], ss_in, None, None, c["eps"], self.tree.pos_id,
+                    c["rope_theta"], self.q, self.layers[l])
+        g.tree_attention(self.q, self.layers[l], self.tree, c["D"] ** -0.5, self.att, self.ws_attn)
+        g.dense_residual(self.att.view(self.R, -1), self.Wo[l], x_in, self.xa, self.ss_a)
+        g.dense_swiglu(self.xa, self.Wg[l], self.Wu[l], self.ss_a, c["eps"], self.act)
+        g.dense_residual(self.act, self.Wd[l], self.xa, self.xa, self.ss_b)
+
+    def step(self):
+        g, c = self.g, self.cfg
+        self.t_len.copy_(self.t0)
+        g.build_tree(self.x_dev, c["N"], self.root, self.t_len, self.tree, self.ws_tree)
+        g.row_sumsq(self.emb, self.ss0)
+        for l in range(c["n_layers"]):
+            self.layer(l)
+        g.lmhead_argmax(self.xa, self.W, self.argmax, self.gap, self.maxlogit, self.ws_lm)
+        g.accept_commit(self.tree, self.argmax, self.layers, self.n_acc, self.acc_tok,
+                        self.new_root, self.ws_c)
+
+    def launches_per_step(self):
+        return 2 + 5 * self.cfg["n_layers"] + 2
+
+    def algorithmic_bytes(self):
+        c = self.cfg
+        R, d, I, D = self.R, c["d"], c["inter"], c["D"]
+        dense = (d * (c["Hq"] + 2 * c["Hkv"]) * D + c["Hq"] * D * d + 3 * d * I) * 2
+        attn = (c["T"] + R) * c["Hkv"] * D * 2 * 2 + 2 * R * c["Hq"] * D * 2
+        return dict(dense_layer=dense, attn_layer=attn, lmhead=d * c["V"] * 2 + R * d * 2,
+                    tree=c["L"] * c["V"] * 4)
+
+
 # ------------------------------------------------------------------ timing
 
 def graph_time_us(fn, reps=20):
@@ -532,6 +632,49 @@ def run_batched(dev, reps=10):
            "lmhead_m512_hbm_frac": round(by["lmhead"] / (st["lmhead_m512"] * 1e-6) / 1e9 / pk["hbm"], 4),
            "data": "synthetic, q/K/V/W drawn on the device (seeded torch generator)"}
     return out
+
+
+def run_forward(dev, reps=10):
+    """The whole verify forward (forward36; secondary measurement): the round
+    and its stages from CUDA-graph replays, each against the HBM roof of its
+    algorithmic bytes."""
+    import torch
+    fw = ForwardWorkload(FORWARD36, dev)
+    c = fw.cfg
+    for _ in range(3):
+        fw.step()
+    torch.cuda.synchronize()
+    st = {"round": graph_time_us(fw.step, reps)}
+    n = c["n_layers"]
+    g = fw.g
+    # each stage over all n layers' weights (distinct, > L2 in total), per launch
+    per = lambda fn: graph_time_us(lambda: [fn(l) for l in range(n)], reps) / n
+    st["layer"] = per(fw.layer)
+    st["qkv"] = per(lambda l: g.dense_qkv(fw.xa, fw.Wqkv[l], c["Hq"], fw.ss_b, None, None, c["eps"],
+                                          fw.tree.pos_id, c["rope_theta"], fw.q, fw.layers[l]))
+    st["attention"] = per(lambda l: g.tree_attention(fw.q, fw.layers[l], fw.tree, c["D"] ** -0.5, fw.att,
+                                                     fw.ws_attn))
+    st["o_proj"] = per(lambda l: g.dense_residual(fw.att.view(fw.R, -1), fw.Wo[l], fw.emb, fw.xa, fw.ss_a))
+    st["swiglu"] = per(lambda l: g.dense_swiglu(fw.xa, fw.Wg[l], fw.Wu[l], fw.ss_a, c["eps"], fw.act))
+    st["down_proj"] = per(lambda l: g.dense_residual(fw.act, fw.Wd[l], fw.emb, fw.xa, fw.ss_b))
+    pk = peaks()
+    by = fw.algorithmic_bytes()
+    total = n * (by["dense_layer"] + by["attn_layer"]) + by["lmhead"] + by["tree"]
+    frac = lambda b, us: round(b / (us * 1e-6) / 1e9 / pk["hbm"], 4)
+    d, I, D = c["d"], c["inter"], c["D"]
+    return {"workload": f"forward36: Qwen3-8B-shaped target, {n} layers (d={d}, {c['Hq']}/{c['Hkv']} heads, "
+                        f"head_dim {D}, inter={I}), T={c['T']}, N={c['N']} (M={fw.R} rows), V={c['V']}",
+            "rounds_per_s": round(1e6 / st["round"], 2),
+            "stages_us": {k: round(v, 2) for k, v in st.items()},
+            "round_bytes": total,
+            "round_hbm_frac": frac(total, st["round"]),
+            "layer_hbm_frac": frac(by["dense_layer"] + by["attn_layer"], st["layer"]),
+            "qkv_hbm_frac": frac(d * (c["Hq"] + 2 * c["Hkv"]) * D * 2, st["qkv"]),
+            "o_proj_hbm_frac": frac(c["Hq"] * D * d * 2, st["o_proj"]),
+            "swiglu_hbm_frac": frac(2 * d * I * 2, st["swiglu"]),
+            "down_proj_hbm_frac": frac(I * d * 2, st["down_proj"]),
+            "gpu_launches_per_round": fw.launches_per_step(),
+            "data": "synthetic, random-init weights, rows and K/V drawn on the device (seeded torch generator)"}
 
 
 def run_case(args):
@@ -650,6 +793,7 @@ def run_gpu(args):
 
     e2e = run_e2e(wl, args.steps)
     batched = run_batched(dev) if (args.batched and rank == 0) else None
+    forward = run_forward(dev) if (args.forward and rank == 0) else None
     code, text = g.device_status()
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": world,
@@ -666,6 +810,8 @@ def run_gpu(args):
     }
     if batched is not None:
         out["ragged8"] = batched
+    if forward is not None:
+        out["forward36"] = forward
     if rank == 0:
         if args.cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(cfg, wl)
@@ -821,6 +967,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--case", default=None, choices=["lmhead512"],
                     help="run one kernel alone on a small case (for profiler captures)")
+    ap.add_argument("--no-forward", dest="forward", action="store_false",
+                    help="skip the forward36 secondary measurement (verify forward with the dense layers)")
     ap.add_argument("--no-batched", dest="batched", action="store_false",
                     help="skip the secondary ragged8 batched-round measurement")
     args = ap.parse_args()
