@@ -154,6 +154,12 @@ size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_heads, const gl
  * out: [N+1][n_q_heads][head_dim], same dtype (bf16 rounded to nearest even).
  * Supported: BF16 with head_dim 128, n_q_heads / n_kv_heads in {1,2,4,8},
  * N + 1 <= 256; F32 with head_dim a multiple of 32 up to 128.
+ * The BF16 call is a programmatic dependent of the previous kernel in the
+ * stream: it may read T and the cache prefix (slots < T) before that kernel
+ * has finished, when that kernel lets dependents start early (this library's
+ * attention and dense calls do; they never write T or the prefix). q and the
+ * tree rows' K/V are read only after it has finished. A T that changes in
+ * between sets device status 3 and the call writes nothing.
  */
 glance_status glance_tree_attention(const void* q, int n_q_heads, const glance_kv* kv,
                                     const glance_tree* tree, float scale, void* out,

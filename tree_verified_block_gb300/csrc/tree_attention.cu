@@ -142,6 +142,7 @@ constexpr int kD = 128;          // head_dim
 constexpr int kBM = 128;         // query rows per tile (MMA M)
 constexpr int kBN = 128;         // key slots per tile (MMA N of S, K of PV)
 constexpr int kStages = 3;       // K/V ring depth
+constexpr int kPreTiles = 1;     // prefix key tiles fetched before the dependency wait
 constexpr int kThreads = 384;    // 12 warps: TMA, MMA, TMEM, idle, 2 x 4 softmax
 constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64 used)
 constexpr int kMaxSplit = 16;    // key splits of one (kv head, q tile)
@@ -391,6 +392,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // The cache prefix (slots < T) and T itself are written only by calls that
+  // let no kernel start early (accept_commit), so the first key tile that
+  // lies wholly inside the prefix can be fetched before the wait; tiles that
+  // hold tree rows (written by the previous kernel) wait for it.
+  int pre = 0, T_pre = -1;
+  if (threadIdx.x == 0) {
+    T_pre = *p.t_len[req];
+    if (T_pre >= 0 && T_pre + p.rows <= p.t_cap[req]) {
+      const int nt = (T_pre + p.rows + kBN - 1) / kBN;
+      const int t0 = static_cast<int>((static_cast<long long>(nt) * split) / n_split);
+      const int t1 = static_cast<int>((static_cast<long long>(nt) * (split + 1)) / n_split);
+      const uint64_t pol_kv = policy_evict_first();
+      for (int j = 0; j < kPreTiles && j < t1 - t0; ++j) {
+        const int key0 = (t0 + j) * kBN;
+        if (key0 + kBN > T_pre) break;
+        unsigned char* stage = sKV + j * kKVStageBytes;
+        mbar_arrive_expect_tx(&bars->k_full[j], 2 * kHalfBytes);
+        tma_load_3d(stage + 0 * kHalfBytes, map_k, &bars->k_full[j], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 1 * kHalfBytes, map_k, &bars->k_full[j], 64, key0, g, pol_kv);
+        mbar_arrive_expect_tx(&bars->v_full[j], 2 * kHalfBytes);
+        tma_load_3d(stage + 2 * kHalfBytes, map_v, &bars->v_full[j], 0, key0, g, pol_kv);
+        tma_load_3d(stage + 3 * kHalfBytes, map_v, &bars->v_full[j], 64, key0, g, pol_kv);
+        ++pre;
+      }
+    }
+  }
   pdl_wait_prior();
 
   // Q does not depend on T: its copy goes out before T is read, so the two
@@ -412,7 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int T = *p.t_len[req];
-  const bool room = T >= 0 && T + p.rows <= p.t_cap[req];
+  // T is not written while a call can still be starting; a caller that breaks
+  // that has the call give up (its prefetched tiles would be the wrong ones)
+  const bool raced = __syncthreads_or(threadIdx.x == 0 && pre > 0 && T != T_pre) != 0;
+  if (raced && threadIdx.x == 0) report(GLANCE_DEV_BAD_TREE);
+  const bool room = !raced && T >= 0 && T + p.rows <= p.t_cap[req];
   // key tiles of this split over slots [0, T + rows)
   const int n_keys = room ? T + p.rows : 0;
   const int n_tiles = (n_keys + kBN - 1) / kBN;
@@ -420,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile1 = static_cast<int>((static_cast<long long>(n_tiles) * (split + 1)) / n_split);
   const int my_tiles = tile1 - tile0;
 
-  if (threadIdx.x == 0 && !room && local == 0) report(GLANCE_DEV_TREE_CAPACITY);
+  if (threadIdx.x == 0 && !room && !raced && local == 0) report(GLANCE_DEV_TREE_CAPACITY);
   // query pieces of this tile that hold no real (head, row): zero them so the
   // MMA reads finite values
   {
@@ -461,13 +492,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && my_tiles == 0) {
-      // Q was issued before T was known: let it land before the CTA exits
+      // Q was issued before T was known (and prefix tiles before the wait):
+      // let them land before the CTA exits
       (void)mbar_wait(&bars->q_full, 0, 50000000ull);
+      for (int j = 0; j < pre; ++j) {
+        (void)mbar_wait(&bars->k_full[j], 0, 50000000ull);
+        (void)mbar_wait(&bars->v_full[j], 0, 50000000ull);
+      }
     }
     if (lane == 0 && my_tiles > 0) {
       const uint64_t pol_kv = policy_evict_first();
-      int issued = 0;
-      for (int j = 0; j < my_tiles; ++j) {
+      int issued = pre;
+      for (int j = pre; j < my_tiles; ++j) {
         const int st = j % kStages;
         // Every CTA of the grid starts at once: the first tile of all of them
         // goes out alone, so that Q and K/V of tile 0 land (and the first MMA
