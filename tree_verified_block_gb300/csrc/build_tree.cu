@@ -290,11 +290,6 @@ struct TreeSmem {
   int16_t p_pos[kMaxN];
 };
 
-__device__ __forceinline__ void set_reg(uint32_t (&a)[kSlotsPerLane], int i, uint32_t v) {
-#pragma unroll
-  for (int t = 0; t < kSlotsPerLane; ++t)
-    if (t == i) a[t] = v;
-}
 __device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlotsPerLane], int i) {
   uint32_t v = 0;
 #pragma unroll
@@ -396,6 +391,39 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
       ko[0] = ord_key(s_logq[0]);
       kc[0] = kRootChild;
     }
+    // node data of a code
+    auto node_of = [&](uint32_t code, PopRec& nd) {
+      if (code == kRootChild) {
+        nd.pscore = 0.f;
+        nd.dep = 1;
+        nd.par = -1;
+        nd.hi = nd.lo = 0ull;
+        return;
+      }
+      const PopRec g = ts.pop[code >> 1];
+      if ((code & 1u) == 0) {  // first child: rank 0 appended (a zero byte)
+        nd.pscore = g.score;
+        nd.dep = g.dep + 1;
+        nd.par = static_cast<int>(code >> 1);
+        nd.hi = g.hi;
+        nd.lo = g.lo;
+      } else {  // next sibling: the last rank + 1
+        nd.pscore = g.pscore;
+        nd.dep = g.dep;
+        nd.par = g.par;
+        nd.hi = g.hi;
+        nd.lo = g.lo;
+        set_rank(nd.hi, nd.lo, g.dep - 1, get_rank(g.hi, g.lo, g.dep - 1) + 1);
+      }
+    };
+    // scores of a node's successors: first child (rank 0 at offset d + 1)
+    // and next sibling (rank r + 1)
+    auto successors = [&](const PopRec& nd, float& c_score, float& s_score) {
+      const int d = nd.dep;
+      const uint32_t r = get_rank(nd.hi, nd.lo, d - 1);
+      c_score = d < L ? nd.score + s_logq[d * K] : 0.f;
+      s_score = static_cast<int>(r) + 1 < K ? nd.pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
+    };
     int cnt = 1;
     for (int k = 0; k < N; ++k) {
       uint32_t bo = 0;
@@ -413,6 +441,20 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
         }
       }
       const uint32_t mmax = __reduce_max_sync(0xffffffffu, bo);
+      // every lane works out its best slot's node and successor scores while
+      // the warp's maximum is in flight (the winner's come by shuffle)
+      PopRec nd;
+      float c_score = 0.f, s_score = 0.f;
+      if (bo != 0) {
+        node_of(get_reg(kc, bi), nd);
+        nd.score = inv_ord_key(bo);
+        successors(nd, c_score, s_score);
+      } else {
+        nd.score = nd.pscore = 0.f;
+        nd.dep = 1;
+        nd.par = -1;
+        nd.hi = nd.lo = 0ull;
+      }
       if (mmax == 0) {  // frontier exhausted: the host checks make this unreachable
         if (lane == 0) report(GLANCE_DEV_BAD_TREE);
         break;
@@ -421,37 +463,17 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
       const bool slow = __popc(cand) > 1 || __ballot_sync(0xffffffffu, bo == mmax && dup) != 0;
       int ws;       // winning slot
       uint32_t wc;  // its code
-      // node data of a code (all lanes compute it for the same code)
-      auto node_of = [&](uint32_t code, uint32_t key, PopRec& nd) {
-        if (code == kRootChild) {
-          nd.score = s_logq[0];
-          nd.pscore = 0.f;
-          nd.dep = 1;
-          nd.par = -1;
-          nd.hi = nd.lo = 0ull;
-          return;
-        }
-        const PopRec g = ts.pop[code >> 1];
-        nd.score = __uint_as_float(key);  // placeholder, replaced by the caller
-        if ((code & 1u) == 0) {  // first child: rank 0 appended (a zero byte)
-          nd.pscore = g.score;
-          nd.dep = g.dep + 1;
-          nd.par = static_cast<int>(code >> 1);
-          nd.hi = g.hi;
-          nd.lo = g.lo;
-        } else {  // next sibling: the last rank + 1
-          nd.pscore = g.pscore;
-          nd.dep = g.dep;
-          nd.par = g.par;
-          nd.hi = g.hi;
-          nd.lo = g.lo;
-          set_rank(nd.hi, nd.lo, g.dep - 1, get_rank(g.hi, g.lo, g.dep - 1) + 1);
-        }
-      };
       if (!slow) {
         const int win = __ffs(cand) - 1;
         ws = __shfl_sync(0xffffffffu, bi * 32 + lane, win);
         wc = __shfl_sync(0xffffffffu, get_reg(kc, bi), win);
+        nd.pscore = __shfl_sync(0xffffffffu, nd.pscore, win);
+        nd.dep = __shfl_sync(0xffffffffu, nd.dep, win);
+        nd.par = __shfl_sync(0xffffffffu, nd.par, win);
+        nd.hi = __shfl_sync(0xffffffffu, nd.hi, win);
+        nd.lo = __shfl_sync(0xffffffffu, nd.lo, win);
+        c_score = __shfl_sync(0xffffffffu, c_score, win);
+        s_score = __shfl_sync(0xffffffffu, s_score, win);
       } else {
         // exact score tie: least (depth, rank vector) among slots with key mmax
         int my = -1;
@@ -460,14 +482,14 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
 #pragma unroll
         for (int i = 0; i < kSlotsPerLane; ++i) {
           if (ko[i] == mmax) {
-            PopRec nd;
-            node_of(kc[i], ko[i], nd);
-            if (my < 0 || tie_less(nd.dep, nd.hi, nd.lo, md, mh, ml)) {
+            PopRec t;
+            node_of(kc[i], t);
+            if (my < 0 || tie_less(t.dep, t.hi, t.lo, md, mh, ml)) {
               my = i * 32 + lane;
               mc = kc[i];
-              md = nd.dep;
-              mh = nd.hi;
-              ml = nd.lo;
+              md = t.dep;
+              mh = t.hi;
+              ml = t.lo;
             }
           }
         }
@@ -488,17 +510,15 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
         }
         ws = my;
         wc = mc;
+        node_of(wc, nd);
+        nd.score = inv_ord_key(mmax);
+        successors(nd, c_score, s_score);
       }
-      PopRec nd;
-      node_of(wc, mmax, nd);
       nd.score = inv_ord_key(mmax);
-      const uint32_t d = static_cast<uint32_t>(nd.dep);
+      const int d = nd.dep;
       const uint32_t r = get_rank(nd.hi, nd.lo, d - 1);
-      const bool has_child = static_cast<int>(d) < L;
+      const bool has_child = d < L;
       const bool has_sib = static_cast<int>(r) + 1 < K;
-      // successors: first child (rank 0 at offset d+1), next sibling (rank r+1)
-      const float c_score = has_child ? nd.score + s_logq[d * K] : 0.f;
-      const float s_score = has_sib ? nd.pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
       if (lane == 0) {
         uint4* dst = reinterpret_cast<uint4*>(&ts.pop[k]);
         dst[0] = make_uint4(__float_as_uint(nd.score), __float_as_uint(nd.pscore),
@@ -507,19 +527,18 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
                             static_cast<uint32_t>(nd.lo), static_cast<uint32_t>(nd.lo >> 32));
       }
       // the popped slot takes the child (else the sibling); a new slot takes
-      // the sibling when both exist
+      // the sibling when both exist (predicated, no divergence)
       const uint32_t k_ws = has_child ? ord_key(c_score) : (has_sib ? ord_key(s_score) : 0u);
       const uint32_t c_ws = (static_cast<uint32_t>(k) << 1) | (has_child ? 0u : 1u);
-      if (lane == (ws & 31)) {
-        set_reg(ko, ws >> 5, k_ws);
-        set_reg(kc, ws >> 5, c_ws);
-      }
-      if (has_child && has_sib) {
-        const int ns = cnt++;
-        if (lane == (ns & 31)) {
-          set_reg(ko, ns >> 5, ord_key(s_score));
-          set_reg(kc, ns >> 5, (static_cast<uint32_t>(k) << 1) | 1u);
-        }
+      const bool both = has_child && has_sib;
+      const int ns = both ? cnt : -1;
+      cnt += both ? 1 : 0;
+      const uint32_t k_ns = ord_key(s_score), c_ns = (static_cast<uint32_t>(k) << 1) | 1u;
+#pragma unroll
+      for (int i = 0; i < kSlotsPerLane; ++i) {
+        const int slot = i * 32 + lane;
+        ko[i] = slot == ws ? k_ws : (slot == ns ? k_ns : ko[i]);
+        kc[i] = slot == ws ? c_ws : (slot == ns ? c_ns : kc[i]);
       }
       __syncwarp();
     }
