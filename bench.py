@@ -34,6 +34,9 @@ SMALL = dict(name="small", T=512, N=31, L=15, V=16384, d=512, n_layers=4, Hq=32,
              path_depth=(3, 15))
 FORWARD36 = dict(name="forward36", T=4096, N=63, L=15, V=151936, d=4096, n_layers=36, Hq=32, Hkv=8,
                  D=128, inter=12288, rope_theta=1e6, eps=1e-6, path_depth=(3, 15))
+ENTROPY36 = dict(name="entropy36", T=2048, L=15, V=151936, d=4096, n_layers=36, Hq=32, Hkv=8, D=128,
+                 entropy=(0.3, 1.5, 4.0), N_set=(31, 63, 127, 255))
+VERIFY1 = dict(name="verify1", T=1024, N=31, L=15, V=151936, n_layers=1, Hq=32, Hkv=8, D=128)
 RAGGED8 = dict(name="ragged8", B=8, T_range=(512, 8192), entropy=(0.3, 1.5, 4.0), N=63, L=15,
                V=151936, d=4096, n_layers=36, Hq=32, Hkv=8, D=128, path_depth=(3, 15))
 
@@ -678,6 +681,136 @@ def run_forward(dev, reps=10):
             "data": "synthetic, random-init weights, rows and K/V drawn on the device (seeded torch generator)"}
 
 
+def mufu_peak():
+    """ex2 per second of the special-function units: 16 per clock per SM
+    (derived: 4 per clock per scheduler) x the SMs x the maximum SM clock."""
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return 16 * props.multi_processor_count * 2.07e9
+
+
+def attn_roof_us(cfg, T, R, anc_sizes, pk):
+    """Binding roof of one attention layer: max of HBM bytes, tensor flops and
+    exponentials, each at its peak (us), and which one binds."""
+    seen = sum(T + a for a in anc_sizes)  # keys each row attends to
+    by = (T + R) * cfg["Hkv"] * cfg["D"] * 2 * 2 + 2 * R * cfg["Hq"] * cfg["D"] * 2
+    fl = 4 * cfg["D"] * cfg["Hq"] * seen
+    ex = cfg["Hq"] * seen
+    t = {"hbm": by / (pk["hbm"] * 1e9) * 1e6, "tensor": fl / (pk["bf16"] * 1e12) * 1e6,
+         "mufu": ex / mufu_peak() * 1e6}
+    bind = max(t, key=t.get)
+    return t[bind], bind, by
+
+
+def run_entropy_sweep(dev, wl_W, reps=10):
+    """Config 4 (secondary): tree build + 36 layers of tree attention at T =
+    2048 for draft marginals of 0.3 / 1.5 / 4.0 nats and N in {31, 63, 127,
+    255}, plus the LM head at M = N + 1 as an extra; each stage against its
+    binding roof (HBM, tensor or exponentials)."""
+    import torch
+    import tree_verified_block_gb300 as g
+    c = ENTROPY36
+    pk = peaks()
+    tg = torch.Generator(device=dev)
+    tg.manual_seed(4000)
+    n_max = max(c["N_set"]) + 1
+    t_cap = c["T"] + n_max + 64
+    rn = lambda *shape: torch.randn(*shape, generator=tg, device=dev).to(torch.bfloat16)
+    k = [rn(c["Hkv"], t_cap, c["D"]) for _ in range(c["n_layers"])]
+    v = [rn(c["Hkv"], t_cap, c["D"]) for _ in range(c["n_layers"])]
+    q_all = [rn(n_max, c["Hq"], c["D"]) for _ in range(c["n_layers"])]
+    h_all = rn(n_max, c["d"])
+    t0 = torch.tensor([c["T"]], dtype=torch.int32, device=dev)
+    t_len = t0.clone()
+    root = torch.tensor([77], dtype=torch.int32, device=dev)
+    layers = [g.KVLayer(kk, vv, t_len) for kk, vv in zip(k, v)]
+    scale = c["D"] ** -0.5
+    out = []
+    for H in c["entropy"]:
+        x = torch.from_numpy(W.draft_logits_entropy(c["L"], c["V"], H, seed=4100 + int(10 * H))).to(dev)
+        for N in c["N_set"]:
+            R = N + 1
+            tree = g.Tree(N, c["L"], dev)
+            ws_tree = g.workspace(g.build_tree_workspace_bytes(c["L"], c["V"], N), dev)
+            ws_attn = g.workspace(g.tree_attention_workspace_bytes(R, c["Hq"], layers[0]), dev)
+            ws_lm = g.workspace(g.lmhead_argmax_workspace_bytes(R, c["d"], c["V"], torch.bfloat16), dev)
+            q = [qq[:R].contiguous() for qq in q_all]
+            o = [torch.empty_like(qq) for qq in q]
+            h = h_all[:R].contiguous()
+            am = torch.empty(R, dtype=torch.int32, device=dev)
+            gp = torch.empty(R, dtype=torch.float32, device=dev)
+            mx = torch.empty(R, dtype=torch.float32, device=dev)
+
+            def tree_fn():
+                t_len.copy_(t0)
+                g.build_tree(x, N, root, t_len, tree, ws_tree)
+            tree_fn()
+            torch.cuda.synchronize()
+            depth = tree.depth.cpu().numpy()
+            st = {"tree": graph_time_us(tree_fn, reps),
+                  "attention_36": graph_time_us(
+                      lambda: [g.tree_attention(q[l], layers[l], tree, scale, o[l], ws_attn)
+                               for l in range(c["n_layers"])], reps),
+                  "lmhead": graph_time_us(lambda: g.lmhead_argmax(h, wl_W, am, gp, mx, ws_lm), reps)}
+            roof_us, bind, by = attn_roof_us(c, c["T"], R, [int(dd) + 1 for dd in depth], pk)
+            per_layer = st["attention_36"] / c["n_layers"]
+            lm_bytes = c["d"] * c["V"] * 2 + R * c["d"] * 2
+            lm_roof = max(lm_bytes / (pk["hbm"] * 1e9), 2 * R * c["d"] * c["V"] / (pk["bf16"] * 1e12)) * 1e6
+            out.append({"H": H, "N": N, "max_depth": int(depth.max()),
+                        "tree_us": round(st["tree"], 2),
+                        "tree_hbm_frac": round(c["L"] * c["V"] * 4 / (st["tree"] * 1e-6) / 1e9 / pk["hbm"], 4),
+                        "attention_layer_us": round(per_layer, 2),
+                        "attention_bound": bind,
+                        "attention_frac_of_binding_roof": round(roof_us / per_layer, 4),
+                        "lmhead_us": round(st["lmhead"], 2),
+                        "lmhead_frac_of_binding_roof": round(lm_roof / st["lmhead"], 4),
+                        "rounds_per_s_tree_attn": round(1e6 / (st["tree"] + st["attention_36"]), 1)})
+    return {"workload": f"entropy36: T={c['T']}, L={c['L']}, V={c['V']}, {c['n_layers']} layers, "
+                        f"draft entropy {list(c['entropy'])} nats x N {list(c['N_set'])}",
+            "mufu_peak_ex2_per_s": mufu_peak(),
+            "points": out,
+            "data": "synthetic: draft logits calibrated to the entropy (seeded numpy), q/K/V/h drawn on the device"}
+
+
+def run_verify1(dev, reps=20):
+    """Config 2 (secondary): one layer at T = 1024, N = 31: tree build and
+    tree attention."""
+    import torch
+    import tree_verified_block_gb300 as g
+    c = VERIFY1
+    pk = peaks()
+    tg = torch.Generator(device=dev)
+    tg.manual_seed(2000)
+    R = c["N"] + 1
+    t_cap = c["T"] + R + 64
+    rn = lambda *shape: torch.randn(*shape, generator=tg, device=dev).to(torch.bfloat16)
+    kv = g.KVLayer(rn(c["Hkv"], t_cap, c["D"]), rn(c["Hkv"], t_cap, c["D"]),
+                   torch.tensor([c["T"]], dtype=torch.int32, device=dev))
+    t0 = kv.t_len.clone()
+    x = torch.from_numpy(W.draft_logits_planted(c["L"], c["V"], seed=2001)).to(dev)
+    root = torch.tensor([5], dtype=torch.int32, device=dev)
+    tree = g.Tree(c["N"], c["L"], dev)
+    ws_tree = g.workspace(g.build_tree_workspace_bytes(c["L"], c["V"], c["N"]), dev)
+    ws_attn = g.workspace(g.tree_attention_workspace_bytes(R, c["Hq"], kv), dev)
+    q = rn(R, c["Hq"], c["D"])
+    o = torch.empty_like(q)
+
+    def tree_fn():
+        kv.t_len.copy_(t0)
+        g.build_tree(x, c["N"], root, kv.t_len, tree, ws_tree)
+    tree_fn()
+    torch.cuda.synchronize()
+    depth = tree.depth.cpu().numpy()
+    t_tree = graph_time_us(tree_fn, reps)
+    t_attn = graph_time_us(lambda: g.tree_attention(q, kv, tree, c["D"] ** -0.5, o, ws_attn), reps)
+    roof_us, bind, by = attn_roof_us(c, c["T"], R, [int(dd) + 1 for dd in depth], pk)
+    return {"workload": f"verify1: 1 layer, T={c['T']}, N={c['N']}, L={c['L']}, V={c['V']}",
+            "tree_us": round(t_tree, 2), "attention_us": round(t_attn, 2),
+            "attention_bound": bind, "attention_frac_of_binding_roof": round(roof_us / t_attn, 4),
+            "tree_hbm_frac": round(c["L"] * c["V"] * 4 / (t_tree * 1e-6) / 1e9 / pk["hbm"], 4),
+            "data": "synthetic: planted-peak draft logits (seeded numpy), q/K/V drawn on the device"}
+
+
 def run_case(args):
     """One workload alone, launched warmup + steps times, for profiler
     captures; prints its graph-timed duration. lmhead512: the LM head over 512
@@ -824,6 +957,8 @@ def run_gpu(args):
     e2e = run_e2e(wl, args.steps)
     batched = run_batched(dev) if (args.batched and rank == 0) else None
     forward = run_forward(dev) if (args.forward and rank == 0) else None
+    sweep = run_entropy_sweep(dev, wl.W) if (args.sweep and rank == 0) else None
+    verify1 = run_verify1(dev) if (args.sweep and rank == 0) else None
     code, text = g.device_status()
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": world,
@@ -842,6 +977,9 @@ def run_gpu(args):
         out["ragged8"] = batched
     if forward is not None:
         out["forward36"] = forward
+    if sweep is not None:
+        out["entropy36"] = sweep
+        out["verify1"] = verify1
     if rank == 0:
         if args.cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(cfg, wl)
@@ -997,6 +1135,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--case", default=None, choices=["lmhead512", "dense_layer", "forward36"],
                     help="run one kernel alone on a small case (for profiler captures)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the entropy36 sweep and the verify1 single-layer case")
     ap.add_argument("--no-forward", dest="forward", action="store_false",
                     help="skip the forward36 secondary measurement (verify forward with the dense layers)")
     ap.add_argument("--no-batched", dest="batched", action="store_false",
