@@ -39,7 +39,6 @@ constexpr int kMaxL = 16;
 constexpr int kMaxN = 255;
 constexpr int kMaxB = 16;       // requests of one batched call
 constexpr int kTicketsPerReq = 32;  // [0, L): row tickets, [kMaxL]: request ticket
-constexpr int kSlotsPerLane = 8;  // frontier capacity 256 >= N + 1
 
 // B requests (blockIdx.y); "global row" = request * L + offset row.
 struct BuildParams {
@@ -288,17 +287,17 @@ struct __align__(16) PopRec {
 struct TreeSmem {
   PopRec pop[kMaxN];
   int16_t p_pos[kMaxN];
+  uint8_t rank[kMaxN];  // a pop's rank at its own depth (the search's record)
 };
 
-__device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlotsPerLane], int i) {
+template <int kSlots>
+__device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlots], int i) {
   uint32_t v = 0;
 #pragma unroll
-  for (int t = 0; t < kSlotsPerLane; ++t)
+  for (int t = 0; t < kSlots; ++t)
     if (t == i) v = a[t];
   return v;
 }
-
-constexpr uint32_t kRootChild = 0xFFFFu;  // code of the first node (rank 0 at offset 1)
 
 // Packs the first n pops of request req (a prefix of the best-first order, so
 // a prefix-closed set) into canonical rows 0..n; rows n+1..N are inactive:
@@ -360,6 +359,176 @@ __device__ void pack_rows(const BuildParams& p, const int* s_tok, TreeSmem& ts, 
   }
 }
 
+// Best-first search in one warp (the calling lanes are 0..31): pops N nodes
+// into ts.pop / ts.rank in best-first order, then rebuilds their rank vectors.
+template <int kSlots>
+__device__ __noinline__ void search_warp(TreeSmem& ts, const float* s_logq, const int N, const int L,
+                                         const int K) {
+    // Lane-owned frontier slots (slot s = lane + 32 i), each a node held in
+    // registers: its 32-bit score key (0 = empty), its parent's score, and
+    // depth | rank << 8 | (parent pop + 1) << 16. A pop then needs no shared
+    // memory: successor scores come from the node's own fields, and the
+    // popped record (score, parent score, depth, parent, rank) is written for
+    // later; the rank vectors are rebuilt from the parent links after the
+    // search (and walked up on the rare exact-tie path).
+    const int lane = threadIdx.x;
+    uint32_t ko[kSlots], ki[kSlots];
+    float kp[kSlots];
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      ko[i] = 0;
+      ki[i] = 0;
+      kp[i] = 0.f;
+    }
+    if (lane == 0) {
+      ko[0] = ord_key(s_logq[0]);
+      ki[0] = 1u;  // depth 1, rank 0, no parent
+    }
+    auto get_f = [&](const float (&a)[kSlots], int i) {
+      float v = 0.f;
+#pragma unroll
+      for (int t2 = 0; t2 < kSlots; ++t2)
+        if (t2 == i) v = a[t2];
+      return v;
+    };
+    // rank vector of a node (depth d, rank r, parent pop par) from the records
+    auto path_of = [&](int d, uint32_t r, int par, unsigned long long& hi, unsigned long long& lo) {
+      hi = lo = 0ull;
+      set_rank(hi, lo, d - 1, r);
+      for (int v = par; v >= 0; v = ts.pop[v].par) set_rank(hi, lo, ts.pop[v].dep - 1, ts.rank[v]);
+    };
+    int cnt = 1;
+    for (int k = 0; k < N; ++k) {
+      uint32_t bo = 0;
+      int bi = 0;
+      bool dup = false;
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        const uint32_t v = ko[i];
+        if (v > bo) {
+          bo = v;
+          bi = i;
+          dup = false;
+        } else if (v == bo && v != 0) {
+          dup = true;
+        }
+      }
+      const uint32_t mmax = __reduce_max_sync(0xffffffffu, bo);
+      // every lane prepares its best slot's successors while the maximum is in flight
+      uint32_t info = get_reg<kSlots>(ki, bi);
+      float ps = get_f(kp, bi);
+      float c_score = 0.f, s_score = 0.f;
+      {
+        const int d = static_cast<int>(info & 0xFFu);
+        const int r = static_cast<int>((info >> 8) & 0xFFu);
+        const float sc = inv_ord_key(bo);
+        if (bo != 0 && d < L) c_score = sc + s_logq[d * K];
+        if (bo != 0 && r + 1 < K) s_score = ps + s_logq[(d - 1) * K + r + 1];
+      }
+      if (mmax == 0) {  // frontier exhausted: the host checks make this unreachable
+        if (lane == 0) report(GLANCE_DEV_BAD_TREE);
+        break;
+      }
+      const unsigned cand = __ballot_sync(0xffffffffu, bo == mmax);
+      const bool slow = __popc(cand) > 1 || __ballot_sync(0xffffffffu, bo == mmax && dup) != 0;
+      int ws;  // winning slot
+      if (!slow) {
+        const int win = __ffs(cand) - 1;
+        ws = __shfl_sync(0xffffffffu, bi * 32 + lane, win);
+        info = __shfl_sync(0xffffffffu, info, win);
+        ps = __shfl_sync(0xffffffffu, ps, win);
+        c_score = __shfl_sync(0xffffffffu, c_score, win);
+        s_score = __shfl_sync(0xffffffffu, s_score, win);
+      } else {
+        // exact score tie: least (depth, rank vector) among slots with key mmax
+        __syncwarp();  // the records written so far are visible to every lane
+        int my = -1;
+        uint32_t md = 0, mi = 0;
+        float mp = 0.f;
+        unsigned long long mh = 0, ml = 0;
+#pragma unroll
+        for (int i = 0; i < kSlots; ++i) {
+          if (ko[i] == mmax) {
+            const int d = static_cast<int>(ki[i] & 0xFFu);
+            unsigned long long h, l;
+            path_of(d, (ki[i] >> 8) & 0xFFu, static_cast<int>(ki[i] >> 16) - 1, h, l);
+            if (my < 0 || tie_less(d, h, l, md, mh, ml)) {
+              my = i * 32 + lane;
+              md = d;
+              mh = h;
+              ml = l;
+              mi = ki[i];
+              mp = kp[i];
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const int oy = __shfl_xor_sync(0xffffffffu, my, o);
+          const uint32_t od = __shfl_xor_sync(0xffffffffu, md, o);
+          const unsigned long long oh = __shfl_xor_sync(0xffffffffu, mh, o);
+          const unsigned long long ol = __shfl_xor_sync(0xffffffffu, ml, o);
+          const uint32_t oi = __shfl_xor_sync(0xffffffffu, mi, o);
+          const float op = __shfl_xor_sync(0xffffffffu, mp, o);
+          if (oy >= 0 && (my < 0 || tie_less(od, oh, ol, md, mh, ml))) {
+            my = oy;
+            md = od;
+            mh = oh;
+            ml = ol;
+            mi = oi;
+            mp = op;
+          }
+        }
+        ws = my;
+        info = mi;
+        ps = mp;
+        const int d = static_cast<int>(info & 0xFFu);
+        const int r = static_cast<int>((info >> 8) & 0xFFu);
+        const float sc = inv_ord_key(mmax);
+        c_score = d < L ? sc + s_logq[d * K] : 0.f;
+        s_score = r + 1 < K ? ps + s_logq[(d - 1) * K + r + 1] : 0.f;
+      }
+      const float score = inv_ord_key(mmax);
+      const int d = static_cast<int>(info & 0xFFu);
+      const uint32_t r = (info >> 8) & 0xFFu;
+      const uint32_t par1 = info >> 16;  // parent pop + 1
+      const bool has_child = d < L;
+      const bool has_sib = static_cast<int>(r) + 1 < K;
+      if (lane == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(&ts.pop[k]);
+        dst[0] = make_uint4(__float_as_uint(score), __float_as_uint(ps), static_cast<uint32_t>(d),
+                            static_cast<uint32_t>(static_cast<int>(par1) - 1));
+        ts.rank[k] = static_cast<uint8_t>(r);
+      }
+      // the popped slot takes the child (else the sibling); a new slot takes
+      // the sibling when both exist (predicated, no divergence)
+      const uint32_t child_info = static_cast<uint32_t>(d + 1) | (static_cast<uint32_t>(k + 1) << 16);
+      const uint32_t sib_info = static_cast<uint32_t>(d) | ((r + 1) << 8) | (par1 << 16);
+      const uint32_t k_ws = has_child ? ord_key(c_score) : (has_sib ? ord_key(s_score) : 0u);
+      const uint32_t i_ws = has_child ? child_info : sib_info;
+      const float p_ws = has_child ? score : ps;
+      const bool both = has_child && has_sib;
+      const int ns = both ? cnt : -1;
+      cnt += both ? 1 : 0;
+      const uint32_t k_ns = ord_key(s_score);
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        const int slot = i * 32 + lane;
+        ko[i] = slot == ws ? k_ws : (slot == ns ? k_ns : ko[i]);
+        ki[i] = slot == ws ? i_ws : (slot == ns ? sib_info : ki[i]);
+        kp[i] = slot == ws ? p_ws : (slot == ns ? ps : kp[i]);
+      }
+    }
+    __syncwarp();
+    // rank vectors of the pops from their parent links (depth <= 16 steps)
+    for (int kk = lane; kk < N; kk += 32) {
+      unsigned long long h, l;
+      path_of(ts.pop[kk].dep, ts.rank[kk], ts.pop[kk].par, h, l);
+      ts.pop[kk].hi = h;
+      ts.pop[kk].lo = l;
+    }
+}
+
 __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int req) {
   // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
   float* s_logq = reinterpret_cast<float*>(dyn);
@@ -376,172 +545,13 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
   const int N = p.N, L = p.L, K = p.K;
 
   if (threadIdx.x < 32) {
-    // Lane-owned frontier slots (slot s = lane + 32 i): a 32-bit score key
-    // (0 = empty) and a code: (k << 1) = first child of pop k, (k << 1) | 1 =
-    // next sibling of pop k. A node's path, depth, parent and parent score
-    // follow from pop k's record, so a slot carries no other data.
-    const int lane = threadIdx.x;
-    uint32_t ko[kSlotsPerLane], kc[kSlotsPerLane];
-#pragma unroll
-    for (int i = 0; i < kSlotsPerLane; ++i) {
-      ko[i] = 0;
-      kc[i] = 0;
-    }
-    if (lane == 0) {
-      ko[0] = ord_key(s_logq[0]);
-      kc[0] = kRootChild;
-    }
-    // node data of a code
-    auto node_of = [&](uint32_t code, PopRec& nd) {
-      if (code == kRootChild) {
-        nd.pscore = 0.f;
-        nd.dep = 1;
-        nd.par = -1;
-        nd.hi = nd.lo = 0ull;
-        return;
-      }
-      const PopRec g = ts.pop[code >> 1];
-      if ((code & 1u) == 0) {  // first child: rank 0 appended (a zero byte)
-        nd.pscore = g.score;
-        nd.dep = g.dep + 1;
-        nd.par = static_cast<int>(code >> 1);
-        nd.hi = g.hi;
-        nd.lo = g.lo;
-      } else {  // next sibling: the last rank + 1
-        nd.pscore = g.pscore;
-        nd.dep = g.dep;
-        nd.par = g.par;
-        nd.hi = g.hi;
-        nd.lo = g.lo;
-        set_rank(nd.hi, nd.lo, g.dep - 1, get_rank(g.hi, g.lo, g.dep - 1) + 1);
-      }
-    };
-    // scores of a node's successors: first child (rank 0 at offset d + 1)
-    // and next sibling (rank r + 1)
-    auto successors = [&](const PopRec& nd, float& c_score, float& s_score) {
-      const int d = nd.dep;
-      const uint32_t r = get_rank(nd.hi, nd.lo, d - 1);
-      c_score = d < L ? nd.score + s_logq[d * K] : 0.f;
-      s_score = static_cast<int>(r) + 1 < K ? nd.pscore + s_logq[(d - 1) * K + r + 1] : 0.f;
-    };
-    int cnt = 1;
-    for (int k = 0; k < N; ++k) {
-      uint32_t bo = 0;
-      int bi = 0;
-      bool dup = false;
-#pragma unroll
-      for (int i = 0; i < kSlotsPerLane; ++i) {
-        const uint32_t v = ko[i];
-        if (v > bo) {
-          bo = v;
-          bi = i;
-          dup = false;
-        } else if (v == bo && v != 0) {
-          dup = true;
-        }
-      }
-      const uint32_t mmax = __reduce_max_sync(0xffffffffu, bo);
-      // every lane works out its best slot's node and successor scores while
-      // the warp's maximum is in flight (the winner's come by shuffle)
-      PopRec nd;
-      float c_score = 0.f, s_score = 0.f;
-      if (bo != 0) {
-        node_of(get_reg(kc, bi), nd);
-        nd.score = inv_ord_key(bo);
-        successors(nd, c_score, s_score);
-      } else {
-        nd.score = nd.pscore = 0.f;
-        nd.dep = 1;
-        nd.par = -1;
-        nd.hi = nd.lo = 0ull;
-      }
-      if (mmax == 0) {  // frontier exhausted: the host checks make this unreachable
-        if (lane == 0) report(GLANCE_DEV_BAD_TREE);
-        break;
-      }
-      const unsigned cand = __ballot_sync(0xffffffffu, bo == mmax);
-      const bool slow = __popc(cand) > 1 || __ballot_sync(0xffffffffu, bo == mmax && dup) != 0;
-      int ws;       // winning slot
-      uint32_t wc;  // its code
-      if (!slow) {
-        const int win = __ffs(cand) - 1;
-        ws = __shfl_sync(0xffffffffu, bi * 32 + lane, win);
-        wc = __shfl_sync(0xffffffffu, get_reg(kc, bi), win);
-        nd.pscore = __shfl_sync(0xffffffffu, nd.pscore, win);
-        nd.dep = __shfl_sync(0xffffffffu, nd.dep, win);
-        nd.par = __shfl_sync(0xffffffffu, nd.par, win);
-        nd.hi = __shfl_sync(0xffffffffu, nd.hi, win);
-        nd.lo = __shfl_sync(0xffffffffu, nd.lo, win);
-        c_score = __shfl_sync(0xffffffffu, c_score, win);
-        s_score = __shfl_sync(0xffffffffu, s_score, win);
-      } else {
-        // exact score tie: least (depth, rank vector) among slots with key mmax
-        int my = -1;
-        uint32_t mc = 0, md = 0;
-        unsigned long long mh = 0, ml = 0;
-#pragma unroll
-        for (int i = 0; i < kSlotsPerLane; ++i) {
-          if (ko[i] == mmax) {
-            PopRec t;
-            node_of(kc[i], t);
-            if (my < 0 || tie_less(t.dep, t.hi, t.lo, md, mh, ml)) {
-              my = i * 32 + lane;
-              mc = kc[i];
-              md = t.dep;
-              mh = t.hi;
-              ml = t.lo;
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const int oy = __shfl_xor_sync(0xffffffffu, my, o);
-          const uint32_t oc = __shfl_xor_sync(0xffffffffu, mc, o);
-          const uint32_t od = __shfl_xor_sync(0xffffffffu, md, o);
-          const unsigned long long oh = __shfl_xor_sync(0xffffffffu, mh, o);
-          const unsigned long long ol = __shfl_xor_sync(0xffffffffu, ml, o);
-          if (oy >= 0 && (my < 0 || tie_less(od, oh, ol, md, mh, ml))) {
-            my = oy;
-            mc = oc;
-            md = od;
-            mh = oh;
-            ml = ol;
-          }
-        }
-        ws = my;
-        wc = mc;
-        node_of(wc, nd);
-        nd.score = inv_ord_key(mmax);
-        successors(nd, c_score, s_score);
-      }
-      nd.score = inv_ord_key(mmax);
-      const int d = nd.dep;
-      const uint32_t r = get_rank(nd.hi, nd.lo, d - 1);
-      const bool has_child = d < L;
-      const bool has_sib = static_cast<int>(r) + 1 < K;
-      if (lane == 0) {
-        uint4* dst = reinterpret_cast<uint4*>(&ts.pop[k]);
-        dst[0] = make_uint4(__float_as_uint(nd.score), __float_as_uint(nd.pscore),
-                            static_cast<uint32_t>(nd.dep), static_cast<uint32_t>(nd.par));
-        dst[1] = make_uint4(static_cast<uint32_t>(nd.hi), static_cast<uint32_t>(nd.hi >> 32),
-                            static_cast<uint32_t>(nd.lo), static_cast<uint32_t>(nd.lo >> 32));
-      }
-      // the popped slot takes the child (else the sibling); a new slot takes
-      // the sibling when both exist (predicated, no divergence)
-      const uint32_t k_ws = has_child ? ord_key(c_score) : (has_sib ? ord_key(s_score) : 0u);
-      const uint32_t c_ws = (static_cast<uint32_t>(k) << 1) | (has_child ? 0u : 1u);
-      const bool both = has_child && has_sib;
-      const int ns = both ? cnt : -1;
-      cnt += both ? 1 : 0;
-      const uint32_t k_ns = ord_key(s_score), c_ns = (static_cast<uint32_t>(k) << 1) | 1u;
-#pragma unroll
-      for (int i = 0; i < kSlotsPerLane; ++i) {
-        const int slot = i * 32 + lane;
-        ko[i] = slot == ws ? k_ws : (slot == ns ? k_ns : ko[i]);
-        kc[i] = slot == ws ? c_ws : (slot == ns ? c_ns : kc[i]);
-      }
-      __syncwarp();
-    }
+    // frontier capacity 32 x slots per lane >= N + 1: fewer slots, shorter pops
+    if (N < 64)
+      search_warp<2>(ts, s_logq, N, L, K);
+    else if (N < 128)
+      search_warp<4>(ts, s_logq, N, L, K);
+    else
+      search_warp<8>(ts, s_logq, N, L, K);
   }
   __syncthreads();
 
