@@ -584,6 +584,9 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
   const int base = chunk * kChunk;
   const int n_valid = min(kChunk, p.V - base);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // The next kernel (tree attention) may start its prologue on SMs this grid
+  // frees: it reads nothing this kernel writes before its own dependency wait.
+  pdl_launch_dependents();
 
   // ---- 1. load the chunk into registers (ids: see id_of below)
   float x[kPerThread];

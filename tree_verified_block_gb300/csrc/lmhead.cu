@@ -474,33 +474,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // W does not depend on the previous kernel in the stream: the first stages'
+  // W slices go out before the programmatic-dependent-launch wait, h after it
+  const uint32_t a_bytes = NB == 1 ? static_cast<uint32_t>(p.a_rows) * kBK * 2 : NB * kABytes;
+  const int n_pre = my_tiles * n_kb < STAGES ? my_tiles * n_kb : STAGES;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_h);
+    tma_prefetch_desc(&map_w);
+    const uint64_t pol_w = policy_evict_first();
+    for (int it = 0; it < n_pre; ++it) {
+      const int v0 = (blockIdx.x + (it / n_kb) * gridDim.x) * BN, kb = it % n_kb;
+      unsigned char* stage = smem + it * Sh::kStageBytes;
+      mbar_arrive_expect_tx(&bars->full[it], a_bytes + Sh::kBBytes);
+#pragma unroll
+      for (int q = 0; q < BN / 64; ++q)
+        tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[it], v0 + 64 * q, kb * kBK,
+                    pol_w);
+    }
+  }
+  pdl_wait_prior();
+
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&map_h);
-      tma_prefetch_desc(&map_w);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
       // NB > 1: boxes of 128 rows; rows past M are filled with zeros by TMA
-      const uint32_t a_bytes = NB == 1 ? static_cast<uint32_t>(p.a_rows) * kBK * 2 : NB * kABytes;
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
         const int v0 = (blockIdx.x + i * gridDim.x) * BN;
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int st = it % STAGES;
-          if (it >= STAGES && !wait_or_abort(&bars->empty[st], ((it / STAGES) - 1) & 1, bars)) {
-            ok = false;
-            break;
-          }
           unsigned char* stage = smem + st * Sh::kStageBytes;
-          mbar_arrive_expect_tx(&bars->full[st], a_bytes + Sh::kBBytes);
+          if (it >= n_pre) {
+            if (it >= STAGES && !wait_or_abort(&bars->empty[st], ((it / STAGES) - 1) & 1, bars)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->full[st], a_bytes + Sh::kBBytes);
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
+                          kb * kBK, pol_w);
+          }
 #pragma unroll
           for (int b = 0; b < NB; ++b)
             tma_load_2d(stage + b * kABytes, &map_h, &bars->full[st], kb * kBK, b * kBM, pol_h);
-#pragma unroll
-          for (int q = 0; q < BN / 64; ++q)
-            tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
-                        kb * kBK, pol_w);
         }
       }
       if (!ok) {
@@ -916,7 +935,19 @@ glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int
   }
   Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket, entropy};
   set_sample(p, sa);
-  lmhead_bf16_kernel<NB, kMode><<<grid, kThreads, Sh::kSmem, s>>>(mh, mw, p);
+  // a programmatic dependent of the previous kernel: W streams in while it ends
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Sh::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lmhead_bf16_kernel<NB, kMode>, mh, mw, p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
   e = cudaGetLastError();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
