@@ -68,6 +68,9 @@ def run_bf16(T, N, Hq, Hkv, dev, seed=0, t_cap=None, head_pad=0, L=15):
     (127, 20, 4, 4),
     (129, 20, 4, 4),
     (1024, 31, 32, 8),    # one Qwen3-VL-8B layer, N=31
+    (0, 63, 32, 8),       # no prefix: tree rows only (nothing fetched before the wait)
+    (128, 63, 32, 8),     # the prefix is exactly the first key tile
+    (256, 255, 4, 1),     # 256 rows
 ])
 def test_bf16_small(dev, clean_status, T, N, Hq, Hkv):
     got, want = run_bf16(T, N, Hq, Hkv, dev, seed=T + N)

@@ -20,10 +20,10 @@
 //     writes (token, log q) using the row's log-sum-exp (fp32: each chunk's
 //     sum is relative to its own max, so every term is at most 8192);
 //  3. the last row-merger overall runs the best-first search in one warp
-//     (frontier slots in shared memory, their 32-bit score keys in registers,
-//     8 slots per lane, one warp max-reduction per pop; exact score ties take
-//     a slow path that compares depth and rank vectors) and the whole CTA packs
-//     the N popped nodes into canonical order.
+//     (frontier nodes in registers, 2 / 4 / 8 slots per lane by N, one warp
+//     max-reduction per pop; exact score ties take a slow path that compares
+//     depth and rank vectors) and the whole CTA packs the N popped nodes into
+//     canonical order.
 #include "glance_internal.cuh"
 
 GLANCE_DEFINE_STATUS_WORD(status_build_tree)
