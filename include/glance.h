@@ -429,8 +429,8 @@ glance_status glance_row_sumsq(const void* x, int M, int d, float* sumsq, void* 
  * eps) and rotate-half RoPE at pos_id [M] with base rope_theta (dims j and
  * j + 64 rotate by pos * theta^(-2j/128)). q goes to q_out [M][Hq][128]; k
  * and v go to the cache kv (bf16, head_dim 128) at slots T + row
- * (T = *kv->t_len, T + M <= t_cap, else device status 2). Hq, Hkv even,
- * Hq % Hkv == 0, d % 64 == 0.
+ * (T = *kv->t_len; if T + M > t_cap, device status 2 and no cache row is
+ * written). Hq, Hkv even, Hq % Hkv == 0, d % 64 == 0.
  */
 glance_status glance_dense_qkv(const void* h, const void* W_qkv, int M, int d, int n_q_heads,
                                const float* in_sumsq, int n_sumsq, const float* q_norm,

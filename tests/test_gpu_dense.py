@@ -203,3 +203,38 @@ def test_full_layer_with_tree_attention(dev, clean_status):
     got = f64(out)
     err = np.abs(got - want) / np.maximum(1.0, np.abs(want))
     assert err.max() < 6e-2 and err.mean() < 5e-3, (err.max(), err.mean())
+
+
+def test_qkv_cache_capacity_and_arguments(dev, clean_status):
+    """Rows whose K/V slots T + row would pass t_cap set device status 2 and
+    leave the cache alone; misaligned or mis-shaped arguments are refused on
+    the host before any launch."""
+    import tree_verified_block_gb300 as g
+    M, d, Hq, Hkv, D = 16, 256, 4, 2, 128
+    t_cap = 40
+    gen = W.rng(99)
+    h = bf16_tensor(W.normal_bf16(gen, (M, d)), dev)
+    Wq = bf16_tensor(W.normal_bf16(gen, (d, (Hq + 2 * Hkv) * D), std=0.02), dev)
+    kb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    kv = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(kb, dev), torch.tensor([t_cap - M + 1], dtype=torch.int32,
+                                                                             device=dev))
+    q = torch.empty((M, Hq, D), dtype=torch.bfloat16, device=dev)
+    pos = torch.arange(M, dtype=torch.int32, device=dev)
+    g.dense_qkv(h, Wq, Hq, None, None, None, 1e-6, pos, 1e6, q, kv)
+    code, _ = g.device_status()
+    assert code == 2
+    g.reset_device_status()
+    assert np.array_equal(kv.k.view(torch.int16).cpu().numpy().view(np.uint16), kb)
+    # host-side refusals: x not 16-byte aligned, N not a multiple of 256, M > 128
+    x_bad = torch.empty(M * d + 1, dtype=torch.bfloat16, device=dev)[1:].view(M, d)
+    res = torch.zeros((M, 256), dtype=torch.bfloat16, device=dev)
+    W256 = torch.zeros((d, 256), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(g.GlanceError):
+        g.dense_residual(x_bad, W256, res, torch.empty_like(res))
+    with pytest.raises(g.GlanceError):
+        g.dense_residual(h, torch.zeros((d, 320), dtype=torch.bfloat16, device=dev), torch.zeros((M, 320),
+                         dtype=torch.bfloat16, device=dev), torch.zeros((M, 320), dtype=torch.bfloat16, device=dev))
+    big = torch.zeros((129, d), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(g.GlanceError):
+        g.dense_residual(big, W256, torch.zeros((129, 256), dtype=torch.bfloat16, device=dev),
+                         torch.zeros((129, 256), dtype=torch.bfloat16, device=dev))

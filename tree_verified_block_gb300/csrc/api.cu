@@ -109,8 +109,8 @@ static glance_status read_all_status(int32_t* code_out, bool reset) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return glance::cuda_fail(e, "glance_device_status");
   int first = 0;
-  cudaError_t (*fns[4])(int*, bool) = {glance::status_build_tree, glance::status_attention,
-                                       glance::status_lmhead, glance::status_commit};
+  cudaError_t (*fns[5])(int*, bool) = {glance::status_build_tree, glance::status_attention,
+                                       glance::status_lmhead, glance::status_commit, glance::status_dense};
   for (auto fn : fns) {
     int v = 0;
     e = fn(&v, reset);

@@ -222,7 +222,7 @@ __device__ void epilogue_regs(const DenseParams& p, float (&a)[8], float (&b)[8]
     }
   }
   if (!valid) return;
-  if (seg > 0 && (T < 0 || T + row >= p.t_cap)) {  // the rows' K/V slots must exist
+  if (seg > 0 && (T < 0 || T + p.M > p.t_cap)) {  // all M rows' K/V slots must exist, else none is written
     report(GLANCE_DEV_TREE_CAPACITY);
     return;
   }

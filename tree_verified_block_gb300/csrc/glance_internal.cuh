@@ -43,6 +43,7 @@ cudaError_t status_build_tree(int* out, bool reset);
 cudaError_t status_attention(int* out, bool reset);
 cudaError_t status_lmhead(int* out, bool reset);
 cudaError_t status_commit(int* out, bool reset);
+cudaError_t status_dense(int* out, bool reset);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
