@@ -20,6 +20,14 @@
  * (ragged) and KV caches. The LM head needs no batched form: the B requests'
  * rows are stacked into one h of M = B (N + 1) <= 512 rows.
  *
+ * Beyond the round itself: the root entropy fused into the LM head
+ * (glance_lmhead_argmax_entropy), a sampled rather than greedy verify
+ * (glance_lmhead_sample), the tie-aware gate on the walk
+ * (glance_accept_commit_gated), one tree budget shared by a batch
+ * (glance_build_tree_shared), and the target's dense layers around tree
+ * attention (glance_dense_qkv, glance_dense_residual, glance_dense_swiglu,
+ * glance_row_sumsq).
+ *
  * Conventions shared by every call
  * --------------------------------
  * - Memory: every array argument is a DEVICE pointer unless its comment says
@@ -74,7 +82,7 @@ typedef enum { GLANCE_F32 = 0, GLANCE_BF16 = 1 } glance_dtype;
 /* Device status word values (glance_device_status). */
 #define GLANCE_DEV_OK 0
 #define GLANCE_DEV_NONFINITE_LOGITS 1 /* a draft logit row held NaN or +-inf */
-#define GLANCE_DEV_TREE_CAPACITY 2    /* T + N + 1 > t_cap at run time */
+#define GLANCE_DEV_TREE_CAPACITY 2    /* the rows' K/V slots do not fit: T + rows > t_cap */
 #define GLANCE_DEV_BAD_TREE 3         /* a tree array was inconsistent */
 #define GLANCE_DEV_PIPELINE_TIMEOUT 4 /* an mbarrier wait hit its iteration cap */
 
