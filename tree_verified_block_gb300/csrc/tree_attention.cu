@@ -336,6 +336,35 @@ __device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char*
   }
 }
 
+// Softmax arithmetic on pairs: the three-input max and the packed f32x2
+// FMA / add of sm_100+ take one instruction per two elements (the softmax
+// warps are bound by instruction issue); each lane of a packed operation
+// rounds as the scalar one does.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long pair_f2(float lo, float hi) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void split_f2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma_f2(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add_f2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // One CTA = (kv head g, q tile, key split). The key splits of one (g, q tile)
 // merge their partial results through the workspace once all have arrived.
 template <int NB>
@@ -624,11 +653,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
+      for (int e = 0; e < 64; e += 8) {
+        mx0 = max3f(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+        mx1 = max3f(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+        mx2 = max3f(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+        mx3 = max3f(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
       }
       // scale_log2 > 0, so the max commutes with the scaling
       const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
@@ -651,16 +680,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
       const float neg_m = -m_use;
-      float ls0 = 0.f, ls1 = 0.f;
       uint32_t pk[32];
+      const unsigned long long sc2 = pair_f2(p.scale_log2, p.scale_log2), nm2 = pair_f2(neg_m, neg_m);
+      unsigned long long ls2 = pair_f2(0.f, 0.f);  // even and odd keys' sums, as two scalar chains
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, neg_m));
-        ls0 += p0;
-        ls1 += p1;
+        float t0, t1;
+        split_f2(fma_f2(pair_f2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2, nm2), t0, t1);
+        const float p0 = ex2_approx(t0);
+        const float p1 = ex2_approx(t1);
+        ls2 = add_f2(ls2, pair_f2(p0, p1));
         pk[e] = pack_bf16x2(p0, p1);
       }
+      float ls0, ls1;
+      split_f2(ls2, ls0, ls1);
       // PV(j-1) must be done with P and O before they are rewritten
       const bool got_o =
           __all_sync(0xffffffffu, j == 0 || wait_or_abort(&bars->o_done, (j - 1) & 1, bars));
