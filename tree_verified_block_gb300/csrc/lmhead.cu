@@ -179,33 +179,43 @@ __device__ __forceinline__ void entropy_chunk(const uint32_t (&r)[32], int col0,
 // the lowest column holding it, and the largest other value; then merged
 // (columns arrive in increasing order, so an equal maximum keeps the earlier
 // id).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 32 values as a tree of three-input maxima (17 instructions).
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  t[10] = fmaxf(x[30], x[31]);
+  const float u0 = max3f(t[0], t[1], t[2]), u1 = max3f(t[3], t[4], t[5]), u2 = max3f(t[6], t[7], t[8]);
+  return fmaxf(max3f(u0, u1, u2), fmaxf(t[9], t[10]));
+}
+
 __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, float& m1,
                                            int& i1, float& m2) {
   const int n = V - col0;
   float x[32];
+  if (n >= 32) {  // every chunk but a row's last
 #pragma unroll
-  for (int e = 0; e < 32; ++e) x[e] = e < n ? __uint_as_float(r[e]) : -INFINITY;
-  float t[16];
+    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+  } else {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) t[e] = fmaxf(x[e], x[e + 16]);
-#pragma unroll
-  for (int w = 8; w; w >>= 1)
-#pragma unroll
-    for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
-  const float cm = t[0];
+    for (int e = 0; e < 32; ++e) x[e] = e < n ? __uint_as_float(r[e]) : -INFINITY;
+  }
+  const float cm = max32(x);
   if (!(cm > m2)) return;  // nothing in the chunk changes the top two
   uint32_t hit = 0;
 #pragma unroll
   for (int e = 0; e < 32; ++e) hit |= (x[e] == cm ? 1u : 0u) << e;
   const int ci = __ffs(static_cast<int>(hit)) - 1;
+  float y[32];
 #pragma unroll
-  for (int e = 0; e < 16; ++e)
-    t[e] = fmaxf(e == ci ? -INFINITY : x[e], e + 16 == ci ? -INFINITY : x[e + 16]);
-#pragma unroll
-  for (int w = 8; w; w >>= 1)
-#pragma unroll
-    for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
-  const float c2 = t[0];
+  for (int e = 0; e < 32; ++e) y[e] = e == ci ? -INFINITY : x[e];
+  const float c2 = max32(y);
   if (cm > m1) {
     m2 = fmaxf(m1, c2);
     m1 = cm;
