@@ -108,3 +108,15 @@ def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         b.lib()
+
+
+def test_host_tensors_are_refused_before_any_call():
+    """A CPU tensor would reach a kernel as an address it cannot read: the
+    binding refuses it (no GPU needed to check)."""
+    import torch
+    import tree_verified_block_gb300 as g
+    with pytest.raises(ValueError):
+        g.Tree(15, 7, "cpu")
+    z = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        g.KVLayer(z, z, torch.zeros(1, dtype=torch.int32))

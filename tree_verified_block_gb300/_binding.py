@@ -152,7 +152,13 @@ def _check(status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a CUDA tensor (None for None). A host tensor would
+    reach a kernel as an address it cannot read, so it is refused here."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("glance: every array argument must be a CUDA tensor (got one on %s)" % t.device)
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream, device):
@@ -188,9 +194,8 @@ class Tree:
         self.pos_id = torch.zeros(rows, **i32)
         self.score = torch.zeros(rows, dtype=torch.float32, device=device)
         self.anc = torch.zeros((rows, self.mask_words), dtype=torch.int64, device=device)
-        self.c = TreeC(N, L, self.mask_words, self.token.data_ptr(), self.parent.data_ptr(),
-                       self.depth.data_ptr(), self.pos_id.data_ptr(), self.score.data_ptr(),
-                       self.anc.data_ptr())
+        self.c = TreeC(N, L, self.mask_words, *(_ptr(t).value for t in (self.token, self.parent, self.depth,
+                                                                            self.pos_id, self.score, self.anc)))
 
     def to_host(self):
         return dict(token=self.token.cpu().numpy(), parent=self.parent.cpu().numpy(),
@@ -207,8 +212,8 @@ class KVLayer:
         assert k.stride(2) == 1, "head_dim must be contiguous"
         self.k, self.v, self.t_len = k, v, t_len
         Hkv, t_cap, D = k.shape
-        self.c = KVC(k.data_ptr(), v.data_ptr(), _dtype_code(k), Hkv, D, t_cap,
-                     k.stride(0), k.stride(1), t_len.data_ptr())
+        self.c = KVC(_ptr(k).value, _ptr(v).value, _dtype_code(k), Hkv, D, t_cap,
+                     k.stride(0), k.stride(1), _ptr(t_len).value)
 
 
 # ------------------------------------------------------------------- calls
