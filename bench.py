@@ -621,6 +621,37 @@ def run_batched(dev, reps=10):
         g.accept_commit_batched(bw.trees, bw.argmax, bw.by_req, bw.n_acc, bw.acc_tok, bw.new_root,
                                 bw.ws_c)
     st["commit"] = graph_time_us(commit, reps)
+    # the NEXT rows on the same batch: shared-budget trees (half the batch's
+    # nodes, entropy-keyed with the pooled law), the LM head with the root
+    # entropy and in sampling mode, the gated walk + commit
+    M = bw.B * bw.R
+    ent = torch.tensor([c["entropy"][r % len(c["entropy"])] for r in range(bw.B)], dtype=torch.float32,
+                       device=bw.x_dev.device)
+    n_active = torch.zeros(bw.B, dtype=torch.int32, device=bw.x_dev.device)
+    ws_sh = g.workspace(g.build_tree_shared_workspace_bytes(bw.B, c["L"], c["V"], c["N"]), bw.x_dev.device)
+
+    def tree_shared():
+        bw.t_len.copy_(bw.t0)
+        g.build_tree_shared(bw.x_dev, c["N"], bw.B * c["N"] // 2, bw.root, bw.t_len, bw.trees, n_active, ws_sh,
+                            root_entropy=ent, law_b0=0.96, law_b1=0.63)
+    st["tree_shared"] = graph_time_us(tree_shared, reps)
+    entropy = torch.empty(M, dtype=torch.float32, device=bw.x_dev.device)
+    st["lmhead_entropy_m512"] = graph_time_us(
+        lambda: g.lmhead_argmax_entropy(bw.h, bw.W, bw.argmax, bw.gap, bw.maxlogit, entropy, bw.ws_lm), reps)
+    pos = torch.arange(M, dtype=torch.int32, device=bw.x_dev.device)
+    seq = torch.zeros(M, dtype=torch.int32, device=bw.x_dev.device)
+    drawn = torch.empty(M, dtype=torch.int32, device=bw.x_dev.device)
+    st["lmhead_sample_m512"] = graph_time_us(
+        lambda: g.lmhead_sample(bw.h, bw.W, 1.0, 1234, pos, seq, drawn, bw.gap, bw.ws_lm), reps)
+    gated = torch.zeros(bw.B, dtype=torch.int32, device=bw.x_dev.device)
+    g.lmhead_argmax(bw.h, bw.W, bw.argmax, bw.gap, bw.maxlogit, bw.ws_lm)
+    tree()  # the full trees again for the walk
+
+    def commit_gated():
+        bw.t_len.copy_(bw.t0)
+        g.accept_commit_gated_batched(bw.trees, bw.argmax, bw.gap, 1e-3, bw.by_req, bw.n_acc, bw.acc_tok,
+                                      bw.new_root, gated, bw.ws_c)
+    st["commit_gated"] = graph_time_us(commit_gated, reps)
     pk = peaks()
     by, fl = bw.algorithmic_bytes(), bw.flops()
     lm_tf = fl["lmhead"] / (st["lmhead_m512"] * 1e-6) / 1e12
