@@ -1255,30 +1255,73 @@ class HostInputs:
         self.h_bits = W.normal_bf16(gen, (R, cfg["d"]))
 
 
+def oracle_step(cfg, src, root, rows=8, l_sub=3):
+    """One bounded reference step: each stage of the round on a small slice,
+    its time scaled to the full stage — the tree build on the first l_sub
+    offsets (x L / l_sub), attention of `rows` rows of one kv head of one layer
+    (x rows of the tree / rows x kv heads x layers), the LM head over
+    src.W_bits' columns (x V / columns), walk + commit on one layer (x layers).
+    Returns (scaled seconds of a full round, per-stage detail)."""
+    from oracle.attention import tree_attention as o_attn
+    from oracle.bf16 import bf16_bits_to_f64
+    from oracle.lmhead import lmhead_argmax as o_lmhead
+    from oracle.tree import build_tree as o_build
+    from oracle.walk import commit as o_commit
+    from oracle.walk import walk as o_walk
+    T, R, G = cfg["T"], cfg["N"] + 1, cfg["Hq"] // cfg["Hkv"]
+    t = {}
+    t0 = time.perf_counter()
+    o_build(src.x[:l_sub].astype(np.float64), cfg["N"], root, T)
+    t["tree"] = (time.perf_counter() - t0) * cfg["L"] / l_sub
+    tree = src.tree  # the full tree (built once) for the stages below
+    t0 = time.perf_counter()
+    o_attn(bf16_bits_to_f64(src.q_bits[0][:rows, :G]), bf16_bits_to_f64(src.k_bits[0][:1, :T + R]),
+           bf16_bits_to_f64(src.v_bits[0][:1, :T + R]), T, tree["anc"][:rows], cfg["D"] ** -0.5)
+    t["attention"] = (time.perf_counter() - t0) * (R / rows) * cfg["Hkv"] * cfg["n_layers"]
+    t0 = time.perf_counter()
+    nv = src.W_bits.shape[1]
+    arg, _, _ = o_lmhead(bf16_bits_to_f64(src.h_bits), bf16_bits_to_f64(src.W_bits))
+    t["lmhead"] = (time.perf_counter() - t0) * cfg["V"] / nv
+    t0 = time.perf_counter()
+    a, path, _, _ = o_walk(tree, arg, cfg["L"])
+    o_commit(src.k_bits[0].copy(), src.v_bits[0].copy(), T, path)
+    t["commit"] = (time.perf_counter() - t0) * cfg["n_layers"]
+    return sum(t.values()), t
+
+
 def run_reference(args):
+    """The oracle (the reference arm of this build), as it stands, on the
+    host cores: every step is a bounded slice of the round (oracle_step, about
+    0.1 s on a GB300 host), scaled to a full round, so that any --steps K
+    ends in a few minutes."""
+    from oracle.tree import build_tree as o_build
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     cfg = SMALL if args.workload == "small" else FULL36
-    src = HostInputs(cfg)
+    src = HostInputs(cfg, n_layers=1, v_frac=1.0 / 1024)
+    src.tree = o_build(src.x.astype(np.float64), cfg["N"], 7, cfg["T"])
     for _ in range(args.warmup):
-        oracle_sample(cfg, src.x, src.q_bits, src.k_bits, src.v_bits, src.h_bits, src.W_bits, 7, 1, 1 / 64)
-    totals = []
+        oracle_step(cfg, src, 7)
+    totals, parts = [], []
     for _ in range(args.steps):
-        t, parts = oracle_sample(cfg, src.x, src.q_bits, src.k_bits, src.v_bits, src.h_bits,
-                                 src.W_bits, 7, 1, 1 / 64)
-        totals.append(t)
+        tt, pp = oracle_step(cfg, src, 7)
+        totals.append(tt)
+        parts.append(pp)
     sec = statistics.median(totals)
     value = 1.0 / sec
-    sample = (f"per step: full tree build; attention on 1 of {cfg['n_layers']} layers; LM head over 1/64 "
-              f"of the vocabulary; walk + commit; times scaled to one full round")
+    sample = (f"per step: tree build on 3 of {cfg['L']} offsets, attention of 8 rows x 1 kv head x 1 of "
+              f"{cfg['n_layers']} layers, LM head over {src.W_bits.shape[1]} of {cfg['V']} columns, walk + "
+              f"commit on 1 layer; each stage's time scaled to the full round")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "rounds/s",
            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": workload_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
            "cpu_baseline": {"value": round(value, 5), "unit": "rounds/s",
-                            "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": sample},
+                            "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": sample,
+                            "stage_seconds_full_round": {k: round(statistics.median(p[k] for p in parts), 3)
+                                                         for k in parts[0]} if parts else {}},
            "e2e": {"value": round(value, 5), "unit": "rounds/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
