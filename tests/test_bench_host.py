@@ -57,3 +57,21 @@ def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch)
     monkeypatch.setitem(bench.NCU_TRAFFIC, "glance_tree_attention", e)
     assert bench.profiled_traffic("glance_tree_attention") is None
     assert bench.profiled_traffic("no_such_kernel") is None
+
+
+def test_reference_arm_prints_one_bounded_line():
+    """The reference arm (the oracle on the host cores) runs on the small
+    workload without a GPU and prints the contract's line."""
+    import json
+    import subprocess
+    import sys
+    import time
+    t0 = time.perf_counter()
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "small", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT, env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "rounds/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert time.perf_counter() - t0 < 120
