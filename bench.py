@@ -81,12 +81,12 @@ def profiled_traffic(kernel):
     return e["bytes"]
 
 
-def workload_config(cfg, world=1):
+def workload_config(cfg):
     return {"workload": f"{cfg['name']}: Qwen3-VL-8B verify round, T={cfg['T']}, N={cfg['N']}, "
                         f"L={cfg['L']}, V={cfg['V']}, d={cfg['d']}, {cfg['n_layers']} layers, "
                         f"{cfg['Hq']}/{cfg['Hkv']} heads x {cfg['D']}",
             "T": cfg["T"], "N": cfg["N"], "L": cfg["L"], "V": cfg["V"], "d": cfg["d"],
-            "n_layers": cfg["n_layers"], "parallelism": f"replicas x{world}",
+            "n_layers": cfg["n_layers"], "parallelism": "one GPU (the path is per request; more GPUs would run replicas)",
             "l2": "no flush: each step streams ~1.9 GB of distinct inputs (> 129 MB L2)",
             "cuda_graph": True}
 
@@ -851,7 +851,7 @@ def run_case(args):
     Inputs drawn on the device."""
     import torch
     import tree_verified_block_gb300 as g
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     if args.case in ("dense_layer", "forward36"):
         cfg = FORWARD36 if args.case == "forward36" else dict(FORWARD36, n_layers=1, V=16384)
@@ -897,36 +897,14 @@ def run_case(args):
                       "tensor_frac": round(tf / pk["bf16"], 4)}), flush=True)
 
 
-def max_over_ranks(ms, dist, device):
-    """Slowest rank's time: the job's time (replicas run independent rounds)."""
-    if dist is None:
-        return ms
-    import torch
-    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def job_value(world, steps, ms_max):
-    """Whole-job rounds/s: every rank ran `steps` rounds within ms_max."""
-    return world * steps / (ms_max / 1e3)
-
-
 def run_gpu(args):
     import torch
     import tree_verified_block_gb300 as g
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     g.lib()
     cfg = SMALL if args.workload == "small" else FULL36
-    wl = Workload(cfg, dev, seed=3000 + rank, keep_host=False)
+    wl = Workload(cfg, dev, seed=3000, keep_host=False)
     torch.cuda.synchronize()
     # warm-up, then capture one round in a CUDA graph
     for _ in range(max(1, args.warmup)):
@@ -940,8 +918,6 @@ def run_gpu(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
         start.record(stream)
@@ -949,11 +925,9 @@ def run_gpu(args):
             graph.replay()
         end.record(stream)
         torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    ms = start.elapsed_time(end)
     ms_per_step = ms / args.steps
-    value = job_value(world, args.steps, ms)
+    value = args.steps / (ms / 1e3)
     # spread of single steps (each replay between its own events, after the timed region)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(100)]
     for a_, b_ in evs:
@@ -995,17 +969,17 @@ def run_gpu(args):
     stages["tree_hbm_frac"] = round(bytes_["tree"] / (st["tree"] * 1e-6) / 1e9 / pk["hbm"], 4)
 
     e2e = run_e2e(wl, args.steps)
-    batched = run_batched(dev) if (args.batched and rank == 0) else None
-    forward = run_forward(dev) if (args.forward and rank == 0) else None
-    sweep = run_entropy_sweep(dev, wl.W) if (args.sweep and rank == 0) else None
-    verify1 = run_verify1(dev) if (args.sweep and rank == 0) else None
+    batched = run_batched(dev) if args.batched else None
+    forward = run_forward(dev) if args.forward else None
+    sweep = run_entropy_sweep(dev, wl.W) if args.sweep else None
+    verify1 = run_verify1(dev) if args.sweep else None
     code, text = g.device_status()
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(cfg, world),
+        "config": workload_config(cfg),
         "roofline": roofline,
         "stages_us": stages,
         "step_us_percentiles": spread,
@@ -1021,12 +995,9 @@ def run_gpu(args):
     if sweep is not None:
         out["entropy36"] = sweep
         out["verify1"] = verify1
-    if rank == 0:
-        if args.cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(cfg, wl)
-        print(json.dumps(out), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    if args.cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(out), flush=True)
 
 
 def run_e2e(wl, steps):
@@ -1190,141 +1161,139 @@ def run_e2e(wl, steps):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_sample(cfg, x, q_bits, k_bits, v_bits, h_bits, W_bits, root, n_attn_layers, v_frac):
-    """One bounded oracle round; returns (seconds extrapolated to a full round, detail)."""
-    from oracle.attention import tree_attention as o_attn
-    from oracle.bf16 import bf16_bits_to_f64
-    from oracle.lmhead import lmhead_argmax as o_lmhead
-    from oracle.tree import build_tree as o_build
-    from oracle.walk import commit as o_commit
-    from oracle.walk import walk as o_walk
-    T, R = cfg["T"], cfg["N"] + 1
-    t = {}
-    t0 = time.perf_counter()
-    tree = o_build(x.astype(np.float64), cfg["N"], root, T)
-    t["tree"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    for l in range(n_attn_layers):
-        o_attn(bf16_bits_to_f64(q_bits[l]), bf16_bits_to_f64(k_bits[l][:, :T + R]),
-               bf16_bits_to_f64(v_bits[l][:, :T + R]), T, tree["anc"], cfg["D"] ** -0.5)
-    t["attention"] = (time.perf_counter() - t0) / n_attn_layers * cfg["n_layers"]
-    t0 = time.perf_counter()
-    nv = max(1, int(cfg["V"] * v_frac))
-    arg, gap, _ = o_lmhead(bf16_bits_to_f64(h_bits), bf16_bits_to_f64(W_bits[:, :nv]))
-    t["lmhead"] = (time.perf_counter() - t0) * cfg["V"] / nv
-    t0 = time.perf_counter()
-    a, path, _, _ = o_walk(tree, arg, cfg["L"])
-    for l in range(n_attn_layers):
-        o_commit(k_bits[l].copy(), v_bits[l].copy(), T, path)
-    t["commit"] = (time.perf_counter() - t0) / n_attn_layers * cfg["n_layers"]
-    return sum(t.values()), t
+# One bounded oracle step, shared by the GPU line's cpu_baseline and the
+# reference arm, so that both time the same sample with the same scaling.
+ORACLE_SAMPLE = dict(l_sub=3, rows=8, kv_heads=1, layers=1, lm_cols=148)
 
 
-def cpu_baseline(cfg, wl=None, seed=3000):
-    """The oracle as it stands on the host cores, on a bounded sample."""
-    n_layers, v_frac = 2, 1.0 / 16
-    if wl is not None and wl.k_bits is not None:
-        src = wl
-    else:
-        src = HostInputs(cfg, seed)
-    total, parts = oracle_sample(cfg, src.x, src.q_bits, src.k_bits, src.v_bits, src.h_bits,
-                                 src.W_bits, 7, n_layers, v_frac)
-    return {"value": round(1.0 / total, 5), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
-            "sample": f"full tree build; attention on {n_layers} of {cfg['n_layers']} layers; LM head over "
-                      f"1/{int(1 / v_frac)} of the vocabulary; walk + commit on {n_layers} layers; "
-                      f"times scaled to one full round",
-            "stage_seconds_full_round": {k: round(v, 3) for k, v in parts.items()}}
+def oracle_sample_text(cfg):
+    o = ORACLE_SAMPLE
+    return (f"per step: tree build on {o['l_sub']} of {cfg['L']} offsets (x {cfg['L'] / o['l_sub']:g}); "
+            f"attention of {o['rows']} of {cfg['N'] + 1} rows x {o['kv_heads']} of {cfg['Hkv']} kv heads x "
+            f"{o['layers']} of {cfg['n_layers']} layers; LM head over {o['lm_cols']} of {cfg['V']} columns; "
+            f"walk + commit on {o['layers']} of {cfg['n_layers']} layers; each stage's time scaled by "
+            f"its sampled fraction to a full round")
 
 
 class HostInputs:
-    """Host-only copy of the workload's inputs (no GPU), for the oracle leg."""
+    """Host-only inputs of the oracle step (no GPU): the full draft logits,
+    one layer of q/K/V, the LM head's h and ORACLE_SAMPLE['lm_cols'] columns
+    of W, and the full tree built once."""
 
-    def __init__(self, cfg, seed=3000, n_layers=2, v_frac=1.0 / 16):
+    def __init__(self, cfg, seed=3000):
+        from oracle.tree import build_tree as o_build
         gen = W.rng(seed)
         R = cfg["N"] + 1
         t_cap = cfg["T"] + R + 64
         self.x = W.draft_logits_planted(cfg["L"], cfg["V"], seed=seed + 1)
-        self.q_bits = [W.normal_bf16(gen, (R, cfg["Hq"], cfg["D"])) for _ in range(cfg["n_layers"])]
-        self.k_bits, self.v_bits = [], []
-        for l in range(n_layers):
-            self.k_bits.append(W.normal_bf16(gen, (cfg["Hkv"], t_cap, cfg["D"])))
-            self.v_bits.append(W.normal_bf16(gen, (cfg["Hkv"], t_cap, cfg["D"])))
-        nv = max(8, int(cfg["V"] * v_frac))
-        self.W_bits = W.normal_bf16(gen, (cfg["d"], nv), std=0.02)
+        self.q_bits = [W.normal_bf16(gen, (R, cfg["Hq"], cfg["D"]))]
+        self.k_bits = [W.normal_bf16(gen, (cfg["Hkv"], t_cap, cfg["D"]))]
+        self.v_bits = [W.normal_bf16(gen, (cfg["Hkv"], t_cap, cfg["D"]))]
+        self.W_bits = W.normal_bf16(gen, (cfg["d"], ORACLE_SAMPLE["lm_cols"]), std=0.02)
         self.h_bits = W.normal_bf16(gen, (R, cfg["d"]))
+        self.tree = o_build(self.x.astype(np.float64), cfg["N"], 7, cfg["T"])
 
 
-def oracle_step(cfg, src, root, rows=8, l_sub=3):
-    """One bounded reference step: each stage of the round on a small slice,
-    its time scaled to the full stage — the tree build on the first l_sub
-    offsets (x L / l_sub), attention of `rows` rows of one kv head of one layer
-    (x rows of the tree / rows x kv heads x layers), the LM head over
-    src.W_bits' columns (x V / columns), walk + commit on one layer (x layers).
-    Returns (scaled seconds of a full round, per-stage detail)."""
+def oracle_step(cfg, src, root=7):
+    """One bounded oracle step: each stage of the round on the slice that
+    ORACLE_SAMPLE names, its time scaled by the sampled fraction to the full
+    stage. Returns (scaled seconds of a full round, per-stage detail, wall
+    seconds the step took)."""
     from oracle.attention import tree_attention as o_attn
     from oracle.bf16 import bf16_bits_to_f64
     from oracle.lmhead import lmhead_argmax as o_lmhead
     from oracle.tree import build_tree as o_build
     from oracle.walk import commit as o_commit
     from oracle.walk import walk as o_walk
+    o = ORACLE_SAMPLE
     T, R, G = cfg["T"], cfg["N"] + 1, cfg["Hq"] // cfg["Hkv"]
     t = {}
+    w0 = time.perf_counter()
     t0 = time.perf_counter()
-    o_build(src.x[:l_sub].astype(np.float64), cfg["N"], root, T)
-    t["tree"] = (time.perf_counter() - t0) * cfg["L"] / l_sub
+    o_build(src.x[:o["l_sub"]].astype(np.float64), cfg["N"], root, T)
+    t["tree"] = (time.perf_counter() - t0) * cfg["L"] / o["l_sub"]
     tree = src.tree  # the full tree (built once) for the stages below
     t0 = time.perf_counter()
-    o_attn(bf16_bits_to_f64(src.q_bits[0][:rows, :G]), bf16_bits_to_f64(src.k_bits[0][:1, :T + R]),
-           bf16_bits_to_f64(src.v_bits[0][:1, :T + R]), T, tree["anc"][:rows], cfg["D"] ** -0.5)
-    t["attention"] = (time.perf_counter() - t0) * (R / rows) * cfg["Hkv"] * cfg["n_layers"]
+    o_attn(bf16_bits_to_f64(src.q_bits[0][:o["rows"], :G * o["kv_heads"]]),
+           bf16_bits_to_f64(src.k_bits[0][:o["kv_heads"], :T + R]),
+           bf16_bits_to_f64(src.v_bits[0][:o["kv_heads"], :T + R]), T, tree["anc"][:o["rows"]],
+           cfg["D"] ** -0.5)
+    t["attention"] = ((time.perf_counter() - t0) * (R / o["rows"]) * (cfg["Hkv"] / o["kv_heads"])
+                      * cfg["n_layers"] / o["layers"])
     t0 = time.perf_counter()
-    nv = src.W_bits.shape[1]
     arg, _, _ = o_lmhead(bf16_bits_to_f64(src.h_bits), bf16_bits_to_f64(src.W_bits))
-    t["lmhead"] = (time.perf_counter() - t0) * cfg["V"] / nv
+    t["lmhead"] = (time.perf_counter() - t0) * cfg["V"] / src.W_bits.shape[1]
     t0 = time.perf_counter()
     a, path, _, _ = o_walk(tree, arg, cfg["L"])
     o_commit(src.k_bits[0].copy(), src.v_bits[0].copy(), T, path)
-    t["commit"] = (time.perf_counter() - t0) * cfg["n_layers"]
-    return sum(t.values()), t
+    t["commit"] = (time.perf_counter() - t0) * cfg["n_layers"] / o["layers"]
+    return sum(t.values()), t, time.perf_counter() - w0
+
+
+def oracle_summary(cfg, totals, parts, walls):
+    sec = statistics.median(totals)
+    return {"value": round(1.0 / sec, 5), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": oracle_sample_text(cfg), "steps_timed": len(totals),
+            "wall_seconds_per_step": round(statistics.median(walls), 4),
+            "rounds_per_step": round(statistics.median(walls) / sec, 8),
+            "stage_seconds_full_round": {k: round(statistics.median(p[k] for p in parts), 3)
+                                         for k in parts[0]}}
+
+
+def cpu_baseline(cfg, seconds=10.0):
+    """The oracle as it stands on the host cores: the same bounded step as
+    the reference arm, repeated for about `seconds` (at least 3 steps);
+    value = 1 / the median scaled round."""
+    src = HostInputs(cfg)
+    oracle_step(cfg, src)
+    totals, parts, walls = [], [], []
+    t0 = time.perf_counter()
+    while len(totals) < 3 or time.perf_counter() - t0 < seconds:
+        tt, pp, ww = oracle_step(cfg, src)
+        totals.append(tt)
+        parts.append(pp)
+        walls.append(ww)
+    return oracle_summary(cfg, totals, parts, walls)
 
 
 def run_reference(args):
     """The oracle (the reference arm of this build), as it stands, on the
-    host cores: every step is a bounded slice of the round (oracle_step, about
-    0.1 s on a GB300 host), scaled to a full round, so that any --steps K
-    ends in a few minutes."""
-    from oracle.tree import build_tree as o_build
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
-        return
+    host cores: every step is the bounded oracle step (about 0.1 s on a GB300
+    host), scaled to a full round, so that any --steps K ends in a few
+    minutes. ms_per_step is the wall time a step took; rounds_per_step is the
+    fraction of a round it covers, so value = rounds_per_step / step time."""
     cfg = SMALL if args.workload == "small" else FULL36
-    src = HostInputs(cfg, n_layers=1, v_frac=1.0 / 1024)
-    src.tree = o_build(src.x.astype(np.float64), cfg["N"], 7, cfg["T"])
+    src = HostInputs(cfg)
     for _ in range(args.warmup):
-        oracle_step(cfg, src, 7)
-    totals, parts = [], []
+        oracle_step(cfg, src)
+    totals, parts, walls = [], [], []
     for _ in range(args.steps):
-        tt, pp = oracle_step(cfg, src, 7)
+        tt, pp, ww = oracle_step(cfg, src)
         totals.append(tt)
         parts.append(pp)
-    sec = statistics.median(totals)
-    value = 1.0 / sec
-    sample = (f"per step: tree build on 3 of {cfg['L']} offsets, attention of 8 rows x 1 kv head x 1 of "
-              f"{cfg['n_layers']} layers, LM head over {src.W_bits.shape[1]} of {cfg['V']} columns, walk + "
-              f"commit on 1 layer; each stage's time scaled to the full round")
-    out = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "rounds/s",
-           "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        walls.append(ww)
+    base = oracle_summary(cfg, totals, parts, walls)
+    value = base["value"]
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(statistics.median(walls) * 1e3, 2),
+           "rounds_per_step": base["rounds_per_step"],
+           "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": workload_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
-           "cpu_baseline": {"value": round(value, 5), "unit": "rounds/s",
-                            "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": sample,
-                            "stage_seconds_full_round": {k: round(statistics.median(p[k] for p in parts), 3)
-                                                         for k in parts[0]} if parts else {}},
-           "e2e": {"value": round(value, 5), "unit": "rounds/s", "h2d_bytes_per_step": 0,
+           "config": workload_config(cfg), "cpu_baseline": base,
+           "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def run_unavailable(args):
+    """More than one GPU: the path is per request (one GPU per request, no
+    exchange), so this benchmark runs on one GPU only."""
+    if os.environ.get("RANK", "0") != "0":
+        return
+    print(json.dumps({"impl": args.impl, "metric": METRIC, "n_gpus": args.gpus,
+                      "unavailable": "single-GPU benchmark: a verify round runs on one GPU; "
+                                     "more GPUs would only run independent replicas"}), flush=True)
 
 
 def main():
@@ -1346,7 +1315,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.case:
+    if args.gpus != 1:
+        run_unavailable(args)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -1,48 +1,15 @@
-"""Host-side logic of bench.py on CPU: the N>1 replica path's max-over-ranks
-timing and whole-job aggregation, run as two gloo ranks."""
+"""Host-side logic of bench.py on CPU: the traffic figures' source guard, the
+reference arm and the CPU baseline (both the oracle on the host cores, on the
+same bounded sample), and the single-GPU refusal of --gpus N > 1."""
+import json
 import os
+import subprocess
 import sys
+import time
 
 import pytest
-import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-
-
-def _rank(rank, world, port, q):
-    import torch.distributed as dist
-    sys.path.insert(0, ROOT)
-    import bench
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    ms = 100.0 + 50.0 * rank          # rank 1 is slower
-    m = bench.max_over_ranks(ms, dist, "cpu")
-    q.put((rank, m, bench.job_value(world, 10, m)))
-    dist.barrier()
-    dist.destroy_process_group()
-
-
-def test_two_gloo_ranks_take_the_slowest_time():
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = 29500 + os.getpid() % 1000
-    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    out = sorted(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    for rank, m, v in out:
-        assert m == 150.0
-        assert v == pytest.approx(2 * 10 / 0.150)
-
-
-def test_single_process_value():
-    sys.path.insert(0, ROOT)
-    import bench
-    assert bench.max_over_ranks(12.5, None, "cpu") == 12.5
-    assert bench.job_value(1, 50, 1000.0) == pytest.approx(50.0)
 
 
 def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch):
@@ -62,10 +29,6 @@ def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch)
 def test_reference_arm_prints_one_bounded_line():
     """The reference arm (the oracle on the host cores) runs on the small
     workload without a GPU and prints the contract's line."""
-    import json
-    import subprocess
-    import sys
-    import time
     t0 = time.perf_counter()
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
                           "small", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300,
@@ -75,3 +38,24 @@ def test_reference_arm_prints_one_bounded_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "rounds/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert time.perf_counter() - t0 < 120
+    assert line["n_gpus"] == 1 and 0 < line["rounds_per_step"] < 1
+    # value = the round fraction a step covers / the step's wall time
+    assert line["value"] == pytest.approx(line["rounds_per_step"] / (line["ms_per_step"] / 1e3), rel=0.05)
+
+
+def test_cpu_baseline_uses_the_reference_arms_sample():
+    sys.path.insert(0, ROOT)
+    import bench
+    cb = bench.cpu_baseline(bench.SMALL, seconds=0.0)
+    assert cb["kind"] == "oracle" and cb["steps_timed"] >= 3 and cb["cores"] >= 1
+    assert cb["sample"] == bench.oracle_sample_text(bench.SMALL)
+    assert set(cb["stage_seconds_full_round"]) == {"tree", "attention", "lmhead", "commit"}
+
+
+def test_more_than_one_gpu_is_refused_with_a_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT,
+                         env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["n_gpus"] == 2 and "unavailable" in line
