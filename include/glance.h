@@ -45,8 +45,9 @@
  *   them (thread-local text). A failed launch returns GLANCE_ERR_CUDA. Errors
  *   that only the device can see (non-finite draft logits, a prefix length
  *   that leaves no room for the tree rows, a pipeline wait that ran out) set a
- *   device status word and the kernel returns early; glance_device_status()
- *   reads it.
+ *   device status word and the kernel returns early; glance_get_status()
+ *   copies the words out in stream order, glance_device_status() reads them
+ *   after a device synchronisation.
  * - Packed tree layout (rows = N + 1; row 0 is the pending root b): rows are
  *   in canonical order: root, then by depth ascending, then by parent row
  *   ascending, then by the node's rank in its offset's candidate list
@@ -475,6 +476,30 @@ glance_status glance_device_status(int32_t* code_out);
 
 /* Clears the device status word of the current device (synchronous). */
 glance_status glance_reset_device_status(void);
+
+/* Number of int32 words glance_get_status writes. */
+#define GLANCE_STATUS_WORDS 6
+
+/*
+ * Stream-ordered read of the device status words: enqueues on `stream`, after
+ * the work already there, copies of the status word of each kernel family
+ * into status_out[1..5] (tree build, tree attention, LM head, walk + commit,
+ * dense layers) and a one-thread kernel that stores the first non-zero of
+ * them in status_out[0] (0 if none). status_out: GLANCE_STATUS_WORDS int32,
+ * device memory or pinned / managed host memory (the caller reads it once
+ * the stream has reached this point). No host or device-wide synchronisation,
+ * so a serving loop can append it to every captured round. The words are not
+ * cleared; glance_clear_status clears them. Null status_out:
+ * GLANCE_ERR_INVALID_ARG. Make the first call on a device outside any stream
+ * capture: resolving the words may load the library's device code.
+ */
+glance_status glance_get_status(int32_t* status_out, void* stream);
+
+/* Stream-ordered clear of every device status word (a memset each, enqueued
+ * on `stream`). The words' addresses are looked up on each call with the
+ * current device; the lookup enqueues nothing. As for glance_get_status, make
+ * the first call on a device outside any stream capture. */
+glance_status glance_clear_status(void* stream);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int glance_version(void);

@@ -11,11 +11,12 @@ The compute lives in ``libglance.so`` (CUDA kernels behind a C ABI declared in
 ``*_batched`` forms run B independent requests (ragged prefix lengths) in one
 launch per step; the LM head takes the B requests' rows stacked.
 """
-from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
+from ._binding import (STATUS_WORDS, BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree, accept_commit,
                        accept_commit_batched, accept_commit_batched_workspace_bytes,
                        accept_commit_gated, accept_commit_gated_batched, lmhead_argmax_entropy,
                        lmhead_sample,
-                       accept_commit_workspace_bytes, build_tree, build_tree_batched,
+                       accept_commit_workspace_bytes, build_tree, build_tree_batched, clear_status,
+                       get_status,
                        build_tree_batched_workspace_bytes, build_tree_shared,
                        build_tree_shared_workspace_bytes, build_tree_workspace_bytes,
                        dense_qkv, dense_residual, dense_swiglu,
@@ -24,11 +25,11 @@ from ._binding import (BF16, EXPORTS, F32, LIB_PATH, GlanceError, KVLayer, Tree,
                        tree_attention_batched, tree_attention_batched_workspace_bytes,
                        tree_attention_workspace_bytes, version, workspace)
 
-__all__ = ["BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
+__all__ = ["STATUS_WORDS", "BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", "KVLayer", "Tree",
            "accept_commit", "accept_commit_batched", "accept_commit_batched_workspace_bytes",
            "accept_commit_gated", "accept_commit_gated_batched", "lmhead_argmax_entropy",
            "lmhead_sample",
-           "accept_commit_workspace_bytes", "build_tree", "build_tree_batched",
+           "accept_commit_workspace_bytes", "build_tree", "build_tree_batched", "clear_status", "get_status",
            "build_tree_batched_workspace_bytes", "build_tree_shared",
            "build_tree_shared_workspace_bytes", "build_tree_workspace_bytes", "dense_qkv",
            "dense_residual", "dense_swiglu", "device_status", "row_sumsq",

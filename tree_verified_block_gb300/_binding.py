@@ -32,7 +32,7 @@ EXPORTS = [
     "glance_dense_residual", "glance_dense_swiglu",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
-    "glance_reset_device_status", "glance_version",
+    "glance_reset_device_status", "glance_get_status", "glance_clear_status", "glance_version",
 ]
 
 
@@ -140,6 +140,10 @@ def lib():
     L.glance_device_status.restype = st
     L.glance_reset_device_status.argtypes = []
     L.glance_reset_device_status.restype = st
+    L.glance_get_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    L.glance_get_status.restype = st
+    L.glance_clear_status.argtypes = [ctypes.c_void_p]
+    L.glance_clear_status.restype = st
     L.glance_version.argtypes = []
     L.glance_version.restype = ctypes.c_int
     _lib = L
@@ -445,6 +449,26 @@ def device_status():
 
 def reset_device_status():
     _check(lib().glance_reset_device_status())
+
+
+STATUS_WORDS = 6
+
+
+def get_status(out, stream=None):
+    """Enqueue the stream-ordered status read: out (int32 [6], CUDA or pinned
+    host tensor) gets the first non-zero word in out[0] and the words of the
+    tree build, attention, LM head, commit and dense kernels in out[1..5]."""
+    assert out.dtype == torch.int32 and out.numel() >= STATUS_WORDS and out.is_contiguous()
+    if not (out.is_cuda or out.is_pinned()):
+        raise ValueError("glance: get_status needs a CUDA or pinned host tensor")
+    dev = out.device if out.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    _check(lib().glance_get_status(ctypes.c_void_p(out.data_ptr()), _stream(stream, dev)))
+
+
+def clear_status(stream=None, device=None):
+    """Enqueue a clear of every device status word on the stream."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(lib().glance_clear_status(_stream(stream, dev)))
 
 
 def version():

@@ -125,6 +125,52 @@ static glance_status read_all_status(int32_t* code_out, bool reset) {
 
 glance_status glance_device_status(int32_t* code_out) { return read_all_status(code_out, false); }
 
+namespace {
+
+// out[0] = the first non-zero of out[1..n] (0 if none)
+__global__ void first_status_kernel(int32_t* out, int n) {
+  int first = 0;
+  for (int i = 1; i <= n; ++i) {
+    const int v = out[i];
+    if (!first && v) first = v;
+  }
+  out[0] = first;
+}
+
+constexpr int kStatusUnits = 5;
+
+}  // namespace
+
+glance_status glance_get_status(int32_t* status_out, void* stream) {
+  if (!status_out) return glance::fail(GLANCE_ERR_INVALID_ARG, "glance_get_status: null status_out");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t (*fns[kStatusUnits])(int*, cudaStream_t) = {
+      glance::status_build_tree_async, glance::status_attention_async, glance::status_lmhead_async,
+      glance::status_commit_async, glance::status_dense_async};
+  for (int i = 0; i < kStatusUnits; ++i) {
+    cudaError_t e = fns[i](status_out + 1 + i, s);
+    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_get_status");
+  }
+  first_status_kernel<<<1, 1, 0, s>>>(status_out, kStatusUnits);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, "glance_get_status");
+  return GLANCE_OK;
+}
+
+glance_status glance_clear_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t (*fns[kStatusUnits])(void**) = {glance::status_build_tree_addr, glance::status_attention_addr,
+                                              glance::status_lmhead_addr, glance::status_commit_addr,
+                                              glance::status_dense_addr};
+  for (int i = 0; i < kStatusUnits; ++i) {
+    void* a = nullptr;
+    cudaError_t e = fns[i](&a);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a, 0, sizeof(int), s);
+    if (e != cudaSuccess) return glance::cuda_fail(e, "glance_clear_status");
+  }
+  return GLANCE_OK;
+}
+
 glance_status glance_reset_device_status(void) {
   int32_t dummy = 0;
   return read_all_status(&dummy, true);

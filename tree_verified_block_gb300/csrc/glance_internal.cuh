@@ -38,12 +38,18 @@ glance_status make_map_bf16(CUtensorMap* map, const void* base, int rank, const 
                             const uint64_t* strides_bytes, const uint32_t* box,
                             CUtensorMapSwizzle swz, const char* what);
 
-// Per translation unit: read (and optionally clear) that unit's status word.
-cudaError_t status_build_tree(int* out, bool reset);
-cudaError_t status_attention(int* out, bool reset);
-cudaError_t status_lmhead(int* out, bool reset);
-cudaError_t status_commit(int* out, bool reset);
-cudaError_t status_dense(int* out, bool reset);
+// Per translation unit: read (and optionally clear) that unit's status word
+// synchronously; enqueue a copy of it to `dst` (any address the copy engine
+// reaches) on a stream; look up its device address (for an asynchronous clear).
+#define GLANCE_DECLARE_STATUS_WORD(fn)                          \
+  cudaError_t fn(int* out, bool reset);                         \
+  cudaError_t fn##_async(int* dst, cudaStream_t stream);        \
+  cudaError_t fn##_addr(void** addr);
+GLANCE_DECLARE_STATUS_WORD(status_build_tree)
+GLANCE_DECLARE_STATUS_WORD(status_attention)
+GLANCE_DECLARE_STATUS_WORD(status_lmhead)
+GLANCE_DECLARE_STATUS_WORD(status_commit)
+GLANCE_DECLARE_STATUS_WORD(status_dense)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -60,6 +66,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
     }                                                                              \
     return e;                                                                      \
   }                                                                                \
+  cudaError_t fn##_async(int* dst, cudaStream_t stream) {                          \
+    return cudaMemcpyFromSymbolAsync(dst, g_status_word, sizeof(int), 0,           \
+                                     cudaMemcpyDefault, stream);                   \
+  }                                                                                \
+  cudaError_t fn##_addr(void** addr) { return cudaGetSymbolAddress(addr, g_status_word); } \
   }                                                                                \
   static __device__ __forceinline__ void report(int code) {                        \
     atomicCAS(&g_status_word, 0, code);                                            \
