@@ -243,15 +243,21 @@ glance_status glance_lmhead_sample(const void* h, const void* W, glance_dtype dt
  * cudaMalloc, or an engine that has reserved all device memory for its own
  * pool and has none to lend.
  *
- * Same computation, arguments and outputs as glance_lmhead_argmax, BF16 only
+ * Same results, arguments and outputs as glance_lmhead_argmax, BF16 only
  * (d % 64 == 0, V % 8 == 0, 1 <= M <= 512; anything else is rejected with an
- * error, F32 with GLANCE_ERR_UNSUPPORTED). Its scratch (a merge ticket and the
+ * error, F32 with GLANCE_ERR_UNSUPPORTED). Cost: the rows run in blocks of
+ * 128, one launch per block, and each launch streams all of W, so a call with
+ * M > 128 reads W ceil(M / 128) times (about 5 GB at M = 512, V = 151936,
+ * d = 4096, against 1.25 GB for glance_lmhead_argmax). Its scratch (a merge ticket and the
  * partial results of at most 160 CTAs, 240 KB in total) is a file-scope device
  * array of the library, held by every GPU that loads the library until the
  * process exits. Each call clears the ticket with cudaMemsetAsync on `stream`;
  * no call makes cudaMalloc, cudaFree or any other allocating call. The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current: make that first call before any stream capture.
+ * The address is kept with the device's context and looked up again (the
+ * same set-up) on the first call after that context changes, e.g. after
+ * cudaDeviceReset.
  * All calls on a device share the array, which keeps the last call's
  * contents, so calls that may overlap on the GPU (other streams or threads)
  * race with each other: serialise them.

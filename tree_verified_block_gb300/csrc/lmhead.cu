@@ -1200,11 +1200,34 @@ constexpr size_t kNoAllocScratchBytes =
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device with that device current (in host code the array's name is only
-// a stand-in, not a device address).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The driver's current context, fetched through the runtime (no link-time
+// dependency on libcuda); null if the entry point is unavailable.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up with
+// that device current (in host code the array's name is only a stand-in, not
+// a device address). The address is kept per device together with the
+// context it was looked up in, and looked up again when the device's context
+// has changed (after cudaDeviceReset, for example).
 glance_status noalloc_scratch(void** out) {
   static void* addr[64] = {nullptr};
+  static CUcontext ctx[64] = {nullptr};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1212,12 +1235,14 @@ glance_status noalloc_scratch(void** out) {
   if (dev < 0 || dev >= 64)
     return glance::fail(GLANCE_ERR_UNSUPPORTED, "glance_lmhead_argmax_noalloc: device index %d", dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const CUcontext cur = current_context();
+  if (!addr[dev] || !cur || cur != ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess)
       return glance::cuda_fail(e, "glance_lmhead_argmax_noalloc: cudaGetSymbolAddress");
     addr[dev] = p;
+    ctx[dev] = current_context();
   }
   *out = addr[dev];
   return GLANCE_OK;
@@ -1253,7 +1278,8 @@ extern "C" glance_status glance_lmhead_argmax_noalloc(const void* h, const void*
   uint32_t* ticket = static_cast<uint32_t*>(scratch);
   Partial* part = reinterpret_cast<Partial*>(static_cast<char*>(scratch) + 256);
   // rows in blocks of 128, one launch each (the scratch holds the partials of
-  // one block for at most kNoAllocMaxCtas CTAs)
+  // one block for at most kNoAllocMaxCtas CTAs): each launch streams all of W,
+  // so a call with M > 128 reads W ceil(M / 128) times
   for (int r0 = 0; r0 < M; r0 += kBM) {
     const int mb = M - r0 < kBM ? M - r0 : kBM;
     st = launch_bf16<1, kGreedy>(static_cast<const uint16_t*>(h) + static_cast<size_t>(r0) * d, W, mb,
