@@ -85,7 +85,7 @@ typedef enum { GLANCE_F32 = 0, GLANCE_BF16 = 1 } glance_dtype;
 #define GLANCE_DEV_NONFINITE_LOGITS 1 /* a draft logit row held NaN or +-inf */
 #define GLANCE_DEV_TREE_CAPACITY 2    /* the rows' K/V slots do not fit: T + rows > t_cap */
 #define GLANCE_DEV_BAD_TREE 3         /* a tree array was inconsistent */
-#define GLANCE_DEV_PIPELINE_TIMEOUT 4 /* an mbarrier wait hit its iteration cap */
+#define GLANCE_DEV_PIPELINE_TIMEOUT 4 /* a pipeline wait ran out of time (2 s) */
 
 /* A packed candidate tree: device arrays with N + 1 rows, caller-allocated. */
 typedef struct {
@@ -173,6 +173,24 @@ size_t glance_tree_attention_workspace_bytes(int n_rows, int n_q_heads, const gl
 glance_status glance_tree_attention(const void* q, int n_q_heads, const glance_kv* kv,
                                     const glance_tree* tree, float scale, void* out,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Check of the bf16 attention kernel's failure path (no counterpart in the
+ * paper; for tests and health checks). Runs glance_tree_attention with every
+ * pipeline wait limited to wait_ns nanoseconds (1 us .. 2 s; the normal call
+ * uses 2 s) and with the copy of each CTA's last key tile of V never made,
+ * unless that tile was fetched before the call's dependency wait, so that the
+ * MMA warp's wait for it runs out. That CTA then sets device status 4
+ * (GLANCE_DEV_PIPELINE_TIMEOUT), lets its other roles leave, waits for its
+ * copies in flight, frees its tensor memory and returns; the launch ends
+ * normally and the context stays usable. out is left undefined. Arguments as
+ * for glance_tree_attention, BF16 only.
+ */
+glance_status glance_tree_attention_timeout_check(const void* q, int n_q_heads,
+                                                  const glance_kv* kv, const glance_tree* tree,
+                                                  float scale, void* out, void* workspace,
+                                                  size_t workspace_bytes,
+                                                  unsigned long long wait_ns, void* stream);
 
 /* ----------------------------------------------------------------- LM head */
 

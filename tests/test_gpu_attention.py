@@ -150,3 +150,33 @@ def test_capacity_error_on_device(dev):
     code, _ = g.device_status()
     g.reset_device_status()
     assert code == 2
+
+
+@pytest.mark.parametrize("T,N", [(1000, 63), (4096, 63), (130, 15)])
+def test_bf16_cache_slots_past_the_tree_may_hold_nan(dev, clean_status, T, N):
+    """Slots T + N + 1 .. t_cap - 1 of the cache are not part of the call
+    (Definition 1: a row sees the prefix and its ancestors only). They may
+    hold anything, NaN included: the output must not change."""
+    import tree_verified_block_gb300 as g
+    D, Hq, Hkv, L = 128, 32, 8, 15
+    rows = N + 1
+    t_cap = T + rows + 200
+    ref = random_tree(N, L, T, 11)
+    gen = W.rng(11, 7)
+    kb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    vb = W.normal_bf16(gen, (Hkv, t_cap, D))
+    qb = W.normal_bf16(gen, (rows, Hq, D))
+    kb[:, T + rows:] = 0x7FC0  # bf16 quiet NaN
+    vb[:, T + rows:] = 0x7FC0
+    t_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    layer = g.KVLayer(bf16_tensor(kb, dev), bf16_tensor(vb, dev), t_len)
+    tree = upload_tree(ref, L, dev)
+    q = bf16_tensor(qb, dev)
+    out = torch.full_like(q, float("nan"))
+    ws = g.workspace(g.tree_attention_workspace_bytes(rows, Hq, layer), dev)
+    g.tree_attention(q, layer, tree, D ** -0.5, out, ws)
+    want = o_attn(bf16_bits_to_f64(qb), bf16_bits_to_f64(kb[:, :T + rows]), bf16_bits_to_f64(vb[:, :T + rows]),
+                  T, ref["anc"], D ** -0.5)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    assert np.abs(got - want).max() < 2e-2

@@ -63,3 +63,45 @@ def test_get_status_refuses_pageable_host_memory(dev):
     import tree_verified_block_gb300 as g
     with pytest.raises(ValueError):
         g.get_status(torch.zeros(g.STATUS_WORDS, dtype=torch.int32))
+
+
+def test_a_pipeline_wait_that_runs_out_sets_status_4_and_returns(dev):
+    """The kernel's bounded waits: with one V copy withheld per CTA and a
+    1 ms limit, the MMA warp's wait runs out; the CTA reports status 4 and
+    leaves (the other roles see its abort flag), the launch ends normally, the
+    context stays usable and the next ordinary call is correct."""
+    import time
+
+    import tree_verified_block_gb300 as g
+    from test_gpu_attention import run_bf16
+    from _util import bf16_tensor
+    import workloads as W
+    T, N, Hq, Hkv, D = 1000, 63, 32, 8, 128
+    rows = N + 1
+    ref = random_tree(N, 15, T, 3)
+    gen = W.rng(3, 7)
+    t_cap = T + rows + 5
+    K = bf16_tensor(W.normal_bf16(gen, (Hkv, t_cap, D)), dev)
+    V = bf16_tensor(W.normal_bf16(gen, (Hkv, t_cap, D)), dev)
+    q = bf16_tensor(W.normal_bf16(gen, (rows, Hq, D)), dev)
+    t_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    layer = g.KVLayer(K, V, t_len)
+    tree = upload_tree(ref, 15, dev)
+    out = torch.empty_like(q)
+    ws = g.workspace(g.tree_attention_workspace_bytes(rows, Hq, layer), dev)
+    g.reset_device_status()
+    status = torch.full((g.STATUS_WORDS,), -1, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+    g.tree_attention_timeout_check(q, layer, tree, D ** -0.5, out, ws, 1_000_000)
+    g.get_status(status)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert status.cpu().tolist() == [4, 0, 4, 0, 0, 0]
+    assert elapsed < 1.5   # 1 ms waits, not the 2 s default
+    g.clear_status()
+    torch.cuda.synchronize()
+    # the context is usable and the ordinary call is right again
+    got, want = run_bf16(T, N, Hq, Hkv, dev, seed=3)
+    assert np.abs(got - want).max() < 2e-2
+    code, _ = g.device_status()
+    assert code == 0

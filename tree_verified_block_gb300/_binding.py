@@ -21,6 +21,7 @@ DEV_STATUS = {0: "ok", 1: "non-finite draft logits", 2: "tree does not fit the c
 EXPORTS = [
     "glance_build_tree_workspace_bytes", "glance_build_tree",
     "glance_tree_attention_workspace_bytes", "glance_tree_attention",
+    "glance_tree_attention_timeout_check",
     "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax", "glance_lmhead_argmax_noalloc",
     "glance_accept_commit_workspace_bytes", "glance_accept_commit",
     "glance_build_tree_batched_workspace_bytes", "glance_build_tree_batched",
@@ -79,6 +80,9 @@ def lib():
     L.glance_tree_attention.argtypes = [vp, i32, ctypes.POINTER(KVC), ctypes.POINTER(TreeC),
                                         ctypes.c_float, vp, vp, sz, vp]
     L.glance_tree_attention.restype = st
+    L.glance_tree_attention_timeout_check.argtypes = [vp, i32, ctypes.POINTER(KVC), ctypes.POINTER(TreeC),
+                                                      ctypes.c_float, vp, vp, sz, ctypes.c_ulonglong, vp]
+    L.glance_tree_attention_timeout_check.restype = st
     L.glance_lmhead_argmax_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.glance_lmhead_argmax_workspace_bytes.restype = sz
     L.glance_lmhead_argmax.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -243,6 +247,17 @@ def tree_attention(q, kv, tree, scale, out, ws, stream=None):
     _check(lib().glance_tree_attention(_ptr(q), q.shape[1], ctypes.byref(kv.c),
                                        ctypes.byref(tree.c), float(scale), _ptr(out), _ptr(ws),
                                        ws.numel(), _stream(stream, q.device)))
+
+
+def tree_attention_timeout_check(q, kv, tree, scale, out, ws, wait_ns, stream=None):
+    """The bf16 attention call with every pipeline wait limited to wait_ns and
+    one key tile's V copy withheld: the kernel must set device status 4 and
+    return (include/glance.h)."""
+    assert q.is_contiguous() and out.is_contiguous() and q.shape == out.shape
+    _check(lib().glance_tree_attention_timeout_check(_ptr(q), q.shape[1], ctypes.byref(kv.c),
+                                                     ctypes.byref(tree.c), float(scale), _ptr(out),
+                                                     _ptr(ws), ws.numel(), int(wait_ns),
+                                                     _stream(stream, q.device)))
 
 
 def lmhead_argmax_workspace_bytes(M, d, V, dtype):

@@ -147,6 +147,7 @@ constexpr int kThreads = 384;    // 12 warps: TMA, MMA, TMEM, idle, 2 x 4 softma
 constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64 used)
 constexpr int kMaxSplit = 16;    // key splits of one (kv head, q tile)
 constexpr int kMaxB = 16;        // requests of one batched call
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // pipeline wait limit: 2 s
 constexpr uint32_t kHalfBytes = kBN * 128;          // 64 head dims x 128 slots, bf16: 16 KB
 constexpr uint32_t kQBytes = 2 * kBM * 128;         // 32 KB
 constexpr uint32_t kKVStageBytes = 4 * kHalfBytes;  // K and V, two halves each: 64 KB
@@ -175,6 +176,9 @@ struct Bf16Params {
   int ticket_merge;          // 1: the last split CTA of a group merges it (any grid);
                              // 0: all splits wait for each other (cooperative launch)
   float scale_log2;          // scale * log2(e)
+  unsigned long long wait_ns;  // limit of every pipeline wait
+  int withhold_v;            // 1: the producer never copies the V of a CTA's last key tile
+                             //    (the timeout check's wait that runs out)
 };
 
 // K and V tensor maps of every request's cache of this layer
@@ -193,6 +197,7 @@ struct __align__(8) Bars {
   uint64_t p_ready;
   uint64_t o_done;
   uint64_t merge_full;       // ticket-mode merge: partials staged in shared memory
+  uint64_t mma_drain;        // every MMA of the CTA has finished
   uint32_t tmem_base;
   int abort_flag;
   float xch[2][kBM];         // [half][row]: partial max / sum exchange
@@ -205,14 +210,15 @@ __device__ __forceinline__ void fail_pipeline(Bars* bars) {
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) return false;
-      if (globaltimer_ns() - t0 > 2000000000ull) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }
@@ -271,7 +277,7 @@ __device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char*
     bulk_copy_g2s(s_o, p.part_o + static_cast<size_t>(slot) * 16 * kBM,
                   static_cast<uint32_t>(c0 * kBM * kD * 2), &bars->merge_full);
   }
-  const bool got = mbar_wait(&bars->merge_full, 0, 2000000000ull);
+  const bool got = mbar_wait(&bars->merge_full, 0, p.wait_ns);
   if (half == 0) {
     float M = -INFINITY;
     for (int sx = 0; sx < S; ++sx) M = fmaxf(M, s_ml[sx * kBM + lrow].x);
@@ -301,7 +307,7 @@ __device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char*
         bulk_copy_g2s(s_o, p.part_o + static_cast<size_t>(slot + base) * 16 * kBM,
                       static_cast<uint32_t>(cnt * kBM * kD * 2), &bars->merge_full);
       }
-      bad = named_bar_or(1, 256, !mbar_wait(&bars->merge_full, k & 1, 2000000000ull));
+      bad = named_bar_or(1, 256, !mbar_wait(&bars->merge_full, k & 1, p.wait_ns));
       if (bad) break;
     }
     for (int sx = 0; sx < cnt; ++sx) {
@@ -409,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->merge_full, 1);
+    mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -532,16 +539,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && my_tiles > 0) {
       const uint64_t pol_kv = policy_evict_first();
       int issued = pre;
+      // the timeout check's copy that is never made (the last tile's V,
+      // unless it went out before the dependency wait)
+      auto withheld = [&](int j) { return p.withhold_v && j == my_tiles - 1 && j >= pre; };
       for (int j = pre; j < my_tiles; ++j) {
         const int st = j % kStages;
         // Every CTA of the grid starts at once: the first tile of all of them
         // goes out alone, so that Q and K/V of tile 0 land (and the first MMA
         // starts) before the rest of the ring competes for DRAM.
-        if (j == 1 && !wait_or_abort(&bars->k_full[0], 0, bars)) {
+        if (j == 1 && !wait_or_abort(&bars->k_full[0], 0, bars, p.wait_ns)) {
           fail_pipeline(bars);
           break;
         }
-        if (j >= kStages && !wait_or_abort(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars)) {
+        if (j >= kStages && !wait_or_abort(&bars->kv_empty[st], ((j / kStages) - 1) & 1, bars, p.wait_ns)) {
           fail_pipeline(bars);
           break;
         }
@@ -552,18 +562,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->k_full[st], 2 * kHalfBytes);
         tma_load_3d(stage + 0 * kHalfBytes, map_k, &bars->k_full[st], 0, key0, g, pol_kv);
         tma_load_3d(stage + 1 * kHalfBytes, map_k, &bars->k_full[st], 64, key0, g, pol_kv);
-        mbar_arrive_expect_tx(&bars->v_full[st], 2 * kHalfBytes);
-        tma_load_3d(stage + 2 * kHalfBytes, map_v, &bars->v_full[st], 0, key0, g, pol_kv);
-        tma_load_3d(stage + 3 * kHalfBytes, map_v, &bars->v_full[st], 64, key0, g, pol_kv);
+        if (!withheld(j)) {
+          mbar_arrive_expect_tx(&bars->v_full[st], 2 * kHalfBytes);
+          tma_load_3d(stage + 2 * kHalfBytes, map_v, &bars->v_full[st], 0, key0, g, pol_kv);
+          tma_load_3d(stage + 3 * kHalfBytes, map_v, &bars->v_full[st], 64, key0, g, pol_kv);
+        }
         ++issued;
       }
-      if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
-        // let copies already in flight land before the CTA's smem is released
+      {
+        // Copies still in flight land before the CTA's smem is released (they
+        // have, unless another role gave up early): Q and the last kStages
+        // tiles issued, the only ones whose stage barrier has not moved on.
         (void)mbar_wait(&bars->q_full, 0, 50000000ull);
         for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
         {
           (void)mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, 50000000ull);
-          (void)mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, 50000000ull);
+          if (!withheld(j)) (void)mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, 50000000ull);
         }
       }
     }
@@ -575,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(sQ);
       auto issue_qk = [&](int j) -> bool {
         const int st = j % kStages;
-        if (!wait_or_abort(&bars->k_full[st], (j / kStages) & 1, bars)) return false;
+        if (!wait_or_abort(&bars->k_full[st], (j / kStages) & 1, bars, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sKV + st * kKVStageBytes);
         const uint32_t tS = tS0 + (j & 1) * 128;
@@ -589,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->s_full[j & 1]);
         return true;
       };
-      bool good = wait_or_abort(&bars->q_full, 0, bars) && issue_qk(0);
+      bool good = wait_or_abort(&bars->q_full, 0, bars, p.wait_ns) && issue_qk(0);
       for (int j = 0; good && j < my_tiles; ++j) {
         // S of the next tile goes into the other buffer while tile j's softmax runs;
         // that buffer was last read by the softmax of tile j-1, which p_ready(j-1) covered
@@ -597,16 +611,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           good = false;
           break;
         }
-        if (!wait_or_abort(&bars->p_ready, j & 1, bars) ||
-            !wait_or_abort(&bars->v_full[j % kStages], (j / kStages) & 1, bars)) {
+        if (!wait_or_abort(&bars->p_ready, j & 1, bars, p.wait_ns) ||
+            !wait_or_abort(&bars->v_full[j % kStages], (j / kStages) & 1, bars, p.wait_ns)) {
           good = false;
           break;
         }
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sKV + (j % kStages) * kKVStageBytes) + 2 * kHalfBytes;
-        // O += P V over 128 key slots = 8 steps of 16 (8 bf16-pair columns of P each)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        // O += P V over the tile's key slots, 16 per step (8 bf16-pair columns
+        // of P each). The last tile of the key range stops at the first step
+        // boundary past T + rows; the V rows of that step beyond T + rows are
+        // never weighted (P = 0) but may hold anything, even NaN (0 * NaN =
+        // NaN), so they are zeroed first.
+        int steps = 8;
+        const int key0 = (tile0 + j) * kBN;
+        if (key0 + kBN > n_keys) {
+          const int valid_rows = n_keys - key0;
+          steps = (valid_rows + 15) / 16;
+          unsigned char* vs = sKV + (j % kStages) * kKVStageBytes + 2 * kHalfBytes;
+          for (int i = valid_rows * 16; i < steps * 16 * 16; ++i)  // (row, 16-byte chunk), 8 chunks per half
+            reinterpret_cast<uint4*>(vs + ((i & 15) >> 3) * kHalfBytes + (i >> 4) * 128)[i & 7] =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        for (int kk = 0; kk < steps; ++kk)
           mma_bf16_ts(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_o,
                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->o_done);
@@ -614,6 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + kStages < my_tiles) mma_commit(&bars->kv_empty[j % kStages]);
       }
       if (!good) fail_pipeline(bars);
+      // every MMA issued has finished before tensor memory is freed
+      mma_commit(&bars->mma_drain);
+      (void)mbar_wait(&bars->mma_drain, 0, 50000000ull);
     }
   } else if (is_sm) {
     // ------------------------------------------------------------ softmax
@@ -627,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < my_tiles; ++j) {
       const int key0 = (tile0 + j) * kBN;
       // warp-uniform: tcgen05.ld / st below are warp-collective
-      const bool got_s = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[j & 1], (j >> 1) & 1, bars));
+      const bool got_s = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[j & 1], (j >> 1) & 1, bars, p.wait_ns));
       if (!got_s) fail_pipeline(bars);
       tc_fence_after();
       const uint32_t tS = tS0 + (j & 1) * 128;
@@ -696,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       split_f2(ls2, ls0, ls1);
       // PV(j-1) must be done with P and O before they are rewritten
       const bool got_o =
-          __all_sync(0xffffffffu, j == 0 || wait_or_abort(&bars->o_done, (j - 1) & 1, bars));
+          __all_sync(0xffffffffu, j == 0 || wait_or_abort(&bars->o_done, (j - 1) & 1, bars, p.wait_ns));
       if (!got_o) fail_pipeline(bars);
       tc_fence_after();
       if (got_o) {
@@ -727,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
     }
-    const bool last_ok = !ok || my_tiles == 0 || wait_or_abort(&bars->o_done, (my_tiles - 1) & 1, bars);
+    const bool last_ok = !ok || my_tiles == 0 || wait_or_abort(&bars->o_done, (my_tiles - 1) & 1, bars, p.wait_ns);
     if (!last_ok) fail_pipeline(bars);
     // one answer for all 256 softmax threads: the epilogue's TMEM loads are
     // warp-collective
@@ -821,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               done = true;
               break;
             }
-            if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) break;
+            if ((i & 63u) == 0 && globaltimer_ns() - t0 > p.wait_ns) break;
           }
           if (!done) report(GLANCE_DEV_PIPELINE_TIMEOUT);
           // the last split to leave resets both counters for the next call
@@ -1036,7 +1067,8 @@ glance_status check_bf16(const char* who, const void* q, int n_q_heads, const gl
 template <int NB>
 glance_status launch_bf16(const char* who, const void* q, int n_q_heads, const glance_kv* kv,
                           const glance_tree* trees, int B, float scale, void* out,
-                          void* workspace, size_t workspace_bytes, cudaStream_t s) {
+                          void* workspace, size_t workspace_bytes, cudaStream_t s,
+                          unsigned long long wait_ns, int withhold_v) {
   using glance::fail;
   glance_status st = check_bf16(who, q, n_q_heads, kv, trees, B, out);
   if (st != GLANCE_OK) return st;
@@ -1111,6 +1143,8 @@ glance_status launch_bf16(const char* who, const void* q, int n_q_heads, const g
   p.box_rows = pl.box_rows;
   p.ticket_merge = pl.ticket;
   p.scale_log2 = scale * kLog2e;
+  p.wait_ns = wait_ns;
+  p.withhold_v = withhold_v;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.cta0[B]);
   cfg.blockDim = dim3(kThreads);
@@ -1184,7 +1218,7 @@ extern "C" glance_status glance_tree_attention(const void* q, int n_q_heads, con
   if (kv->dtype != GLANCE_BF16)
     return fail(GLANCE_ERR_INVALID_ARG, "glance_tree_attention: dtype must be F32 or BF16");
   return launch_bf16<1>("glance_tree_attention", q, n_q_heads, kv, tree, 1, scale, out,
-                        workspace, workspace_bytes, s);
+                        workspace, workspace_bytes, s, kDefaultWaitNs, 0);
 }
 
 extern "C" size_t glance_tree_attention_batched_workspace_bytes(int B, int n_rows, int n_q_heads,
@@ -1203,5 +1237,22 @@ extern "C" glance_status glance_tree_attention_batched(const void* q, int n_q_he
                                                        float scale, void* out, void* workspace,
                                                        size_t workspace_bytes, void* stream) {
   return launch_bf16<kMaxB>("glance_tree_attention_batched", q, n_q_heads, kv, trees, B, scale,
-                            out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+                            out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                            kDefaultWaitNs, 0);
+}
+
+extern "C" glance_status glance_tree_attention_timeout_check(
+    const void* q, int n_q_heads, const glance_kv* kv, const glance_tree* tree, float scale,
+    void* out, void* workspace, size_t workspace_bytes, unsigned long long wait_ns, void* stream) {
+  using glance::fail;
+  glance_status st = check_common(q, n_q_heads, kv, tree, out);
+  if (st != GLANCE_OK) return st;
+  if (kv->dtype != GLANCE_BF16)
+    return fail(GLANCE_ERR_UNSUPPORTED, "glance_tree_attention_timeout_check: BF16 only");
+  if (wait_ns < 1000ull || wait_ns > kDefaultWaitNs)
+    return fail(GLANCE_ERR_INVALID_ARG,
+                "glance_tree_attention_timeout_check: wait_ns must be in [1 us, 2 s]");
+  return launch_bf16<1>("glance_tree_attention_timeout_check", q, n_q_heads, kv, tree, 1, scale,
+                        out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                        wait_ns, 1);
 }
