@@ -1014,11 +1014,11 @@ def run_e2e(wl, steps):
     import torch
     c = wl.cfg
     R, T = wl.R, c["T"]
-    # pinned host image of the step's inputs: logits | q x 36 | h | K rows x 36 | V rows x 36
+    # pinned host image of the step's inputs: logits | q x 36 | h | tree rows' K/V
+    # [36][2][Hkv][R][D] (the layout glance_kv_write_rows scatters from)
+    kv_rows = torch.stack([torch.stack([k[:, T:T + R], v[:, T:T + R]]) for k, v in zip(wl.k, wl.v)])
     parts = [wl.x_dev.view(torch.uint8).reshape(-1)] + [q.view(torch.uint8).reshape(-1) for q in wl.q] + \
-            [wl.h.view(torch.uint8).reshape(-1)] + \
-            [k[:, T:T + R].contiguous().view(torch.uint8).reshape(-1) for k in wl.k] + \
-            [v[:, T:T + R].contiguous().view(torch.uint8).reshape(-1) for v in wl.v]
+            [wl.h.view(torch.uint8).reshape(-1), kv_rows.contiguous().view(torch.uint8).reshape(-1)]
     sizes = [int(t.numel()) for t in parts]
     offs = np.cumsum([0] + sizes)
     host = torch.empty(int(offs[-1]), dtype=torch.uint8, pin_memory=True)
@@ -1030,12 +1030,12 @@ def run_e2e(wl, steps):
     x_s = view(0, wl.x_dev)
     q_s = [view(1 + l, wl.q[l]) for l in range(n)]
     h_s = view(1 + n, wl.h)
-    k_s = [view(2 + n + l, wl.k[l][:, T:T + R]) for l in range(n)]
-    v_s = [view(2 + 2 * n + l, wl.v[l][:, T:T + R]) for l in range(n)]
+    kv_s = view(2 + n, kv_rows)
     res = torch.empty(2 + c["L"], dtype=torch.int32, pin_memory=True)
     h2d = int(offs[-1])
     d2h = res.numel() * 4
     saved = (wl.x_dev, wl.q, wl.h)
+    kv_e = torch.empty_like(kv_rows)
 
     def readback():
         res[0:1].copy_(wl.n_acc, non_blocking=True)
@@ -1044,9 +1044,7 @@ def run_e2e(wl, steps):
 
     def staged():
         stage.copy_(host, non_blocking=True)
-        for l in range(n):
-            wl.k[l][:, T:T + R].copy_(k_s[l], non_blocking=True)
-            wl.v[l][:, T:T + R].copy_(v_s[l], non_blocking=True)
+        wl.g.kv_write_rows(kv_s, wl.layers, R)
         wl.step()
         readback()
 
@@ -1055,10 +1053,9 @@ def run_e2e(wl, steps):
         for l in range(n):
             wl.q[l].copy_(host[int(offs[1 + l]):int(offs[2 + l])].view(wl.q[l].dtype).view(wl.q[l].shape),
                           non_blocking=True)
-            wl.k[l][:, T:T + R].copy_(host[int(offs[2 + n + l]):int(offs[3 + n + l])].view(torch.bfloat16)
-                                      .view(k_s[l].shape), non_blocking=True)
-            wl.v[l][:, T:T + R].copy_(host[int(offs[2 + 2 * n + l]):int(offs[3 + 2 * n + l])].view(torch.bfloat16)
-                                      .view(v_s[l].shape), non_blocking=True)
+        kv_e.copy_(host[int(offs[2 + n]):int(offs[3 + n])].view(torch.bfloat16).view(kv_rows.shape),
+                   non_blocking=True)
+        wl.g.kv_write_rows(kv_e, wl.layers, R)
         wl.h.copy_(host[int(offs[1 + n]):int(offs[2 + n])].view(torch.bfloat16).view(wl.h.shape), non_blocking=True)
         wl.step()
         readback()
@@ -1103,15 +1100,12 @@ def run_e2e(wl, steps):
     for b in range(2):
         vw = lambda i, like, b=b: stages[b][int(offs[i]):int(offs[i + 1])].view(like.dtype).view(like.shape)
         xb, qb, hb = vw(0, saved[0]), [vw(1 + l, saved[1][l]) for l in range(n)], vw(1 + n, saved[2])
-        kb = [vw(2 + n + l, k_s[l]) for l in range(n)]
-        vb = [vw(2 + 2 * n + l, v_s[l]) for l in range(n)]
+        kvb = vw(2 + n, kv_rows)
         wl.x_dev, wl.q, wl.h = xb, qb, hb
         rb = results[b]
 
-        def body(kb=kb, vb=vb, rb=rb):
-            for l in range(n):
-                wl.k[l][:, T:T + R].copy_(kb[l], non_blocking=True)
-                wl.v[l][:, T:T + R].copy_(vb[l], non_blocking=True)
+        def body(kvb=kvb, rb=rb):
+            wl.g.kv_write_rows(kvb, wl.layers, R)
             wl.step()
             rb[0:1].copy_(wl.n_acc, non_blocking=True)
             rb[1:2].copy_(wl.new_root, non_blocking=True)
@@ -1153,10 +1147,11 @@ def run_e2e(wl, steps):
     return {"value": round(steps / dt, 2), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": int(d2h), "serial_value": round(serial_rate, 2),
             "eager_value": round(eager_rate, 2),
-            "note": "each step: one pinned host->device copy of its inputs (copy stream) and its round + "
-                    "read-back (one CUDA graph); step i + 1's copy overlaps step i's round, the host reads "
-                    "every result. serial_value: copy, round and read-back back to back; eager_value: "
-                    "inputs copied tensor by tensor and every call launched from Python"}
+            "note": "each step: one pinned host->device copy of its inputs (copy stream), then one "
+                    "glance_kv_write_rows launch puts the tree rows' K/V of all layers into the caches, "
+                    "the round and the read-back (one CUDA graph); step i + 1's copy overlaps step i's "
+                    "round, the host reads every result. serial_value: copy, round and read-back back to "
+                    "back; eager_value: inputs copied tensor by tensor and every call launched from Python"}
 
 
 # ------------------------------------------------------------------ oracle

@@ -310,6 +310,22 @@ glance_status glance_accept_commit(const glance_tree* tree, const int32_t* argma
                                    int32_t* accepted_tok, int32_t* new_root, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/*
+ * Tree rows' K/V into the caches (Definition 1: the verify pass evaluates the
+ * packed rows in one pass with the prefix, so their K/V sit at slots
+ * T..T+N of each layer's cache while tree attention runs; row r at T + r).
+ * For callers whose rows' K/V come from elsewhere (another device, the host):
+ * one launch writes every layer's rows.
+ * src: device, [n_layers][2][n_kv_heads][rows][head_dim] elements of the
+ * layers' dtype (K before V), contiguous, 16-byte aligned.
+ * layers: host array [n_layers] of views with the same t_len, dtype and
+ * geometry; T = *t_len is read on the device. If T + rows > t_cap the call
+ * sets device status 2 and writes nothing. Limits: 1 <= n_layers <= 128,
+ * 1 <= rows <= 256, rows and strides multiples of 16 bytes.
+ */
+glance_status glance_kv_write_rows(const void* src, const glance_kv* layers, int n_layers, int rows,
+                                   void* stream);
+
 /* ----------------------------------------------------------------- batched */
 
 /*

@@ -14,10 +14,25 @@ itself. Reading taken here: a pre-norm decoder layer,
   x' -> RMSNorm(g2) -> SiLU(. W_gate) * (. W_up) -> . W_down -> + x' residual
 
 RMSNorm(x) = x / sqrt(mean(x^2) + eps) * g. Everything in float64 here.
+
+The layer can also round the five values that a bf16 implementation stores
+between its steps (q, the K/V rows, the attention output, the residual
+output x', the SwiGLU activation) to bf16, nearest-even: `store=round_bf16`.
+That is the same function with those stores made explicit (reading R27 of
+the design notes: each call normalises exactly the bf16 rows the previous
+call stored), so a bf16 implementation can be held to the per-step
+tolerance over a whole layer.
 """
 import numpy as np
 
 from .attention import tree_attention
+from .bf16 import bf16_bits_to_f64, f32_to_bf16_bits
+
+
+def round_bf16(x):
+    """x rounded to the nearest bf16 value (ties to even), via float32."""
+    x = np.asarray(x, dtype=np.float64)
+    return bf16_bits_to_f64(f32_to_bf16_bits(x.astype(np.float32))).reshape(x.shape)
 
 
 def rms_scale(x, eps):
@@ -69,17 +84,21 @@ def residual(res, a, W):
     return np.asarray(res, dtype=np.float64) + np.asarray(a, dtype=np.float64) @ np.asarray(W, dtype=np.float64)
 
 
-def dense_layer(x, lw, pos, T, K_cache, V_cache, anc, Hq, Hkv, D, theta, eps):
+def dense_layer(x, lw, pos, T, K_cache, V_cache, anc, Hq, Hkv, D, theta, eps, store=None):
     """One decoder layer over the packed rows x (R, d); the rows' K/V go to
     cache slots T..T+R-1 (row i at T + i) of K_cache/V_cache (Hkv, t_cap, D),
     which are updated in place. lw: g1, W_qkv, q_norm, k_norm, W_o, g2, W_gate,
-    W_up, W_down. Returns the layer's output rows."""
+    W_up, W_down. store: applied to each value the layer keeps between its
+    steps (q, K/V rows, attention output, x', activation); None keeps float64.
+    Returns the layer's output rows (before any store)."""
+    keep = (lambda a: a) if store is None else store
     R = x.shape[0]
     q, k, v = qkv(x, lw.get("g1"), lw["W_qkv"], Hq, Hkv, D, pos, theta, eps,
                   lw.get("q_norm"), lw.get("k_norm"))
+    q, k, v = keep(q), keep(k), keep(v)
     K_cache[:, T:T + R] = k.transpose(1, 0, 2)
     V_cache[:, T:T + R] = v.transpose(1, 0, 2)
-    att = tree_attention(q, K_cache[:, :T + R], V_cache[:, :T + R], T, anc, 1.0 / np.sqrt(D))
-    x1 = residual(x, att.reshape(R, Hq * D), lw["W_o"])
-    act = swiglu(x1, lw.get("g2"), lw["W_gate"], lw["W_up"], eps)
+    att = keep(tree_attention(q, K_cache[:, :T + R], V_cache[:, :T + R], T, anc, 1.0 / np.sqrt(D)))
+    x1 = keep(residual(x, att.reshape(R, Hq * D), lw["W_o"]))
+    act = keep(swiglu(x1, lw.get("g2"), lw["W_gate"], lw["W_up"], eps))
     return residual(x1, act, lw["W_down"])

@@ -16,7 +16,7 @@ from _util import bf16_tensor
 from oracle.attention import tree_attention as o_attn
 from oracle.bf16 import bf16_bits_to_f64
 from oracle.dense import dense_layer, qkv as o_qkv, residual as o_residual, rms_scale as o_rms
-from oracle.dense import swiglu as o_swiglu
+from oracle.dense import round_bf16, swiglu as o_swiglu
 from test_gpu_attention import random_tree, upload_tree
 
 pytestmark = pytest.mark.gpu
@@ -192,17 +192,39 @@ def test_full_layer_with_tree_attention(dev, clean_status):
     close(f64(out), o_residual(f64(x1), f64(act), bf16_bits_to_f64(Wd)))
     got_r = scale_from_sumsq(ss2.cpu().numpy(), d, 1e-6)
     assert np.all(np.abs(got_r - o_rms(f64(out), 1e-6)) <= 1e-5 * got_r)
-    # and the whole layer against the fp64 oracle layer: the five bf16 stores
-    # between the calls (q, K/V rows, att, x1, act; each within 2^-9 relative)
-    # move the 12288-term down projection by up to a few 1e-2 at the tails
+    # and the whole layer, against the oracle layer that rounds the five values
+    # the calls store in bf16 (q, K/V rows, att, x1, act) at the same points.
+    # Each call above is within 2e-2 of the oracle on its own inputs, but a
+    # chain of bf16 stores is sensitive to where each value falls against a
+    # rounding boundary: a difference far below a bf16 step flips some stored
+    # values by one step, and the 12288-term down projection sums the flips.
+    # The bound is taken from the oracle itself: oracle chains whose stored
+    # values carry the noise the kernels' own arithmetic brings (one bf16 step,
+    # 2^-9 relative, on the attention output, whose probabilities enter the PV
+    # product as bf16; float32-level, 2^-20, on the other stores) spread by D
+    # around the rounded chain; the GPU chain must stay within 2 D of it.
     lw = dict(W_qkv=bf16_bits_to_f64(Wqkv), W_o=bf16_bits_to_f64(Wo), W_gate=bf16_bits_to_f64(Wg),
               W_up=bf16_bits_to_f64(Wu), W_down=bf16_bits_to_f64(Wd), q_norm=qn.astype(np.float64),
               k_norm=kn.astype(np.float64))
-    want = dense_layer(x0, lw, pos, T, bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), ref["anc"], Hq, Hkv, D,
-                       1e6, 1e-6)
-    got = f64(out)
-    err = np.abs(got - want) / np.maximum(1.0, np.abs(want))
-    assert err.max() < 6e-2 and err.mean() < 5e-3, (err.max(), err.mean())
+    layer = lambda store: dense_layer(x0, lw, pos, T, bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), ref["anc"],
+                                      Hq, Hkv, D, 1e6, 1e-6, store=store)
+    rel = lambda a, b: np.abs(a - b) / np.maximum(1.0, np.abs(b))
+    want = layer(round_bf16)
+    spread_max, spread_mean = 0.0, 0.0
+    for seed in (0, 1):
+        noise = np.random.default_rng(seed)
+        n_store = [0]
+
+        def noisy(a):  # stores in the layer's order: q, k, v, att, x1, act
+            n_store[0] += 1
+            level = 2.0 ** -9 if n_store[0] == 4 else 2.0 ** -20
+            return round_bf16(a * (1 + level * noise.standard_normal(a.shape)))
+        alt = layer(noisy)
+        spread_max = max(spread_max, rel(alt, want).max())
+        spread_mean = max(spread_mean, rel(alt, want).mean())
+    err = rel(f64(out), want)
+    assert err.max() <= 2 * spread_max and err.mean() <= 2 * spread_mean, (err.max(), err.mean(),
+                                                                          spread_max, spread_mean)
 
 
 def test_qkv_cache_capacity_and_arguments(dev, clean_status):

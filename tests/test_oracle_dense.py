@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads as W
-from oracle.dense import dense_layer, qkv, rms_scale, rmsnorm, rope, swiglu
+from oracle.dense import dense_layer, qkv, rms_scale, rmsnorm, rope, round_bf16, swiglu
 from oracle.toy import ToyTarget
 
 
@@ -93,3 +93,38 @@ def test_qk_norm_normalises_each_head():
     q, k, v = qkv(x, None, Wqkv, 2, 1, 8, [0, 0, 0, 0], 1e4, 1e-6, np.ones(8), np.ones(8))
     assert np.allclose(np.sqrt((q ** 2).mean(axis=-1)), 1.0, atol=1e-5)
     assert np.allclose(np.sqrt((k ** 2).mean(axis=-1)), 1.0, atol=1e-5)
+
+
+def test_round_bf16_is_torchs_bfloat16_conversion():
+    """The store rounding of the layer's bf16 path is round-to-nearest-even
+    to bfloat16, as torch converts float32 (an independent implementation)."""
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.standard_normal(4000) * 10 ** g.uniform(-6, 6, 4000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0, 3.0e38]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(round_bf16(x), want)
+
+
+def test_layer_with_bf16_stores_keeps_only_the_store_rounding():
+    """store=round_bf16 changes the layer only through the five stores: an
+    identity store gives the float64 layer bit for bit, and the rounded layer
+    stays within the rounding's propagated size of it (a store that skipped
+    the activation or the residual would move the tails far more)."""
+    g = np.random.default_rng(6)
+    R, d, Hq, Hkv, D, I, T = 8, 64, 4, 2, 16, 96, 5
+    x = g.standard_normal((R, d))
+    lw = dict(W_qkv=g.standard_normal((d, (Hq + 2 * Hkv) * D)) * 0.1, W_o=g.standard_normal((Hq * D, d)) * 0.1,
+              W_gate=g.standard_normal((d, I)) * 0.1, W_up=g.standard_normal((d, I)) * 0.1,
+              W_down=g.standard_normal((I, d)) * 0.1)
+    Kc = g.standard_normal((Hkv, T + R, D))
+    Vc = g.standard_normal((Hkv, T + R, D))
+    anc = np.zeros((R, 1), dtype=np.uint64)
+    for i in range(R):  # a chain: row i sees rows 0..i
+        anc[i, 0] = np.uint64((1 << (i + 1)) - 1)
+    pos = T + np.arange(R)
+    base = dense_layer(x, lw, pos, T, Kc.copy(), Vc.copy(), anc, Hq, Hkv, D, 1e4, 1e-6)
+    same = dense_layer(x, lw, pos, T, Kc.copy(), Vc.copy(), anc, Hq, Hkv, D, 1e4, 1e-6, store=lambda a: a)
+    assert np.array_equal(base, same)
+    rounded = dense_layer(x, lw, pos, T, Kc.copy(), Vc.copy(), anc, Hq, Hkv, D, 1e4, 1e-6, store=round_bf16)
+    rel = np.abs(rounded - base) / np.maximum(1.0, np.abs(base))
+    assert 0 < rel.max() < 3e-2

@@ -16,7 +16,7 @@ from ._binding import (STATUS_WORDS, BF16, EXPORTS, F32, LIB_PATH, GlanceError, 
                        accept_commit_gated, accept_commit_gated_batched, lmhead_argmax_entropy,
                        lmhead_sample,
                        accept_commit_workspace_bytes, build_tree, build_tree_batched, clear_status,
-                       get_status,
+                       get_status, kv_write_rows,
                        build_tree_batched_workspace_bytes, build_tree_shared,
                        build_tree_shared_workspace_bytes, build_tree_workspace_bytes,
                        dense_qkv, dense_residual, dense_swiglu,
@@ -29,7 +29,7 @@ __all__ = ["STATUS_WORDS", "BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", 
            "accept_commit", "accept_commit_batched", "accept_commit_batched_workspace_bytes",
            "accept_commit_gated", "accept_commit_gated_batched", "lmhead_argmax_entropy",
            "lmhead_sample",
-           "accept_commit_workspace_bytes", "build_tree", "build_tree_batched", "clear_status", "get_status",
+           "accept_commit_workspace_bytes", "build_tree", "build_tree_batched", "clear_status", "get_status", "kv_write_rows",
            "build_tree_batched_workspace_bytes", "build_tree_shared",
            "build_tree_shared_workspace_bytes", "build_tree_workspace_bytes", "dense_qkv",
            "dense_residual", "dense_swiglu", "device_status", "row_sumsq",

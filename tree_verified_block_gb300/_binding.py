@@ -33,7 +33,7 @@ EXPORTS = [
     "glance_dense_residual", "glance_dense_swiglu",
     "glance_accept_commit_gated_batched",
     "glance_last_error", "glance_status_string", "glance_device_status",
-    "glance_reset_device_status", "glance_get_status", "glance_clear_status", "glance_version",
+    "glance_reset_device_status", "glance_get_status", "glance_kv_write_rows", "glance_clear_status", "glance_version",
 ]
 
 
@@ -144,6 +144,8 @@ def lib():
     L.glance_device_status.restype = st
     L.glance_reset_device_status.argtypes = []
     L.glance_reset_device_status.restype = st
+    L.glance_kv_write_rows.argtypes = [vp, ctypes.POINTER(KVC), i32, i32, vp]
+    L.glance_kv_write_rows.restype = st
     L.glance_get_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     L.glance_get_status.restype = st
     L.glance_clear_status.argtypes = [ctypes.c_void_p]
@@ -464,6 +466,14 @@ def device_status():
 
 def reset_device_status():
     _check(lib().glance_reset_device_status())
+
+
+def kv_write_rows(src, layers, rows, stream=None):
+    """Scatter src [n_layers, 2, n_kv_heads, rows, head_dim] (K before V) into
+    every layer's cache at slots T..T+rows-1 (T read on the device)."""
+    assert src.is_contiguous()
+    arr = (KVC * len(layers))(*[l.c for l in layers])
+    _check(lib().glance_kv_write_rows(_ptr(src), arr, len(layers), int(rows), _stream(stream, src.device)))
 
 
 STATUS_WORDS = 6

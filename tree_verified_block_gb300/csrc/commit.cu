@@ -347,3 +347,85 @@ extern "C" glance_status glance_accept_commit_gated_batched(
                        gate_threshold, gated, layers, n_layers, n_accepted, accepted_tok, new_root,
                        workspace, workspace_bytes, stream);
 }
+
+// ------------------------------------------------------ tree rows into caches
+//
+// The verify pass writes the K/V of the packed tree rows into every layer's
+// cache at slots T..T+rows-1 (row r at T + r) before tree attention reads them
+// (Definition 1: the rows are evaluated in the same pass as the prefix). This
+// call does that for K/V rows computed elsewhere (e.g. uploaded from the
+// host): one CTA per (layer, K or V, kv head) copies that head's rows with
+// 16-byte loads and stores.
+
+namespace {
+
+constexpr int kRowsThreads = 256;
+
+struct RowsParams {
+  const char* src;            // [n_layers][2][n_kv_heads][rows][row_bytes]
+  char* dst[2 * kMaxLayers];  // per (layer, K/V): the cache
+  const int32_t* t_len;
+  long long head_stride_bytes, row_stride_bytes;
+  int n_kv_heads, rows, row_bytes, t_cap;
+};
+
+__global__ void __launch_bounds__(kRowsThreads) kv_write_rows_kernel(const __grid_constant__ RowsParams p) {
+  const int head = blockIdx.x % p.n_kv_heads;
+  const int lkv = blockIdx.x / p.n_kv_heads;  // layer * 2 + (0: K, 1: V)
+  const int T = *p.t_len;
+  if (T < 0 || T + p.rows > p.t_cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(GLANCE_DEV_TREE_CAPACITY);
+    return;
+  }
+  const int per_row = p.row_bytes / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      p.src + (static_cast<size_t>(lkv) * p.n_kv_heads + head) * p.rows * p.row_bytes);
+  char* dst = p.dst[lkv] + head * p.head_stride_bytes + static_cast<long long>(T) * p.row_stride_bytes;
+  for (int i = threadIdx.x; i < p.rows * per_row; i += kRowsThreads) {
+    const int r = i / per_row, c = i - r * per_row;
+    reinterpret_cast<uint4*>(dst + r * p.row_stride_bytes)[c] = __ldg(src + i);
+  }
+}
+
+}  // namespace
+
+extern "C" glance_status glance_kv_write_rows(const void* src, const glance_kv* layers, int n_layers,
+                                              int rows, void* stream) {
+  using glance::fail;
+  const char* who = "glance_kv_write_rows";
+  if (!src || !layers) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (n_layers < 1 || n_layers > kMaxLayers || rows < 1 || rows > 256)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= n_layers <= %d and 1 <= rows <= 256", who,
+                kMaxLayers);
+  const glance_kv& l0 = layers[0];
+  const int esize = l0.dtype == GLANCE_BF16 ? 2 : 4;
+  RowsParams p;
+  p.src = static_cast<const char*>(src);
+  p.t_len = l0.t_len;
+  p.head_stride_bytes = l0.head_stride * esize;
+  p.row_stride_bytes = l0.row_stride * esize;
+  p.n_kv_heads = l0.n_kv_heads;
+  p.rows = rows;
+  p.row_bytes = l0.head_dim * esize;
+  p.t_cap = l0.t_cap;
+  if (!glance::aligned16(src) || p.row_bytes % 16 || p.row_stride_bytes % 16 || p.head_stride_bytes % 16)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: src, rows and strides must be 16-byte aligned", who);
+  for (int l = 0; l < n_layers; ++l) {
+    const glance_kv& x = layers[l];
+    if (!x.k || !x.v || x.t_len != l0.t_len || x.dtype != l0.dtype || x.n_kv_heads != l0.n_kv_heads ||
+        x.head_dim != l0.head_dim || x.t_cap != l0.t_cap || x.head_stride != l0.head_stride ||
+        x.row_stride != l0.row_stride || x.n_kv_heads < 1 || x.t_cap < rows ||
+        x.row_stride < x.head_dim || x.head_stride < static_cast<int64_t>(x.t_cap) * x.row_stride)
+      return fail(GLANCE_ERR_INVALID_ARG,
+                  "%s: every layer needs k, v, the same t_len, dtype and geometry (layer %d)", who, l);
+    if (!glance::aligned16(x.k) || !glance::aligned16(x.v))
+      return fail(GLANCE_ERR_INVALID_ARG, "%s: k and v must be 16-byte aligned (layer %d)", who, l);
+    p.dst[2 * l] = static_cast<char*>(x.k);
+    p.dst[2 * l + 1] = static_cast<char*>(x.v);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kv_write_rows_kernel<<<n_layers * 2 * l0.n_kv_heads, kRowsThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
