@@ -56,7 +56,7 @@ def peaks():
 # the listed files, and a changed source reports traffic null.
 CSRC = os.path.join("tree_verified_block_gb300", "csrc")
 NCU_TRAFFIC = {
-    "glance_tree_attention": dict(bytes=17_898_240, digest="94530a57ae843380",
+    "glance_tree_attention": dict(bytes=17_900_288, digest="c3618947c828eb8f",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
     "glance_lmhead_argmax": dict(bytes=1_245_317_376 + 2_755_840, digest="4536d90ed80de2dc",
@@ -877,6 +877,9 @@ def run_case(args):
         print(json.dumps({"case": args.case, "us": round(us, 2),
                           "hbm_frac": round(b / (us * 1e-6) / 1e9 / peaks()["hbm"], 4)}), flush=True)
         return
+    if args.case in ("attn255", "attn_ragged8"):
+        run_attn_case(args, dev)
+        return
     M, d, V = 512, 4096, 151936
     tg = torch.Generator(device=dev)
     tg.manual_seed(7)
@@ -886,7 +889,12 @@ def run_case(args):
     gap = torch.empty(M, dtype=torch.float32, device=dev)
     mx = torch.empty(M, dtype=torch.float32, device=dev)
     ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.bfloat16), dev)
-    fn = lambda: g.lmhead_argmax(h, Wt, am, gap, mx, ws)
+    ent = torch.empty(M, dtype=torch.float32, device=dev)
+    pos = torch.arange(M, dtype=torch.int32, device=dev) % 64 + 4096
+    seq = torch.arange(M, dtype=torch.int32, device=dev) // 64
+    fn = {"lmhead512": lambda: g.lmhead_argmax(h, Wt, am, gap, mx, ws),
+          "lmhead512_entropy": lambda: g.lmhead_argmax_entropy(h, Wt, am, gap, mx, ent, ws),
+          "lmhead512_sample": lambda: g.lmhead_sample(h, Wt, 1.0, 5, pos, seq, am, gap, ws)}[args.case]
     for _ in range(args.warmup + args.steps):
         fn()
     torch.cuda.synchronize()
@@ -1281,6 +1289,46 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_attn_case(args, dev):
+    """One tree-attention layer alone, for profiler captures: attn255 = one
+    layer at T = 2048, N = 255 (1024 query rows per kv head: tensor / MUFU
+    bound); attn_ragged8 = one batched layer of the ragged8 batch (8 requests,
+    T ~ U{512..8192}, N = 63). Inputs drawn on the device."""
+    import torch
+    import tree_verified_block_gb300 as g
+    tg = torch.Generator(device=dev)
+    tg.manual_seed(11)
+    rn = lambda *shape: torch.randn(*shape, generator=tg, device=dev).to(torch.bfloat16)
+    scale = 128 ** -0.5
+    if args.case == "attn255":
+        c = dict(ENTROPY36, N=255)
+        R = c["N"] + 1
+        t_len = torch.tensor([c["T"]], dtype=torch.int32, device=dev)
+        layer = g.KVLayer(rn(c["Hkv"], c["T"] + R + 64, c["D"]), rn(c["Hkv"], c["T"] + R + 64, c["D"]), t_len)
+        x = torch.from_numpy(W.draft_logits_entropy(c["L"], c["V"], 4.0, seed=4140)).to(dev)
+        tree = g.Tree(c["N"], c["L"], dev)
+        g.build_tree(x, c["N"], torch.tensor([77], dtype=torch.int32, device=dev), t_len, tree,
+                     g.workspace(g.build_tree_workspace_bytes(c["L"], c["V"], c["N"]), dev))
+        q = rn(R, c["Hq"], c["D"])
+        o = torch.empty_like(q)
+        ws = g.workspace(g.tree_attention_workspace_bytes(R, c["Hq"], layer), dev)
+        fn = lambda: g.tree_attention(q, layer, tree, scale, o, ws)
+        flops = sum(4 * c["D"] * c["Hq"] * (c["T"] + int(bin(int(w)).count("1")))
+                    for w in tree.to_host()["anc"].reshape(R, -1)[:, 0])
+    else:
+        bw = BatchedWorkload(RAGGED8, dev, host=False, n_layers=1)
+        fn = lambda: g.tree_attention_batched(bw.q[0], bw.layers[0], bw.trees, scale, bw.out[0], bw.ws_attn)
+        flops = None
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    us = graph_time_us(fn, 10)
+    out = {"case": args.case, "us": round(us, 2)}
+    if flops:
+        out["tflops"] = round(flops / (us * 1e-6) / 1e12, 1)
+    print(json.dumps(out), flush=True)
+
+
 def run_unavailable(args):
     """More than one GPU: the path is per request (one GPU per request, no
     exchange), so this benchmark runs on one GPU only."""
@@ -1299,7 +1347,8 @@ def main():
     ap.add_argument("--impl", default="glance", choices=["glance", "reference"])
     ap.add_argument("--workload", default="full36", choices=["full36", "small"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--case", default=None, choices=["lmhead512", "dense_layer", "forward36"],
+    ap.add_argument("--case", default=None, choices=["lmhead512", "lmhead512_entropy", "lmhead512_sample",
+                                                     "attn255", "attn_ragged8", "dense_layer", "forward36"],
                     help="run one kernel alone on a small case (for profiler captures)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the entropy36 sweep and the verify1 single-layer case")

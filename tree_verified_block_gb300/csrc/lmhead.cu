@@ -86,8 +86,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += kW0;
       k1 += kW1;
     }
-    const uint32_t lo0 = c.x * kM0, hi0 = __umulhi(c.x, kM0);
-    const uint32_t lo1 = c.z * kM1, hi1 = __umulhi(c.z, kM1);
+    // each 32 x 32 -> 64-bit product as one wide multiply
+    const unsigned long long p0 = static_cast<unsigned long long>(c.x) * kM0;
+    const unsigned long long p1 = static_cast<unsigned long long>(c.z) * kM1;
+    const uint32_t lo0 = static_cast<uint32_t>(p0), hi0 = static_cast<uint32_t>(p0 >> 32);
+    const uint32_t lo1 = static_cast<uint32_t>(p1), hi1 = static_cast<uint32_t>(p1 >> 32);
     c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
   }
   return c;
@@ -679,12 +682,19 @@ struct PairShape {
   static constexpr uint32_t kBBytes = kBK * BN * 2;
   static constexpr uint32_t kStageBytes = NB * kABytes + kBBytes;
   static constexpr size_t kSmem = 1024 + STAGES * kStageBytes + 256;
+  // epilogue warpgroups: with one accumulator set (NB = 2) the MMAs of the
+  // next tile wait for the whole fold, so each row block gets its own
+  // warpgroup (two epilogue warps per scheduler, half the fold each). Four
+  // (a column half each) measured slower: 512 threads cap registers at 128.
+  static constexpr int EPI = NB == 2 ? 2 : 1;
+  static constexpr int CH = EPI / NB > 0 ? EPI / NB : 1;  // column groups per row block
+  static constexpr int kThreads = 128 + 128 * EPI;
   static_assert(NB * BN * NBUF <= 512, "tensor memory");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
 template <int NB, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PairShape<NB>::kThreads, 1)
     lmhead_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_h,
                             const __grid_constant__ CUtensorMap map_w, const Bf16Params p) {
   using Sh = PairShape<NB>;
@@ -711,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->acc_full[b], 1);
-      mbar_init(&bars->acc_empty[b], 128);
+      mbar_init(&bars->acc_empty[b], 128 * Sh::EPI);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -803,27 +813,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) fail_pipeline(bars);
     }
   } else if (warp >= 4) {
-    const int quarter = warp - 4;
+    // warpgroup eg folds column group eg / NB (of CH) of row blocks
+    // eg % NB, eg % NB + EPI, ... of the tile
+    constexpr int EPI = Sh::EPI, CH = Sh::CH, NBW = (NB * CH + EPI - 1) / EPI;  // row blocks per warp
+    constexpr int kCh = BN / 32 / CH;  // 32-column chunks per column group
+    const int quarter = warp & 3, egw = (warp - 4) >> 2;
+    const int eg = egw % (EPI / CH), cg = egw / (EPI / CH);  // row-block lane, column group
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m1[NB], m2[NB], hm[NB], hs[NB], hu[NB];
-    int i1[NB];
+    float m1[NBW], m2[NBW], hm[NBW], hs[NBW], hu[NBW];
+    int i1[NBW];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      m1[b] = -INFINITY;
-      m2[b] = -INFINITY;
-      i1[b] = 0x7FFFFFFF;
-      hm[b] = -INFINITY;
-      hs[b] = 0.f;
-      hu[b] = 0.f;
+    for (int bb = 0; bb < NBW; ++bb) {
+      m1[bb] = -INFINITY;
+      m2[bb] = -INFINITY;
+      i1[bb] = 0x7FFFFFFF;
+      hm[bb] = -INFINITY;
+      hs[bb] = 0.f;
+      hu[bb] = 0.f;
     }
     // sampling: each of this thread's rows' predicted position and stream
-    uint32_t spos[NB], sseq[NB];
+    uint32_t spos[NBW], sseq[NBW];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const int gr = row0 + b * kBM + row;
-      spos[b] = (kS && gr < p.M) ? static_cast<uint32_t>(p.position[gr]) : 0u;
-      sseq[b] = (kS && gr < p.M && p.seq) ? static_cast<uint32_t>(p.seq[gr]) : 0u;
+    for (int bb = 0; bb < NBW; ++bb) {
+      const int gr = row0 + (eg + bb * EPI) * kBM + row;
+      spos[bb] = (kS && gr < p.M) ? static_cast<uint32_t>(p.position[gr]) : 0u;
+      sseq[bb] = (kS && gr < p.M && p.seq) ? static_cast<uint32_t>(p.seq[gr]) : 0u;
     }
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -836,17 +851,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int v0 = (pair + i * n_pairs) * BN;
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
+      for (int bb = 0; bb < NBW; ++bb) {
+        const int b = eg + bb * EPI;
         const uint32_t t_acc = tmem + buf * (NB * BN) + b * BN + lane_off;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = cg * kCh; c < (cg + 1) * kCh; ++c) {
           uint32_t r[32];
           tmem_ld32(t_acc + c * 32, r);
           tmem_ld_wait();
           const int col0 = v0 + c * 32;
-          if (kS) perturb_chunk(r, col0, p.inv_temp, spos[b], sseq[b], p.seed_lo, p.seed_hi);
-          fold_chunk(r, col0, p.V, m1[b], i1[b], m2[b]);
-          if (kH) entropy_chunk(r, col0, p.V, m1[b], hm[b], hs[b], hu[b]);
+          if (kS) perturb_chunk(r, col0, p.inv_temp, spos[bb], sseq[bb], p.seed_lo, p.seed_hi);
+          fold_chunk(r, col0, p.V, m1[bb], i1[bb], m2[bb]);
+          if (kH) entropy_chunk(r, col0, p.V, m1[bb], hm[bb], hs[bb], hu[bb]);
         }
       }
       tc_fence_before();
@@ -854,14 +870,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) fail_pipeline(bars);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const int grow = row0 + b * kBM + row;
+    for (int bb = 0; bb < NBW; ++bb) {
+      const int grow = row0 + (eg + bb * EPI) * kBM + row;
       if (grow < p.M) {
-        const size_t at = static_cast<size_t>(pair) * (2 * NB * kBM) + grow;
+        const size_t at = (static_cast<size_t>(pair) * CH + cg) * (2 * NB * kBM) + grow;
         if (kH)
-          static_cast<PartialH*>(p.part)[at] = PartialH{m1[b], i1[b], m2[b], hs[b], hu[b]};
+          static_cast<PartialH*>(p.part)[at] = PartialH{m1[bb], i1[bb], m2[bb], hs[bb], hu[bb]};
         else
-          static_cast<Partial*>(p.part)[at] = Partial{m1[b], i1[b], m2[b]};
+          static_cast<Partial*>(p.part)[at] = Partial{m1[bb], i1[bb], m2[bb]};
       }
     }
   }
@@ -881,11 +897,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
   if (kH)
-    merge_partials_h(static_cast<const PartialH*>(p.part), n_pairs, 2 * NB * kBM, p.M, p.argmax,
-                     p.gap, p.maxlogit, p.entropy);
+    merge_partials_h(static_cast<const PartialH*>(p.part), n_pairs * Sh::CH, 2 * NB * kBM, p.M,
+                     p.argmax, p.gap, p.maxlogit, p.entropy);
   else
-    merge_partials(static_cast<const Partial*>(p.part), n_pairs, 2 * NB * kBM, p.M, p.argmax,
-                   p.gap, p.maxlogit);
+    merge_partials(static_cast<const Partial*>(p.part), n_pairs * Sh::CH, 2 * NB * kBM, p.M,
+                   p.argmax, p.gap, p.maxlogit);
 }
 
 int row_blocks(int M) { return (M + kBM - 1) / kBM; }
@@ -981,7 +997,7 @@ int max_pairs() {
   if (cached[dev] == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * glance::num_sms());
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(PairShape<NB>::kThreads);
     cfg.dynamicSmemBytes = PairShape<NB>::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1033,7 +1049,7 @@ glance_status launch_pair(const void* h, const void* W, int M, int d, int V, int
   set_sample(p, sa);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Sh::kThreads);
   cfg.dynamicSmemBytes = Sh::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
