@@ -223,6 +223,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
+// Key run of one split: [k0, k1) of [0, n_keys), equal runs of `per` slots
+// (a multiple of 32), so that the splits of a group finish together; its key
+// tiles are the 128-slot pieces of the run, the last one `cols` wide (rounded
+// up to 32; the QK^T and PV products of that tile stop there).
+struct SplitRun {
+  int k0, k1, n_tiles;
+  __device__ __forceinline__ int tile_key0(int j) const { return k0 + j * kBN; }
+  __device__ __forceinline__ int tile_cols(int j) const {
+    const int c = (k1 - tile_key0(j) + 31) / 32 * 32;
+    return c > kBN ? kBN : c;
+  }
+};
+__device__ __forceinline__ SplitRun split_run(int n_keys, int n_split, int split) {
+  const int per = ((n_keys + n_split - 1) / n_split + 31) / 32 * 32;
+  SplitRun r;
+  r.k0 = split * per;
+  r.k1 = r.k0 + per < n_keys ? r.k0 + per : n_keys;
+  r.n_tiles = r.k1 > r.k0 ? (r.k1 - r.k0 + kBN - 1) / kBN : 0;
+  if (r.n_tiles == 0) r.k1 = r.k0;
+  return r;
+}
+
 // word w (0..3) of a row's ancestor mask, 0 outside, without dynamic indexing
 __device__ __forceinline__ uint64_t anc_word(const uint64_t (&a)[4], int w) {
   return w == 0 ? a[0] : w == 1 ? a[1] : w == 2 ? a[2] : w == 3 ? a[3] : 0ull;
@@ -436,13 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     T_pre = *p.t_len[req];
     if (T_pre >= 0 && T_pre + p.rows <= p.t_cap[req]) {
-      const int nt = (T_pre + p.rows + kBN - 1) / kBN;
-      const int t0 = static_cast<int>((static_cast<long long>(nt) * split) / n_split);
-      const int t1 = static_cast<int>((static_cast<long long>(nt) * (split + 1)) / n_split);
+      const SplitRun run_pre = split_run(T_pre + p.rows, n_split, split);
       const uint64_t pol_kv = policy_evict_first();
-      for (int j = 0; j < kPreTiles && j < t1 - t0; ++j) {
-        const int key0 = (t0 + j) * kBN;
-        if (key0 + kBN > T_pre) break;
+      for (int j = 0; j < kPreTiles && j < run_pre.n_tiles; ++j) {
+        const int key0 = run_pre.tile_key0(j);
+        if (key0 + run_pre.tile_cols(j) > T_pre) break;
         unsigned char* stage = sKV + j * kKVStageBytes;
         mbar_arrive_expect_tx(&bars->k_full[j], 2 * kHalfBytes);
         tma_load_3d(stage + 0 * kHalfBytes, map_k, &bars->k_full[j], 0, key0, g, pol_kv);
@@ -482,10 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool room = !raced && T >= 0 && T + p.rows <= p.t_cap[req];
   // key tiles of this split over slots [0, T + rows)
   const int n_keys = room ? T + p.rows : 0;
-  const int n_tiles = (n_keys + kBN - 1) / kBN;
-  const int tile0 = static_cast<int>((static_cast<long long>(n_tiles) * split) / n_split);
-  const int tile1 = static_cast<int>((static_cast<long long>(n_tiles) * (split + 1)) / n_split);
-  const int my_tiles = tile1 - tile0;
+  const SplitRun run = split_run(n_keys, n_split, split);
+  const int my_tiles = run.n_tiles;
 
   if (threadIdx.x == 0 && !room && !raced && local == 0) report(GLANCE_DEV_TREE_CAPACITY);
   // query pieces of this tile that hold no real (head, row): zero them so the
@@ -556,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         unsigned char* stage = sKV + st * kKVStageBytes;
-        const int key0 = (tile0 + j) * kBN;
+        const int key0 = run.tile_key0(j);
         // K and V of a tile complete separately: QK^T needs only K, and V
         // lands while the tile's softmax runs
         mbar_arrive_expect_tx(&bars->k_full[st], 2 * kHalfBytes);
@@ -584,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && my_tiles > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);
       const uint32_t q_addr = smem_u32(sQ);
       auto issue_qk = [&](int j) -> bool {
@@ -593,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sKV + st * kKVStageBytes);
         const uint32_t tS = tS0 + (j & 1) * 128;
+        const uint32_t idesc_s = idesc_bf16_f32(kBM, run.tile_cols(j), false, false);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
@@ -623,9 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // boundary past T + rows; the V rows of that step beyond T + rows are
         // never weighted (P = 0) but may hold anything, even NaN (0 * NaN =
         // NaN), so they are zeroed first.
-        int steps = 8;
-        const int key0 = (tile0 + j) * kBN;
-        if (key0 + kBN > n_keys) {
+        const int key0 = run.tile_key0(j);
+        int steps = run.tile_cols(j) / 16;
+        if (key0 + steps * 16 > n_keys) {
           const int valid_rows = n_keys - key0;
           steps = (valid_rows + 15) / 16;
           unsigned char* vs = sKV + (j % kStages) * kKVStageBytes + 2 * kHalfBytes;
@@ -656,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait raises the CTA's abort flag, and all threads leave the loop
     // together right after the first barrier.
     for (int j = 0; j < my_tiles; ++j) {
-      const int key0 = (tile0 + j) * kBN;
+      const int key0 = run.tile_key0(j);
       // warp-uniform: tcgen05.ld / st below are warp-collective
       const bool got_s = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[j & 1], (j >> 1) & 1, bars, p.wait_ns));
       if (!got_s) fail_pipeline(bars);
@@ -672,11 +690,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; ++e) sr[e] = 0xFF800000u;
       }
-      if (key0 + kBN > T) {
-        // slots >= T: visible only on the row's ancestor list (and < T + rows)
+      if (key0 + kBN > T || key0 + kBN > run.k1) {
+        // slots >= T: visible only on the row's ancestor list (and < T + rows);
+        // slots past this split's run (columns of the tile the products did
+        // not compute, or the next split's keys) are not this CTA's
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t vm = visible32(anc, key0 + 64 * half + 32 * c - T, p.rows);
+          const int s0 = key0 + 64 * half + 32 * c;
+          uint32_t vm = visible32(anc, s0 - T, p.rows);
+          const int lim_end = run.k1 - s0;
+          if (lim_end < 32) vm &= lim_end <= 0 ? 0u : ((1u << lim_end) - 1u);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             sr[32 * c + e] = ((vm >> e) & 1u) ? sr[32 * c + e] : 0xFF800000u;  // -inf
