@@ -224,9 +224,11 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 }
 
 // Key run of one split: [k0, k1) of [0, n_keys), equal runs of `per` slots
-// (a multiple of 32), so that the splits of a group finish together; its key
-// tiles are the 128-slot pieces of the run, the last one `cols` wide (rounded
-// up to 32; the QK^T and PV products of that tile stop there).
+// (a multiple of `align`: 32 when the splits of a group wait for each other,
+// so that they finish together; a whole tile in ticket mode, where a split
+// that finishes early frees its SM for the next wave); its key tiles are the
+// 128-slot pieces of the run, the last one `cols` wide (rounded up to 32; the
+// QK^T and PV products of that tile stop there).
 struct SplitRun {
   int k0, k1, n_tiles;
   __device__ __forceinline__ int tile_key0(int j) const { return k0 + j * kBN; }
@@ -235,14 +237,22 @@ struct SplitRun {
     return c > kBN ? kBN : c;
   }
 };
-__device__ __forceinline__ SplitRun split_run(int n_keys, int n_split, int split) {
-  const int per = ((n_keys + n_split - 1) / n_split + 31) / 32 * 32;
+__device__ __forceinline__ SplitRun split_run(int n_keys, int n_split, int split, int align) {
+  const int per = ((n_keys + n_split - 1) / n_split + align - 1) / align * align;
   SplitRun r;
   r.k0 = split * per;
   r.k1 = r.k0 + per < n_keys ? r.k0 + per : n_keys;
   r.n_tiles = r.k1 > r.k0 ? (r.k1 - r.k0 + kBN - 1) / kBN : 0;
   if (r.n_tiles == 0) r.k1 = r.k0;
   return r;
+}
+
+// PV steps of 16 slots for key tile j: up to the tile's columns, and for the
+// last tile of the key range up to the first step boundary past n_keys.
+__device__ __forceinline__ int pv_steps(const SplitRun& run, int j, int n_keys) {
+  const int key0 = run.tile_key0(j);
+  const int steps = run.tile_cols(j) / 16;
+  return key0 + steps * 16 > n_keys ? (n_keys - key0 + 15) / 16 : steps;
 }
 
 // word w (0..3) of a row's ancestor mask, 0 outside, without dynamic indexing
@@ -458,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     T_pre = *p.t_len[req];
     if (T_pre >= 0 && T_pre + p.rows <= p.t_cap[req]) {
-      const SplitRun run_pre = split_run(T_pre + p.rows, n_split, split);
+      const SplitRun run_pre = split_run(T_pre + p.rows, n_split, split, p.ticket_merge ? kBN : 32);
       const uint64_t pol_kv = policy_evict_first();
       for (int j = 0; j < kPreTiles && j < run_pre.n_tiles; ++j) {
         const int key0 = run_pre.tile_key0(j);
@@ -502,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool room = !raced && T >= 0 && T + p.rows <= p.t_cap[req];
   // key tiles of this split over slots [0, T + rows)
   const int n_keys = room ? T + p.rows : 0;
-  const SplitRun run = split_run(n_keys, n_split, split);
+  const SplitRun run = split_run(n_keys, n_split, split, p.ticket_merge ? kBN : 32);
   const int my_tiles = run.n_tiles;
 
   if (threadIdx.x == 0 && !room && !raced && local == 0) report(GLANCE_DEV_TREE_CAPACITY);
@@ -542,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int head = g * p.G + hl;
   float m = -INFINITY, lh = 0.f;
   bool ok = true;
+  int n_issued = 0;  // K/V tiles the producer issued (after an abort: which may still land)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -587,17 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++issued;
       }
-      {
-        // Copies still in flight land before the CTA's smem is released (they
-        // have, unless another role gave up early): Q and the last kStages
-        // tiles issued, the only ones whose stage barrier has not moved on.
-        (void)mbar_wait(&bars->q_full, 0, 50000000ull);
-        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        {
-          (void)mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, 50000000ull);
-          if (!withheld(j)) (void)mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, 50000000ull);
-        }
-      }
+      n_issued = issued;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -637,21 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sKV + (j % kStages) * kKVStageBytes) + 2 * kHalfBytes;
         // O += P V over the tile's key slots, 16 per step (8 bf16-pair columns
-        // of P each). The last tile of the key range stops at the first step
-        // boundary past T + rows; the V rows of that step beyond T + rows are
-        // never weighted (P = 0) but may hold anything, even NaN (0 * NaN =
-        // NaN), so they are zeroed first.
-        const int key0 = run.tile_key0(j);
-        int steps = run.tile_cols(j) / 16;
-        if (key0 + steps * 16 > n_keys) {
-          const int valid_rows = n_keys - key0;
-          steps = (valid_rows + 15) / 16;
-          unsigned char* vs = sKV + (j % kStages) * kKVStageBytes + 2 * kHalfBytes;
-          for (int i = valid_rows * 16; i < steps * 16 * 16; ++i)  // (row, 16-byte chunk), 8 chunks per half
-            reinterpret_cast<uint4*>(vs + ((i & 15) >> 3) * kHalfBytes + (i >> 4) * 128)[i & 7] =
-                make_uint4(0u, 0u, 0u, 0u);
-          fence_proxy_async_smem();
-        }
+        // of P each); the last tile of the key range stops at the first step
+        // boundary past T + rows (the softmax threads zeroed the V rows of
+        // that step beyond T + rows before releasing P).
+        const int steps = pv_steps(run, j, n_keys);
         for (int kk = 0; kk < steps; ++kk)
           mma_bf16_ts(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_o,
                       (j > 0 || kk > 0) ? 1u : 0u);
@@ -660,9 +650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + kStages < my_tiles) mma_commit(&bars->kv_empty[j % kStages]);
       }
       if (!good) fail_pipeline(bars);
-      // every MMA issued has finished before tensor memory is freed
-      mma_commit(&bars->mma_drain);
-      (void)mbar_wait(&bars->mma_drain, 0, 50000000ull);
     }
   } else if (is_sm) {
     // ------------------------------------------------------------ softmax
@@ -778,6 +765,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       lh = lh * alpha + (ls0 + ls1);
       m = m_new;
+      // The V rows of the key range's last PV step beyond T + rows are never
+      // weighted (P = 0) but may hold anything, even NaN (0 * NaN = NaN): the
+      // 256 softmax threads zero them (at most 15 rows of 256 bytes, one
+      // 16-byte store each) once the tile's V has landed, before P is released.
+      {
+        const int key0z = run.tile_key0(j);
+        const int zrows = pv_steps(run, j, n_keys) * 16 - (n_keys - key0z);
+        if (zrows > 0) {
+          const int t = threadIdx.x - 128;
+          if (wait_or_abort(&bars->v_full[j % kStages], (j / kStages) & 1, bars, p.wait_ns)) {
+            if (t < zrows * 16) {
+              unsigned char* vs = sKV + (j % kStages) * kKVStageBytes + 2 * kHalfBytes;
+              const int r = n_keys - key0z + (t >> 4), c = t & 15;  // row, 16-byte chunk (8 per half)
+              reinterpret_cast<uint4*>(vs + (c >> 3) * kHalfBytes + r * 128)[c & 7] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          } else {
+            fail_pipeline(bars);
+          }
+        }
+      }
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
     }
@@ -952,6 +960,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // On the normal path every copy has landed and every MMA has finished (the
+  // MMA thread waited for each tile's copies, the softmax threads for the
+  // last product). After an abort some may still be in flight: the producer
+  // waits for Q and its last kStages tiles (the only ones whose stage
+  // barriers have not moved on) and the MMA thread for its products before
+  // shared and tensor memory are released. Checked only here, after every
+  // role is done, so that no role spins on them while the others work.
+  if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) {
+    if (threadIdx.x == 0 && my_tiles > 0) {
+      const int withhold_from = p.withhold_v ? my_tiles - 1 : my_tiles;
+      (void)mbar_wait(&bars->q_full, 0, 50000000ull);
+      for (int j = n_issued > kStages ? n_issued - kStages : 0; j < n_issued; ++j) {
+        (void)mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, 50000000ull);
+        if (j < withhold_from || j < pre) (void)mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, 50000000ull);
+      }
+    }
+    if (warp == 1 && lane == 0 && my_tiles > 0) {
+      mma_commit(&bars->mma_drain);
+      (void)mbar_wait(&bars->mma_drain, 0, 50000000ull);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
