@@ -129,6 +129,29 @@ def test_constant_rows_lowest_ids_win(dev, clean_status):
     assert_same_tree(got, ref)
 
 
+def test_tied_block_beyond_expansion_capacity(dev, clean_status):
+    # 100 equal logits per row, the rest far below: 10000 depth-2 strings tie
+    # exactly at the N-th score, more than the threshold expansion holds, so
+    # the build falls back to the one-warp search; ties go to the lower rank
+    # vector either way
+    x = np.full((3, 1000), -30.0, np.float32)
+    x[:, 200:300] = 0.0
+    got = gpu_tree(x, 255, 5, 64, dev)
+    ref = o_build(x.astype(np.float64), 255, 5, 64)
+    assert_same_tree(got, ref)
+
+
+def test_tied_block_within_expansion_capacity(dev, clean_status):
+    # 15 equal logits per row, N = 60: the 15 depth-1 nodes and 45 of the
+    # 225 exactly tied depth-2 strings; the expansion ranks the tie by rank
+    # vectors
+    x = np.full((3, 1000), -30.0, np.float32)
+    x[:, 100:115] = 0.0
+    got = gpu_tree(x, 60, 5, 64, dev)
+    ref = o_build(x.astype(np.float64), 60, 5, 64)
+    assert_same_tree(got, ref)
+
+
 def test_root_and_T_read_from_device(dev, clean_status):
     x = W.draft_logits_planted(4, 300, seed=3)
     got = gpu_tree(x, 9, 123456, 77777, dev)

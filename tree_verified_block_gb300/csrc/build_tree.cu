@@ -26,6 +26,8 @@
 //     canonical order.
 #include "glance_internal.cuh"
 
+#include <cstddef>
+
 GLANCE_DEFINE_STATUS_WORD(status_build_tree)
 
 using namespace glance_dev;
@@ -284,7 +286,7 @@ struct __align__(16) PopRec {
   unsigned long long hi, lo;  // rank bytes of the path
 };
 
-struct TreeSmem {
+struct TreeSmem {  // sizeof is a multiple of 16 (PopRec alignment)
   PopRec pop[kMaxN];
   int16_t p_pos[kMaxN];
   uint8_t rank[kMaxN];  // a pop's rank at its own depth (the search's record)
@@ -529,8 +531,378 @@ __device__ __noinline__ void search_warp(TreeSmem& ts, const float* s_logq, cons
     }
 }
 
+// ------------------------------------------------- threshold level expansion
+//
+// The best-first order pops the nodes in the total order (score desc, then
+// depth, then rank vector): a node's parent and its left sibling both precede
+// it, so the N pops are exactly the N first nodes of that order, and every
+// one of them scores at least the N-th score tau. The expansion below builds
+// a superset of them without popping one node at a time:
+//  - t starts as a lower bound on tau: the N-th score of the one-deviation
+//    nodes (0, .., 0, r), which are N real nodes;
+//  - depth by depth, every node with score >= t gets all its children with
+//    score >= t (a prefix of its rank list: the log q rows are sorted), so
+//    after the last depth the set holds every node scoring >= t;
+//  - t is raised during the expansion to the score below which fewer than N
+//    generated nodes lie (a score histogram; the value stays a lower bound
+//    on tau because it counts real nodes);
+//  - the nodes scoring >= the final t are ranked by the total order and the
+//    N first become the pops, in best-first order.
+// Scores are computed exactly as the search adds them (parent score plus the
+// child's log q, fp32), so the pops are identical. If the set would outgrow
+// its capacity the expansion gives up and the one-warp search runs instead.
+constexpr int kLvCap = 2048;  // generated nodes
+constexpr int kLvBuckets = 256;
+constexpr int kLvDirect = 8;  // children a parent writes itself
+constexpr int kLvMaxCand = 512;  // nodes ranked at the end
+
+struct LevelSmem {
+  float sc[kLvCap];        // score
+  uint32_t meta[kLvCap];   // depth | rank << 5 | (parent + 1) << 13
+  float csc[kLvCap];       // candidates' scores (read as float4)
+  uint32_t off[kLvCap + 1];
+  uint16_t cand[kLvCap];
+  uint16_t pop_of[kLvCap];
+  unsigned long long chi[kLvMaxCand], clo[kLvMaxCand];  // candidates' rank vectors
+  uint8_t cdep[kLvMaxCand];
+  uint32_t hcnt[kLvBuckets];
+  float P[kMaxL + 1];      // chain scores: P[d] = score of 0^d
+  uint32_t warp_tot[kThreads / 32];
+  float t;
+  int m;
+};
+static_assert(offsetof(LevelSmem, csc) % 16 == 0, "candidate scores are read as float4");
+static_assert(sizeof(TreeSmem) % 16 == 0, "LevelSmem follows TreeSmem 16-byte aligned");
+
+__device__ __forceinline__ int lv_dep(uint32_t m) { return static_cast<int>(m & 31u); }
+__device__ __forceinline__ uint32_t lv_rank(uint32_t m) { return (m >> 5) & 0xFFu; }
+__device__ __forceinline__ int lv_par(uint32_t m) { return static_cast<int>(m >> 13) - 1; }
+
+// Score histogram from the best score s_max down: bucket b holds scores in
+// (s_max - (b+1) w, s_max - b w]; monotone in the score.
+struct LvBuckets {
+  float s_max, inv_w, w;
+  __device__ int operator()(float s) const {
+    const float x = (s_max - s) * inv_w;
+    if (!(x < static_cast<float>(kLvBuckets - 1))) return kLvBuckets - 1;
+    return x > 0.f ? static_cast<int>(x) : 0;
+  }
+};
+
+// Threads 0..31: the bucket b* where the count from the top reaches N. Every
+// counted node scores above s_max - (b* + 1) w up to rounding, which the
+// bucket width (at least 2^-18 of the largest magnitude) keeps far below one
+// bucket, so t = s_max - (b* + 2) w has N real nodes at or above it. Writes
+// max(t_cur, t) to S.t; the caller syncs before reading it.
+__device__ void lv_propose(LevelSmem& S, const LvBuckets& bk, int N, float t_cur) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  constexpr int per = kLvBuckets / 32;
+  uint32_t c[per], local = 0;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    c[i] = S.hcnt[lane * per + i];
+    local += c[i];
+  }
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  uint32_t run = incl - local;
+  int bs = -1;
+#pragma unroll
+  for (int i = 0; i < per; ++i) {
+    if (bs < 0 && run + c[i] >= static_cast<uint32_t>(N)) bs = lane * per + i;
+    run += c[i];
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, bs >= 0);
+  const int b = __shfl_sync(0xffffffffu, bs, hit ? __ffs(hit) - 1 : 0);
+  if (lane == 0) {
+    float t = t_cur;
+    if (hit && b < kLvBuckets - 2) t = fmaxf(t_cur, bk.s_max - static_cast<float>(b + 2) * bk.w);
+    S.t = t;
+  }
+}
+
+// Number of ranks r < K with s + row[r] >= t (a prefix: the row is sorted
+// descending and fp32 addition is monotone): galloping, then bisection.
+__device__ __forceinline__ int lv_prefix_count(float s, const float* row, int K, float t) {
+  if (!(s + row[0] >= t)) return 0;
+  int lo = 1, step = 1;  // ranks below lo pass
+  while (lo < K && s + row[min(lo + step - 1, K - 1)] >= t) {
+    lo = min(lo + step, K);
+    step <<= 1;
+  }
+  int hi = min(lo + step - 1, K);  // the first failing rank is in [lo, hi]
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s + row[mid] >= t) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// (depth, rank vector) of a generated node, from its parent links
+__device__ __forceinline__ void lv_path(const LevelSmem& S, int u, uint32_t& dep,
+                                        unsigned long long& hi, unsigned long long& lo) {
+  hi = lo = 0ull;
+  const uint32_t m0 = S.meta[u];
+  dep = static_cast<uint32_t>(lv_dep(m0));
+  for (int v = u; v >= 0;) {
+    const uint32_t m = S.meta[v];
+    set_rank(hi, lo, lv_dep(m) - 1, lv_rank(m));
+    v = lv_par(m);
+  }
+}
+
+// All threads of the CTA. Returns false (uniformly) when the node set would
+// outgrow kLvCap or more than kLvMaxCand nodes tie into the final bound;
+// ts.pop is then untouched.
+__device__ bool expand_levels(TreeSmem& ts, LevelSmem& S, const float* s_logq, const int N,
+                              const int L, const int K) {
+  const int tid = threadIdx.x;
+  if (K < N) return false;  // V < N: the depth-1 row cannot seed the bound
+  const float t_lo = s_logq[N - 1], s_max = s_logq[0];
+  LvBuckets bk;
+  bk.s_max = s_max;
+  bk.w = fmaxf((s_max - t_lo) / static_cast<float>(kLvBuckets), fabsf(t_lo) * 0x1p-18f);
+  bk.inv_w = bk.w > 0.f ? 1.f / bk.w : 0.f;
+  for (int i = tid; i < kLvBuckets; i += kThreads) S.hcnt[i] = 0u;
+  if (tid == 0) {
+    float v[kMaxL];
+#pragma unroll
+    for (int d = 0; d < kMaxL; ++d) v[d] = d < L ? s_logq[d * K] : 0.f;
+    float pd = 0.f;
+    S.P[0] = 0.f;
+#pragma unroll
+    for (int d = 0; d < kMaxL; ++d) {
+      pd = pd + v[d];
+      S.P[d + 1] = pd;
+    }
+  }
+  __syncthreads();
+  // one-deviation nodes (0^(d-1), r); consecutive threads take different rows
+  for (int i = tid; i < L * K; i += kThreads) {
+    const int d = i % L, r = i / L;
+    const float f = S.P[d] + s_logq[d * K + r];
+    if (f >= t_lo) atomicAdd(&S.hcnt[bk(f)], 1u);
+  }
+  __syncthreads();
+  lv_propose(S, bk, N, t_lo);
+  __syncthreads();
+  float t = S.t;
+  for (int i = tid; i < kLvBuckets; i += kThreads) S.hcnt[i] = 0u;
+  // depth 1: the ranks with log q >= t
+  int total;
+  {
+    int a = 0, b = K;
+    while (a < b) {
+      const int mid = (a + b) >> 1;
+      if (s_logq[mid] >= t) a = mid + 1;
+      else b = mid;
+    }
+    total = a;
+  }
+  __syncthreads();
+  for (int r = tid; r < total; r += kThreads) {
+    const float s = s_logq[r];
+    S.sc[r] = s;
+    S.meta[r] = 1u | (static_cast<uint32_t>(r) << 5);
+    atomicAdd(&S.hcnt[bk(s)], 1u);
+  }
+  __syncthreads();
+  int lb = 0, le = total, last_raise = 0;
+  for (int d = 2; d <= L && le > lb; ++d) {
+    if (total > 2 * N && total - last_raise >= N / 2) {
+      lv_propose(S, bk, N, t);
+      __syncthreads();
+      t = S.t;
+      last_raise = total;
+    }
+    const float* row = s_logq + (d - 1) * K;
+    const int n = le - lb;
+    const int q = (n + kThreads - 1) / kThreads;  // nodes per thread, <= kLvCap / kThreads
+    const int u0 = lb + tid * q, u1 = min(u0 + q, le);
+    uint32_t excl = 0, tot_new = 0;
+    for (int attempt = 0;; ++attempt) {
+      // child counts, kept in off[] until the offsets replace them
+      uint32_t local = 0;
+#pragma unroll 1
+      for (int u = u0; u < u1; ++u) {
+        const float s = S.sc[u];
+        const uint32_t c = s >= t ? static_cast<uint32_t>(lv_prefix_count(s, row, K, t)) : 0u;
+        S.off[u - lb] = c;
+        local += c;
+      }
+      const uint32_t incl = block_incl_scan(local, S.warp_tot);
+      excl = incl - local;
+      if (tid == kThreads - 1) S.off[kLvCap] = incl;
+      __syncthreads();
+      tot_new = S.off[kLvCap];
+      if (total + static_cast<int>(tot_new) <= kLvCap) break;
+      if (attempt > 0 || total < N) return false;
+      lv_propose(S, bk, N, t);
+      __syncthreads();
+      t = S.t;
+      last_raise = total;
+    }
+    // children: each parent writes its first kLvDirect itself
+    bool big = false;
+    {
+      uint32_t o = excl;
+#pragma unroll 1
+      for (int u = u0; u < u1; ++u) {
+        const int nc = static_cast<int>(S.off[u - lb]);
+        S.off[u - lb] = o;
+        big |= nc > kLvDirect;
+        const float s = S.sc[u];
+#pragma unroll 1
+        for (int c = 0; c < min(nc, kLvDirect); ++c) {
+          const int idx = total + static_cast<int>(o) + c;
+          const float sc = s + row[c];
+          S.sc[idx] = sc;
+          S.meta[idx] = static_cast<uint32_t>(d) | (static_cast<uint32_t>(c) << 5) |
+                        (static_cast<uint32_t>(u + 1) << 13);
+          atomicAdd(&S.hcnt[bk(sc)], 1u);
+        }
+        o += static_cast<uint32_t>(nc);
+      }
+    }
+    if (__syncthreads_or(big)) {
+      // the remaining children, spread over the CTA; a child's parent is the
+      // last node of the depth whose offset is <= the child's slot
+      for (int c = tid; c < static_cast<int>(tot_new); c += kThreads) {
+        int a = 0, b = n - 1;
+        while (a < b) {
+          const int mid = (a + b + 1) >> 1;
+          if (S.off[mid] <= static_cast<uint32_t>(c)) a = mid;
+          else b = mid - 1;
+        }
+        const int j = c - static_cast<int>(S.off[a]);
+        if (j < kLvDirect) continue;
+        const int u = lb + a;
+        const float sc = S.sc[u] + row[j];
+        const int idx = total + c;
+        S.sc[idx] = sc;
+        S.meta[idx] = static_cast<uint32_t>(d) | (static_cast<uint32_t>(j) << 5) |
+                      (static_cast<uint32_t>(u + 1) << 13);
+        atomicAdd(&S.hcnt[bk(sc)], 1u);
+      }
+      __syncthreads();
+    }
+    lb = total;
+    total += static_cast<int>(tot_new);
+    le = total;
+  }
+  // candidates: the nodes scoring >= the final bound
+  lv_propose(S, bk, N, t);
+  __syncthreads();
+  t = S.t;
+  {
+    const int q = (total + kThreads - 1) / kThreads;
+    uint32_t local = 0;
+    for (int j = 0; j < q; ++j) {
+      const int u = tid * q + j;
+      if (u < total && S.sc[u] >= t) ++local;
+    }
+    const uint32_t incl = block_incl_scan(local, S.warp_tot);
+    uint32_t o = incl - local;
+    for (int j = 0; j < q; ++j) {
+      const int u = tid * q + j;
+      if (u < total && S.sc[u] >= t) {
+        S.cand[o] = static_cast<uint16_t>(u);
+        S.csc[o] = S.sc[u];
+        ++o;
+      }
+    }
+    if (tid == kThreads - 1) S.m = static_cast<int>(incl);
+  }
+  __syncthreads();
+  const int M = S.m;
+  if (M > kLvMaxCand) return false;
+  for (int i = tid; i < M; i += kThreads) {
+    uint32_t dep;
+    lv_path(S, S.cand[i], dep, S.chi[i], S.clo[i]);
+    S.cdep[i] = static_cast<uint8_t>(dep);
+  }
+  __syncthreads();
+  // rank of every candidate in the total order, by counting: the scores
+  // first (four at a time), the (depth, rank vector) keys only among equal
+  // scores
+  for (int i = tid; i < M; i += kThreads) {
+    const float su = S.csc[i];
+    int above = 0, eq = 0, j = 0;
+    for (; j + 4 <= M; j += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(&S.csc[j]);
+      above += (v.x > su) + (v.y > su) + (v.z > su) + (v.w > su);
+      eq += (v.x == su) + (v.y == su) + (v.z == su) + (v.w == su);
+    }
+    for (; j < M; ++j) {
+      const float v = S.csc[j];
+      above += v > su;
+      eq += v == su;
+    }
+    int rank = above;
+    const int u = S.cand[i];
+    if (eq > 1) {
+      const uint32_t du = S.cdep[i];
+      const unsigned long long hu = S.chi[i], lu = S.clo[i];
+      for (int k = 0; k < M; ++k) {
+        if (S.csc[k] != su || k == i) continue;
+        rank += tie_less(S.cdep[k], S.chi[k], S.clo[k], du, hu, lu);
+      }
+    }
+    if (rank < N) {
+      S.off[rank] = static_cast<uint32_t>(i);  // pop rank -> candidate
+      S.pop_of[u] = static_cast<uint16_t>(rank);
+    }
+  }
+  __syncthreads();
+  // the pops, in best-first order; a pop's parent pops before it
+  for (int k = tid; k < N; k += kThreads) {
+    const int i = static_cast<int>(S.off[k]);
+    const int u = S.cand[i];
+    const int par = lv_par(S.meta[u]);
+    PopRec pr;
+    pr.score = S.sc[u];
+    pr.pscore = par >= 0 ? S.sc[par] : 0.f;
+    pr.dep = static_cast<int>(S.cdep[i]);
+    pr.par = par >= 0 ? static_cast<int>(S.pop_of[par]) : -1;
+    pr.hi = S.chi[i];
+    pr.lo = S.clo[i];
+    ts.pop[k] = pr;
+  }
+  __syncthreads();
+  return true;
+}
+
+// Which search is cheaper. The expansion costs about 8000 + 2000 D cycles
+// for D depths, the one-warp search about 600 cycles per pop (both measured
+// on GB300). D is bounded by the deepest chain 0^d scoring at least the N-th
+// depth-1 score, the expansion's loosest bound. All threads; uniform result.
+__device__ bool use_levels(LevelSmem& S, const float* s_logq, const int N, const int L,
+                           const int K) {
+  if (K < N) return false;
+  if (threadIdx.x == 0) {
+    const float t_lo = s_logq[N - 1];
+    float pd = 0.f;
+    int D = 0;
+    for (int d = 0; d < L; ++d) {
+      pd = pd + s_logq[d * K];
+      if (pd >= t_lo) D = d + 1;
+    }
+    S.m = 8000 + 2000 * D < 600 * N ? 1 : 0;
+  }
+  __syncthreads();
+  const bool r = S.m != 0;
+  __syncthreads();
+  return r;
+}
+
 __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int req) {
-  // dynamic smem: logq [L][K] floats, tok [L][K] ints, then TreeSmem
+  // dynamic smem: logq [L][K] floats, tok [L][K] ints, TreeSmem, LevelSmem
   float* s_logq = reinterpret_cast<float*>(dyn);
   int* s_tok = reinterpret_cast<int*>(dyn + sizeof(float) * p.L * p.K);
   TreeSmem& ts = *reinterpret_cast<TreeSmem*>(
@@ -544,16 +916,19 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
   __syncthreads();
   const int N = p.N, L = p.L, K = p.K;
 
-  if (threadIdx.x < 32) {
-    // frontier capacity 32 x slots per lane >= N + 1: fewer slots, shorter pops
-    if (N < 64)
-      search_warp<2>(ts, s_logq, N, L, K);
-    else if (N < 128)
-      search_warp<4>(ts, s_logq, N, L, K);
-    else
-      search_warp<8>(ts, s_logq, N, L, K);
+  LevelSmem& ls = *reinterpret_cast<LevelSmem*>(reinterpret_cast<unsigned char*>(&ts) + sizeof(TreeSmem));
+  if (!use_levels(ls, s_logq, N, L, K) || !expand_levels(ts, ls, s_logq, N, L, K)) {
+    if (threadIdx.x < 32) {
+      // frontier capacity 32 x slots per lane >= N + 1: fewer slots, shorter pops
+      if (N < 64)
+        search_warp<2>(ts, s_logq, N, L, K);
+      else if (N < 128)
+        search_warp<4>(ts, s_logq, N, L, K);
+      else
+        search_warp<8>(ts, s_logq, N, L, K);
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   if (p.search_only) {
     // shared budget: hand the pops (in best-first order) to the pack kernel
@@ -933,7 +1308,7 @@ glance_status launch_build(const char* who, const void* draft_logits, glance_dty
   // dynamic smem: the chunk's logits during selection, the tree search after
   // dynamic smem: the chunk's logits during selection, the row's candidate
   // keys during the row merge, the tree search after
-  size_t dyn = 16 * ((sizeof(float) * 2 * L * p.K + 15) / 16) + sizeof(TreeSmem);
+  size_t dyn = 16 * ((sizeof(float) * 2 * L * p.K + 15) / 16) + sizeof(TreeSmem) + sizeof(LevelSmem);
   if (dyn < sizeof(float) * kChunk) dyn = sizeof(float) * kChunk;
   const size_t cand_bytes = sizeof(unsigned long long) * static_cast<size_t>(p.C) * p.K;
   if (dyn < cand_bytes) dyn = cand_bytes;
