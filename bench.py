@@ -880,6 +880,9 @@ def run_case(args):
     if args.case in ("attn255", "attn_ragged8"):
         run_attn_case(args, dev)
         return
+    if args.case in ("tree63", "tree255"):
+        run_tree_case(args, dev)
+        return
     M, d, V = 512, 4096, 151936
     tg = torch.Generator(device=dev)
     tg.manual_seed(7)
@@ -1289,6 +1292,31 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_tree_case(args, dev):
+    """The draft-to-tree build alone, for profiler captures: tree63 = the
+    full36 draft marginals (15 x 151936 planted logits, N = 63); tree255 =
+    4.0-nat marginals at N = 255 (the entropy sweep's bushiest tree).
+    Inputs drawn on the host from seeded generators and copied once."""
+    import torch
+    import tree_verified_block_gb300 as g
+    L, V = FULL36["L"], FULL36["V"]
+    if args.case == "tree63":
+        N, x = 63, W.draft_logits_planted(L, V, seed=3001)
+    else:
+        N, x = 255, W.draft_logits_entropy(L, V, 4.0, seed=4140)
+    xd = torch.from_numpy(x).to(dev)
+    tree = g.Tree(N, L, dev)
+    ws = g.workspace(g.build_tree_workspace_bytes(L, V, N), dev)
+    t_len = torch.tensor([FULL36["T"]], dtype=torch.int32, device=dev)
+    root = torch.tensor([1234], dtype=torch.int32, device=dev)
+    fn = lambda: g.build_tree(xd, N, root, t_len, tree, ws)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    us = graph_time_us(fn, 20)
+    print(json.dumps({"case": args.case, "us": round(us, 2)}), flush=True)
+
+
 def run_attn_case(args, dev):
     """One tree-attention layer alone, for profiler captures: attn255 = one
     layer at T = 2048, N = 255 (1024 query rows per kv head: tensor / MUFU
@@ -1348,7 +1376,8 @@ def main():
     ap.add_argument("--workload", default="full36", choices=["full36", "small"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--case", default=None, choices=["lmhead512", "lmhead512_entropy", "lmhead512_sample",
-                                                     "attn255", "attn_ragged8", "dense_layer", "forward36"],
+                                                     "attn255", "attn_ragged8", "dense_layer", "forward36",
+                                                     "tree63", "tree255"],
                     help="run one kernel alone on a small case (for profiler captures)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the entropy36 sweep and the verify1 single-layer case")

@@ -74,6 +74,7 @@ struct SelectSmem {
   uint32_t above, cnt;
   uint32_t digit, above2, cnt2;
   uint32_t nb;
+  uint32_t pos;  // pass-2 output count
   unsigned long long bnd[kBoundary];
 };
 
@@ -110,7 +111,7 @@ __device__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
   return v + add;
 }
 
-// Selects the `want` best items (by unique 64-bit key) of kPerThread items per
+// Selects the `want` best items (by unique 64-bit key) of n_per items per
 // thread and writes their keys, in any order, to out[0..want). item(e, v, x, k)
 // gives item e's validity, logit and key; m is the maximum valid logit.
 // Pass 1 histograms the gap to m in 1/64-nat buckets; the buckets above the
@@ -119,14 +120,17 @@ __device__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
 // boundary bucket of more than kBoundary items (massive exact ties) falls back
 // to a radix select over the items.
 template <typename Item>
-__device__ void select_top(Item item, uint32_t want, float m, unsigned long long* out,
+__device__ void select_top(Item item, const int n_per, uint32_t want, float m, unsigned long long* out,
                            SelectSmem& sm) {
   if (want == 0) return;  // uniform across the block
   for (int i = threadIdx.x; i < kBuckets; i += kThreads) sm.hist[i] = 0;
-  if (threadIdx.x == 0) sm.nb = 0;
+  if (threadIdx.x == 0) {
+    sm.nb = 0;
+    sm.pos = 0;
+  }
   __syncthreads();
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
+#pragma unroll 4
+  for (int e = 0; e < n_per; ++e) {
     bool v;
     float x;
     unsigned long long k;
@@ -160,30 +164,26 @@ __device__ void select_top(Item item, uint32_t want, float m, unsigned long long
   const bool whole = sm.cnt == need;
   const bool small = sm.cnt <= static_cast<uint32_t>(kBoundary);
   // pass 2: buckets above the boundary (and the boundary when it is taken
-  // whole) go straight to out; boundary items go to the shared list
-  uint32_t c1 = 0;
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
+  // whole) go straight to out, compacted per warp by ballot (any order);
+  // boundary items go to the shared list
+  const int lane = threadIdx.x & 31;
+#pragma unroll 4
+  for (int e = 0; e < n_per; ++e) {
     bool v;
     float x;
     unsigned long long k;
     item(e, v, x, k);
     const int b = v ? bucket_of(m, x) : kBuckets;
-    c1 += (b < bstar || (whole && b == bstar));
-  }
-  uint32_t pos = block_incl_scan(c1, sm.warp_tot) - c1;
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    bool v;
-    float x;
-    unsigned long long k;
-    item(e, v, x, k);
-    const int b = v ? bucket_of(m, x) : kBuckets;
-    if (b < bstar || (whole && b == bstar)) {
-      out[pos++] = k;
-    } else if (b == bstar && small) {
-      sm.bnd[atomicAdd(&sm.nb, 1u)] = k;
+    const bool sel = b < bstar || (whole && b == bstar);
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    if (bal != 0u) {
+      const int leader = __ffs(bal) - 1;
+      uint32_t base = 0;
+      if (lane == leader) base = atomicAdd(&sm.pos, static_cast<uint32_t>(__popc(bal)));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (sel) out[base + __popc(bal & ((1u << lane) - 1u))] = k;
     }
+    if (!sel && b == bstar && small) sm.bnd[atomicAdd(&sm.nb, 1u)] = k;
   }
   if (whole) return;  // uniform: `whole` is read from shared memory
   __syncthreads();
@@ -205,7 +205,7 @@ __device__ void select_top(Item item, uint32_t want, float m, unsigned long long
     sm.hist[threadIdx.x] = 0;
     __syncthreads();
 #pragma unroll 2
-    for (int e = 0; e < kPerThread; ++e) {
+    for (int e = 0; e < n_per; ++e) {
       bool v;
       float x;
       unsigned long long k;
@@ -234,7 +234,7 @@ __device__ void select_top(Item item, uint32_t want, float m, unsigned long long
   }
   uint32_t c2 = 0;
 #pragma unroll 2
-  for (int e = 0; e < kPerThread; ++e) {
+  for (int e = 0; e < n_per; ++e) {
     bool v;
     float x;
     unsigned long long k;
@@ -243,7 +243,7 @@ __device__ void select_top(Item item, uint32_t want, float m, unsigned long long
   }
   uint32_t pos2 = above + block_incl_scan(c2, sm.warp_tot) - c2;
 #pragma unroll 2
-  for (int e = 0; e < kPerThread; ++e) {
+  for (int e = 0; e < n_per; ++e) {
     bool v;
     float x;
     unsigned long long k;
@@ -1050,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
         xv = xs[e * kThreads + threadIdx.x];
         k = make_key(xv, static_cast<uint32_t>(id_of(e)));
       },
-      static_cast<uint32_t>(kc), m, my_cand, sm);
+      kPerThread, static_cast<uint32_t>(kc), m, my_cand, sm);
   if (threadIdx.x == 0) {
     float tot = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) tot += red_d[w];
@@ -1107,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
         v = k != 0ull;
         xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
       },
-      static_cast<uint32_t>(p.K), row_max, sel, sm);
+      (n_cand + kThreads - 1) / kThreads, static_cast<uint32_t>(p.K), row_max, sel, sm);
   __syncthreads();
   // rank of each selected key among the K (keys are unique), by counting
   if (threadIdx.x < p.K) {
