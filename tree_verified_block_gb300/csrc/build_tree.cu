@@ -306,13 +306,14 @@ __device__ __forceinline__ uint32_t get_reg(const uint32_t (&a)[kSlots], int i) 
 // token -1, parent -1 (never a child, so the walk never reaches them), depth
 // 0, pos_id T, score -inf, ancestor mask = the row itself.
 __device__ void pack_rows(const BuildParams& p, const int* s_tok, TreeSmem& ts, const int req,
-                          const int n) {
+                          const int n, const bool have_pos) {
   const int N = p.N, K = p.K;
   // canonical position: 1 + number of nodes before it in (depth, rank vector)
+  // (given in ts.p_pos when have_pos)
   const int T = p.t_len[req];
   const glance_tree& tree = p.tree[req];
   const int W = tree.mask_words;
-  for (int kk = threadIdx.x; kk < n; kk += kThreads) {
+  for (int kk = have_pos ? n : threadIdx.x; kk < n; kk += kThreads) {
     const uint32_t dk = ts.pop[kk].dep;
     const unsigned long long hk = ts.pop[kk].hi, lk = ts.pop[kk].lo;
     int pos = 1;
@@ -827,6 +828,7 @@ __device__ bool expand_levels(TreeSmem& ts, LevelSmem& S, const float* s_logq, c
     lv_path(S, S.cand[i], dep, S.chi[i], S.clo[i]);
     S.cdep[i] = static_cast<uint8_t>(dep);
   }
+  for (int u = tid; u < total; u += kThreads) S.pop_of[u] = 0xFFFFu;  // not a pop
   __syncthreads();
   // rank of every candidate in the total order, by counting: the scores
   // first (four at a time), the (depth, rank vector) keys only among equal
@@ -874,14 +876,31 @@ __device__ bool expand_levels(TreeSmem& ts, LevelSmem& S, const float* s_logq, c
     pr.lo = S.clo[i];
     ts.pop[k] = pr;
   }
+  // Canonical positions. Nodes are stored depth by depth, and a depth's nodes
+  // follow their parents' order and then their own rank, so the storage order
+  // is the (depth, rank vector) order; a pop's row is 1 + the pops stored
+  // before it.
+  {
+    const int q = (total + kThreads - 1) / kThreads;
+    const int u0 = tid * q, u1 = min(u0 + q, total);
+    uint32_t local = 0;
+    for (int u = u0; u < u1; ++u) local += S.pop_of[u] != 0xFFFFu;
+    uint32_t at = block_incl_scan(local, S.warp_tot) - local;
+    for (int u = u0; u < u1; ++u) {
+      const uint32_t k = S.pop_of[u];
+      if (k != 0xFFFFu) ts.p_pos[k] = static_cast<int16_t>(1 + at++);
+    }
+  }
   __syncthreads();
   return true;
 }
 
-// Which search is cheaper. The expansion costs about 8000 + 2000 D cycles
-// for D depths, the one-warp search about 600 cycles per pop (both measured
-// on GB300). D is bounded by the deepest chain 0^d scoring at least the N-th
-// depth-1 score, the expansion's loosest bound. All threads; uniform result.
+// Which search is cheaper, packing included. The expansion costs about
+// 8000 + 2000 D cycles for D depths and hands the canonical rows over
+// (~1400 cycles); the one-warp search costs about 600 cycles per pop and its
+// packing about 4000 + 100 N (all measured on GB300). D is bounded by the
+// deepest chain 0^d scoring at least the N-th depth-1 score, the expansion's
+// loosest bound. All threads; uniform result.
 __device__ bool use_levels(LevelSmem& S, const float* s_logq, const int N, const int L,
                            const int K) {
   if (K < N) return false;
@@ -893,7 +912,7 @@ __device__ bool use_levels(LevelSmem& S, const float* s_logq, const int N, const
       pd = pd + s_logq[d * K];
       if (pd >= t_lo) D = d + 1;
     }
-    S.m = 8000 + 2000 * D < 600 * N ? 1 : 0;
+    S.m = 8000 + 2000 * D + 1400 < 600 * N + 4000 + 100 * N ? 1 : 0;
   }
   __syncthreads();
   const bool r = S.m != 0;
@@ -917,7 +936,8 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
   const int N = p.N, L = p.L, K = p.K;
 
   LevelSmem& ls = *reinterpret_cast<LevelSmem*>(reinterpret_cast<unsigned char*>(&ts) + sizeof(TreeSmem));
-  if (!use_levels(ls, s_logq, N, L, K) || !expand_levels(ts, ls, s_logq, N, L, K)) {
+  bool have_pos = use_levels(ls, s_logq, N, L, K) && expand_levels(ts, ls, s_logq, N, L, K);
+  if (!have_pos) {
     if (threadIdx.x < 32) {
       // frontier capacity 32 x slots per lane >= N + 1: fewer slots, shorter pops
       if (N < 64)
@@ -936,7 +956,7 @@ __device__ void tree_phase(const BuildParams& p, unsigned char* dyn, const int r
     for (int kk = threadIdx.x; kk < N; kk += kThreads) dst[kk] = ts.pop[kk];
     return;
   }
-  pack_rows(p, s_tok, ts, req, N);
+  pack_rows(p, s_tok, ts, req, N, have_pos);
 }
 
 // ------------------------------------------------------------------- kernel
@@ -1200,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads) shared_pack_kernel(const __grid_cons
   __syncthreads();
   const int n = s_cnt;
   if (threadIdx.x == 0) sa.n_active[req] = n;
-  pack_rows(p, s_tok, ts, req, n);
+  pack_rows(p, s_tok, ts, req, n, false);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
