@@ -59,7 +59,7 @@ NCU_TRAFFIC = {
     "glance_tree_attention": dict(bytes=17_900_800, digest="17c06640bb3ee913",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
-    "glance_lmhead_argmax": dict(bytes=1_245_317_376 + 2_755_840, digest="4536d90ed80de2dc",
+    "glance_lmhead_argmax": dict(bytes=1_245_446_144 + 3_010_304, digest="360ccb62ed8929c7",
                                  files=["lmhead.cu", "glance_internal.cuh"],
                                  profile="profiles/lmhead_argmax_full36.md"),
 }
