@@ -836,6 +836,7 @@ __device__ bool expand_levels(TreeSmem& ts, LevelSmem& S, const float* s_logq, c
   for (int i = tid; i < M; i += kThreads) {
     const float su = S.csc[i];
     int above = 0, eq = 0, j = 0;
+#pragma unroll 4
     for (; j + 4 <= M; j += 4) {
       const float4 v = *reinterpret_cast<const float4*>(&S.csc[j]);
       above += (v.x > su) + (v.y > su) + (v.z > su) + (v.w > su);
