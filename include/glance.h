@@ -86,6 +86,8 @@ typedef enum { GLANCE_F32 = 0, GLANCE_BF16 = 1 } glance_dtype;
 #define GLANCE_DEV_TREE_CAPACITY 2    /* the rows' K/V slots do not fit: T + rows > t_cap */
 #define GLANCE_DEV_BAD_TREE 3         /* a tree array was inconsistent */
 #define GLANCE_DEV_PIPELINE_TIMEOUT 4 /* a pipeline wait ran out of time (2 s) */
+#define GLANCE_DEV_OUT_OF_BOUNDS 5    /* bounds-checked build (GLANCE_CHECK) only: a computed
+                                        index fell outside its buffer; the access was skipped */
 
 /* A packed candidate tree: device arrays with N + 1 rows, caller-allocated. */
 typedef struct {

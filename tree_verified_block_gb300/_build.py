@@ -1,7 +1,11 @@
 """Build libglance.so in-tree with nvcc (sm_103a only).
 
 Each CUDA translation unit is compiled in parallel, then linked into one
-shared library under ``tree_verified_block_gb300/_lib/``. A unit is rebuilt
+shared library under ``tree_verified_block_gb300/_lib/``. The same units are
+also compiled with -DGLANCE_CHECK into ``libglance_check.so`` (objects under
+``_lib/check/``): the bounds-checked build, in which every computed global
+index is tested and an out-of-range one reports GLANCE_DEV_OUT_OF_BOUNDS
+instead of being accessed. A unit is rebuilt
 unless the sha256 digest stored beside its object matches the digest of its
 source, the internal header, the public header and the compiler flags; the
 library is relinked unless its stored digest matches those of its objects.
@@ -19,6 +23,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libglance.so")
+CHECK_OUT = os.path.join(OUT, "check")
+LIB_CHECK = os.path.join(OUT, "libglance_check.so")
 UNITS = ["api", "build_tree", "tree_attention", "lmhead", "commit", "dense"]
 HEADERS = [os.path.join(CSRC, "glance_internal.cuh"), os.path.join(ROOT, "include", "glance.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -61,11 +67,12 @@ def _store(path, digest):
         f.write(digest + "\n")
 
 
-def _compile(unit, force):
+def _compile(unit, force, checked=False):
     src = os.path.join(CSRC, unit + ".cu")
-    obj = os.path.join(OUT, unit + ".o")
-    cmd = [nvcc()] + ARCH + FLAGS + ["-c", src, "-o", obj]
-    want = _digest([src] + HEADERS, ARCH + FLAGS)
+    obj = os.path.join(CHECK_OUT if checked else OUT, unit + ".o")
+    flags = FLAGS + (["-DGLANCE_CHECK"] if checked else [])
+    cmd = [nvcc()] + ARCH + flags + ["-c", src, "-o", obj]
+    want = _digest([src] + HEADERS, ARCH + flags)
     if not force and os.path.exists(obj) and _stored(obj) == want:
         return obj, False
     if os.path.exists(obj + ".sha256"):
@@ -77,23 +84,32 @@ def _compile(unit, force):
     return obj, True
 
 
-def build(force=False, verbose=False):
-    """Compile and link; returns the library path."""
-    os.makedirs(OUT, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
-        results = list(ex.map(lambda u: _compile(u, force), UNITS))
-    objs = [o for o, _ in results]
+def _link(objs, lib, force, verbose):
     want = _digest(objs)
-    if force or not os.path.exists(LIB) or _stored(LIB) != want:
-        tmp = LIB + ".tmp"
+    if force or not os.path.exists(lib) or _stored(lib) != want:
+        tmp = lib + ".tmp"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-        _store(LIB, want)
+        os.replace(tmp, lib)
+        _store(lib, want)
         if verbose:
-            print("built", LIB)
+            print("built", lib)
+
+
+def build(force=False, verbose=False, checked=True):
+    """Compile and link libglance.so (and, with checked, libglance_check.so);
+    returns the path of libglance.so."""
+    os.makedirs(OUT, exist_ok=True)
+    os.makedirs(CHECK_OUT, exist_ok=True)
+    jobs = [(u, False) for u in UNITS] + ([(u, True) for u in UNITS] if checked else [])
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(lambda j: _compile(j[0], force, j[1]), jobs))
+    objs = [o for (o, _), (_, c) in zip(results, jobs) if not c]
+    _link(objs, LIB, force, verbose)
+    if checked:
+        _link([o for (o, _), (_, c) in zip(results, jobs) if c], LIB_CHECK, force, verbose)
     return LIB
 
 

@@ -181,7 +181,8 @@ __device__ void select_top(Item item, const int n_per, uint32_t want, float m, u
       uint32_t base = 0;
       if (lane == leader) base = atomicAdd(&sm.pos, static_cast<uint32_t>(__popc(bal)));
       base = __shfl_sync(0xffffffffu, base, leader);
-      if (sel) out[base + __popc(bal & ((1u << lane) - 1u))] = k;
+      const uint32_t at = base + __popc(bal & ((1u << lane) - 1u));
+      if (sel && GLANCE_IN_BOUNDS(at, want)) out[at] = k;
     }
     if (!sel && b == bstar && small) sm.bnd[atomicAdd(&sm.nb, 1u)] = k;
   }
@@ -248,7 +249,10 @@ __device__ void select_top(Item item, const int n_per, uint32_t want, float m, u
     float x;
     unsigned long long k;
     item(e, v, x, k);
-    if (v && bucket_of(m, x) == bstar && (k & mask) >= prefix) out[pos2++] = k;
+    if (v && bucket_of(m, x) == bstar && (k & mask) >= prefix) {
+      if (GLANCE_IN_BOUNDS(pos2, want)) out[pos2] = k;
+      ++pos2;
+    }
   }
 }
 
@@ -344,6 +348,7 @@ __device__ void pack_rows(const BuildParams& p, const int* s_tok, TreeSmem& ts, 
       continue;
     }
     const int row = ts.p_pos[kk];
+    if (!GLANCE_IN_BOUNDS(row, N + 1)) continue;
     const int d = ts.pop[kk].dep;
     const uint32_t r = get_rank(ts.pop[kk].hi, ts.pop[kk].lo, d - 1);
     const int par = ts.pop[kk].par;
@@ -992,7 +997,8 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
     for (int q = 0; q < kPerThread / 4; ++q) {
       const int v = threadIdx.x + kThreads * q;
       const int id0 = base + 4 * v;
-      if (4 * v < n_valid) {  // n_valid % 4 == 0 when vectorised
+      if (4 * v < n_valid &&  // n_valid % 4 == 0 when vectorised
+          GLANCE_IN_BOUNDS(static_cast<size_t>(row) * p.V + id0 + 3, static_cast<size_t>(p.B) * p.L * p.V)) {
         if (kBF16) {
           const uint2 raw = *reinterpret_cast<const uint2*>(
               static_cast<const uint16_t*>(p.logits) + static_cast<size_t>(row) * p.V + id0);
@@ -1017,8 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
       const int local = threadIdx.x + kThreads * e;
-      if (local < n_valid) {
-        const size_t gi = static_cast<size_t>(row) * p.V + base + local;
+      const size_t gi = static_cast<size_t>(row) * p.V + base + local;
+      if (local < n_valid && GLANCE_IN_BOUNDS(gi, static_cast<size_t>(p.B) * p.L * p.V)) {
         x[e] = kBF16 ? bf16_to_f32(static_cast<const uint16_t*>(p.logits)[gi])
                      : static_cast<const float*>(p.logits)[gi];
       } else {
@@ -1075,8 +1081,10 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
   if (threadIdx.x == 0) {
     float tot = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) tot += red_d[w];
-    p.chunk_m[row * p.C + chunk] = m;
-    p.chunk_s[row * p.C + chunk] = tot;
+    if (GLANCE_IN_BOUNDS(row * p.C + chunk, p.B * p.L * p.C)) {
+      p.chunk_m[row * p.C + chunk] = m;
+      p.chunk_s[row * p.C + chunk] = tot;
+    }
   }
 
   // ---- 2. last CTA of this row merges
@@ -1138,8 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 2) build_tree_kernel(const __grid_co
     for (int j = 0; j < p.K; ++j) rank += sel[j] > k;
     const float xv = inv_ord_key(static_cast<uint32_t>(k >> 32));
     const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
-    p.top_tok[row * p.K + rank] = static_cast<int32_t>(id);
-    p.top_logq[row * p.K + rank] = xv - s_lse;
+    if (GLANCE_IN_BOUNDS(row * p.K + rank, p.B * p.L * p.K)) {
+      p.top_tok[row * p.K + rank] = static_cast<int32_t>(id);
+      p.top_logq[row * p.K + rank] = xv - s_lse;
+    }
   }
 
   // ---- 3. last row-merger builds the tree

@@ -146,14 +146,15 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = threadIdx.x; i < total; i += kThreads) {
       const int r = i / vec_per_row, c = i - r * vec_per_row;
       const char* src = base + static_cast<long long>(T + s_path[r]) * rq.row_stride_bytes + 16 * c;
-      *reinterpret_cast<uint4*>(stage + r * p.row_bytes + 16 * c) =
-          *reinterpret_cast<const uint4*>(src);
+      if (GLANCE_IN_BOUNDS(T + s_path[r], rq.t_cap))
+        *reinterpret_cast<uint4*>(stage + r * p.row_bytes + 16 * c) = *reinterpret_cast<const uint4*>(src);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < total; i += kThreads) {
       const int r = i / vec_per_row, c = i - r * vec_per_row;
       char* dst = base + static_cast<long long>(T + r) * rq.row_stride_bytes + 16 * c;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(stage + r * p.row_bytes + 16 * c);
+      if (GLANCE_IN_BOUNDS(T + r, rq.t_cap))
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(stage + r * p.row_bytes + 16 * c);
     }
   }
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads)
     if (p.gated) p.gated[req] = s_gated;
     if (room) *rq.t_len = T + a + 1;
   }
-  if (threadIdx.x >= 1 && threadIdx.x <= a)
+  if (threadIdx.x >= 1 && threadIdx.x <= a && GLANCE_IN_BOUNDS(s_path[threadIdx.x], p.rows))
     p.accepted_tok[req * p.L + threadIdx.x - 1] = s_tok[s_path[threadIdx.x]];
 }
 
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kRowsThreads) kv_write_rows_kernel(const __gri
   char* dst = p.dst[lkv] + head * p.head_stride_bytes + static_cast<long long>(T) * p.row_stride_bytes;
   for (int i = threadIdx.x; i < p.rows * per_row; i += kRowsThreads) {
     const int r = i / per_row, c = i - r * per_row;
-    reinterpret_cast<uint4*>(dst + r * p.row_stride_bytes)[c] = __ldg(src + i);
+    if (GLANCE_IN_BOUNDS(T + r, p.t_cap)) reinterpret_cast<uint4*>(dst + r * p.row_stride_bytes)[c] = __ldg(src + i);
   }
 }
 

@@ -74,7 +74,26 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
   }                                                                                \
   static __device__ __forceinline__ void report(int code) {                        \
     atomicCAS(&g_status_word, 0, code);                                            \
+  }                                                                                \
+  static __device__ __forceinline__ bool glance_in_bounds_checked(long long i,     \
+                                                                  long long n) {   \
+    if (i >= 0 && i < n) return true;                                              \
+    report(GLANCE_DEV_OUT_OF_BOUNDS);                                              \
+    return false;                                                                  \
   }
+
+// Bounds-checked build (-DGLANCE_CHECK, libglance_check.so): every computed
+// global index the kernels store to or load from goes through
+// GLANCE_IN_BOUNDS(i, n). Out of [0, n) it reports GLANCE_DEV_OUT_OF_BOUNDS on
+// the unit's status word and yields false, and the caller skips the access
+// instead of faulting. In the normal build it is the constant true and costs
+// nothing. (TMA copies are bounded by their tensor maps in either build.)
+#ifdef GLANCE_CHECK
+#define GLANCE_IN_BOUNDS(i, n) \
+  glance_in_bounds_checked(static_cast<long long>(i), static_cast<long long>(n))
+#else
+#define GLANCE_IN_BOUNDS(i, n) true
+#endif
 
 // ---------------------------------------------------------------- device side
 

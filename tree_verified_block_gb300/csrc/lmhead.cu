@@ -366,7 +366,8 @@ __global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p)
   if (threadIdx.x < kF32Rows && r0 + threadIdx.x < p.M) {
     Partial a = s_red[0][threadIdx.x];
     for (int w = 1; w < kF32Cols / 32; ++w) merge(a, s_red[w][threadIdx.x]);
-    p.part[static_cast<size_t>(colblk) * p.M + r0 + threadIdx.x] = a;
+    const size_t at = static_cast<size_t>(colblk) * p.M + r0 + threadIdx.x;
+    if (GLANCE_IN_BOUNDS(at, static_cast<size_t>(gridDim.x) * p.M)) p.part[at] = a;
   }
   __threadfence();
   __syncthreads();
@@ -644,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < NB; ++b)
       if (b * kBM + row < p.M) {
         const size_t at = static_cast<size_t>(blockIdx.x) * (NB * kBM) + b * kBM + row;
+        if (!GLANCE_IN_BOUNDS(at, static_cast<size_t>(gridDim.x) * (NB * kBM))) continue;
         if (kH)
           static_cast<PartialH*>(p.part)[at] = PartialH{m1[b], i1[b], m2[b], hs[b], hu[b]};
         else
@@ -882,6 +884,7 @@ __global__ void __launch_bounds__(PairShape<NB>::kThreads, 1)
       const int grow = row0 + (eg + bb * EPI) * kBM + row;
       if (grow < p.M) {
         const size_t at = (static_cast<size_t>(pair) * CH + cg) * (2 * NB * kBM) + grow;
+        if (!GLANCE_IN_BOUNDS(at, static_cast<size_t>(n_pairs) * CH * (2 * NB * kBM))) continue;
         if (kH)
           static_cast<PartialH*>(p.part)[at] = PartialH{m1[bb], i1[bb], m2[bb], hs[bb], hu[bb]};
         else

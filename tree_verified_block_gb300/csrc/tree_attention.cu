@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kF32Threads) tree_attention_f32_kernel(const F
     float s = -INFINITY;
     if (j < n_keys) {
       const int slot = j < T ? j : T + s_tree[j - T];
-      const float* kr = kh + slot * p.row_stride;
+      const float* kr = kh + (GLANCE_IN_BOUNDS(slot, p.t_cap) ? slot : 0) * p.row_stride;
       float dot = 0.f;
       for (int d = 0; d < p.D; ++d) dot = fmaf(s_q[d], kr[d], dot);
       s = dot * p.scale;
@@ -126,14 +126,15 @@ __global__ void __launch_bounds__(kF32Threads) tree_attention_f32_kernel(const F
       for (int jj = 0; jj < cn; ++jj) {
         const int jk = c0 + jj;
         const int slot = jk < T ? jk : T + s_tree[jk - T];
-        a = fmaf(s_p[jj], vh[slot * p.row_stride + threadIdx.x], a);
+        if (GLANCE_IN_BOUNDS(slot, p.t_cap)) a = fmaf(s_p[jj], vh[slot * p.row_stride + threadIdx.x], a);
       }
       acc = a;
     }
     m = m_new;
     __syncthreads();
   }
-  if (threadIdx.x < p.D) p.out[(static_cast<size_t>(i) * p.Hq + h) * p.D + threadIdx.x] = acc / l;
+  const size_t oidx = (static_cast<size_t>(i) * p.Hq + h) * p.D + threadIdx.x;
+  if (threadIdx.x < p.D && GLANCE_IN_BOUNDS(oidx, static_cast<size_t>(p.rows) * p.Hq * p.D)) p.out[oidx] = acc / l;
 }
 
 // ------------------------------------------------------------------ bf16 path
@@ -179,6 +180,7 @@ struct Bf16Params {
   unsigned long long wait_ns;  // limit of every pipeline wait
   int withhold_v;            // 1: the producer never copies the V of a CTA's last key tile
                              //    (the timeout check's wait that runs out)
+  int n_slots;               // partial slots in the workspace (bounds-checked build)
 };
 
 // K and V tensor maps of every request's cache of this layer
@@ -293,6 +295,7 @@ constexpr int kMergeChunk =
 template <typename P>
 __device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char* area, int slot, int S, int qt,
                              int g, int q_row0, int half, int lrow) {
+  if (!GLANCE_IN_BOUNDS(slot + S - 1, p.n_slots)) return;  // uniform across the 256 threads
   const float2* s_ml = reinterpret_cast<const float2*>(area);
   float* s_w = reinterpret_cast<float*>(area + kMergeMlBytes);
   unsigned char* s_o = area + kMergeMlBytes + kMergeWBytes;
@@ -364,9 +367,10 @@ __device__ __noinline__ void ticket_merge(const P& p, Bars* bars, unsigned char*
   }
   const int oq = qt * kBM + lrow;
   const int ohl = oq / p.Rp, oprow = oq % p.Rp;
-  if (ohl < p.G && oprow < p.rows) {
-    uint4* dst = reinterpret_cast<uint4*>(
-        p.out + (static_cast<size_t>(q_row0 + oprow) * p.Hq + g * p.G + ohl) * kD + 64 * half);
+  const size_t oidx = (static_cast<size_t>(q_row0 + oprow) * p.Hq + g * p.G + ohl) * kD + 64 * half;
+  if (ohl < p.G && oprow < p.rows &&
+      GLANCE_IN_BOUNDS(oidx + 63, static_cast<size_t>(p.B) * p.rows * p.Hq * kD)) {
+    uint4* dst = reinterpret_cast<uint4*>(p.out + oidx);
 #pragma unroll
     for (int o = 0; o < 8; ++o)
       dst[o] = make_uint4(pack_bf16x2(acc[8 * o], acc[8 * o + 1]), pack_bf16x2(acc[8 * o + 2], acc[8 * o + 3]),
@@ -808,7 +812,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_split == 1) {
     if (is_sm && ok && my_tiles > 0) {
       const float inv = 1.f / l;
-      __nv_bfloat16* dst = p.out + (static_cast<size_t>(q_row0 + prow) * p.Hq + head) * kD + 64 * half;
+      const size_t oidx = (static_cast<size_t>(q_row0 + prow) * p.Hq + head) * kD + 64 * half;
+      const bool out_ok = valid && GLANCE_IN_BOUNDS(oidx + 63, static_cast<size_t>(p.B) * p.rows * p.Hq * kD);
+      __nv_bfloat16* dst = p.out + oidx;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
@@ -818,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-        if (valid) {
+        if (out_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -842,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (is_sm) {
       // column-major (dim octet, row): a warp's store covers 32 consecutive rows
       uint4* po = p.part_o + (static_cast<size_t>(slot) + split) * 16 * kBM + lrow;
+      const bool slot_ok = GLANCE_IN_BOUNDS(slot + split, p.n_slots);
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
@@ -860,14 +867,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16x2(__uint_as_float(r[8 * v8 + 2 * e]) * inv_l,
                                __uint_as_float(r[8 * v8 + 2 * e + 1]) * inv_l);
-          po[(8 * half + 4 * c + v8) * kBM] = make_uint4(w[0], w[1], w[2], w[3]);
+          if (slot_ok) po[(8 * half + 4 * c + v8) * kBM] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      if (half == 0)
+      if (half == 0 && slot_ok)
         p.part_ml[(static_cast<size_t>(slot) + split) * kBM + lrow] =
             make_float2(my_tiles > 0 && ok ? m : -INFINITY, l);
       named_bar(1, 256);  // this CTA's partial is written (CTA scope)
-      if (threadIdx.x == 128) {
+      if (threadIdx.x == 128 && GLANCE_IN_BOUNDS(grp, p.B * p.Hkv * p.n_qt)) {
         uint32_t* arrived = p.arrive + grp;
         if (p.ticket_merge) {
           const uint32_t before = atom_add_acq_rel_gpu(arrived, 1u);
@@ -903,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rpo = (kBM + S - 1) / S;  // rows per owner
         own0 = split * rpo;
         own_rows = own0 >= kBM ? 0 : (kBM - own0 < rpo ? kBM - own0 : rpo);
+        if (!GLANCE_IN_BOUNDS(slot + S - 1, p.n_slots)) own_rows = 0;
       }
       // this CTA merges tile rows [own0, own0 + own_rows): (row, 8 dims) per
       // item, rows fastest so that neighbouring threads read neighbouring rows
@@ -946,7 +954,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int oq = qt * kBM + orow;
         const int ohl = oq / p.Rp, oprow = oq % p.Rp;
-        if (ohl < p.G && oprow < p.rows) {
+        if (ohl < p.G && oprow < p.rows &&
+            GLANCE_IN_BOUNDS((static_cast<size_t>(q_row0 + oprow) * p.Hq + g * p.G + ohl) * kD + 8 * c8 + 7,
+                             static_cast<size_t>(p.B) * p.rows * p.Hq * kD)) {
           uint4 v;
           v.x = pack_bf16x2(acc[0], acc[1]);
           v.y = pack_bf16x2(acc[2], acc[3]);
@@ -1203,6 +1213,7 @@ glance_status launch_bf16(const char* who, const void* q, int n_q_heads, const g
     p.part_ml = reinterpret_cast<float2*>(ws + pl.counters_bytes +
                                           pl.slots * kBM * kD * sizeof(__nv_bfloat16));
   }
+  p.n_slots = static_cast<int>(pl.slots);
   p.B = B;
   p.rows = rows;
   p.Hq = n_q_heads;
