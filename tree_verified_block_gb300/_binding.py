@@ -16,7 +16,8 @@ F32, BF16 = 0, 1
 STATUS = {0: "GLANCE_OK", 1: "GLANCE_ERR_INVALID_ARG", 2: "GLANCE_ERR_UNSUPPORTED",
           3: "GLANCE_ERR_CAPACITY", 4: "GLANCE_ERR_CUDA", 5: "GLANCE_ERR_DEVICE"}
 DEV_STATUS = {0: "ok", 1: "non-finite draft logits", 2: "tree does not fit the cache",
-              3: "inconsistent tree", 4: "pipeline wait timed out"}
+              3: "inconsistent tree", 4: "pipeline wait timed out",
+              5: "index out of bounds (bounds-checked build)"}
 
 EXPORTS = [
     "glance_build_tree_workspace_bytes", "glance_build_tree",
