@@ -152,6 +152,29 @@ def test_tied_block_within_expansion_capacity(dev, clean_status):
     assert_same_tree(got, ref)
 
 
+def test_random_shapes_sweep(dev, clean_status):
+    # seeded shapes and temperatures: shallow and deep trees, K < N and
+    # K >= N, so that both searches (and the choice between them) are hit
+    g = np.random.default_rng(2024)
+    done = 0
+    while done < 40:
+        L = int(g.integers(1, 17))
+        V = int(g.integers(20, 3000))
+        N = int(g.integers(1, 256))
+        total, pw = 0, 1
+        for _ in range(L):
+            pw *= V
+            total += pw
+            if total >= N:
+                break
+        if total < N:
+            continue
+        scale = float(g.choice([0.3, 1.0, 3.0, 8.0]))
+        x = (g.standard_normal((L, V)) * scale).astype(np.float32)
+        check(x, N, dev, root=int(g.integers(0, V)), T=int(g.integers(0, 5000)))
+        done += 1
+
+
 def test_root_and_T_read_from_device(dev, clean_status):
     x = W.draft_logits_planted(4, 300, seed=3)
     got = gpu_tree(x, 9, 123456, 77777, dev)
