@@ -681,25 +681,34 @@ __device__ bool expand_levels(TreeSmem& ts, LevelSmem& S, const float* s_logq, c
 #pragma unroll
     for (int d = 0; d < kMaxL; ++d) v[d] = d < L ? s_logq[d * K] : 0.f;
     float pd = 0.f;
+    int deep = 0;  // deepest rank-0 chain scoring >= t_lo
     S.P[0] = 0.f;
 #pragma unroll
     for (int d = 0; d < kMaxL; ++d) {
       pd = pd + v[d];
       S.P[d + 1] = pd;
+      if (d < L && pd >= t_lo) deep = d + 1;
     }
+    S.m = deep;
   }
   __syncthreads();
-  // one-deviation nodes (0^(d-1), r); consecutive threads take different rows
-  for (int i = tid; i < L * K; i += kThreads) {
-    const int d = i % L, r = i / L;
-    const float f = S.P[d] + s_logq[d * K + r];
-    if (f >= t_lo) atomicAdd(&S.hcnt[bk(f)], 1u);
+  // The one-deviation bound pays for its histogram only on deep trees: with
+  // the rank-0 chain at most 3 deep above t_lo, t_lo itself leaves few nodes
+  // past the N best.
+  float t = t_lo;
+  if (S.m > 3) {
+    // one-deviation nodes (0^(d-1), r); consecutive threads take different rows
+    for (int i = tid; i < L * K; i += kThreads) {
+      const int d = i % L, r = i / L;
+      const float f = S.P[d] + s_logq[d * K + r];
+      if (f >= t_lo) atomicAdd(&S.hcnt[bk(f)], 1u);
+    }
+    __syncthreads();
+    lv_propose(S, bk, N, t_lo);
+    __syncthreads();
+    t = S.t;
+    for (int i = tid; i < kLvBuckets; i += kThreads) S.hcnt[i] = 0u;
   }
-  __syncthreads();
-  lv_propose(S, bk, N, t_lo);
-  __syncthreads();
-  float t = S.t;
-  for (int i = tid; i < kLvBuckets; i += kThreads) S.hcnt[i] = 0u;
   // depth 1: the ranks with log q >= t
   int total;
   {
