@@ -20,7 +20,8 @@
 //   tensor-memory S buffers, so the next tile's S is computed while this
 //   tile's softmax runs, then O += P V with P read from tensor memory.
 //   Warps 4..11 run the softmax, two threads per query row (one TMEM lane,
-//   64 keys each; the halves exchange their row maxima through shared memory):
+//   64 keys each, lanes t and t + 16 of one warp; they exchange their row
+//   maxima and sums with a shuffle):
 //   they read S with tcgen05.ld, apply the key mask in registers (the row's
 //   ancestor words sit in registers and become one 32-bit visibility word per
 //   32 slots), run the online softmax in base 2, write P as bf16 pairs and
@@ -202,7 +203,7 @@ struct __align__(8) Bars {
   uint64_t mma_drain;        // every MMA of the CTA has finished
   uint32_t tmem_base;
   int abort_flag;
-  float xch[2][kBM];         // [half][row]: partial max / sum exchange
+  int ticket_last;           // ticket mode: this CTA completed the group's count and merges it
 };
 static_assert(sizeof(Bars) <= 1280, "barrier block");
 
@@ -544,11 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tP = tmem + 384;    // P (bf16 pairs, 64 cols)
 
   // softmax-thread state, live until the merge
+  // Softmax warp (quarter, sub) holds the 16 rows 32 quarter + 16 sub + (lane & 15)
+  // of the tile; lanes 0-15 hold keys / output dims 0-63 of those rows and
+  // lanes 16-31 the other 64, so both halves of a row sit in one warp and meet
+  // through a shuffle (TMEM access shape 16x32bx2).
   const bool is_sm = warp >= 4;
-  const int half = is_sm ? (warp - 4) >> 2 : 0;  // which 64 keys / 64 output dims
-  const int quarter = warp & 3;                   // TMEM lane quarter
-  const int lrow = quarter * 32 + lane;
-  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const int half = is_sm ? lane >> 4 : 0;  // which 64 keys / 64 output dims
+  const int quarter = warp & 3;            // TMEM lane quarter
+  const int sub = is_sm ? (warp - 4) >> 2 : 0;
+  const int lrow = quarter * 32 + sub * 16 + (lane & 15);
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32 + sub * 16) << 16;
   const int qrow = qt * kBM + lrow;  // index within the kv head's query rows
   const int hl = qrow / p.Rp;
   const int prow = qrow % p.Rp;
@@ -661,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 0; w < 4; ++w)
       if (valid && w < p.W) anc[w] = p.anc[req][prow * p.W + w];
-    // Every softmax thread reaches both named barriers of every tile; a failed
-    // wait raises the CTA's abort flag, and all threads leave the loop
-    // together right after the first barrier.
+    // A failed wait raises the CTA's abort flag; each warp leaves the loop as
+    // a whole (warp vote) at the first tile where it sees the flag, and the
+    // other warps' later waits give up on the same flag.
     for (int j = 0; j < my_tiles; ++j) {
       const int key0 = run.tile_key0(j);
       // warp-uniform: tcgen05.ld / st below are warp-collective
@@ -674,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this thread's 64 keys of the S row
       uint32_t sr[64];
       if (got_s) {
-        tmem_ld32(tS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(tS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld32x2<64>(tS + lane_off, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32x2<64>(tS + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -706,20 +712,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // scale_log2 > 0, so the max commutes with the scaling
       const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
-      // the other half of the row holds the other 64 keys
-      bars->xch[half][lrow] = pm;
       const bool seen = *reinterpret_cast<volatile int*>(&bars->abort_flag) != 0;
-      if (named_bar_or(1, 256, seen || !got_s)) {
+      if (__any_sync(0xffffffffu, seen || !got_s)) {
         ok = false;
-        break;  // the barrier's OR gives every softmax thread the same answer
+        break;  // the vote gives the whole warp the same answer
       }
-      const float mt = fmaxf(pm, bars->xch[half ^ 1][lrow]);
-      named_bar(1, 256);  // both halves have read before the array is reused
+      // lane ^ 16 holds the other 64 keys of the row
+      const float mt = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
       // The running max only moves when some row of the warp grew by more than
       // 8 (base 2) or had no max yet: a stale max keeps P <= 2^8, cancels
-      // between O and l, and lets most tiles skip the O rescale. The two warps
-      // that hold the halves of these 32 rows see the same (mt, m) per row, so
-      // their votes, and their maxima, agree.
+      // between O and l, and lets most tiles skip the O rescale. Both halves
+      // of each of the warp's 16 rows take part in the vote, so they keep the
+      // same max.
       const bool grow = __any_sync(0xffffffffu, mt > m + 8.f);
       const float m_new = grow ? fmaxf(m, mt) : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -745,15 +749,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!got_o) fail_pipeline(bars);
       tc_fence_after();
       if (got_o) {
-        tmem_st16(tP + lane_off + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-        tmem_st16(tP + lane_off + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+        tmem_st16x2<32>(tP + lane_off, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+        tmem_st16x2<32>(tP + lane_off + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
         // rescale this half's 64 output dims when the running max grew
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t r[32];
-            const uint32_t ta = tO + lane_off + 64 * half + 32 * c;
-            tmem_ld32(ta, r);
+            const uint32_t ta = tO + lane_off + 32 * c;
+            tmem_ld32x2<64>(ta, r);
             tmem_ld_wait();
             uint32_t a[16], b[16];
 #pragma unroll
@@ -761,8 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
               b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
             }
-            tmem_st16(ta, a);
-            tmem_st16(ta + 16, b);
+            tmem_st16x2<64>(ta, a);
+            tmem_st16x2<64>(ta + 16, b);
           }
         }
         tmem_st_wait();
@@ -804,11 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- output
   // total l of the row = sum of the two halves' partial sums (same max)
   float l = 0.f;
-  if (is_sm) {
-    bars->xch[half][lrow] = lh;
-    named_bar(1, 256);
-    l = lh + bars->xch[half ^ 1][lrow];
-  }
+  if (is_sm) l = lh + __shfl_xor_sync(0xffffffffu, lh, 16);
   if (n_split == 1) {
     if (is_sm && ok && my_tiles > 0) {
       const float inv = 1.f / l;
@@ -818,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        tmem_ld32(tO + lane_off + 64 * half + 32 * c, r);
+        tmem_ld32x2<64>(tO + lane_off + 32 * c, r);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
         if (my_tiles > 0 && ok) {
-          tmem_ld32(tO + lane_off + 64 * half + 32 * c, r);
+          tmem_ld32x2<64>(tO + lane_off + 32 * c, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t before = atom_add_acq_rel_gpu(arrived, 1u);
           const bool last = before == static_cast<uint32_t>(S - 1);
           if (last) *arrived = 0u;  // every split has added: ready for the next call
-          bars->xch[0][0] = last ? 1.f : 0.f;
+          bars->ticket_last = last ? 1 : 0;
         } else {
           atom_add_release_gpu(arrived, 1u);  // cumulative release of the CTA's writes
           const uint64_t t0 = globaltimer_ns();
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.ticket_merge) {
         own0 = 0;
         own_rows = 0;
-        if (bars->xch[0][0] != 0.f) ticket_merge(p, bars, sQ, slot, S, qt, g, q_row0, half, lrow);
+        if (bars->ticket_last != 0) ticket_merge(p, bars, sQ, slot, S, qt, g, q_row0, half, lrow);
       } else {
         const int rpo = (kBM + S - 1) / S;  // rows per owner
         own0 = split * rpo;
