@@ -56,10 +56,10 @@ def peaks():
 # the listed files, and a changed source reports traffic null.
 CSRC = os.path.join("tree_verified_block_gb300", "csrc")
 NCU_TRAFFIC = {
-    "glance_tree_attention": dict(bytes=17_900_800, digest="c394559b6395a824",
+    "glance_tree_attention": dict(bytes=17_900_544, digest="2a48df6ce2abfedc",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
-    "glance_lmhead_argmax": dict(bytes=1_245_317_376 + 2_925_312, digest="2cd90fb3722754ca",
+    "glance_lmhead_argmax": dict(bytes=1_245_317_632 + 2_967_296, digest="50ccc1b3abb05a27",
                                  files=["lmhead.cu", "glance_internal.cuh"],
                                  profile="profiles/lmhead_argmax_full36.md"),
 }
