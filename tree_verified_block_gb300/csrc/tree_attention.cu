@@ -146,7 +146,7 @@ constexpr int kBN = 128;         // key slots per tile (MMA N of S, K of PV)
 constexpr int kStages = 3;       // K/V ring depth
 constexpr int kPreTiles = 1;     // prefix key tiles fetched before the dependency wait
 constexpr int kThreads = 384;    // 12 warps: TMA, MMA, TMEM, idle, 2 x 4 softmax
-constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64 used)
+constexpr int kTmemCols = 512;   // S0 (128) | S1 (128) | O (128) | P (64) | Q (64)
 constexpr int kMaxSplit = 16;    // key splits of one (kv head, q tile)
 constexpr int kMaxB = 16;        // requests of one batched call
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // pipeline wait limit: 2 s
@@ -193,6 +193,7 @@ struct KVMaps {
 
 struct __align__(8) Bars {
   uint64_t q_full;
+  uint64_t q_tmem;           // Q copied from shared to tensor memory (the softmax threads)
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t kv_empty[kStages];
@@ -442,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_tmem, 256);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tS0 = tmem;         // S, double-buffered (fp32, 128 cols each)
   const uint32_t tO = tmem + 256;    // O (fp32, 128 cols)
   const uint32_t tP = tmem + 384;    // P (bf16 pairs, 64 cols)
+  const uint32_t tQ = tmem + 448;    // Q (bf16 pairs, 64 cols): the A operand of S = Q K^T
 
   // softmax-thread state, live until the merge
   // Softmax warp (quarter, sub) holds the 16 rows 32 quarter + 16 sub + (lane & 15)
@@ -614,7 +617,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && my_tiles > 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);
-      const uint32_t q_addr = smem_u32(sQ);
       auto issue_qk = [&](int j) -> bool {
         const int st = j % kStages;
         if (!wait_or_abort(&bars->k_full[st], (j / kStages) & 1, bars, p.wait_ns)) return false;
@@ -622,17 +624,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_addr = smem_u32(sKV + st * kKVStageBytes);
         const uint32_t tS = tS0 + (j & 1) * 128;
         const uint32_t idesc_s = idesc_bf16_f32(kBM, run.tile_cols(j), false, false);
+        // A = Q from tensor memory (dims 16 kk .. 16 kk + 15 in columns 8 kk ..),
+        // B = the K tile (K-major, 128-byte swizzle): only K is read from
+        // shared memory, 4 KB per MMA instead of 8
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + offk, 16, 1024),
-                      idesc_s, kk > 0);
+          mma_bf16_ts(tS, tQ + kk * 8, sdesc_sw128(k_addr + offk, 16, 1024), idesc_s, kk > 0);
         }
         mma_commit(&bars->s_full[j & 1]);
         return true;
       };
-      bool good = wait_or_abort(&bars->q_full, 0, bars, p.wait_ns) && issue_qk(0);
+      bool good = wait_or_abort(&bars->q_tmem, 0, bars, p.wait_ns) && issue_qk(0);
       for (int j = 0; good && j < my_tiles; ++j) {
         // S of the next tile goes into the other buffer while tile j's softmax runs;
         // that buffer was last read by the softmax of tile j-1, which p_ready(j-1) covered
@@ -667,6 +670,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 0; w < 4; ++w)
       if (valid && w < p.W) anc[w] = p.anc[req][prow * p.W + w];
+    // Q into tensor memory, in the layout of P: row = lane, column c = dims
+    // (2c, 2c + 1). The Q tile in shared memory is two 128-byte-swizzled
+    // halves of 64 dims (16-byte chunk c of row r at r * 128 + ((c ^ (r & 7)) * 16));
+    // this thread copies the 64 dims of its half of row lrow.
+    if (my_tiles > 0) {
+      const bool got_q = __all_sync(0xffffffffu, wait_or_abort(&bars->q_full, 0, bars, p.wait_ns));
+      if (!got_q) fail_pipeline(bars);
+      uint32_t qv[32];
+      const unsigned char* qrow_s = sQ + half * (kBM * 128) + lrow * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = got_q ? *reinterpret_cast<const uint4*>(qrow_s + ((c ^ (lrow & 7)) << 4))
+                              : make_uint4(0u, 0u, 0u, 0u);
+        qv[4 * c] = v.x;
+        qv[4 * c + 1] = v.y;
+        qv[4 * c + 2] = v.z;
+        qv[4 * c + 3] = v.w;
+      }
+      tmem_st16x2<32>(tQ + lane_off, *reinterpret_cast<const uint32_t(*)[16]>(qv));
+      tmem_st16x2<32>(tQ + lane_off + 16, *reinterpret_cast<const uint32_t(*)[16]>(qv + 16));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->q_tmem);
+    }
     // A failed wait raises the CTA's abort flag; each warp leaves the loop as
     // a whole (warp vote) at the first tile where it sees the flag, and the
     // other warps' later waits give up on the same flag.
