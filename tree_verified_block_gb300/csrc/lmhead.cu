@@ -68,6 +68,17 @@ struct PartialH {
   float u;
 };
 
+template <typename P>
+__device__ __forceinline__ P neutral_partial();
+template <>
+__device__ __forceinline__ Partial neutral_partial<Partial>() {
+  return Partial{-INFINITY, 0x7FFFFFFF, -INFINITY};
+}
+template <>
+__device__ __forceinline__ PartialH neutral_partial<PartialH>() {
+  return PartialH{-INFINITY, 0x7FFFFFFF, -INFINITY, 0.f, 0.f};
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // What the bf16 kernels fold per row.
@@ -237,56 +248,72 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
 }
 
 // Last CTA: one warp per row merges every CTA's partial for that row.
-__device__ void merge_partials_h(const PartialH* part, int n_parts, int part_stride, int M,
-                                 int32_t* argmax, float* gap, float* maxlogit, float* entropy) {
+__device__ __forceinline__ Partial load_partial(const Partial* q) {
+  return Partial{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2)};
+}
+__device__ __forceinline__ PartialH load_partial(const PartialH* q) {
+  return PartialH{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2), __ldcg(&q->s), __ldcg(&q->u)};
+}
+
+// Last CTA: merges every CTA's partial of each row (part[c * part_stride + r]).
+// One CTA's partials are contiguous over rows, so lane i of a warp takes row
+// 32 b + i of a row block b and each step's 32 loads are one contiguous run.
+// The warps split the row blocks and, when there are fewer row blocks than
+// warps, the CTAs too (groups); each thread issues 8 loads before it folds
+// them, so the whole merge costs a few L2 round trips. The groups meet in
+// `scratch` (shared memory, blockDim / 32 x 32 partials). Every fold is a
+// top-2 with lowest-id ties, so the argmax, gap and maximum do not depend on
+// the order; the entropy sums are rebased to the running maximum at each fold.
+template <typename P, typename Out>
+__device__ void merge_rows(const P* part, int n_parts, int part_stride, int M, P* scratch, Out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  for (int r = warp; r < M; r += nwarps) {
-    PartialH a{-INFINITY, 0x7FFFFFFF, -INFINITY, 0.f, 0.f};
-    for (int c = lane; c < n_parts; c += 32) {
-      const PartialH* q = part + static_cast<size_t>(c) * part_stride + r;
-      merge(a, PartialH{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2), __ldcg(&q->s), __ldcg(&q->u)});
-    }
+  const int n_rb = (M + 31) / 32;
+  for (int rb0 = 0; rb0 < n_rb; rb0 += nwarps) {
+    const int nb = n_rb - rb0 < nwarps ? n_rb - rb0 : nwarps;  // row blocks of this pass
+    const int groups = nwarps / nb;
+    const int rbl = warp % nb, grp = warp / nb;
+    const int r = (rb0 + rbl) * 32 + lane;
+    P a = neutral_partial<P>();
+    if (grp < groups && r < M) {
+      for (int c0 = grp; c0 < n_parts; c0 += 8 * groups) {
+        P b[8];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      PartialH b{__shfl_xor_sync(0xffffffffu, a.m1, o), __shfl_xor_sync(0xffffffffu, a.i1, o),
-                 __shfl_xor_sync(0xffffffffu, a.m2, o), __shfl_xor_sync(0xffffffffu, a.s, o),
-                 __shfl_xor_sync(0xffffffffu, a.u, o)};
-      merge(a, b);
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u * groups;
+          b[u] = c < n_parts ? load_partial(part + static_cast<size_t>(c) * part_stride + r) : neutral_partial<P>();
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) merge(a, b[u]);
+      }
     }
-    if (lane == 0) {
-      argmax[r] = a.i1;
-      gap[r] = a.m1 - a.m2;
-      if (maxlogit) maxlogit[r] = a.m1;
-      entropy[r] = logf(a.s) - a.u / a.s;
+    scratch[warp * 32 + lane] = a;
+    __syncthreads();
+    if (grp == 0 && r < M) {
+      for (int gi = 1; gi < groups; ++gi) merge(a, scratch[(gi * nb + rbl) * 32 + lane]);
+      out(r, a);
     }
+    __syncthreads();
   }
 }
 
-// Last CTA: one warp per row merges every CTA's partial for that row.
-__device__ void merge_partials(const Partial* part, int n_parts, int part_stride, int M,
+__device__ void merge_partials_h(const PartialH* part, int n_parts, int part_stride, int M, PartialH* scratch,
+                                 int32_t* argmax, float* gap, float* maxlogit, float* entropy) {
+  merge_rows(part, n_parts, part_stride, M, scratch, [&](int r, const PartialH& a) {
+    argmax[r] = a.i1;
+    gap[r] = a.m1 - a.m2;
+    if (maxlogit) maxlogit[r] = a.m1;
+    entropy[r] = logf(a.s) - a.u / a.s;
+  });
+}
+
+__device__ void merge_partials(const Partial* part, int n_parts, int part_stride, int M, Partial* scratch,
                                int32_t* argmax, float* gap, float* maxlogit) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  for (int r = warp; r < M; r += nwarps) {
-    Partial a{-INFINITY, 0x7FFFFFFF, -INFINITY};
-    for (int c = lane; c < n_parts; c += 32) {
-      const Partial* q = part + static_cast<size_t>(c) * part_stride + r;
-      Partial b{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2)};
-      merge(a, b);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      Partial b{__shfl_xor_sync(0xffffffffu, a.m1, o), __shfl_xor_sync(0xffffffffu, a.i1, o),
-                __shfl_xor_sync(0xffffffffu, a.m2, o)};
-      merge(a, b);
-    }
-    if (lane == 0) {
-      argmax[r] = a.i1;
-      gap[r] = a.m1 - a.m2;
-      if (maxlogit) maxlogit[r] = a.m1;
-    }
-  }
+  merge_rows(part, n_parts, part_stride, M, scratch, [&](int r, const Partial& a) {
+    argmax[r] = a.i1;
+    gap[r] = a.m1 - a.m2;
+    if (maxlogit) maxlogit[r] = a.m1;
+  });
 }
 
 // ------------------------------------------------------------------ fp32 path
@@ -376,7 +403,8 @@ __global__ void __launch_bounds__(kF32Cols) lmhead_f32_kernel(const F32Params p)
   if (s_ticket != gridDim.x * gridDim.y - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
-  merge_partials(p.part, gridDim.x, p.M, p.M, p.argmax, p.gap, p.maxlogit);
+  __shared__ Partial s_merge[kF32Cols];  // one per thread
+  merge_partials(p.part, gridDim.x, p.M, p.M, s_merge, p.argmax, p.gap, p.maxlogit);
 }
 
 // ------------------------------------------------------------------ bf16 path
@@ -665,12 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
+  // the stage ring is idle now: it holds the merge's scratch
   if (kH)
-    merge_partials_h(static_cast<const PartialH*>(p.part), gridDim.x, NB * kBM, p.M, p.argmax, p.gap,
-                     p.maxlogit, p.entropy);
+    merge_partials_h(static_cast<const PartialH*>(p.part), gridDim.x, NB * kBM, p.M,
+                     reinterpret_cast<PartialH*>(smem), p.argmax, p.gap, p.maxlogit, p.entropy);
   else
-    merge_partials(static_cast<const Partial*>(p.part), gridDim.x, NB * kBM, p.M, p.argmax, p.gap,
-                   p.maxlogit);
+    merge_partials(static_cast<const Partial*>(p.part), gridDim.x, NB * kBM, p.M,
+                   reinterpret_cast<Partial*>(smem), p.argmax, p.gap, p.maxlogit);
 }
 
 // ---------------------------------------------- bf16, M > 128: CTA pairs
@@ -907,12 +936,14 @@ __global__ void __launch_bounds__(PairShape<NB>::kThreads, 1)
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
   if (threadIdx.x == 0) *p.ticket = 0;
+  // the stage ring is idle now (every copy into it, the partner's multicasts
+  // included, has landed): it holds the merge's scratch
   if (kH)
     merge_partials_h(static_cast<const PartialH*>(p.part), n_pairs * Sh::CH, 2 * NB * kBM, p.M,
-                     p.argmax, p.gap, p.maxlogit, p.entropy);
+                     reinterpret_cast<PartialH*>(smem), p.argmax, p.gap, p.maxlogit, p.entropy);
   else
     merge_partials(static_cast<const Partial*>(p.part), n_pairs * Sh::CH, 2 * NB * kBM, p.M,
-                   p.argmax, p.gap, p.maxlogit);
+                   reinterpret_cast<Partial*>(smem), p.argmax, p.gap, p.maxlogit);
 }
 
 int row_blocks(int M) { return (M + kBM - 1) / kBM; }
