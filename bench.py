@@ -56,10 +56,10 @@ def peaks():
 # the listed files, and a changed source reports traffic null.
 CSRC = os.path.join("tree_verified_block_gb300", "csrc")
 NCU_TRAFFIC = {
-    "glance_tree_attention": dict(bytes=17_900_544, digest="2a48df6ce2abfedc",
+    "glance_tree_attention": dict(bytes=17_901_312, digest="a2dbddb2f779c4b0",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
-    "glance_lmhead_argmax": dict(bytes=1_245_317_632 + 2_967_296, digest="50ccc1b3abb05a27",
+    "glance_lmhead_argmax": dict(bytes=1_245_285_376 + 3_017_216, digest="b847d770bd7c38db",
                                  files=["lmhead.cu", "glance_internal.cuh"],
                                  profile="profiles/lmhead_argmax_full36.md"),
 }
