@@ -17,7 +17,7 @@
 // read the tile's 256 fp32 logits and fold them into a running
 // (max, argmax, second max) held in registers across tiles, while the MMA
 // warp fills the other accumulator. CTAs write per-row partials; the last CTA
-// (atomic ticket) merges them, one warp per row. M > 128 (rows of several
+// (atomic ticket) merges them, lanes over rows. M > 128 (rows of several
 // requests stacked, up to 512): clusters of two CTAs split the rows and share
 // each W tile through TMA multicast, one launch, W read from HBM once.
 // fp32 path: CUDA cores, 128 vocabulary columns x 8 rows per CTA.
@@ -247,7 +247,6 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
   }
 }
 
-// Last CTA: one warp per row merges every CTA's partial for that row.
 __device__ __forceinline__ Partial load_partial(const Partial* q) {
   return Partial{__ldcg(&q->m1), __ldcg(&q->i1), __ldcg(&q->m2)};
 }
