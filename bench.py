@@ -56,7 +56,7 @@ def peaks():
 # the listed files, and a changed source reports traffic null.
 CSRC = os.path.join("tree_verified_block_gb300", "csrc")
 NCU_TRAFFIC = {
-    "glance_tree_attention": dict(bytes=17_901_312, digest="a2dbddb2f779c4b0",
+    "glance_tree_attention": dict(bytes=17_901_312, digest="0a37add0e235cce0",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
     "glance_lmhead_argmax": dict(bytes=1_245_285_376 + 3_017_216, digest="e95fb0f3e89d49b5",

@@ -18,7 +18,9 @@
 //   two. Warp 0 issues TMA loads (Q once, then K and V tiles of 128 slots into
 //   a three-stage ring); warp 1 issues the MMAs: S = Q K^T into one of two
 //   tensor-memory S buffers, so the next tile's S is computed while this
-//   tile's softmax runs, then O += P V with P read from tensor memory.
+//   tile's softmax runs, then O += P V with P read from tensor memory. Q is
+//   an operand from tensor memory too: the softmax threads copy the landed
+//   Q tile there once, so the S products read only K from shared memory.
 //   Warps 4..11 run the softmax, two threads per query row (one TMEM lane,
 //   64 keys each, lanes t and t + 16 of one warp; they exchange their row
 //   maxima and sums with a shuffle):
