@@ -334,6 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   pdl_wait_prior();
 
+  // rows are owned in blocks of rows_per: CTA o of the cluster sums and
+  // finishes rows o * rows_per ..
+  const int rows_per = (p.M + S - 1) / S;
+  const int r_begin = rank * rows_per;
+  const int r_end = min(p.M, r_begin + rows_per);
+
   // ------------------------------------------------------------ phase 1
   bool ok = true;
   if (warp == 0) {
@@ -390,6 +396,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = false;
       fail_pipeline(bars);
     }
+  } else if (p.in_sumsq) {
+    // warps 2 and 3: the RMSNorm row scales 1 / rms of this CTA's rows, from
+    // the sums of squares the previous kernel emitted per output tile, while
+    // the stages stream (8 loads in flight, summed in tile order)
+    for (int lrow = threadIdx.x - 64; lrow < r_end - r_begin; lrow += 64) {
+      float ss = 0.f;
+      for (int t0 = 0; t0 < p.n_sumsq; t0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = t0 + u < p.n_sumsq ? p.in_sumsq[static_cast<size_t>(t0 + u) * p.M + r_begin + lrow] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ss += v[u];
+      }
+      bars->r[lrow] = rsqrtf(ss / p.K + p.eps);
+    }
   }
   // every role is done with its own stage area (or gave up and drained)
   const bool bad = __syncthreads_or(!ok || *reinterpret_cast<volatile int*>(&bars->abort_flag)) != 0;
@@ -400,10 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x < S) peer_bad = dsmem_ld_s32(dsmem_addr(&bars->failed, threadIdx.x)) != 0;
   const bool any_bad = __syncthreads_or(peer_bad) != 0;
 
-  // rows are owned in blocks of rows_per: CTA o of the cluster sums and
-  // finishes rows o * rows_per .. ; each CTA sends its partial of every row
-  // to the row's owner (remote stores into the owner's stage area)
-  const int rows_per = (p.M + S - 1) / S;
+  // each CTA sends its partial of every row to the row's owner (remote stores
+  // into the owner's stage area)
   if (!any_bad && warp >= 4) {
     tc_fence_after();
     const int quarter = warp - 4;
@@ -437,16 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ phase 2
   if (!any_bad) {
     const int T = p.mode == kQKV ? *p.t_len : 0;
-    const int r_begin = rank * rows_per;
-    const int r_end = min(p.M, r_begin + rows_per);
-    if (p.in_sumsq) {
-      for (int lrow = threadIdx.x; lrow < r_end - r_begin; lrow += kThreads) {
-        float ss = 0.f;
-        for (int t = 0; t < p.n_sumsq; ++t) ss += p.in_sumsq[static_cast<size_t>(t) * p.M + r_begin + lrow];
-        bars->r[lrow] = rsqrtf(ss / p.K + p.eps);
-      }
-      __syncthreads();
-    }
     int col_a, col_b;
     epilogue_cols(p.mode, threadIdx.x, col_a, col_b);
     for (int r0 = r_begin; r0 < r_end; r0 += kChunkRows) {
