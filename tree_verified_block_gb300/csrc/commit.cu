@@ -81,6 +81,9 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int s_gated;
 
   // slice: blockIdx.x = ((request * n_layers + layer) * 2 + kv) * n_kv_heads + head
+  // launched as a programmatic dependent of the LM head: nothing is read
+  // before its writes are visible
+  pdl_wait_prior();
   const int per_req = p.n_layers * 2 * p.n_kv_heads;
   const int req = blockIdx.x / per_req;
   const ReqInfo& rq = p.req[req];
@@ -283,8 +286,24 @@ glance_status fill_and_launch(const char* who, const glance_tree* trees, int B,
   p.new_root = new_root;
   p.ticket = static_cast<uint32_t*>(workspace);
   const int grid = B * n_layers * 2 * l0.n_kv_heads;
-  accept_commit_kernel<kEntries><<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent of the previous kernel (the LM head lets it
+  // launch once every CTA has written its partial; the kernel waits at its
+  // first instruction). It lets no kernel after it start early: the cache
+  // prefix and T it writes are read before the dependency wait by the next
+  // attention call.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, accept_commit_kernel<kEntries>, p);
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return glance::cuda_fail(e, who);
   return GLANCE_OK;
 }

@@ -685,6 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // this CTA's part is done: the next kernel in the stream (the acceptance
+  // walk) may launch and wait for the merge at its dependency wait
+  pdl_launch_dependents();
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_ticket = atomicAdd(p.ticket, 1u);
@@ -928,6 +931,9 @@ __global__ void __launch_bounds__(PairShape<NB>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // this CTA's part is done: the next kernel in the stream (the acceptance
+  // walk) may launch and wait for the merge at its dependency wait
+  pdl_launch_dependents();
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_ticket = atomicAdd(p.ticket, 1u);
