@@ -59,7 +59,7 @@ NCU_TRAFFIC = {
     "glance_tree_attention": dict(bytes=17_901_312, digest="0a37add0e235cce0",
                                   files=["tree_attention.cu", "glance_internal.cuh"],
                                   profile="profiles/tree_attention_full36.md"),
-    "glance_lmhead_argmax": dict(bytes=1_245_285_376 + 3_017_216, digest="e95fb0f3e89d49b5",
+    "glance_lmhead_argmax": dict(bytes=1_245_318_144 + 2_936_576, digest="526945d6caa263ef",
                                  files=["lmhead.cu", "glance_internal.cuh"],
                                  profile="profiles/lmhead_argmax_full36.md"),
 }
