@@ -286,6 +286,35 @@ glance_status glance_lmhead_argmax_noalloc(const void* h, const void* W, glance_
                                            int M, int d, int V, int32_t* argmax, float* gap,
                                            float* maxlogit, void* stream);
 
+/*
+ * W as the LM head streams it, for glance_lmhead_argmax_packed: the same
+ * computation as glance_lmhead_argmax (Section 3.1; Appendix B.1), with W
+ * read in one contiguous 32 KB copy per pipeline stage instead of 64-column
+ * boxes of rows 303 KB apart. W is a model constant: pack it once.
+ *
+ * glance_lmhead_packed_w_bytes: the size of the packed buffer for a BF16 W
+ * [d][V] (ceil(V / 256) * (d / 64) * 32 KB), or 0 unless d % 64 == 0,
+ * d >= 64, V % 8 == 0.
+ *
+ * glance_lmhead_pack_w: W (device BF16 [d][V], row-major) -> W_packed (device,
+ * caller-owned, packed_bytes >= the size above; both 16-byte aligned), on
+ * `stream`. Layout: block (t, kb), t the 256-column tile and kb the 64-row
+ * slice of d, at byte (t * (d / 64) + kb) * 32768; inside it four 8 KB boxes
+ * of 64 columns; row r of a box at r * 128 bytes, its 16-byte chunk c
+ * (columns 8c..8c+7) at chunk position c XOR (r mod 8); columns >= V zero.
+ * Errors: null pointers, unsupported shapes, a short buffer, misalignment.
+ *
+ * glance_lmhead_argmax_packed: glance_lmhead_argmax (greedy) with W given
+ * packed; BF16, 1 <= M <= 128, the same workspace
+ * (glance_lmhead_argmax_workspace_bytes) and outputs, bit-identical results.
+ */
+size_t glance_lmhead_packed_w_bytes(int d, int V);
+glance_status glance_lmhead_pack_w(const void* W, int d, int V, void* W_packed, size_t packed_bytes,
+                                   void* stream);
+glance_status glance_lmhead_argmax_packed(const void* h, const void* W_packed, int M, int d, int V,
+                                          int32_t* argmax, float* gap, float* maxlogit, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------ commit */
 
 /* Workspace bytes for glance_accept_commit. */

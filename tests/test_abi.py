@@ -87,6 +87,27 @@ def test_lmhead_rejects_bad_arguments(glib):
     assert glib.glance_lmhead_argmax_workspace_bytes(0, 10, 10, 1) == 0
 
 
+def test_packed_lmhead_sizes_and_bad_arguments(glib):
+    # ceil(V / 256) x (d / 64) blocks of 32 KB; 0 for shapes the kernel has no layout for
+    assert glib.glance_lmhead_packed_w_bytes(4096, 151936) == 594 * 64 * 32768
+    assert glib.glance_lmhead_packed_w_bytes(64, 8) == 32768
+    assert glib.glance_lmhead_packed_w_bytes(4096, 151937) == 0
+    assert glib.glance_lmhead_packed_w_bytes(100, 1024) == 0
+    assert glib.glance_lmhead_packed_w_bytes(0, 1024) == 0
+    one = ctypes.c_void_p(256)
+    need = 4 * 2 * 32768  # d = 128, V = 1000: 4 tiles x 2 row slices
+    assert glib.glance_lmhead_pack_w(None, 128, 1000, one, need, None) == 1
+    assert glib.glance_lmhead_pack_w(one, 100, 1000, one, need, None) == 2
+    assert glib.glance_lmhead_pack_w(one, 128, 1000, one, need - 16, None) == 3
+    assert glib.glance_lmhead_pack_w(ctypes.c_void_p(264), 128, 1000, one, need, None) == 1
+    # M <= 128 only; the same workspace as glance_lmhead_argmax
+    assert glib.glance_lmhead_argmax_packed(one, one, 129, 128, 1000, one, one, None, one, 1 << 20, None) == 1
+    assert glib.glance_lmhead_argmax_packed(one, one, 0, 128, 1000, one, one, None, one, 1 << 20, None) == 1
+    assert glib.glance_lmhead_argmax_packed(one, None, 64, 128, 1000, one, one, None, one, 1 << 20, None) == 1
+    assert glib.glance_lmhead_argmax_packed(one, one, 64, 100, 1000, one, one, None, one, 1 << 20, None) == 2
+    assert glib.glance_lmhead_argmax_packed(one, one, 64, 128, 1000, one, one, None, one, 16, None) == 3
+
+
 def test_commit_rejects_bad_arguments(glib):
     import tree_verified_block_gb300._binding as b
     tree = b.TreeC(15, 7, 1, 16, 16, 16, 16, 16, 16)

@@ -158,3 +158,37 @@ def test_entropy_rejects_f32(dev):
     ws = g.workspace(1 << 16, dev)
     with pytest.raises(g.GlanceError):
         g.lmhead_argmax_entropy(h, Wt, out, f, f, f, ws)
+
+
+def run_bf16_packed(hb, Wb, dev):
+    """The same call with W packed once (glance_lmhead_pack_w) and read through
+    glance_lmhead_argmax_packed."""
+    import tree_verified_block_gb300 as g
+    M, d = hb.shape
+    V = Wb.shape[1]
+    Wt = bf16_tensor(Wb, dev)
+    Wp = torch.empty(g.lmhead_packed_w_bytes(d, V), dtype=torch.uint8, device=dev)
+    g.lmhead_pack_w(Wt, Wp)
+    am = torch.full((M,), -1, dtype=torch.int32, device=dev)
+    gap = torch.empty(M, dtype=torch.float32, device=dev)
+    mx = torch.empty(M, dtype=torch.float32, device=dev)
+    ws = g.workspace(g.lmhead_argmax_workspace_bytes(M, d, V, torch.bfloat16), dev)
+    g.lmhead_argmax_packed(bf16_tensor(hb, dev), Wp, V, am, gap, mx, ws)
+    return am.cpu().numpy(), gap.cpu().numpy(), mx.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,d,V", [(1, 64, 8), (16, 128, 1000), (64, 256, 5000), (128, 512, 4104),
+                                   (64, 4096, 151936)])
+def test_bf16_packed_w_is_bit_identical(dev, clean_status, M, d, V):
+    # same MMA inputs in the same order: argmax, gap and max equal the unpacked
+    # call's bit for bit, and the unpacked call is held to the oracle above;
+    # V not a multiple of 256 leaves a partial last tile (zero columns)
+    gen = W.rng(M, d, V, 7)
+    hb = W.normal_bf16(gen, (M, d))
+    Wb = W.normal_bf16(gen, (d, V), std=0.02)
+    got = run_bf16_packed(hb, Wb, dev)
+    ref = run_bf16(hb, Wb, dev)
+    for a, b in zip(got, ref):
+        assert np.array_equal(a, b)
+    if V <= 5000:
+        compare(got, o_lmhead(bf16_bits_to_f64(hb), bf16_bits_to_f64(Wb)), 2e-2)

@@ -21,6 +21,7 @@ from ._binding import (STATUS_WORDS, BF16, EXPORTS, F32, LIB_PATH, GlanceError, 
                        build_tree_shared_workspace_bytes, build_tree_workspace_bytes,
                        dense_qkv, dense_residual, dense_swiglu,
                        device_status, lib, lmhead_argmax, lmhead_argmax_noalloc, row_sumsq,
+                       lmhead_argmax_packed, lmhead_pack_w, lmhead_packed_w_bytes,
                        lmhead_argmax_workspace_bytes, reset_device_status, tree_attention,
                        tree_attention_timeout_check, tree_attention_batched, tree_attention_batched_workspace_bytes,
                        tree_attention_workspace_bytes, version, workspace)
@@ -34,6 +35,7 @@ __all__ = ["STATUS_WORDS", "BF16", "EXPORTS", "F32", "LIB_PATH", "GlanceError", 
            "build_tree_shared_workspace_bytes", "build_tree_workspace_bytes", "dense_qkv",
            "dense_residual", "dense_swiglu", "device_status", "row_sumsq",
            "lib", "lmhead_argmax", "lmhead_argmax_noalloc", "lmhead_argmax_workspace_bytes",
+           "lmhead_argmax_packed", "lmhead_pack_w", "lmhead_packed_w_bytes",
            "reset_device_status", "tree_attention", "tree_attention_timeout_check", "tree_attention_batched",
            "tree_attention_batched_workspace_bytes", "tree_attention_workspace_bytes", "version",
            "workspace"]

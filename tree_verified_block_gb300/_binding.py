@@ -24,6 +24,7 @@ EXPORTS = [
     "glance_tree_attention_workspace_bytes", "glance_tree_attention",
     "glance_tree_attention_timeout_check",
     "glance_lmhead_argmax_workspace_bytes", "glance_lmhead_argmax", "glance_lmhead_argmax_noalloc",
+    "glance_lmhead_packed_w_bytes", "glance_lmhead_pack_w", "glance_lmhead_argmax_packed",
     "glance_accept_commit_workspace_bytes", "glance_accept_commit",
     "glance_build_tree_batched_workspace_bytes", "glance_build_tree_batched",
     "glance_tree_attention_batched_workspace_bytes", "glance_tree_attention_batched",
@@ -90,6 +91,12 @@ def lib():
     L.glance_lmhead_argmax.restype = st
     L.glance_lmhead_argmax_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.glance_lmhead_argmax_noalloc.restype = st
+    L.glance_lmhead_packed_w_bytes.argtypes = [i32, i32]
+    L.glance_lmhead_packed_w_bytes.restype = sz
+    L.glance_lmhead_pack_w.argtypes = [vp, i32, i32, vp, sz, vp]
+    L.glance_lmhead_pack_w.restype = st
+    L.glance_lmhead_argmax_packed.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.glance_lmhead_argmax_packed.restype = st
     L.glance_accept_commit_workspace_bytes.argtypes = [i32]
     L.glance_accept_commit_workspace_bytes.restype = sz
     L.glance_accept_commit.argtypes = [ctypes.POINTER(TreeC), vp, ctypes.POINTER(KVC), i32, vp, vp,
@@ -284,6 +291,27 @@ def lmhead_argmax_noalloc(h, W, argmax, gap, maxlogit, stream=None):
     _check(lib().glance_lmhead_argmax_noalloc(_ptr(h), _ptr(W), _dtype_code(h), M, d, W.shape[1],
                                               _ptr(argmax), _ptr(gap), _ptr(maxlogit),
                                               _stream(stream, h.device)))
+
+
+def lmhead_packed_w_bytes(d, V):
+    return lib().glance_lmhead_packed_w_bytes(d, V)
+
+
+def lmhead_pack_w(W, W_packed, stream=None):
+    """W (bf16 [d][V]) -> W_packed (any contiguous device tensor of at least
+    lmhead_packed_w_bytes(d, V) bytes), the layout lmhead_argmax_packed reads."""
+    d, V = W.shape
+    assert W.is_contiguous() and W.dtype == torch.bfloat16 and W_packed.is_contiguous()
+    _check(lib().glance_lmhead_pack_w(_ptr(W), d, V, _ptr(W_packed), W_packed.numel() * W_packed.element_size(),
+                                      _stream(stream, W.device)))
+
+
+def lmhead_argmax_packed(h, W_packed, V, argmax, gap, maxlogit, ws, stream=None):
+    """lmhead_argmax (bf16, M <= 128) with W given as lmhead_pack_w wrote it."""
+    M, d = h.shape
+    assert h.is_contiguous() and h.dtype == torch.bfloat16 and W_packed.is_contiguous()
+    _check(lib().glance_lmhead_argmax_packed(_ptr(h), _ptr(W_packed), M, d, V, _ptr(argmax), _ptr(gap),
+                                             _ptr(maxlogit), _ptr(ws), ws.numel(), _stream(stream, h.device)))
 
 
 def lmhead_argmax_entropy(h, W, argmax, gap, maxlogit, entropy, ws, stream=None):

@@ -444,7 +444,21 @@ struct Bf16Params {
   uint32_t seed_lo, seed_hi;
   const int32_t* position;  // [M] absolute position of the token each row predicts
   const int32_t* seq;       // [M] stream of each row, or null (0)
+  // W packed as stage images (glance_lmhead_pack_w; NB = 1 only), or null:
+  // W through its tensor map
+  const unsigned char* w_packed;
 };
+
+// One contiguous copy of a packed W stage, evict-first in L2 like the
+// tensor-map copies of W.
+__device__ __forceinline__ void bulk_copy_g2s_evict_first(void* dst, const void* src, uint32_t bytes,
+                                                          uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 
 template <int STAGES>
 struct __align__(8) Bars {
@@ -527,18 +541,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // W slices go out before the programmatic-dependent-launch wait, h after it
   const uint32_t a_bytes = NB == 1 ? static_cast<uint32_t>(p.a_rows) * kBK * 2 : NB * kABytes;
   const int n_pre = my_tiles * n_kb < STAGES ? my_tiles * n_kb : STAGES;
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&map_h);
-    tma_prefetch_desc(&map_w);
-    const uint64_t pol_w = policy_evict_first();
-    for (int it = 0; it < n_pre; ++it) {
-      const int v0 = (blockIdx.x + (it / n_kb) * gridDim.x) * BN, kb = it % n_kb;
-      unsigned char* stage = smem + it * Sh::kStageBytes;
-      mbar_arrive_expect_tx(&bars->full[it], a_bytes + Sh::kBBytes);
+  // W slice (tile, kb) of one stage: four tensor-map boxes of 64 x 64, or one
+  // contiguous copy of the same shared-memory image when W is packed
+  auto load_w = [&](unsigned char* stage, uint64_t* bar, int tile, int kb, uint64_t pol) {
+    if (NB == 1 && p.w_packed != nullptr) {
+      bulk_copy_g2s_evict_first(stage + NB * kABytes,
+                                p.w_packed + (static_cast<size_t>(tile) * n_kb + kb) * Sh::kBBytes,
+                                Sh::kBBytes, bar, pol);
+    } else {
 #pragma unroll
       for (int q = 0; q < BN / 64; ++q)
-        tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[it], v0 + 64 * q, kb * kBK,
-                    pol_w);
+        tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, bar, tile * BN + 64 * q, kb * kBK, pol);
+    }
+  };
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_h);
+    if (p.w_packed == nullptr) tma_prefetch_desc(&map_w);
+    const uint64_t pol_w = policy_evict_first();
+    for (int it = 0; it < n_pre; ++it) {
+      const int tile = blockIdx.x + (it / n_kb) * gridDim.x, kb = it % n_kb;
+      unsigned char* stage = smem + it * Sh::kStageBytes;
+      mbar_arrive_expect_tx(&bars->full[it], a_bytes + Sh::kBBytes);
+      load_w(stage, &bars->full[it], tile, kb, pol_w);
     }
   }
   pdl_wait_prior();
@@ -551,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
-        const int v0 = (blockIdx.x + i * gridDim.x) * BN;
+        const int tile = blockIdx.x + i * gridDim.x;
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int st = it % STAGES;
           unsigned char* stage = smem + st * Sh::kStageBytes;
@@ -561,10 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&bars->full[st], a_bytes + Sh::kBBytes);
-#pragma unroll
-            for (int q = 0; q < BN / 64; ++q)
-              tma_load_2d(stage + NB * kABytes + q * kWBoxBytes, &map_w, &bars->full[st], v0 + 64 * q,
-                          kb * kBK, pol_w);
+            load_w(stage, &bars->full[st], tile, kb, pol_w);
           }
 #pragma unroll
           for (int b = 0; b < NB; ++b)
@@ -975,11 +996,41 @@ void set_sample(Bf16Params& p, const SampleArgs& sa) {
   p.seq = sa.seq;
 }
 
+// W [d][V] (bf16, row-major) as the shared-memory images of the M <= 128
+// kernel's W stages: block (t, kb) (256 columns t, 64 rows kb of d) is 32 KB,
+// four 8 KB boxes q of columns 64 q.., row r of a box at r * 128 bytes with
+// its 16-byte chunk c (columns 8 c..) at chunk position c ^ (r % 8) (the
+// 128-byte swizzle the tensor-map copies produce); columns >= V are zero.
+// Thread i writes stored chunk i; a warp reads four whole 128-byte row
+// segments.
+__global__ void __launch_bounds__(256) lmhead_pack_w_kernel(const uint16_t* W, int d, int V, int n_tiles,
+                                                             uint4* out) {
+  const int n_kb = d / kBK;
+  const size_t n_chunks = static_cast<size_t>(n_tiles) * n_kb * 4 * 64 * 8;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_chunks;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int cs = static_cast<int>(i & 7);
+    size_t j = i >> 3;
+    const int r = static_cast<int>(j & 63);
+    j >>= 6;
+    const int q = static_cast<int>(j & 3);
+    j >>= 2;
+    const int kb = static_cast<int>(j % n_kb);
+    const int t = static_cast<int>(j / n_kb);
+    const int col = t * 256 + q * 64 + 8 * (cs ^ (r & 7));  // V % 8 == 0: all 8 or none valid
+    const int row = kb * kBK + r;
+    out[i] = col < V ? *reinterpret_cast<const uint4*>(W + static_cast<size_t>(row) * V + col)
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// W_packed: W as stage images (NB = 1), or null. With it, W is only used to
+// describe a valid (never read) tensor map: pass the packed buffer.
 template <int NB, int kMode>
 glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int32_t* argmax,
                           float* gap, float* maxlogit, float* entropy, void* part, uint32_t* ticket,
                           int max_grid, cudaStream_t s, const char* who,
-                          const SampleArgs& sa = SampleArgs()) {
+                          const SampleArgs& sa = SampleArgs(), const void* w_packed = nullptr) {
   using Sh = Shape<NB>;
   const int n_tiles = (V + Sh::BN - 1) / Sh::BN;
   int grid = glance::num_sms();
@@ -1008,6 +1059,7 @@ glance_status launch_bf16(const void* h, const void* W, int M, int d, int V, int
   }
   Bf16Params p{M, d, V, n_tiles, a_rows, argmax, gap, maxlogit, part, ticket, entropy};
   set_sample(p, sa);
+  p.w_packed = static_cast<const unsigned char*>(w_packed);
   // a programmatic dependent of the previous kernel: W streams in while it ends
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1180,6 +1232,53 @@ extern "C" glance_status glance_lmhead_argmax(const void* h, const void* W, glan
   if (st != GLANCE_OK) return st;
   return lmhead_bf16<kGreedy>(h, W, M, d, V, argmax, gap, maxlogit, nullptr, part, ticket, s,
                               "glance_lmhead_argmax");
+}
+
+extern "C" size_t glance_lmhead_packed_w_bytes(int d, int V) {
+  if (d < kBK || d % kBK != 0 || V < 8 || V % 8 != 0) return 0;
+  return static_cast<size_t>((V + 255) / 256) * (d / kBK) * Shape<1>::kBBytes;
+}
+
+extern "C" glance_status glance_lmhead_pack_w(const void* W, int d, int V, void* W_packed,
+                                              size_t packed_bytes, void* stream) {
+  using glance::fail;
+  const char* who = "glance_lmhead_pack_w";
+  if (!W || !W_packed) return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  const size_t need = glance_lmhead_packed_w_bytes(d, V);
+  if (need == 0)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: needs d %% 64 == 0 (d >= 64) and V %% 8 == 0", who);
+  if (packed_bytes < need)
+    return fail(GLANCE_ERR_CAPACITY, "%s: W_packed holds %zu bytes < %zu needed", who, packed_bytes, need);
+  if (!glance::aligned16(W) || !glance::aligned16(W_packed))
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: W and W_packed must be 16-byte aligned", who);
+  const int n_tiles = (V + 255) / 256;
+  lmhead_pack_w_kernel<<<4 * glance::num_sms(), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(W), d, V, n_tiles, static_cast<uint4*>(W_packed));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return glance::cuda_fail(e, who);
+  return GLANCE_OK;
+}
+
+extern "C" glance_status glance_lmhead_argmax_packed(const void* h, const void* W_packed, int M, int d,
+                                                     int V, int32_t* argmax, float* gap, float* maxlogit,
+                                                     void* workspace, size_t workspace_bytes,
+                                                     void* stream) {
+  using glance::fail;
+  const char* who = "glance_lmhead_argmax_packed";
+  if (!h || !W_packed || !argmax || !gap || !workspace)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: null pointer argument", who);
+  if (M < 1 || M > kBM || d < 1 || V < 1)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: need 1 <= M <= 128, d >= 1, V >= 1", who);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(GLANCE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (glance_lmhead_packed_w_bytes(d, V) == 0)
+    return fail(GLANCE_ERR_UNSUPPORTED, "%s: needs d %% 64 == 0 (d >= 64) and V %% 8 == 0", who);
+  glance_status st = check_bf16_call(who, h, W_packed, M, d, V, workspace, workspace_bytes);
+  if (st != GLANCE_OK) return st;
+  uint32_t* ticket = static_cast<uint32_t*>(workspace);
+  Partial* part = reinterpret_cast<Partial*>(static_cast<char*>(workspace) + 256);
+  return launch_bf16<1, kGreedy>(h, W_packed, M, d, V, argmax, gap, maxlogit, nullptr, part, ticket, 1 << 30,
+                                 static_cast<cudaStream_t>(stream), who, SampleArgs(), W_packed);
 }
 
 extern "C" glance_status glance_lmhead_argmax_entropy(const void* h, const void* W,
